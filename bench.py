@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark: mixed-format (FP8 / TQ3) paged decode attention on GB300.
+
+One step = one decode step of the whole hot path over the workload's batch:
+extend every request by one token (page-table bookkeeping), demote pages
+that left the Recent window (FP8 -> TQ3 kernel), then for each of the 16
+layers append the new K/V token (FP8 quantise kernel) and run mixed-format
+decode attention (partial-attention kernel + LSE merge kernel).
+
+value       = algorithmic KV bytes read by decode attention / timed seconds
+              (inputs resident in HBM; the per-layer working set cycled over
+              16 layers exceeds L2).
+e2e         = the same metric with each step's q/k/v copied from pinned host
+              memory and out/lse copied back inside the timed region.
+roofline    = the partial-attention kernel alone, timed per launch with CUDA
+              events on its stream, against the measured HBM copy bandwidth.
+cpu_baseline = the CPU oracle (fp64 numpy) on a bounded sample, host cores.
+
+Multi-GPU: every rank runs an independent replica of the batch (requests
+are independent; no collective on the data path); value sums all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s read & ctx-tokens/s per layer; fraction of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+ROW_BYTES = {"fp8": 2 * (256 + 2), "tq3": 2 * (96 + 2)}   # K+V bytes per token per kv head
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mkv", "reference"], default="mkv")
+    ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("mkv_kernels.cu", "mkv_internal.h"):
+        with open(os.path.join(ROOT, "mixed_format_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    """Per-launch DRAM bytes of the partial-attention kernel from the committed
+    ncu summary, only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def job_totals(local_ms: float, local_bytes: float, world: int, device=None):
+    """Whole-job figures over ranks: the slowest rank's time and the bytes of
+    all ranks (each rank runs an independent replica)."""
+    if world <= 1:
+        return local_ms, local_bytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    b = torch.tensor([local_bytes], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+def kv_bytes_now(pool, P, L):
+    """Algorithmic KV bytes one decode pass over every live sequence reads, all
+    layers: every valid token once per kv head, K and V, at its tier's size."""
+    st = pool.stats()
+    tq3_tok = st.stale_pages * P
+    fp8_tok = st.live_tokens - tq3_tok
+    per_layer = pool.num_kv_heads * (fp8_tok * ROW_BYTES["fp8"] + tq3_tok * ROW_BYTES["tq3"])
+    return L * per_layer, st.live_tokens
+
+
+# ----------------------------------------------------------------- CPU oracle sample
+def oracle_sample(w, pages_by_req, seconds: float):
+    """Time the oracle's streaming decode over (request, kv head) samples until
+    `seconds` have passed.  Returns (GB/s, bytes, seconds, description)."""
+    import numpy as np
+    from oracle.paged import TIER_STALE, decode_attention_streaming
+    t0 = time.perf_counter()
+    nbytes = 0
+    done = []
+    rng = np.random.default_rng(0)
+    reqs = list(pages_by_req)
+    i = 0
+    while time.perf_counter() - t0 < seconds and i < 64:
+        r = reqs[i % len(reqs)]
+        kvh = int(rng.integers(0, w.Hkv))
+        pages = pages_by_req[r]
+        q = np.asarray(rng.standard_normal((w.Hq, w.D)))
+        decode_attention_streaming(q, pages, w.P, w.Hkv, w.D, 99, kv_heads=[kvh])
+        for t, _, n in pages:
+            nbytes += n * (ROW_BYTES["tq3"] if t == TIER_STALE else ROW_BYTES["fp8"])
+        done.append((r, kvh))
+        i += 1
+    dt = time.perf_counter() - t0
+    desc = (f"oracle streaming decode (fp64 numpy) of {len(done)} (request, kv head) pairs of workload "
+            f"{w.name}, layer 0, {sum(len(pages_by_req[r]) for r, _ in done)} pages")
+    return nbytes / dt / 1e9, nbytes, dt, desc
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args):
+    """Time the CPU oracle, as it stands, on the same workload: each step is a
+    bounded sample (one request's layer-0 pages, one kv head), its pages built
+    by the oracle's own encoders from the workload's inputs."""
+    import numpy as np
+    import torch
+
+    from mixed_format_paged_gb300 import workloads
+    from oracle.paged import TIER_STALE, decode_attention_streaming, demote_page, encode_fp8_page
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workloads.make(args.workload)
+    r = 0
+    K, V = w.prefill_kv(0, r, device="cpu")
+    K = K.float().numpy()
+    V = V.float().numpy()
+    npg = w.npages(r)
+    max_pages = 48
+    pages = []
+    for p in range(max(0, npg - max_pages), npg):
+        nv = min(w.P, w.lengths[r] - p * w.P)
+        pg = encode_fp8_page(K[p * w.P:p * w.P + nv], V[p * w.P:p * w.P + nv], w.P)
+        t = w.tier(r, p)
+        if t == TIER_STALE:
+            pg = demote_page(pg, w.P, w.Hkv, w.D, 99)[0]
+        pages.append((t, pg, nv))
+    step_bytes = sum(n * (ROW_BYTES["tq3"] if t == TIER_STALE else ROW_BYTES["fp8"]) for t, _, n in pages)
+    q = np.random.default_rng(0).standard_normal((w.Hq, w.D))
+    for _ in range(args.warmup):
+        decode_attention_streaming(q, pages, w.P, w.Hkv, w.D, 99, kv_heads=[0])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        decode_attention_streaming(q, pages, w.P, w.Hkv, w.D, 99, kv_heads=[0])
+    dt = time.perf_counter() - t0
+    gbs = step_bytes * args.steps / dt / 1e9
+    sample = (f"oracle streaming decode of request 0, layer 0, kv head 0, last {len(pages)} pages "
+              f"({step_bytes} KV bytes) of workload {w.name}, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "sample": sample},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_mkv(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from mixed_format_paged_gb300 import binding as B
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import Stepper, make_pool, prefill
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    w = workloads.make(args.workload)
+    L, P = w.num_layers, w.P
+    e2e_steps = 0 if args.no_e2e else args.steps
+    total_steps = args.warmup + args.steps + e2e_steps
+    pool = make_pool(w, device=dev, extra_steps=total_steps + 1, seed=99)
+    prefill(pool, w, device=dev)
+    torch.cuda.synchronize()
+    stepper = Stepper(pool, w, device=dev)
+    # per-step inputs, resident on the device before the timed region
+    ins = []
+    for s in range(args.warmup + args.steps):
+        row = []
+        for layer in range(L):
+            k, v = w.step_kv(layer, s, device=dev)
+            row.append((k, v, w.query(layer, s, device=dev)))
+        ins.append(row)
+    outs = [(torch.empty((w.n, w.Hq, w.D), device=dev), torch.empty((w.n, w.Hq), device=dev)) for _ in range(L)]
+    demotes = [0]
+    orig_demote = pool.demote
+
+    def counting_demote(*a, **kw):
+        demotes[0] += 1
+        return orig_demote(*a, **kw)
+    pool.demote = counting_demote
+
+    def step(s, ev_pairs=None, bytes_acc=None):
+        stepper.pre_step()
+        if bytes_acc is not None:
+            bytes_acc.append(kv_bytes_now(pool, P, L))
+        for layer in range(L):
+            k, v, q = ins[s][layer]
+            if ev_pairs is not None:
+                B.mkv_set_timing_events(pool.handle, *ev_pairs[layer])
+            stepper.layer(layer, k, v, q, *outs[layer])
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    # ---------------- timed region (device-resident inputs)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(args.steps)]
+    bytes_acc = []
+    barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    demotes[0] = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i, ev[i], bytes_acc)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    pool.check_device_errors()
+    ms = e0.elapsed_time(e1)
+    timed_demotes = demotes[0]
+    kv_total = sum(b for b, _ in bytes_acc)
+    t_max, kv_job = job_totals(ms, kv_total, world, dev)
+    ctx_total = sum(c for _, c in bytes_acc)
+    kernel_ms = [a.elapsed_time(b) for row in ev for a, b in row]
+    kernel_bytes = [b / L for b, _ in bytes_acc for _ in range(L)]
+    achieved = (sum(kernel_bytes) / len(kernel_bytes)) / (sum(kernel_ms) / len(kernel_ms) * 1e-3) / 1e9
+    peak, peak_src = measured_peaks()
+    gpu_launches = args.steps * L * 3 + timed_demotes
+    # ---------------- e2e through host buffers
+    e2e = None
+    if e2e_steps:
+        hq = [[torch.empty((w.n, w.Hq, w.D), dtype=w.q_dtype).pin_memory() for _ in range(L)]
+              for _ in range(e2e_steps)]
+        hk = [[torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype).pin_memory() for _ in range(L)]
+              for _ in range(e2e_steps)]
+        hv = [[torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype).pin_memory() for _ in range(L)]
+              for _ in range(e2e_steps)]
+        for s in range(e2e_steps):
+            for layer in range(L):
+                k, v = w.step_kv(layer, 10_000 + s)
+                hk[s][layer].copy_(k)
+                hv[s][layer].copy_(v)
+                hq[s][layer].copy_(w.query(layer, 10_000 + s))
+        ho = [torch.empty((w.n, w.Hq, w.D), dtype=torch.float32).pin_memory() for _ in range(L)]
+        hl = [torch.empty((w.n, w.Hq), dtype=torch.float32).pin_memory() for _ in range(L)]
+        dq = torch.empty((w.n, w.Hq, w.D), dtype=w.q_dtype, device=dev)
+        dk = torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype, device=dev)
+        dv = torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype, device=dev)
+        e2e_bytes = []
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for s in range(e2e_steps):
+            stepper.pre_step()
+            e2e_bytes.append(kv_bytes_now(pool, P, L)[0])
+            for layer in range(L):
+                dq.copy_(hq[s][layer], non_blocking=True)
+                dk.copy_(hk[s][layer], non_blocking=True)
+                dv.copy_(hv[s][layer], non_blocking=True)
+                o, l_ = stepper.layer(layer, dk, dv, dq, *outs[layer])
+                ho[layer].copy_(o, non_blocking=True)
+                hl[layer].copy_(l_, non_blocking=True)
+        f1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+        e2e_ms, e2e_job = job_totals(max(f0.elapsed_time(f1), wall * 1e3), sum(e2e_bytes), world, dev)
+        elt = lambda dt: torch.tensor([], dtype=dt).element_size()
+        h2d = L * w.n * (w.Hq * w.D * elt(w.q_dtype) + 2 * w.Hkv * w.D * elt(w.kv_dtype))
+        d2h = L * w.n * (w.Hq * w.D * 4 + w.Hq * 4)
+        e2e = {"value": e2e_job / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps}
+    # ---------------- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pages_by_req = {}
+        for r in range(min(w.n, 4)):
+            pages_by_req[r] = []
+            for p in range(pool.seq_info(r)[1]):
+                b, t, nv = pool.export_page(0, r, p)
+                pages_by_req[r].append((t, np.frombuffer(b, dtype=np.uint8).copy(), nv))
+        gbs, nb, dt, desc = oracle_sample(w, pages_by_req, args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc,
+               "seconds": dt}
+    if rank != 0:
+        return
+    value = kv_job / (t_max * 1e-3) / 1e9
+    per_layer_step_s = (t_max * 1e-3) / (args.steps * L)
+    st = pool.stats()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16xf16->f32 (fp8/tq3 storage)", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "requests": w.n, "layers": L, "page_size": P,
+                   "heads": f"{w.Hq}q/{w.Hkv}kv x {w.D}",
+                   "context_tokens": int(ctx_total / max(1, len(bytes_acc))),
+                   "l2": "inputs larger than L2: per-layer KV working set cycled over 16 layers",
+                   "parallelism": f"replicas x{world}"},
+        "kv_gbs": value,
+        "ctx_tokens_per_s_per_layer": world * (ctx_total / len(bytes_acc)) / per_layer_step_s,
+        "us_per_layer_step": per_layer_step_s * 1e6,
+        "frac_of_hbm_peak": value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": committed_traffic(w.name), "kernel": "mkv_decode_kernel (partial attention)",
+                     "peak_source": peak_src, "launches": len(kernel_ms),
+                     "avg_launch_us": 1e3 * sum(kernel_ms) / len(kernel_ms)},
+        "bytes_per_token_per_tier": {"fp8": 2064 * L, "tq3": 784 * L, "bf16": 4096 * L,
+                                     "pool_kv_bytes_per_live_token": st.kv_bytes_per_live_token,
+                                     "pages_reported_kib_per_token": 18.3},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mkv(args)
+
+
+if __name__ == "__main__":
+    main()

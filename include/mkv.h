@@ -1,0 +1,281 @@
+/*
+ * mkv.h -- C ABI of the mixed-format paged decode-attention library
+ * (GB300 / sm_103a).
+ *
+ * What it implements
+ * ------------------
+ * The decode hot path of "Minima-KV: Retention-Preserving KV Cache
+ * Compression with Mixed-Format Paged Attention" (arXiv 2608.23834).  From
+ * the abstract (mlsanity.com paper page): Recent and protected Anchor pages
+ * remain in FP8, older non-anchor pages move to packed TQ3, every
+ * live-request page remains addressable, and format-specific kernels compute
+ * partial attention states that a globally normalised online-softmax merge
+ * combines, so decode runs over the heterogeneous cache without a cache-sized
+ * dense shadow.  The setupai.cc summary ("Technical Deep Dive") adds that the
+ * mixed formats share PagedAttention's block structure and that TQ3 is a
+ * 3-bit format.
+ *
+ * Calls: mkv_pool_create (page pool + page table + tier tags),
+ * mkv_append_tokens (FP8 quantise into the tail page), mkv_demote_pages
+ * (FP8 -> TQ3 repack), mkv_decode_attention (FP8 partials + TQ3 partials +
+ * LSE merge).  Every step runs in this library's CUDA kernels; there is no
+ * CPU or dense fallback.
+ *
+ * ============================================================ Storage formats
+ * The pages name FP8 and TQ3 but define neither; this section is the
+ * library's definition.  Notation: d = head_dim (256), P = page_size (a
+ * multiple of 16), a "row" = one token, one kv head, K or V.
+ *
+ * FP8 row (Recent, Anchor): E4M3 "fn" codes (OCP FP8; bias 7, max 448, no
+ * infinities) plus one IEEE fp16 scale per row:
+ *     s      = fp16_rn( fp32_rn( max_i |x_i| / 448 ) )
+ *     code_i = e4m3_rn_satfinite( fp32_rn( x_i / s ) )   (all +0 when s == 0)
+ *     x_hat_i = value(code_i) * s                         (exact in fp32)
+ * Inputs x are fp32 or bf16; divisions are IEEE fp32 round-to-nearest-even.
+ *
+ * TQ3 row (Stale): produced from the FP8-dequantised row x_hat by
+ *     y     = R x_hat,  R = H_d D / sqrt(d)
+ *             H_d: Sylvester Hadamard matrix, natural order;
+ *             D = diag(sign_i): sign_i = -1 iff bit (i mod 64) of output
+ *             floor(i/64) of SplitMix64(rotation_seed) is 1 (signs first,
+ *             then H; the same R for K and V, all layers and heads)
+ *     sigma = fp16_rn( ||x_hat||_2 / sqrt(d) )
+ *     u_i   = y_i / sigma  (0 when sigma == 0)
+ *     code_i = #{k in 1..7 : tau_k <= u_i}          (0..7, ties to upper)
+ *     x_tilde = R^T ( sigma * L[code] )
+ * Codebook: L_k = fp16_rn(c_k), c_0 < ... < c_7 the 8-level Lloyd-Max
+ * quantiser of N(0,1) (fp64 fixed point); tau_k = (L_{k-1} + L_k) / 2
+ * (exact).  mkv_tq3_codebook() returns the values.
+ *
+ * Page layout: one (layer, slot) page holds P tokens.  For kv head
+ * h = 0..H_kv-1 in order: a K plane, then a V plane.  A plane is the code
+ * bytes followed by P little-endian fp16 scales in token order.
+ *   FP8 plane codes (P*d bytes):
+ *     K: byte t*d + j                      (row-major)
+ *     V: byte (t/2)*2d + 2j + (t%2)        (rows of a token pair interleaved)
+ *   TQ3 plane codes (P*3d/8 bytes, 8 codes per 3 bytes): 12-byte units of
+ *   32 codes = three little-endian 32-bit words W0, W1, W2:
+ *     bits [4i, 4i+3) of W_k = code (8k + i)           i = 0..7, k = 0..2
+ *     bit  4i+3       of W_k = bit k of code (24 + i)
+ *     K: unit t*(d/32) + j/32, code j%32
+ *     V: unit (t/2)*(d/16) + j/16, code 2*(j%16) + (t%2)
+ * Sizes per page, d = 256, 4 kv heads: FP8 P*2064 B (132,096 at P = 64),
+ * TQ3 P*784 B (50,176 at P = 64); slot s of layer l is at
+ * arena + (l * slots + s) * page_bytes.
+ *
+ * ============================================================ Attention
+ * For a request of length n, query head h (kv head floor(h/G), G =
+ * H_q/H_kv): s_t = q_h . k_t / sqrt(d) over all n tokens (FP8 or TQ3
+ * dequantised per the page's tier), out = sum_t softmax(s)_t v_t (fp32),
+ * lse = ln sum_t exp(s_t) (fp32).  TQ3 pages are scored in the rotated
+ * domain with q' = R q and their output is rotated back once (R^T) after
+ * the TQ3 partials are merged.
+ *
+ * ============================================================ Conventions
+ * Ownership: every device buffer (pool memory, q, k, v, out, lse) belongs to
+ * the caller; the pool keeps non-owning pointers into device_buf, which must
+ * outlive it.  Host arrays are read only during the call.
+ * Streams: GPU work is enqueued on the stream passed in (NULL = legacy default
+ * stream); calls return without waiting unless stated.  Slots freed by
+ * demotion or release are reused in stream order, so a pool must be driven
+ * from one stream (or the caller orders its streams).
+ * Errors: every call returns an mkv_status; no C++ exception crosses the ABI;
+ * mkv_last_error() gives a thread-local message.  A failing call changes no
+ * pool state.  Non-finite inputs are undefined behaviour (not checked).
+ * Threads: a pool is not thread-safe.
+ */
+#ifndef MKV_H_
+#define MKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (CUDA runtime) / CUstream (driver). */
+typedef struct CUstream_st* mkv_stream_t;
+
+typedef enum {
+  MKV_OK = 0,
+  MKV_ERR_INVALID_ARGUMENT = 1, /* bad pointer, id, shape, dtype or range */
+  MKV_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. d != 256) */
+  MKV_ERR_OUT_OF_PAGES = 3,     /* no free slot in the needed arena */
+  MKV_ERR_INVALID_STATE = 4,    /* illegal tier transition or page state */
+  MKV_ERR_CUDA = 5,             /* a CUDA runtime call or launch failed */
+  MKV_ERR_DEVICE_CHECK = 6,     /* a kernel reported a failed check or timeout */
+  MKV_ERR_CAPACITY = 7          /* a per-call limit of the pool was exceeded */
+} mkv_status;
+
+/* Tier tags (the pages' three-tier hierarchy R / A / S).  R and A pages are
+ * FP8, S pages are TQ3. */
+typedef enum {
+  MKV_TIER_NONE = 0,
+  MKV_TIER_RECENT = 1,
+  MKV_TIER_ANCHOR = 2,
+  MKV_TIER_STALE = 3
+} mkv_tier;
+
+typedef enum { MKV_F32 = 0, MKV_BF16 = 1 } mkv_dtype;
+
+/* mkv_pool_config.flags */
+#define MKV_POOL_HOST_ONLY 1 /* bookkeeping only: no device memory is touched and
+                                GPU calls validate, update state and skip the
+                                launch (used by host-logic tests) */
+
+typedef struct {
+  int32_t num_layers;        /* layers sharing one page table */
+  int32_t num_q_heads;       /* H_q */
+  int32_t num_kv_heads;      /* H_kv; G = H_q / H_kv must be 1..8 */
+  int32_t head_dim;          /* d; the kernels support 256 */
+  int32_t page_size;         /* P tokens per page: 64 or 128 */
+  int32_t fp8_slots;         /* FP8 arena capacity in pages (per layer) */
+  int32_t tq3_slots;         /* TQ3 arena capacity in pages (per layer) */
+  int32_t max_seqs;          /* sequence ids are 0..max_seqs-1 */
+  int32_t max_pages_per_seq; /* longest sequence = this * page_size tokens */
+  int32_t max_batch;         /* most sequences in one decode/append call (0: max_seqs) */
+  int32_t flags;             /* MKV_POOL_* */
+  int32_t reserved;          /* must be 0 */
+  uint64_t rotation_seed;    /* SplitMix64 seed of the TQ3 rotation signs */
+} mkv_pool_config;
+
+typedef struct mkv_pool mkv_pool;
+
+typedef struct {
+  int64_t recent_pages, anchor_pages, stale_pages; /* live logical pages per tier */
+  int64_t live_tokens;                             /* sum of sequence lengths */
+  int64_t fp8_bytes, tq3_bytes;                    /* live page bytes, all layers */
+  double kv_bytes_per_live_token;                  /* (fp8+tq3 bytes) / live tokens */
+  int32_t fp8_slots_free, tq3_slots_free;
+  int64_t device_bytes;                            /* size of the pool's device buffer */
+  int64_t workspace_bytes;                         /* partial-state workspace inside it */
+} mkv_stats;
+
+/* ---------------------------------------------------------------- pool */
+
+/* Bytes of device memory a pool with this config needs (arenas, page-table
+ * and plan regions, partial-state workspace).  No device access. */
+mkv_status mkv_pool_required_bytes(const mkv_pool_config* cfg, size_t* device_bytes);
+
+/* Create a pool over the caller's device buffer (>= required bytes, 256-byte
+ * aligned; may be NULL with MKV_POOL_HOST_ONLY).  Zero-fills the FP8 arena on
+ * `stream` so every stored byte is a finite FP8 value.  *out receives the
+ * handle.  Pages: the paged cache extends PagedAttention ("PagedAttention
+ * Integration", setupai.cc "Technical Deep Dive"). */
+mkv_status mkv_pool_create(const mkv_pool_config* cfg, void* device_buf, size_t bytes,
+                           mkv_stream_t stream, mkv_pool** out);
+
+/* Destroy the handle (host memory only; the device buffer stays the caller's).
+ * The caller must make sure no work that uses the pool is still running. */
+mkv_status mkv_pool_destroy(mkv_pool* pool);
+
+/* ---------------------------------------------------------------- sequences */
+
+/* Host bookkeeping: sequence seq_ids[i] grows by n_new[i] >= 0 tokens; every
+ * page it opens takes a free FP8 slot and is tagged RECENT.  All-or-nothing:
+ * MKV_ERR_OUT_OF_PAGES (or a bad id / length past max_pages_per_seq) leaves
+ * every sequence unchanged.  The caller then writes the new tokens of every
+ * layer with mkv_append_tokens before they are attended to. */
+mkv_status mkv_seq_extend(mkv_pool* pool, int32_t n, const int32_t* seq_ids, const int32_t* n_new);
+
+/* Drop a sequence: its slots return to the free lists (reused in stream
+ * order) and its length becomes 0. */
+mkv_status mkv_seq_release(mkv_pool* pool, int32_t seq);
+
+/* Length in tokens and number of pages of a sequence. */
+mkv_status mkv_seq_info(const mkv_pool* pool, int32_t seq, int32_t* length, int32_t* num_pages);
+
+/* Tier and physical slot of logical page `page` of `seq`. */
+mkv_status mkv_page_info(const mkv_pool* pool, int32_t seq, int32_t page, mkv_tier* tier,
+                         int32_t* slot);
+
+/* ---------------------------------------------------------------- write path */
+
+/* FP8 append / quantise (Recent pages stay in FP8: abstract, mlsanity.com).
+ * For layer `layer`, write the last n_new[i] tokens of each sequence
+ * seq_ids[i] (the tokens the preceding mkv_seq_extend added).  k, v: device
+ * arrays [sum_i n_new[i], H_kv, d] of `dtype`, rows in call order.
+ * Each row is quantised as "FP8 row" above into its page.  Enqueued on
+ * `stream`.  Errors: INVALID_ARGUMENT (ids, layer, dtype, n_new larger than
+ * the sequence), INVALID_STATE (a target page is not FP8). */
+mkv_status mkv_append_tokens(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids,
+                             const int32_t* n_new, const void* k, const void* v, mkv_dtype dtype,
+                             mkv_stream_t stream);
+
+/* Re-tag an FP8 page: MKV_TIER_ANCHOR protects it from demotion ("protected
+ * Anchor pages remain in FP8", abstract), MKV_TIER_RECENT unprotects it.
+ * INVALID_STATE for a TQ3 page or for MKV_TIER_STALE (use demotion). */
+mkv_status mkv_set_tier(mkv_pool* pool, int32_t seq, int32_t page, mkv_tier tier);
+
+/* FP8 -> TQ3 demotion ("older non-anchor pages move to packed TQ3",
+ * abstract): for each (seq_ids[i], pages[i]), re-encode the page of every
+ * layer as "TQ3 row" above into a fresh TQ3 slot, tag it STALE and free its
+ * FP8 slot (stream-ordered reuse).  All-or-nothing checks first:
+ * INVALID_STATE for an Anchor page, a TQ3 page, a partial (not full) page or
+ * a page listed twice; OUT_OF_PAGES when the TQ3 arena is short. */
+mkv_status mkv_demote_pages(mkv_pool* pool, int32_t n, const int32_t* seq_ids, const int32_t* pages,
+                            mkv_stream_t stream);
+
+/* ---------------------------------------------------------------- decode */
+
+/* Mixed-format decode attention for one layer ("Format-specific kernels
+ * compute partial attention states and combine them through a globally
+ * normalized online-softmax merge", abstract).  q: device [n, H_q, d] of
+ * `dtype`; out: device fp32 [n, H_q, d]; lse: device fp32 [n, H_q] (natural
+ * log).  Attends over all tokens of each sequence (length >= 1).
+ * Workspace use is O(#splits x H_q x d), independent of context length.
+ * Errors: INVALID_ARGUMENT (n > max_batch, empty sequence, repeated id,
+ * layer, dtype, NULL pointers). */
+mkv_status mkv_decode_attention(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids,
+                                const void* q, mkv_dtype dtype, float* out, float* lse,
+                                mkv_stream_t stream);
+
+/* ---------------------------------------------------------------- inspection */
+
+/* Live pages and bytes per tier and KV bytes per live token (the pages'
+ * deployment accounting, abstract: 18.3 KiB per live token on their model). */
+mkv_status mkv_pool_stats(const mkv_pool* pool, mkv_stats* stats);
+
+/* Copy the raw bytes of one (layer, seq, page) into host_dst (cap bytes
+ * available; needs the page size of its tier).  Synchronises `stream`.
+ * *tier and *n_valid (tokens written) are filled when non-NULL. */
+mkv_status mkv_export_page(mkv_pool* pool, int32_t layer, int32_t seq, int32_t page, void* host_dst,
+                           size_t cap, mkv_tier* tier, int32_t* n_valid, mkv_stream_t stream);
+
+/* The pool's rotation signs (d entries, +1 / -1). */
+mkv_status mkv_rotation_signs(const mkv_pool* pool, int8_t* host_dst, int32_t cap);
+
+/* The stored TQ3 codebook: levels[8] (fp16 values, ascending) and
+ * thresholds[7].  Library constant, computed at load time by the library's
+ * own Lloyd-Max iteration. */
+mkv_status mkv_tq3_codebook(float* levels8, float* thresholds7);
+
+/* Decode plan for a batch (host only, no device access): the number of
+ * partial-state splits the decode kernels would use, and per split 6 ints
+ * {batch index, kv head, tier (1 = FP8, 3 = TQ3), first page entry, page
+ * count, tokens}.  chunks may be NULL to query the count. */
+mkv_status mkv_plan_decode(mkv_pool* pool, int32_t n, const int32_t* seq_ids, int32_t* chunks,
+                           int32_t cap, int32_t* n_chunks);
+
+/* Synchronise `stream` and report (and clear) the pool's device error word:
+ * MKV_ERR_DEVICE_CHECK if a kernel flagged a failed check or a bounded wait
+ * that ran out. */
+mkv_status mkv_check_device_errors(mkv_pool* pool, mkv_stream_t stream);
+
+/* Instrumentation: when `start` / `stop` (cudaEvent_t handles owned by the
+ * caller) are non-NULL, the next mkv_decode_attention call records `start`
+ * right before its partial-attention kernel and `stop` right after it, on the
+ * call's stream, then forgets them.  Lets a caller time that kernel alone. */
+mkv_status mkv_set_timing_events(mkv_pool* pool, void* start, void* stop);
+
+/* Thread-local text of the last error (never NULL). */
+const char* mkv_last_error(void);
+
+/* Library version string. */
+const char* mkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MKV_H_ */

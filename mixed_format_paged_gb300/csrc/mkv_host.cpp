@@ -1,0 +1,966 @@
+// Host side of the mixed-format paged decode-attention library: page pool,
+// page table and tier tags, free lists, decode planning, uploads and the C
+// ABI declared in include/mkv.h.
+//
+// Method: "Minima-KV: Retention-Preserving KV Cache Compression with
+// Mixed-Format Paged Attention" (arXiv 2608.23834), abstract (mlsanity.com):
+// Recent and protected Anchor pages in FP8, older non-anchor pages in packed
+// TQ3, every live-request page addressable; the setupai.cc summary
+// ("Technical Deep Dive") places the formats in PagedAttention's block
+// structure.  Everything here is bookkeeping; all arithmetic on cache data
+// runs in mkv_kernels.cu.
+#include "mkv.h"
+#include "mkv_internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <string>
+#include <utility>
+#include <vector>
+
+namespace {
+
+using namespace mkv;
+
+thread_local std::string g_last_error = "no error";
+
+mkv_status fail(mkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------------ codebook
+// 8-level Lloyd-Max quantiser for N(0,1) (Lloyd's alternation: thresholds at
+// midpoints, levels at cell centroids), levels rounded to fp16.  Written from
+// the mathematics; independent of any other implementation in the repository.
+double phi(double x) { return std::isfinite(x) ? std::exp(-0.5 * x * x) / std::sqrt(2.0 * M_PI) : 0.0; }
+double Phi(double x) {
+  if (x == INFINITY) return 1.0;
+  if (x == -INFINITY) return 0.0;
+  return 0.5 * std::erfc(-x / std::sqrt(2.0));
+}
+
+// IEEE binary16 round-to-nearest-even of a double; returns the value and bits.
+double round_fp16(double v, uint16_t* bits) {
+  const uint16_t sign = std::signbit(v) ? 0x8000 : 0;
+  double a = std::fabs(v);
+  if (a == 0.0) {
+    *bits = sign;
+    return v;
+  }
+  int e;
+  std::frexp(a, &e);          // a = f * 2^e, f in [0.5, 1)
+  int ex = std::max(e - 1, -14);
+  const double q = std::ldexp(1.0, ex - 10);
+  double r = std::nearbyint(a / q) * q;   // default rounding mode: ties to even
+  if (r > 65504.0) {
+    *bits = sign | 0x7C00;
+    return std::copysign(INFINITY, v);
+  }
+  // encode
+  uint16_t b;
+  if (r < std::ldexp(1.0, -14)) {
+    b = static_cast<uint16_t>(std::nearbyint(r / std::ldexp(1.0, -24)));
+  } else {
+    int er;
+    const double f = std::frexp(r, &er);   // r = f 2^er
+    const int E = er - 1;                  // r in [2^E, 2^(E+1))
+    const int man = static_cast<int>(std::nearbyint((f * 2.0 - 1.0) * 1024.0));
+    b = static_cast<uint16_t>(((E + 15) << 10) | man);
+  }
+  *bits = sign | b;
+  return std::copysign(r, v);
+}
+
+Codebook make_codebook() {
+  double lv[8];
+  for (int k = 0; k < 8; ++k) lv[k] = -2.0 + 4.0 * k / 7.0;
+  for (int it = 0; it < 10000; ++it) {
+    double edge[9];
+    edge[0] = -INFINITY;
+    edge[8] = INFINITY;
+    for (int k = 1; k < 8; ++k) edge[k] = 0.5 * (lv[k - 1] + lv[k]);
+    double delta = 0.0;
+    for (int k = 0; k < 8; ++k) {
+      const double c = (phi(edge[k]) - phi(edge[k + 1])) / (Phi(edge[k + 1]) - Phi(edge[k]));
+      delta = std::max(delta, std::fabs(c - lv[k]));
+      lv[k] = c;
+    }
+    if (delta < 1e-15) break;
+  }
+  Codebook cb;
+  for (int k = 0; k < 8; ++k) cb.level[k] = static_cast<float>(round_fp16(lv[k], &cb.level_bits[k]));
+  for (int k = 1; k < 8; ++k) cb.thr[k - 1] = static_cast<float>(0.5 * (double(cb.level[k - 1]) + cb.level[k]));
+  return cb;
+}
+
+const Codebook& codebook() {
+  static const Codebook cb = make_codebook();
+  return cb;
+}
+
+Lut make_lut(const Codebook& cb) {
+  Lut t{};
+  for (int k = 0; k < 4; ++k) {
+    t.lo_a |= uint32_t(cb.level_bits[k] & 0xff) << (8 * k);
+    t.lo_b |= uint32_t(cb.level_bits[k + 4] & 0xff) << (8 * k);
+    t.hi_a |= uint32_t(cb.level_bits[k] >> 8) << (8 * k);
+    t.hi_b |= uint32_t(cb.level_bits[k + 4] >> 8) << (8 * k);
+  }
+  return t;
+}
+
+// ------------------------------------------------------------------ SplitMix64
+// Steele, Lea, Flood, "Fast splittable pseudorandom number generators"
+// (OOPSLA 2014): state advances by the golden gamma, output is the state
+// mixed by two xor-shift-multiply rounds and a final xor-shift.
+uint64_t splitmix64_next(uint64_t& state) {
+  state += 0x9E3779B97F4A7C15ull;
+  uint64_t z = state;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// ------------------------------------------------------------------ pool
+struct PageRec {
+  int32_t slot;
+  int8_t tier;   // mkv_tier
+};
+
+struct SeqRec {
+  int32_t len = 0;
+  std::vector<PageRec> pages;
+};
+
+struct Staging {          // pinned host buffer + event guarding reuse
+  void* host = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t ev = nullptr;
+  bool pending = false;
+};
+
+}  // namespace
+
+struct mkv_pool {
+  mkv_pool_config cfg{};
+  bool host_only = false;
+  int device = 0;
+  int n_sm = 152;
+  int G = 0;
+  int64_t fp8_page_bytes = 0, tq3_page_bytes = 0;
+  // device carve
+  uint8_t* base = nullptr;
+  size_t bytes = 0;
+  uint8_t* fp8_arena = nullptr;
+  uint8_t* tq3_arena = nullptr;
+  uint8_t* plan_region = nullptr;
+  size_t plan_bytes = 0;
+  uint32_t* append_region = nullptr;
+  int append_cap = 0;
+  int2* demote_region = nullptr;
+  int demote_cap = 0;
+  float* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  int* err = nullptr;
+  int chunk_cap = 0;
+  int entry_cap = 0;
+  // host state
+  std::vector<SeqRec> seqs;
+  std::vector<int32_t> free_fp8, free_tq3;
+  uint64_t generation = 1;
+  uint64_t signs[4] = {0, 0, 0, 0};
+  Lut lut{};
+  // staging
+  Staging st_plan, st_append, st_demote;
+  // plan cache
+  uint64_t plan_gen = 0;
+  std::vector<int32_t> plan_ids;
+  DecodeParams plan_params{};
+  MergeParams merge_params{};
+  std::vector<int32_t> plan_debug;   // 6 ints per chunk
+  // one-shot timing events around the next decode kernel
+  cudaEvent_t t_start = nullptr, t_stop = nullptr;
+  // append cache
+  uint64_t app_gen = 0;
+  std::vector<int32_t> app_ids, app_new;
+  int app_ntok = 0;
+};
+
+namespace {
+
+struct PlanLayout {
+  size_t entries, chunks, cta_chunks, cta_start, merge, total;
+};
+
+PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
+  PlanLayout L;
+  size_t off = 0;
+  L.entries = off;
+  off += align256(size_t(entry_cap) * sizeof(PageEntry));
+  L.chunks = off;
+  off += align256(size_t(chunk_cap) * sizeof(Chunk));
+  L.cta_chunks = off;
+  off += align256(size_t(chunk_cap) * sizeof(int32_t));
+  L.cta_start = off;
+  off += align256(size_t(kMaxCtas + 1) * sizeof(int32_t));
+  L.merge = off;
+  off += align256(size_t(max_batch) * Hkv * sizeof(MergeDesc));
+  L.total = off;
+  return L;
+}
+
+constexpr int kAppendCap = 65536;   // tokens per append launch
+constexpr int kDemoteCap = 16384;   // pages per demote launch
+
+int effective_batch(const mkv_pool_config& c) { return c.max_batch > 0 ? c.max_batch : c.max_seqs; }
+
+mkv_status validate_config(const mkv_pool_config* c) {
+  if (!c) return fail(MKV_ERR_INVALID_ARGUMENT, "config is NULL");
+  if (c->num_layers < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1 || c->head_dim < 1 || c->page_size < 1 ||
+      c->fp8_slots < 1 || c->tq3_slots < 0 || c->max_seqs < 1 || c->max_pages_per_seq < 1 || c->max_batch < 0)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "config fields must be positive");
+  if (c->reserved != 0 || (c->flags & ~MKV_POOL_HOST_ONLY))
+    return fail(MKV_ERR_INVALID_ARGUMENT, "unknown config flags / reserved field not 0");
+  if (c->num_q_heads % c->num_kv_heads)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "num_q_heads must be a multiple of num_kv_heads");
+  const int G = c->num_q_heads / c->num_kv_heads;
+  if (G > kMaxGroup) return fail(MKV_ERR_UNSUPPORTED, "GQA group %d > %d", G, kMaxGroup);
+  if (c->head_dim != kHeadDim) return fail(MKV_ERR_UNSUPPORTED, "head_dim %d: the kernels support 256", c->head_dim);
+  if (c->page_size != 64 && c->page_size != 128)
+    return fail(MKV_ERR_UNSUPPORTED, "page_size %d: supported 64 and 128", c->page_size);
+  if (effective_batch(*c) > c->max_seqs) return fail(MKV_ERR_INVALID_ARGUMENT, "max_batch > max_seqs");
+  if (int64_t(c->fp8_slots) >= (1 << 24) || int64_t(c->tq3_slots) >= (1 << 24))
+    return fail(MKV_ERR_UNSUPPORTED, "slot counts must be < 2^24");
+  return MKV_OK;
+}
+
+struct Sizes {
+  int64_t fp8_page, tq3_page;
+  size_t fp8_arena, tq3_arena, plan, append, demote, workspace, err, total;
+  int entry_cap, chunk_cap;
+};
+
+Sizes compute_sizes(const mkv_pool_config& c) {
+  Sizes s;
+  const int P = c.page_size, H = c.num_kv_heads, D = c.head_dim;
+  s.fp8_page = int64_t(H) * 2 * P * (D + 2);
+  s.tq3_page = int64_t(H) * 2 * P * (3 * D / 8 + 2);
+  s.fp8_arena = align256(size_t(c.num_layers) * c.fp8_slots * s.fp8_page);
+  s.tq3_arena = align256(size_t(c.num_layers) * c.tq3_slots * s.tq3_page);
+  const int mb = effective_batch(c);
+  s.entry_cap = mb * c.max_pages_per_seq;
+  s.chunk_cap = mb * H * 2 + 4 * kMaxCtas;
+  s.plan = plan_layout(s.entry_cap, s.chunk_cap, mb, H).total;
+  s.append = align256(size_t(kAppendCap) * 4);
+  s.demote = align256(size_t(kDemoteCap) * 8);
+  const int G = c.num_q_heads / c.num_kv_heads;
+  s.workspace = align256(size_t(s.chunk_cap) * G * (2 + D) * 4);
+  s.err = 256;
+  s.total = s.fp8_arena + s.tq3_arena + s.plan + s.append + s.demote + s.workspace + s.err;
+  return s;
+}
+
+mkv_status staging_alloc(Staging& st, size_t bytes) {
+  st.bytes = bytes;
+  cudaError_t e = cudaHostAlloc(&st.host, bytes, cudaHostAllocDefault);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc");
+  e = cudaEventCreateWithFlags(&st.ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  return MKV_OK;
+}
+
+void staging_free(Staging& st) {
+  if (st.ev) {
+    cudaEventSynchronize(st.ev);
+    cudaEventDestroy(st.ev);
+  }
+  if (st.host) cudaFreeHost(st.host);
+  st = Staging{};
+}
+
+// Make the pinned buffer safe to overwrite (its previous copy has finished).
+mkv_status staging_acquire(Staging& st) {
+  if (st.pending) {
+    const cudaError_t e = cudaEventSynchronize(st.ev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    st.pending = false;
+  }
+  return MKV_OK;
+}
+
+mkv_status staging_upload(Staging& st, void* dev, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return MKV_OK;
+  cudaError_t e = cudaMemcpyAsync(dev, st.host, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (upload)");
+  e = cudaEventRecord(st.ev, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  st.pending = true;
+  return MKV_OK;
+}
+
+bool valid_seq(const mkv_pool* p, int32_t s) { return s >= 0 && s < p->cfg.max_seqs; }
+
+int npages_for(int len, int P) { return (len + P - 1) / P; }
+
+// ------------------------------------------------------------------ planner
+// Split the batch's pages into partial-state chunks, balanced by bytes, and
+// assign chunks to CTAs (longest first onto the least-loaded CTA).  CTAs
+// [0, n_ctas_fp8) run the FP8 body, the rest the TQ3 body; the CTA split is
+// proportional to each format's bytes.
+mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, cudaStream_t stream) {
+  const int P = p->cfg.page_size, H = p->cfg.num_kv_heads;
+  const PlanLayout L = plan_layout(p->entry_cap, p->chunk_cap, effective_batch(p->cfg), H);
+  std::vector<PageEntry> entries;
+  entries.reserve(size_t(n) * 64);
+  struct BatchPages {
+    int f_first, f_count, t_first, t_count;
+    int64_t f_tok, t_tok;
+  };
+  std::vector<BatchPages> bp(n);
+  int64_t fp8_tok = 0, tq3_tok = 0;
+  for (int b = 0; b < n; ++b) {
+    const SeqRec& s = p->seqs[ids[b]];
+    const int np = int(s.pages.size());
+    BatchPages& B = bp[b];
+    B.f_first = int(entries.size());
+    B.f_tok = B.t_tok = 0;
+    for (int i = 0; i < np; ++i) {
+      const int nv = (i == np - 1) ? s.len - i * P : P;
+      if (s.pages[i].tier != MKV_TIER_STALE) {
+        entries.push_back({s.pages[i].slot, nv});
+        B.f_tok += nv;
+      }
+    }
+    B.f_count = int(entries.size()) - B.f_first;
+    B.t_first = int(entries.size());
+    for (int i = 0; i < np; ++i) {
+      if (s.pages[i].tier == MKV_TIER_STALE) {
+        entries.push_back({s.pages[i].slot, P});
+        B.t_tok += P;
+      }
+    }
+    B.t_count = int(entries.size()) - B.t_first;
+    fp8_tok += B.f_tok;
+    tq3_tok += B.t_tok;
+  }
+  if (int(entries.size()) > p->entry_cap) return fail(MKV_ERR_CAPACITY, "plan entries exceed capacity");
+  const double fbytes = double(fp8_tok) * 2 * (kHeadDim + 2);
+  const double tbytes = double(tq3_tok) * 2 * (3 * kHeadDim / 8 + 2);
+  const int nsm = std::min(p->n_sm, kMaxCtas);
+  int nf = 0, nt = 0;
+  if (fbytes > 0 && tbytes > 0) {
+    nf = int(std::lround(nsm * fbytes / (fbytes + tbytes)));
+    nf = std::max(1, std::min(nf, nsm - 1));
+    nt = nsm - nf;
+  } else if (fbytes > 0) {
+    nf = nsm;
+  } else {
+    nt = nsm;
+  }
+  // chunking
+  std::vector<Chunk> chunks;
+  std::vector<MergeDesc> md(size_t(n) * H);
+  const int per_cta = 2;
+  auto split = [&](int b, int kvh, int fmt, int first, int count, const int64_t target) {
+    if (count == 0) return;
+    int64_t tok = 0;
+    for (int i = 0; i < count; ++i) tok += entries[first + i].nvalid;
+    int nc = int(std::max<int64_t>(1, (tok + target / 2) / std::max<int64_t>(1, target)));
+    nc = std::min(nc, count);
+    for (int c = 0; c < nc; ++c) {
+      const int a = first + int(int64_t(count) * c / nc);
+      const int e = first + int(int64_t(count) * (c + 1) / nc);
+      Chunk ch{};
+      ch.b = b;
+      ch.kvh = kvh;
+      ch.fmt = fmt;
+      ch.entry0 = a;
+      ch.nentry = e - a;
+      int t = 0;
+      for (int i = a; i < e; ++i) t += entries[i].nvalid;
+      ch.tokens = t;
+      chunks.push_back(ch);
+    }
+  };
+  const int64_t ftarget = nf ? std::max<int64_t>(1, fp8_tok * H / (int64_t(nf) * per_cta)) : 1;
+  const int64_t ttarget = nt ? std::max<int64_t>(1, tq3_tok * H / (int64_t(nt) * per_cta)) : 1;
+  for (int b = 0; b < n; ++b) {
+    for (int kvh = 0; kvh < H; ++kvh) {
+      MergeDesc& m = md[size_t(b) * H + kvh];
+      m.tq3_first = int(chunks.size());
+      split(b, kvh, 1, bp[b].t_first, bp[b].t_count, ttarget);
+      m.tq3_count = int(chunks.size()) - m.tq3_first;
+      m.fp8_first = int(chunks.size());
+      split(b, kvh, 0, bp[b].f_first, bp[b].f_count, ftarget);
+      m.fp8_count = int(chunks.size()) - m.fp8_first;
+    }
+  }
+  if (int(chunks.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan chunks exceed capacity");
+  // LPT assignment per format
+  std::vector<std::vector<int32_t>> per_cta_list(size_t(nf + nt));
+  for (int fmt = 0; fmt < 2; ++fmt) {
+    const int c0 = fmt == 0 ? 0 : nf;
+    const int nc = fmt == 0 ? nf : nt;
+    if (nc == 0) continue;
+    std::vector<int32_t> ids_f;
+    for (int i = 0; i < int(chunks.size()); ++i)
+      if (chunks[i].fmt == fmt) ids_f.push_back(i);
+    std::stable_sort(ids_f.begin(), ids_f.end(),
+                     [&](int a, int b) { return chunks[a].tokens > chunks[b].tokens; });
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < nc; ++c) heap.push({0, c});
+    for (int id : ids_f) {
+      Load l = heap.top();
+      heap.pop();
+      per_cta_list[c0 + l.second].push_back(id);
+      l.first += chunks[id].tokens;
+      heap.push(l);
+    }
+  }
+  // drop empty CTAs at the end of each format range is not needed: empty CTAs exit at once
+  std::vector<int32_t> cta_chunks, cta_start;
+  cta_start.push_back(0);
+  for (auto& l : per_cta_list) {
+    for (int id : l) cta_chunks.push_back(id);
+    cta_start.push_back(int(cta_chunks.size()));
+  }
+  // debug record
+  p->plan_debug.clear();
+  for (const Chunk& c : chunks) {
+    const int tier = c.fmt == 0 ? 1 : 3;
+    const int32_t rec[6] = {c.b, c.kvh, tier, c.entry0, c.nentry, c.tokens};
+    p->plan_debug.insert(p->plan_debug.end(), rec, rec + 6);
+  }
+  // params
+  DecodeParams& dp = p->plan_params;
+  dp = DecodeParams{};
+  dp.entries = reinterpret_cast<const PageEntry*>(p->plan_region + L.entries);
+  dp.chunks = reinterpret_cast<const Chunk*>(p->plan_region + L.chunks);
+  dp.cta_chunks = reinterpret_cast<const int32_t*>(p->plan_region + L.cta_chunks);
+  dp.cta_start = reinterpret_cast<const int32_t*>(p->plan_region + L.cta_start);
+  dp.n_ctas_fp8 = nf;
+  dp.n_ctas = nf + nt;
+  dp.fp8_page_bytes = p->fp8_page_bytes;
+  dp.tq3_page_bytes = p->tq3_page_bytes;
+  dp.fp8_slots = p->cfg.fp8_slots;
+  dp.tq3_slots = p->cfg.tq3_slots;
+  dp.Hq = p->cfg.num_q_heads;
+  dp.Hkv = H;
+  dp.G = p->G;
+  dp.P = P;
+  dp.part = p->workspace;
+  std::memcpy(dp.signs, p->signs, sizeof dp.signs);
+  dp.score_scale = float(1.4426950408889634 / std::sqrt(double(kHeadDim)));
+  dp.lut = p->lut;
+  dp.err = p->err;
+  MergeParams& mp = p->merge_params;
+  mp = MergeParams{};
+  mp.part = p->workspace;
+  mp.desc = reinterpret_cast<const MergeDesc*>(p->plan_region + L.merge);
+  mp.n = n;
+  mp.Hq = p->cfg.num_q_heads;
+  mp.Hkv = H;
+  mp.G = p->G;
+  std::memcpy(mp.signs, p->signs, sizeof mp.signs);
+  if (!upload) return MKV_OK;
+  // stage and upload (one copy of the used span)
+  mkv_status st = staging_acquire(p->st_plan);
+  if (st != MKV_OK) return st;
+  uint8_t* h = static_cast<uint8_t*>(p->st_plan.host);
+  std::memcpy(h + L.entries, entries.data(), entries.size() * sizeof(PageEntry));
+  std::memcpy(h + L.chunks, chunks.data(), chunks.size() * sizeof(Chunk));
+  std::memcpy(h + L.cta_chunks, cta_chunks.data(), cta_chunks.size() * sizeof(int32_t));
+  std::memcpy(h + L.cta_start, cta_start.data(), cta_start.size() * sizeof(int32_t));
+  std::memcpy(h + L.merge, md.data(), md.size() * sizeof(MergeDesc));
+  return staging_upload(p->st_plan, p->plan_region, L.total, stream);
+}
+
+mkv_status check_batch(const mkv_pool* p, int32_t n, const int32_t* ids, bool need_nonempty) {
+  if (n < 0 || (n > 0 && !ids)) return fail(MKV_ERR_INVALID_ARGUMENT, "bad batch");
+  if (n > effective_batch(p->cfg)) return fail(MKV_ERR_INVALID_ARGUMENT, "batch %d > max_batch", n);
+  std::vector<int32_t> sorted(ids, ids + n);
+  std::sort(sorted.begin(), sorted.end());
+  for (int i = 0; i < n; ++i) {
+    if (!valid_seq(p, sorted[i])) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", sorted[i]);
+    if (i && sorted[i] == sorted[i - 1]) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d repeated", sorted[i]);
+    if (need_nonempty && p->seqs[sorted[i]].len == 0)
+      return fail(MKV_ERR_INVALID_ARGUMENT, "sequence %d is empty", sorted[i]);
+  }
+  return MKV_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+extern "C" {
+
+const char* mkv_last_error(void) { return g_last_error.c_str(); }
+
+const char* mkv_version(void) { return "mkv 0.1.0 (sm_103a)"; }
+
+mkv_status mkv_pool_required_bytes(const mkv_pool_config* cfg, size_t* device_bytes) {
+  mkv_status st = validate_config(cfg);
+  if (st != MKV_OK) return st;
+  if (!device_bytes) return fail(MKV_ERR_INVALID_ARGUMENT, "device_bytes is NULL");
+  *device_bytes = compute_sizes(*cfg).total;
+  return MKV_OK;
+}
+
+mkv_status mkv_pool_create(const mkv_pool_config* cfg, void* device_buf, size_t bytes, mkv_stream_t stream,
+                           mkv_pool** out) {
+  mkv_status st = validate_config(cfg);
+  if (st != MKV_OK) return st;
+  if (!out) return fail(MKV_ERR_INVALID_ARGUMENT, "out is NULL");
+  const bool host_only = (cfg->flags & MKV_POOL_HOST_ONLY) != 0;
+  const Sizes S = compute_sizes(*cfg);
+  if (!host_only) {
+    if (!device_buf) return fail(MKV_ERR_INVALID_ARGUMENT, "device_buf is NULL");
+    if (reinterpret_cast<uintptr_t>(device_buf) & 255) return fail(MKV_ERR_INVALID_ARGUMENT, "device_buf not 256-byte aligned");
+    if (bytes < S.total) return fail(MKV_ERR_INVALID_ARGUMENT, "device buffer %zu < required %zu", bytes, S.total);
+  }
+  mkv_pool* p = new (std::nothrow) mkv_pool();
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "out of host memory");
+  p->cfg = *cfg;
+  p->host_only = host_only;
+  p->G = cfg->num_q_heads / cfg->num_kv_heads;
+  p->fp8_page_bytes = S.fp8_page;
+  p->tq3_page_bytes = S.tq3_page;
+  p->entry_cap = S.entry_cap;
+  p->chunk_cap = S.chunk_cap;
+  p->append_cap = kAppendCap;
+  p->demote_cap = kDemoteCap;
+  p->workspace_bytes = S.workspace;
+  p->seqs.resize(cfg->max_seqs);
+  for (int s = cfg->fp8_slots - 1; s >= 0; --s) p->free_fp8.push_back(s);
+  for (int s = cfg->tq3_slots - 1; s >= 0; --s) p->free_tq3.push_back(s);
+  uint64_t state = cfg->rotation_seed;
+  for (int w = 0; w < 4; ++w) p->signs[w] = splitmix64_next(state);
+  p->lut = make_lut(codebook());
+  if (!host_only) {
+    uint8_t* b = static_cast<uint8_t*>(device_buf);
+    p->base = b;
+    p->bytes = bytes;
+    size_t off = 0;
+    p->fp8_arena = b + off;
+    off += S.fp8_arena;
+    p->tq3_arena = b + off;
+    off += S.tq3_arena;
+    p->plan_region = b + off;
+    p->plan_bytes = S.plan;
+    off += S.plan;
+    p->append_region = reinterpret_cast<uint32_t*>(b + off);
+    off += S.append;
+    p->demote_region = reinterpret_cast<int2*>(b + off);
+    off += S.demote;
+    p->workspace = reinterpret_cast<float*>(b + off);
+    off += S.workspace;
+    p->err = reinterpret_cast<int*>(b + off);
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->n_sm, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+      delete p;
+      return cuda_fail(e, "device query");
+    }
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(p->fp8_arena, 0, S.fp8_arena, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->err, 0, S.err, s);
+    if (e != cudaSuccess) {
+      delete p;
+      return cuda_fail(e, "cudaMemsetAsync");
+    }
+    if ((st = staging_alloc(p->st_plan, S.plan)) != MKV_OK || (st = staging_alloc(p->st_append, S.append)) != MKV_OK ||
+        (st = staging_alloc(p->st_demote, S.demote)) != MKV_OK) {
+      staging_free(p->st_plan);
+      staging_free(p->st_append);
+      staging_free(p->st_demote);
+      delete p;
+      return st;
+    }
+  }
+  *out = p;
+  return MKV_OK;
+}
+
+mkv_status mkv_pool_destroy(mkv_pool* p) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (!p->host_only) {
+    staging_free(p->st_plan);
+    staging_free(p->st_append);
+    staging_free(p->st_demote);
+  }
+  delete p;
+  return MKV_OK;
+}
+
+mkv_status mkv_seq_extend(mkv_pool* p, int32_t n, const int32_t* ids, const int32_t* n_new) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (n < 0 || (n > 0 && (!ids || !n_new))) return fail(MKV_ERR_INVALID_ARGUMENT, "bad arguments");
+  const int P = p->cfg.page_size;
+  std::vector<int32_t> seen(ids, ids + n);
+  std::sort(seen.begin(), seen.end());
+  int64_t need = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!valid_seq(p, ids[i])) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", ids[i]);
+    if (i && seen[i] == seen[i - 1]) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d repeated", seen[i]);
+    if (n_new[i] < 0) return fail(MKV_ERR_INVALID_ARGUMENT, "negative n_new");
+    const SeqRec& s = p->seqs[ids[i]];
+    const int64_t nl = int64_t(s.len) + n_new[i];
+    if (nl > int64_t(p->cfg.max_pages_per_seq) * P)
+      return fail(MKV_ERR_INVALID_ARGUMENT, "sequence %d would exceed max_pages_per_seq", ids[i]);
+    need += npages_for(int(nl), P) - int64_t(s.pages.size());
+  }
+  if (need > int64_t(p->free_fp8.size()))
+    return fail(MKV_ERR_OUT_OF_PAGES, "FP8 arena: need %lld free slots, have %zu", (long long)need, p->free_fp8.size());
+  for (int i = 0; i < n; ++i) {
+    SeqRec& s = p->seqs[ids[i]];
+    s.len += n_new[i];
+    const int np = npages_for(s.len, P);
+    while (int(s.pages.size()) < np) {
+      const int32_t slot = p->free_fp8.back();
+      p->free_fp8.pop_back();
+      s.pages.push_back({slot, int8_t(MKV_TIER_RECENT)});
+    }
+  }
+  if (n) ++p->generation;
+  return MKV_OK;
+}
+
+mkv_status mkv_seq_release(mkv_pool* p, int32_t seq) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (!valid_seq(p, seq)) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", seq);
+  SeqRec& s = p->seqs[seq];
+  for (const PageRec& r : s.pages) (r.tier == MKV_TIER_STALE ? p->free_tq3 : p->free_fp8).push_back(r.slot);
+  s.pages.clear();
+  s.len = 0;
+  ++p->generation;
+  return MKV_OK;
+}
+
+mkv_status mkv_seq_info(const mkv_pool* p, int32_t seq, int32_t* length, int32_t* num_pages) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (!valid_seq(p, seq)) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", seq);
+  if (length) *length = p->seqs[seq].len;
+  if (num_pages) *num_pages = int32_t(p->seqs[seq].pages.size());
+  return MKV_OK;
+}
+
+mkv_status mkv_page_info(const mkv_pool* p, int32_t seq, int32_t page, mkv_tier* tier, int32_t* slot) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (!valid_seq(p, seq)) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", seq);
+  const SeqRec& s = p->seqs[seq];
+  if (page < 0 || page >= int(s.pages.size())) return fail(MKV_ERR_INVALID_ARGUMENT, "page %d out of range", page);
+  if (tier) *tier = mkv_tier(s.pages[page].tier);
+  if (slot) *slot = s.pages[page].slot;
+  return MKV_OK;
+}
+
+mkv_status mkv_append_tokens(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const int32_t* n_new,
+                             const void* k, const void* v, mkv_dtype dtype, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (dtype != MKV_F32 && dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, false);
+  if (st != MKV_OK) return st;
+  if (n > 0 && !n_new) return fail(MKV_ERR_INVALID_ARGUMENT, "n_new is NULL");
+  const int P = p->cfg.page_size;
+  int64_t ntok = 0;
+  for (int i = 0; i < n; ++i) {
+    const SeqRec& s = p->seqs[ids[i]];
+    if (n_new[i] < 0 || n_new[i] > s.len)
+      return fail(MKV_ERR_INVALID_ARGUMENT, "n_new[%d] = %d outside [0, length %d]", i, n_new[i], s.len);
+    for (int pos = s.len - n_new[i]; pos < s.len; pos += P - (pos % P)) {
+      if (s.pages[pos / P].tier == MKV_TIER_STALE)
+        return fail(MKV_ERR_INVALID_STATE, "sequence %d page %d is TQ3; append writes FP8 pages", ids[i], pos / P);
+    }
+    ntok += n_new[i];
+  }
+  if (ntok > 0 && (!k || !v)) return fail(MKV_ERR_INVALID_ARGUMENT, "k or v is NULL");
+  if (ntok == 0 || p->host_only) return MKV_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // destinations (cached across layers for the same batch and pool state)
+  const bool cached = p->app_gen == p->generation && p->app_ntok == ntok && p->app_ids.size() == size_t(n) &&
+                      std::equal(ids, ids + n, p->app_ids.begin()) && std::equal(n_new, n_new + n, p->app_new.begin());
+  std::vector<uint32_t> dest;
+  if (!cached || ntok > p->append_cap) {
+    dest.reserve(size_t(ntok));
+    for (int i = 0; i < n; ++i) {
+      const SeqRec& sq = p->seqs[ids[i]];
+      for (int pos = sq.len - n_new[i]; pos < sq.len; ++pos)
+        dest.push_back((uint32_t(sq.pages[pos / P].slot) << 8) | uint32_t(pos % P));
+    }
+  }
+  AppendParams ap{};
+  ap.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  ap.fp8_page_bytes = p->fp8_page_bytes;
+  ap.kv_bf16 = dtype == MKV_BF16;
+  ap.Hkv = p->cfg.num_kv_heads;
+  ap.P = P;
+  const size_t elt = dtype == MKV_BF16 ? 2 : 4;
+  const size_t row = size_t(p->cfg.num_kv_heads) * kHeadDim * elt;
+  for (int64_t t0 = 0; t0 < ntok; t0 += p->append_cap) {
+    const int cnt = int(std::min<int64_t>(p->append_cap, ntok - t0));
+    if (!(cached && ntok <= p->append_cap)) {
+      if ((st = staging_acquire(p->st_append)) != MKV_OK) return st;
+      std::memcpy(p->st_append.host, dest.data() + t0, size_t(cnt) * 4);
+      if ((st = staging_upload(p->st_append, p->append_region, size_t(cnt) * 4, s)) != MKV_OK) return st;
+    }
+    ap.dest = p->append_region;
+    ap.k = static_cast<const uint8_t*>(k) + t0 * row;
+    ap.v = static_cast<const uint8_t*>(v) + t0 * row;
+    ap.ntok = cnt;
+    const cudaError_t e = launch_append(ap, s);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  }
+  if (ntok <= p->append_cap) {
+    p->app_gen = p->generation;
+    p->app_ntok = int(ntok);
+    p->app_ids.assign(ids, ids + n);
+    p->app_new.assign(n_new, n_new + n);
+  } else {
+    p->app_gen = 0;
+  }
+  return MKV_OK;
+}
+
+mkv_status mkv_set_tier(mkv_pool* p, int32_t seq, int32_t page, mkv_tier tier) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (!valid_seq(p, seq)) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", seq);
+  SeqRec& s = p->seqs[seq];
+  if (page < 0 || page >= int(s.pages.size())) return fail(MKV_ERR_INVALID_ARGUMENT, "page %d out of range", page);
+  if (tier != MKV_TIER_RECENT && tier != MKV_TIER_ANCHOR && tier != MKV_TIER_STALE)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "tier %d", int(tier));
+  if (tier == MKV_TIER_STALE) return fail(MKV_ERR_INVALID_STATE, "use mkv_demote_pages to make a page STALE");
+  if (s.pages[page].tier == MKV_TIER_STALE)
+    return fail(MKV_ERR_INVALID_STATE, "page %d of sequence %d is TQ3; only FP8 pages change tier", page, seq);
+  s.pages[page].tier = int8_t(tier);
+  return MKV_OK;
+}
+
+mkv_status mkv_demote_pages(mkv_pool* p, int32_t n, const int32_t* ids, const int32_t* pages, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (n < 0 || (n > 0 && (!ids || !pages))) return fail(MKV_ERR_INVALID_ARGUMENT, "bad arguments");
+  const int P = p->cfg.page_size;
+  std::vector<std::pair<int32_t, int32_t>> seen;
+  for (int i = 0; i < n; ++i) {
+    if (!valid_seq(p, ids[i])) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", ids[i]);
+    const SeqRec& s = p->seqs[ids[i]];
+    if (pages[i] < 0 || pages[i] >= int(s.pages.size()))
+      return fail(MKV_ERR_INVALID_ARGUMENT, "page %d of sequence %d out of range", pages[i], ids[i]);
+    const PageRec& r = s.pages[pages[i]];
+    if (r.tier == MKV_TIER_ANCHOR)
+      return fail(MKV_ERR_INVALID_STATE, "page %d of sequence %d is an Anchor", pages[i], ids[i]);
+    if (r.tier == MKV_TIER_STALE)
+      return fail(MKV_ERR_INVALID_STATE, "page %d of sequence %d is already TQ3", pages[i], ids[i]);
+    if (int64_t(pages[i] + 1) * P > s.len)
+      return fail(MKV_ERR_INVALID_STATE, "page %d of sequence %d is not full", pages[i], ids[i]);
+    seen.push_back({ids[i], pages[i]});
+  }
+  std::sort(seen.begin(), seen.end());
+  for (size_t i = 1; i < seen.size(); ++i)
+    if (seen[i] == seen[i - 1]) return fail(MKV_ERR_INVALID_STATE, "page listed twice");
+  if (int64_t(n) > int64_t(p->free_tq3.size()))
+    return fail(MKV_ERR_OUT_OF_PAGES, "TQ3 arena: need %d free slots, have %zu", n, p->free_tq3.size());
+  if (n == 0) return MKV_OK;
+  std::vector<int2> pairs(n);
+  for (int i = 0; i < n; ++i) {
+    pairs[i].x = p->seqs[ids[i]].pages[pages[i]].slot;
+    pairs[i].y = p->free_tq3[p->free_tq3.size() - 1 - i];
+  }
+  if (!p->host_only) {
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DemoteParams dp{};
+    dp.fp8_arena = p->fp8_arena;
+    dp.tq3_arena = p->tq3_arena;
+    dp.fp8_page_bytes = p->fp8_page_bytes;
+    dp.tq3_page_bytes = p->tq3_page_bytes;
+    dp.fp8_layer_stride = int64_t(p->cfg.fp8_slots) * p->fp8_page_bytes;
+    dp.tq3_layer_stride = int64_t(p->cfg.tq3_slots) * p->tq3_page_bytes;
+    dp.L = p->cfg.num_layers;
+    dp.Hkv = p->cfg.num_kv_heads;
+    dp.P = P;
+    std::memcpy(dp.signs, p->signs, sizeof dp.signs);
+    std::memcpy(dp.thr, codebook().thr, sizeof dp.thr);
+    for (int i0 = 0; i0 < n; i0 += p->demote_cap) {
+      const int cnt = std::min(p->demote_cap, n - i0);
+      mkv_status st = staging_acquire(p->st_demote);
+      if (st != MKV_OK) return st;
+      std::memcpy(p->st_demote.host, pairs.data() + i0, size_t(cnt) * sizeof(int2));
+      if ((st = staging_upload(p->st_demote, p->demote_region, size_t(cnt) * sizeof(int2), s)) != MKV_OK) return st;
+      dp.pairs = p->demote_region;
+      dp.npairs = cnt;
+      const cudaError_t e = launch_demote(dp, s);
+      if (e != cudaSuccess) return cuda_fail(e, "demote launch");
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    PageRec& r = p->seqs[ids[i]].pages[pages[i]];
+    p->free_fp8.push_back(r.slot);
+    r.slot = pairs[i].y;
+    r.tier = int8_t(MKV_TIER_STALE);
+  }
+  p->free_tq3.resize(p->free_tq3.size() - n);
+  ++p->generation;
+  return MKV_OK;
+}
+
+mkv_status mkv_decode_attention(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const void* q,
+                                mkv_dtype dtype, float* out, float* lse, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (dtype != MKV_F32 && dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if (n == 0) return MKV_OK;
+  if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool cached = p->plan_gen == p->generation && p->plan_ids.size() == size_t(n) &&
+                      std::equal(ids, ids + n, p->plan_ids.begin());
+  if (!cached) {
+    if ((st = build_plan(p, n, ids, !p->host_only, s)) != MKV_OK) {
+      p->plan_gen = 0;
+      return st;
+    }
+    p->plan_gen = p->generation;
+    p->plan_ids.assign(ids, ids + n);
+  }
+  if (p->host_only) return MKV_OK;
+  DecodeParams dp = p->plan_params;
+  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
+  dp.q = q;
+  dp.q_bf16 = dtype == MKV_BF16;
+  cudaError_t e = cudaSuccess;
+  if (p->t_start) e = cudaEventRecord(p->t_start, s);
+  if (e == cudaSuccess) e = launch_decode(dp, s);
+  if (e == cudaSuccess && p->t_stop) e = cudaEventRecord(p->t_stop, s);
+  p->t_start = p->t_stop = nullptr;
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  MergeParams mp = p->merge_params;
+  mp.out = out;
+  mp.lse = lse;
+  e = launch_merge(mp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return MKV_OK;
+}
+
+mkv_status mkv_pool_stats(const mkv_pool* p, mkv_stats* out) {
+  if (!p || !out) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
+  mkv_stats st{};
+  for (const SeqRec& s : p->seqs) {
+    st.live_tokens += s.len;
+    for (const PageRec& r : s.pages) {
+      if (r.tier == MKV_TIER_RECENT) ++st.recent_pages;
+      if (r.tier == MKV_TIER_ANCHOR) ++st.anchor_pages;
+      if (r.tier == MKV_TIER_STALE) ++st.stale_pages;
+    }
+  }
+  const int64_t L = p->cfg.num_layers;
+  st.fp8_bytes = (st.recent_pages + st.anchor_pages) * p->fp8_page_bytes * L;
+  st.tq3_bytes = st.stale_pages * p->tq3_page_bytes * L;
+  st.kv_bytes_per_live_token = st.live_tokens ? double(st.fp8_bytes + st.tq3_bytes) / double(st.live_tokens) : 0.0;
+  st.fp8_slots_free = int32_t(p->free_fp8.size());
+  st.tq3_slots_free = int32_t(p->free_tq3.size());
+  st.device_bytes = int64_t(compute_sizes(p->cfg).total);
+  st.workspace_bytes = int64_t(p->workspace_bytes);
+  *out = st;
+  return MKV_OK;
+}
+
+mkv_status mkv_export_page(mkv_pool* p, int32_t layer, int32_t seq, int32_t page, void* host_dst, size_t cap,
+                           mkv_tier* tier, int32_t* n_valid, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (!valid_seq(p, seq)) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", seq);
+  const SeqRec& s = p->seqs[seq];
+  if (page < 0 || page >= int(s.pages.size())) return fail(MKV_ERR_INVALID_ARGUMENT, "page %d out of range", page);
+  const PageRec r = s.pages[page];
+  const bool tq3 = r.tier == MKV_TIER_STALE;
+  const int64_t pb = tq3 ? p->tq3_page_bytes : p->fp8_page_bytes;
+  if (tier) *tier = mkv_tier(r.tier);
+  if (n_valid) *n_valid = std::min(p->cfg.page_size, s.len - page * p->cfg.page_size);
+  if (!host_dst || cap < size_t(pb)) return fail(MKV_ERR_INVALID_ARGUMENT, "host_dst too small (%lld bytes needed)", (long long)pb);
+  if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool has no page bytes");
+  const uint8_t* src = (tq3 ? p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * pb
+                            : p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * pb) +
+                       int64_t(r.slot) * pb;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host_dst, src, size_t(pb), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "export copy");
+  return MKV_OK;
+}
+
+mkv_status mkv_rotation_signs(const mkv_pool* p, int8_t* dst, int32_t cap) {
+  if (!p || !dst) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
+  if (cap < p->cfg.head_dim) return fail(MKV_ERR_INVALID_ARGUMENT, "cap < head_dim");
+  for (int i = 0; i < p->cfg.head_dim; ++i) dst[i] = ((p->signs[i >> 6] >> (i & 63)) & 1) ? -1 : 1;
+  return MKV_OK;
+}
+
+mkv_status mkv_tq3_codebook(float* levels8, float* thresholds7) {
+  if (!levels8 || !thresholds7) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
+  const Codebook& cb = codebook();
+  std::memcpy(levels8, cb.level, sizeof cb.level);
+  std::memcpy(thresholds7, cb.thr, sizeof cb.thr);
+  return MKV_OK;
+}
+
+mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* chunks, int32_t cap, int32_t* n_chunks) {
+  if (!p || !n_chunks) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if ((st = build_plan(p, n, ids, false, nullptr)) != MKV_OK) return st;
+  p->plan_gen = 0;   // the device copy (if any) no longer matches
+  const int nc = int(p->plan_debug.size() / 6);
+  *n_chunks = nc;
+  if (chunks) {
+    if (cap < nc) return fail(MKV_ERR_INVALID_ARGUMENT, "cap %d < %d chunks", cap, nc);
+    std::memcpy(chunks, p->plan_debug.data(), p->plan_debug.size() * sizeof(int32_t));
+  }
+  return MKV_OK;
+}
+
+mkv_status mkv_set_timing_events(mkv_pool* p, void* start, void* stop) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  p->t_start = static_cast<cudaEvent_t>(start);
+  p->t_stop = static_cast<cudaEvent_t>(stop);
+  return MKV_OK;
+}
+
+mkv_status mkv_check_device_errors(mkv_pool* p, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (p->host_only) return MKV_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, p->err, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "error word read");
+  if (h) {
+    e = cudaMemsetAsync(p->err, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return fail(MKV_ERR_DEVICE_CHECK, "device error word 0x%x (%s%s)", h, (h & kErrWaitTimeout) ? "wait timeout " : "",
+                (h & kErrBadPlan) ? "bad plan entry" : "");
+  }
+  return MKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Internal structures shared by the host pool (mkv_host.cpp) and the CUDA
+// kernels (mkv_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mkv {
+
+constexpr int kHeadDim = 256;      // head_dim the kernels are written for
+constexpr int kMaxGroup = 8;       // q heads per kv head held in one MMA tile
+constexpr int kStageTokens = 64;   // tokens per staged page block
+constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
+constexpr int kMaxCtas = 1024;     // upper bound on decode CTAs
+
+// Error bits written by kernels into the pool's device error word.
+enum : int {
+  kErrWaitTimeout = 1,     // a bounded mbarrier wait ran out
+  kErrBadPlan = 2,         // a plan entry pointed outside the arena
+};
+
+struct PageEntry {         // one page of one batch entry in a decode plan
+  int32_t slot;            // physical slot in the tier's arena
+  int32_t nvalid;          // tokens written in the page (1..P)
+};
+
+struct Chunk {             // one partial-state split (one CTA work item)
+  int32_t b;               // batch index
+  int32_t kvh;             // kv head
+  int32_t fmt;             // 0 = FP8 (Recent/Anchor), 1 = TQ3 (Stale)
+  int32_t entry0;          // first PageEntry
+  int32_t nentry;          // number of PageEntry
+  int32_t tokens;          // valid tokens covered (host bookkeeping)
+  int32_t pad0, pad1;
+};
+
+struct MergeDesc {         // partial-state index ranges of one (b, kvh)
+  int32_t tq3_first, tq3_count, fp8_first, fp8_count;
+};
+
+struct Codebook {          // stored TQ3 codebook (library constant)
+  float level[8];          // fp16-valued levels, ascending
+  float thr[7];            // thresholds (exact midpoints)
+  uint16_t level_bits[8];  // fp16 bit patterns of the levels
+};
+
+struct Lut {               // byte tables for the PRMT level lookup
+  uint32_t lo_a, lo_b, hi_a, hi_b;
+};
+
+struct DecodeParams {
+  const uint8_t* fp8_layer;        // FP8 arena base of this layer
+  const uint8_t* tq3_layer;        // TQ3 arena base of this layer
+  int64_t fp8_page_bytes, tq3_page_bytes;
+  int32_t fp8_slots, tq3_slots;
+  const PageEntry* entries;
+  const Chunk* chunks;             // indexed by chunk id (= partial index)
+  const int32_t* cta_chunks;       // chunk ids in per-CTA order
+  const int32_t* cta_start;        // [n_ctas + 1] into cta_chunks
+  int32_t n_ctas_fp8;              // CTAs [0, n_ctas_fp8) run the FP8 body
+  int32_t n_ctas;
+  const void* q;                   // [n, Hq, D]
+  int32_t q_bf16;
+  int32_t Hq, Hkv, G, P;
+  float* part;                     // [chunks][G][2 + D] (m in log2 units, l, o)
+  uint64_t signs[4];               // bit i set -> sign_i = -1
+  float score_scale;               // log2(e) / sqrt(d)
+  Lut lut;
+  int* err;
+};
+
+struct MergeParams {
+  const float* part;
+  const MergeDesc* desc;           // [n * Hkv]
+  float* out;                      // [n, Hq, D]
+  float* lse;                      // [n, Hq]
+  int32_t n, Hq, Hkv, G;
+  uint64_t signs[4];
+};
+
+struct AppendParams {
+  uint8_t* fp8_layer;              // FP8 arena base of this layer
+  int64_t fp8_page_bytes;
+  const uint32_t* dest;            // per token: (slot << 8) | position in page
+  const void* k;                   // [ntok, Hkv, D]
+  const void* v;
+  int32_t kv_bf16;
+  int32_t ntok, Hkv, P;
+};
+
+struct DemoteParams {
+  const uint8_t* fp8_arena;
+  uint8_t* tq3_arena;
+  int64_t fp8_page_bytes, tq3_page_bytes;
+  int64_t fp8_layer_stride, tq3_layer_stride;   // bytes between layers
+  const int2* pairs;               // (fp8 slot, tq3 slot)
+  int32_t npairs, L, Hkv, P;
+  uint64_t signs[4];
+  float thr[7];
+};
+
+// Kernel launchers (mkv_kernels.cu).  Return cudaGetLastError() of the launch.
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+size_t decode_smem_bytes();
+int decode_threads();
+
+}  // namespace mkv

@@ -127,3 +127,31 @@ def decode_attention_partials(q: np.ndarray, pages, P: int, Hkv: int, D: int, se
         out[kv * G:(kv + 1) * G] = o
         lse[kv * G:(kv + 1) * G] = l
     return out, lse
+
+
+def decode_attention_streaming(q: np.ndarray, pages, P: int, Hkv: int, D: int, seed: int,
+                               kv_heads=None):
+    """Same result as ``decode_attention`` computed page by page: one partial
+    state per page (FP8 pages scored as stored, TQ3 pages dequantised to the
+    original domain), merged at the end.  Memory stays O(page) so large
+    contexts can be checked.  ``kv_heads`` restricts the work to some kv
+    heads (other outputs are NaN)."""
+    q = np.asarray(q, dtype=np.float64)
+    Hq = q.shape[0]
+    G = Hq // Hkv
+    heads = range(Hkv) if kv_heads is None else kv_heads
+    out = np.full((Hq, D), np.nan)
+    lse = np.full(Hq, np.nan)
+    states = {kv: [] for kv in heads}
+    for tier, page, n in pages:
+        if tier == TIER_STALE:
+            K, V = tq3_page_dequant(page, P, Hkv, D, seed)
+        else:
+            K, V = fp8_page_dequant(page, P, Hkv, D)
+        for kv in heads:
+            states[kv].append(partial_state(q[kv * G:(kv + 1) * G], K[:n, kv], V[:n, kv]))
+    for kv in heads:
+        o, l = merge_states(states[kv])
+        out[kv * G:(kv + 1) * G] = o
+        lse[kv * G:(kv + 1) * G] = l
+    return out, lse

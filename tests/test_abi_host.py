@@ -1,0 +1,237 @@
+"""CPU tests of the C-ABI library: it loads, exports every symbol the header
+declares, and its host logic (pool bookkeeping, tier transitions, errors,
+decode planning, accounting) behaves as specified.  No GPU work: pools are
+created with MKV_POOL_HOST_ONLY."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def mkv():
+    lib_path = os.path.join(ROOT, "mixed_format_paged_gb300", "libmkv.so")
+    if not os.path.exists(lib_path):
+        from mixed_format_paged_gb300 import build as b
+        b.build()
+    import mixed_format_paged_gb300 as m
+    return m
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "mkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(mkv):
+    declared = _declared_symbols()
+    assert len(declared) >= 19
+    lib = mkv.binding.lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", mkv.binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (mkv_[a-z0-9_]+)", out))
+    assert set(declared) <= exported
+    assert set(mkv.binding.EXPORTED) == set(declared)
+
+
+def test_codebook_matches_oracle(mkv):
+    from oracle.codebook import tq3_codebook
+    lv, th = mkv.mkv_tq3_codebook()
+    L, T = tq3_codebook()
+    assert np.array_equal(np.array(lv, dtype=np.float64), L)
+    assert np.array_equal(np.array(th, dtype=np.float64), T)
+
+
+def _host_pool(mkv, **kw):
+    args = dict(num_layers=2, num_q_heads=24, num_kv_heads=4, head_dim=256, page_size=64, fp8_slots=12,
+                tq3_slots=6, max_seqs=4, max_pages_per_seq=16, max_batch=4, rotation_seed=99)
+    args.update(kw)
+    return mkv.MkvPool(host_only=True, **args)
+
+
+def test_rotation_signs_match_oracle(mkv):
+    from oracle.rotation import rotation_signs
+    for seed in (0, 99, 2 ** 63 + 5):
+        p = _host_pool(mkv, rotation_seed=seed)
+        assert np.array_equal(np.array(p.rotation_signs(), dtype=np.float64), rotation_signs(seed, 256))
+
+
+def test_required_bytes_closed_form(mkv):
+    cfg = mkv.PoolConfig(16, 24, 4, 256, 64, 100, 300, 8, 600, 8, 0, 0, 1)
+    nbytes = mkv.mkv_pool_required_bytes(cfg)
+    arenas = 16 * 100 * 132096 + 16 * 300 * 50176
+    assert arenas <= nbytes <= arenas + 64 * 2 ** 20
+    # no dense shadow: the non-arena part does not grow with context length
+    cfg2 = mkv.PoolConfig(16, 24, 4, 256, 64, 100, 300, 8, 600, 8, 0, 0, 1)
+    cfg2.fp8_slots, cfg2.tq3_slots = 1000, 3000
+    extra1 = nbytes - arenas
+    extra2 = mkv.mkv_pool_required_bytes(cfg2) - (16 * 1000 * 132096 + 16 * 3000 * 50176)
+    assert abs(extra1 - extra2) < 512
+
+
+def test_config_validation(mkv):
+    bad = [dict(head_dim=128), dict(page_size=32), dict(num_q_heads=25), dict(num_q_heads=72)]
+    for b in bad:
+        with pytest.raises(mkv.MkvError) as e:
+            _host_pool(mkv, **b)
+        assert e.value.status in (1, 2)
+
+
+def test_extend_all_or_nothing_and_release(mkv):
+    p = _host_pool(mkv)
+    p.extend([0, 1], [64 * 5, 64 * 4 + 1])           # 5 + 5 pages = 10 of 12 FP8 slots
+    assert p.seq_info(0) == (320, 5) and p.seq_info(1) == (257, 5)
+    with pytest.raises(mkv.MkvError) as e:
+        p.extend([2, 3], [64, 64 * 2])               # needs 3 slots, 2 free
+    assert e.value.status == 3
+    assert p.seq_info(2) == (0, 0) and p.seq_info(3) == (0, 0)
+    with pytest.raises(mkv.MkvError):
+        p.extend([0, 0], [1, 1])                     # repeated id
+    with pytest.raises(mkv.MkvError):
+        p.extend([7], [1])                           # bad id
+    with pytest.raises(mkv.MkvError):
+        p.extend([2], [64 * 17])                     # beyond max_pages_per_seq
+    st = p.stats()
+    assert st.fp8_slots_free == 2 and st.recent_pages == 10
+    p.release(0)
+    assert p.seq_info(0) == (0, 0) and p.stats().fp8_slots_free == 7
+
+
+def test_tier_transitions(mkv):
+    p = _host_pool(mkv)
+    p.extend([0], [64 * 6 + 10])                     # 7 pages, tail partial
+    p.set_tier(0, 0, 2)
+    assert p.page_info(0, 0)[0] == 2
+    with pytest.raises(mkv.MkvError) as e:
+        p.demote([0], [0])                           # Anchor
+    assert e.value.status == 4
+    with pytest.raises(mkv.MkvError) as e:
+        p.demote([0], [6])                           # partial tail page
+    assert e.value.status == 4
+    with pytest.raises(mkv.MkvError) as e:
+        p.demote([0, 0], [2, 2])                     # listed twice
+    assert e.value.status == 4
+    with pytest.raises(mkv.MkvError) as e:
+        p.set_tier(0, 1, 3)                          # STALE only through demotion
+    assert e.value.status == 4
+    free_fp8 = p.stats().fp8_slots_free
+    p.demote([0, 0, 0], [1, 2, 3])
+    st = p.stats()
+    assert st.stale_pages == 3 and st.fp8_slots_free == free_fp8 + 3 and st.tq3_slots_free == 3
+    with pytest.raises(mkv.MkvError) as e:
+        p.demote([0], [2])                           # already TQ3
+    assert e.value.status == 4
+    with pytest.raises(mkv.MkvError) as e:
+        p.set_tier(0, 2, 2)                          # TQ3 page cannot become Anchor
+    assert e.value.status == 4
+    # OUT_OF_PAGES is all-or-nothing: 3 TQ3 slots left, ask for 4
+    p.set_tier(0, 0, 1)
+    with pytest.raises(mkv.MkvError) as e:
+        p.demote([0, 0, 0, 0], [0, 4, 5, 6 - 1])
+    assert e.value.status in (3, 4)
+    assert p.stats().stale_pages == 3
+    # appending into a TQ3 page is refused
+    with pytest.raises(mkv.MkvError) as e:
+        p.append(0, [0], [64 * 6 + 10], _FakeTensor(), _FakeTensor())
+    assert e.value.status in (1, 4)
+    p.release(0)
+    st = p.stats()
+    assert st.tq3_slots_free == 6 and st.fp8_slots_free == 12
+
+
+class _FakeTensor:
+    """Stands in for a device tensor in host-only calls (never dereferenced)."""
+    dtype = None
+
+    def __init__(self):
+        import torch
+        self.dtype = torch.float32
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return 0x1000
+
+
+def test_stats_accounting(mkv):
+    from oracle.accounting import bytes_per_token_layer
+    p = _host_pool(mkv, num_layers=16, fp8_slots=20, tq3_slots=20)
+    p.extend([0], [64 * 10])
+    p.demote([0] * 6, list(range(6)))
+    st = p.stats()
+    fp8_tok, tq3_tok = 4 * 64, 6 * 64
+    exp = 16 * (fp8_tok * bytes_per_token_layer("fp8") + tq3_tok * bytes_per_token_layer("tq3"))
+    assert st.fp8_bytes + st.tq3_bytes == exp
+    assert abs(st.kv_bytes_per_live_token - exp / 640) < 1e-9
+
+
+def _check_plan_covers(mkv, pool, ids, lengths, tiers_of):
+    plan = pool.plan(ids)
+    H = 4
+    for b, r in enumerate(ids):
+        tiers = tiers_of(r)
+        fp8_pages = [i for i, t in enumerate(tiers) if t != 3]
+        tq3_pages = [i for i, t in enumerate(tiers) if t == 3]
+        for kvh in range(H):
+            mine = [c for c in plan if c[0] == b and c[1] == kvh]
+            f = sorted((c[3], c[4]) for c in mine if c[2] == 1)
+            t = sorted((c[3], c[4]) for c in mine if c[2] == 3)
+            # chunk entry ranges tile each tier's page list exactly once
+            for ranges, pages in ((f, fp8_pages), (t, tq3_pages)):
+                covered = sum(n for _, n in ranges)
+                assert covered == len(pages)
+                pos = [a for a, _ in ranges]
+                assert pos == sorted(pos)
+                for (a, n), (a2, _) in zip(ranges, ranges[1:]):
+                    assert a + n == a2
+            assert sum(c[5] for c in mine) == lengths[b]
+    return plan
+
+
+def test_plan_covers_every_page_once(mkv):
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import make_pool
+    for name in ("cfg1", "cfg2", "cfg4"):
+        w = workloads.make(name)
+        w.num_layers = 1
+        pool = make_pool(w, host_only=True, extra_steps=0)
+        for r in range(w.n):
+            pool.extend([r], [w.lengths[r]])
+            tiers = w.tiers(r)
+            for pg, t in enumerate(tiers):
+                if t == 2:
+                    pool.set_tier(r, pg, 2)
+            stale = [pg for pg, t in enumerate(tiers) if t == 3]
+            if stale:
+                pool.demote([r] * len(stale), stale)
+        ids = list(range(w.n))
+        plan = _check_plan_covers(mkv, pool, ids, w.lengths, w.tiers)
+        # byte balance: no TQ3 chunk is more than ~3x the mean (LPT assignment
+        # handles the rest); there are at most a few chunks per CTA
+        tq = [c[5] for c in plan if c[2] == 3]
+        if tq:
+            assert max(tq) <= 3 * np.mean(tq) + 64
+        assert len(plan) <= w.n * 4 * 2 + 4 * 1024
+
+
+def test_decode_argument_errors(mkv):
+    p = _host_pool(mkv)
+    p.extend([0], [100])
+    q = _FakeTensor()
+    with pytest.raises(mkv.MkvError):
+        mkv.mkv_decode_attention(p.handle, 0, [1], q, 0, q, q)        # empty sequence
+    with pytest.raises(mkv.MkvError):
+        mkv.mkv_decode_attention(p.handle, 5, [0], q, 0, q, q)        # bad layer
+    with pytest.raises(mkv.MkvError):
+        mkv.mkv_decode_attention(p.handle, 0, [0, 0], q, 0, q, q)     # repeated id
+    with pytest.raises(mkv.MkvError):
+        mkv.mkv_decode_attention(p.handle, 0, [0], None, 0, q, q)     # NULL q
+    mkv.mkv_decode_attention(p.handle, 0, [0], q, 0, q, q)            # host-only: validates, no launch

@@ -1,0 +1,311 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Criteria (the library's spec, include/mkv.h):
+* FP8 codes and scales: bit-exact (the quantiser decides in IEEE fp32 on both
+  sides).
+* TQ3 codes: bit-exact except where the oracle's fp64 pre-decision value lies
+  within 1e-6 (relative) of a threshold; such codes must be <= 0.01 %.  TQ3
+  scales: exact except at fp16 rounding ties (same 1e-6 rule).  Codes are
+  compared by re-encoding with the oracle given the GPU's FP8 bytes and fp16
+  scale, so a scale tie cannot cascade.
+* decode: max|out - out_oracle| <= 2e-3 * max|out_oracle| per request and
+  |lse - lse_oracle| <= 1e-4, with the oracle reading the GPU's stored pages;
+  an end-to-end check from raw inputs runs on the small workload.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-3
+LSE_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def mkv():
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if not os.path.exists(os.path.join(root, "mixed_format_paged_gb300", "libmkv.so")):
+        from mixed_format_paged_gb300 import build as b
+        b.build()
+    import mixed_format_paged_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+DEV = "cuda:0"
+
+
+def _export(pool, layer, r):
+    pages = []
+    for p in range(pool.seq_info(r)[1]):
+        b, tier, nv = pool.export_page(layer, r, p)
+        pages.append((tier, np.frombuffer(b, dtype=np.uint8).copy(), nv))
+    return pages
+
+
+def _check_decode(pool, layer, ids, q, out, lse, seed, D=256):
+    from oracle.paged import decode_attention_streaming
+    H, P = pool.num_kv_heads, pool.page_size
+    worst = (0.0, 0.0)
+    for b, r in enumerate(ids):
+        pages = _export(pool, layer, r)
+        ro, rl = decode_attention_streaming(q[b].double().cpu().numpy(), pages, P, H, D, seed)
+        o = out[b].double().cpu().numpy()
+        l_ = lse[b].double().cpu().numpy()
+        eo = np.abs(o - ro).max() / np.abs(ro).max()
+        el = np.abs(l_ - rl).max()
+        assert eo <= OUT_TOL, f"request {r}: relative out error {eo:.3e}"
+        assert el <= LSE_TOL, f"request {r}: lse error {el:.3e}"
+        worst = (max(worst[0], eo), max(worst[1], el))
+    return worst
+
+
+def _tq3_check(fp8_page, tq3_page, P, H, D, seed):
+    """Return (#code mismatches, #codes) after the boundary exemption; raise on
+    a non-exempt mismatch."""
+    from oracle import layout
+    from oracle.paged import fp8_page_dequant
+    from oracle.tq3 import boundary_distance, fp16_tie_distance, tq3_encode_rows, tq3_sigma_raw
+    Kh, Vh = fp8_page_dequant(fp8_page, P, H, D)
+    kc, ks, vc, vs = layout.unpack_tq3_page(tq3_page, P, H, D)
+    mism = 0
+    for X, codes, sig in ((Kh, kc, ks), (Vh, vc, vs)):
+        raw = tq3_sigma_raw(X)
+        _, s_or, _ = tq3_encode_rows(X, seed)
+        bad_s = sig != s_or
+        assert np.all(fp16_tie_distance(raw[bad_s]) <= 1e-6), "TQ3 scale mismatch away from an fp16 tie"
+        ref, _, u = tq3_encode_rows(X, seed, sigma=sig)
+        diff = codes != ref
+        if diff.any():
+            assert np.all(boundary_distance(u[diff]) <= 1e-6), "TQ3 code mismatch away from a threshold"
+        mism += int(diff.sum())
+    return mism, 2 * Kh.size
+
+
+def _small_pool(mkv, P=64, layers=1, fp8=64, tq3=64, nseq=8, maxp=32, seed=4321):
+    return mkv.MkvPool(layers, 24, 4, 256, P, fp8, tq3, max_seqs=nseq, max_pages_per_seq=maxp, max_batch=nseq,
+                       rotation_seed=seed, device=DEV)
+
+
+def _kv(n, dtype, g, outlier=True):
+    K = torch.randn(n, 4, 256, generator=g)
+    V = torch.randn(n, 4, 256, generator=g)
+    if outlier:
+        K[..., 5] += 8.0
+        K[..., 200] -= 8.0
+    return K.to(dtype), V.to(dtype)
+
+
+# ------------------------------------------------------------------ append
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_append_fp8_bit_exact(mkv, P, dtype):
+    from oracle.paged import encode_fp8_page
+    g = torch.Generator().manual_seed(1)
+    pool = _small_pool(mkv, P=P)
+    n0 = 2 * P + 37
+    K, V = _kv(n0 + 2, dtype, g)
+    K[3] = 0.0                                   # an all-zero row (scale 0)
+    V[4, 1] = torch.tensor(1e-30).to(dtype)      # tiny values
+    pool.extend([0], [n0])
+    pool.append(0, [0], [n0], K[:n0].to(DEV), V[:n0].to(DEV))
+    for t in (n0, n0 + 1):                       # two single-token appends
+        pool.extend([0], [1])
+        pool.append(0, [0], [1], K[t:t + 1].to(DEV).contiguous(), V[t:t + 1].to(DEV).contiguous())
+    torch.cuda.synchronize()
+    pages = _export(pool, 0, 0)
+    Kf, Vf = K.float().numpy(), V.float().numpy()
+    for p, (tier, b, nv) in enumerate(pages):
+        exp = encode_fp8_page(Kf[p * P: p * P + nv], Vf[p * P: p * P + nv], P)
+        assert np.array_equal(b, exp), f"page {p}: {int((b != exp).sum())} bytes differ"
+    pool.check_device_errors()
+
+
+# ------------------------------------------------------------------ demote
+@pytest.mark.parametrize("P", [64, 128])
+def test_demote_tq3_codes(mkv, P):
+    g = torch.Generator().manual_seed(2)
+    pool = _small_pool(mkv, P=P, layers=2)
+    n = 6 * P
+    pool.extend([0], [n])
+    for layer in range(2):
+        K, V = _kv(n, torch.bfloat16, g)
+        if layer == 1:
+            V = (V.float() * torch.linspace(0.01, 30, n)[:, None, None]).to(torch.bfloat16)
+        pool.append(layer, [0], [n], K.to(DEV), V.to(DEV))
+    torch.cuda.synchronize()
+    before = {(l_, p): _export(pool, l_, 0)[p][1] for l_ in range(2) for p in range(6)}
+    pool.demote([0] * 4, [0, 2, 3, 4])
+    torch.cuda.synchronize()
+    total_m, total = 0, 0
+    for l_ in range(2):
+        after = _export(pool, l_, 0)
+        for p in (0, 2, 3, 4):
+            assert after[p][0] == 3
+            m, t = _tq3_check(before[(l_, p)], after[p][1], P, 4, 256, 4321)
+            total_m += m
+            total += t
+        for p in (1, 5):
+            assert np.array_equal(after[p][1], before[(l_, p)])      # untouched FP8 pages
+    assert total_m <= 1e-4 * total
+    pool.check_device_errors()
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("qdtype", [torch.float32, torch.bfloat16])
+def test_decode_mixed_layouts(mkv, P, qdtype):
+    g = torch.Generator().manual_seed(3)
+    pool = _small_pool(mkv, P=P, fp8=96, tq3=96, maxp=24)
+    # request layouts: (tokens, anchors, stale pages)
+    specs = [
+        (1, [], []),                                   # a single token
+        (P, [], []),                                   # one full FP8 page
+        (5 * P + 1, [0], [1, 2, 3]),                   # tail of 1 token
+        (9 * P + 33, [], list(range(8))),              # mostly TQ3
+        (3 * P + 5, [0, 1, 2], []),                    # all FP8 with Anchors
+        (12 * P, [4], [0, 1, 2, 3, 5, 6, 7, 8, 9, 10]),  # full tail page, TQ3 around an Anchor
+    ]
+    for r, (n, anc, st) in enumerate(specs):
+        K, V = _kv(n, torch.bfloat16, g)
+        pool.extend([r], [n])
+        pool.append(0, [r], [n], K.to(DEV), V.to(DEV))
+        for a in anc:
+            pool.set_tier(r, a, 2)
+        if st:
+            pool.demote([r] * len(st), st)
+    ids = list(range(len(specs)))
+    q = torch.randn(len(ids), 24, 256, generator=g).to(qdtype)
+    out, lse = pool.decode(0, ids, q.to(DEV))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    _check_decode(pool, 0, ids, q.float(), out, lse, 4321)
+    # a sub-batch in another order gives the same rows
+    out2, lse2 = pool.decode(0, [5, 2], q[[5, 2]].to(DEV).contiguous())
+    torch.cuda.synchronize()
+    assert torch.allclose(out2, out[[5, 2]], atol=1e-5, rtol=0)
+    assert torch.allclose(lse2, lse[[5, 2]], atol=1e-5, rtol=0)
+
+
+def test_decode_repeatable(mkv):
+    g = torch.Generator().manual_seed(4)
+    pool = _small_pool(mkv)
+    K, V = _kv(700, torch.bfloat16, g)
+    pool.extend([0], [700])
+    pool.append(0, [0], [700], K.to(DEV), V.to(DEV))
+    pool.demote([0] * 5, [0, 1, 2, 3, 4])
+    q = torch.randn(1, 24, 256, generator=g).to(torch.bfloat16).to(DEV)
+    a = pool.decode(0, [0], q)
+    b = pool.decode(0, [0], q)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------ workload cfg1 end to end
+def test_cfg1_end_to_end(mkv):
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import make_pool, prefill
+    from oracle.paged import TIER_STALE, decode_attention, demote_page, encode_fp8_page
+    w = workloads.make("cfg1")
+    pool = make_pool(w, device=DEV, extra_steps=0, seed=777)
+    raw = prefill(pool, w, device=DEV, keep_raw=True)
+    q = w.query(0, 0)
+    out, lse = pool.decode(0, [0], q.to(DEV))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    pages = _export(pool, 0, 0)
+    tiers = [t for t, _, _ in pages]
+    assert tiers.count(TIER_STALE) == 55 and tiers[0] == 2 and tiers[56:] == [1] * 8
+    # codecs: FP8 pages bit-exact; TQ3 pages within the boundary exemption
+    K, V = (x.float().numpy() for x in raw[(0, 0)])
+    mism = total = 0
+    oracle_pages = []
+    for p, (tier, b, nv) in enumerate(pages):
+        f8 = encode_fp8_page(K[p * 64:(p + 1) * 64], V[p * 64:(p + 1) * 64], 64)
+        if tier == TIER_STALE:
+            m, t = _tq3_check(f8, b, 64, 4, 256, 777)
+            mism += m
+            total += t
+            oracle_pages.append((tier, demote_page(f8, 64, 4, 256, 777)[0], nv))
+        else:
+            assert np.array_equal(b, f8)
+            oracle_pages.append((tier, f8, nv))
+    assert mism <= 1e-4 * total
+    # decode against the stored pages
+    _check_decode(pool, 0, [0], q, out, lse, 777)
+    # end to end from the raw fp32 inputs (oracle encodes every page itself)
+    ro, rl = decode_attention(q[0].double().numpy(), oracle_pages, 64, 4, 256, 777)
+    o = out[0].double().cpu().numpy()
+    assert np.abs(o - ro).max() <= OUT_TOL * np.abs(ro).max()
+    assert np.abs(lse[0].double().cpu().numpy() - rl).max() <= LSE_TOL
+
+
+# ------------------------------------------------------------------ decode steps with demotion
+def test_decode_steps_with_demotion(mkv):
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import Stepper, make_pool, prefill
+    w = workloads.make("cfg3")
+    w.lengths = [64 * 20 - 3, 64 * 31 - 1]      # short, both about to roll over
+    w.anchors = [{2, 5}, {1}]
+    w.num_layers = 2
+    w.steps = 70
+    pool = make_pool(w, device=DEV, seed=31)
+    prefill(pool, w, device=DEV)
+    st = Stepper(pool, w, device=DEV)
+    for step in range(w.steps):
+        st.pre_step()
+        for layer in range(w.num_layers):
+            k, v = w.step_kv(layer, step)
+            q = w.query(layer, step)
+            out, lse = st.layer(layer, k.to(DEV), v.to(DEV), q.to(DEV))
+        if step in (0, 3, 69):
+            torch.cuda.synchronize()
+            _check_decode(pool, w.num_layers - 1, st.ids, q.float(), out, lse, 31)
+    pool.check_device_errors()
+    for r in range(2):
+        tiers = [pool.page_info(r, p)[0] for p in range(pool.seq_info(r)[1])]
+        npg = len(tiers)
+        assert all(t != 3 for t in tiers[npg - w.windows[r]:])
+        assert all(tiers[a] == 2 for a in w.anchors[r])
+        assert sum(t == 3 for t in tiers) == npg - w.windows[r] - len(w.anchors[r])
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+@pytest.mark.parametrize("name", ["cfg2", "cfg3", "cfg4", "cfg5"])
+def test_full_size_sampled(mkv, name):
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import Stepper, make_pool, prefill
+    w = workloads.make(name)
+    rng = np.random.default_rng(5)
+    layers = [0, w.num_layers - 1]
+    pool = make_pool(w, device=DEV, extra_steps=2, seed=99)
+    prefill(pool, w, device=DEV, layers=layers)
+    st = Stepper(pool, w, device=DEV)
+    st.pre_step()
+    outs = {}
+    for layer in layers:
+        k, v = w.step_kv(layer, 0)
+        q = w.query(layer, 0)
+        outs[layer] = (q,) + tuple(x.clone() for x in st.layer(layer, k.to(DEV), v.to(DEV), q.to(DEV)))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    nsample = 2 if name == "cfg5" else 3
+    for layer in layers:
+        q, out, lse = outs[layer]
+        rs = sorted(rng.choice(w.n, size=min(nsample, w.n), replace=False).tolist())
+        from oracle.paged import decode_attention_streaming
+        for r in rs:
+            pages = _export(pool, layer, r)
+            kvh = [int(rng.integers(0, 4))]
+            ro, rl = decode_attention_streaming(q[r].double().numpy(), pages, w.P, 4, 256, 99, kv_heads=kvh)
+            sl = slice(kvh[0] * 6, kvh[0] * 6 + 6)
+            o = out[r].double().cpu().numpy()[sl]
+            assert np.abs(o - ro[sl]).max() <= OUT_TOL * np.abs(ro[sl]).max()
+            assert np.abs(lse[r].double().cpu().numpy()[sl] - rl[sl]).max() <= LSE_TOL
+    # a property that holds at any size: every live page is addressable and the
+    # workspace does not depend on context length
+    s = pool.stats()
+    assert s.live_tokens == sum(st.lengths)
+    assert s.workspace_bytes < 64 * 2 ** 20

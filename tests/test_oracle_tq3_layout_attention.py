@@ -254,3 +254,17 @@ def test_bytes_per_token_closed_form():
     r = bytes_per_token("bf16") / mixed_bytes_per_token(44 * 64, 878 * 64)
     assert abs(r - 4.847) < 1e-3
     assert abs(fp8_fraction_for_ratio_vs_bf16(3.5) - 0.3018) < 1e-3
+
+
+def test_streaming_equals_dense():
+    rng = np.random.default_rng(18)
+    P, Hkv, D = 16, 2, 64
+    tiers = [TIER_ANCHOR, TIER_STALE, TIER_STALE, TIER_RECENT, TIER_RECENT]
+    pages = _pages(rng, P, Hkv, D, tiers, 5)
+    q = rng.standard_normal((6, D))
+    from oracle.paged import decode_attention_streaming
+    a = decode_attention(q, pages, P, Hkv, D, SEED)
+    b = decode_attention_streaming(q, pages, P, Hkv, D, SEED)
+    assert np.allclose(a[0], b[0], atol=1e-12) and np.allclose(a[1], b[1], atol=1e-12)
+    c = decode_attention_streaming(q, pages, P, Hkv, D, SEED, kv_heads=[1])
+    assert np.allclose(c[0][3:], a[0][3:], atol=1e-12) and np.all(np.isnan(c[0][:3]))
