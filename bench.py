@@ -304,6 +304,10 @@ def run_mkv(args):
     # ---------------- timed region (device-resident inputs)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
           for _ in range(args.steps)]
+    for row in ev:                   # torch creates the CUDA event on first record
+        for a, b in row:
+            a.record()
+            b.record()
     bytes_acc = []
     barrier()
     torch.cuda.synchronize()

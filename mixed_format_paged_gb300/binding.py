@@ -107,9 +107,21 @@ def check(status: int, where: str) -> None:
         raise MkvError(status, where, lib().mkv_last_error().decode())
 
 
+_I32_CACHE: dict = {}
+
+
 def _i32(values):
-    vals = [int(v) for v in values]
-    return (ctypes.c_int32 * max(1, len(vals)))(*vals), len(vals)
+    """int32 C array of `values` (small arrays are cached: the same batch is
+    passed for every layer of a decode step)."""
+    key = tuple(int(v) for v in values)
+    hit = _I32_CACHE.get(key)
+    if hit is None:
+        hit = ((ctypes.c_int32 * max(1, len(key)))(*key), len(key))
+        if len(key) <= 256:
+            if len(_I32_CACHE) > 4096:
+                _I32_CACHE.clear()
+            _I32_CACHE[key] = hit
+    return hit
 
 
 def _ptr(x) -> ctypes.c_void_p:
@@ -237,6 +249,8 @@ def mkv_set_timing_events(pool, start_event, stop_event) -> None:
     def h(e):
         if e is None:
             return ctypes.c_void_p(None)
+        if not e.cuda_event:
+            raise ValueError("torch creates a CUDA event on its first record(); record it once before passing it")
         return ctypes.c_void_p(e.cuda_event)
     check(lib().mkv_set_timing_events(pool, h(start_event), h(stop_event)), "mkv_set_timing_events")
 

@@ -5,7 +5,7 @@ inputs from ``workloads``; it computes nothing on cache data.
 Tier policy (the pages name Recent, Anchor and Stale pages but give no
 schedule): the last W pages of a request, including its partial tail page,
 are Recent; when a request opens page n, page n - W leaves the window and is
-demoted to TQ3 unless it is an Anchor.
+demoted to TQ3, or re-tagged Anchor when it is one (Anchors stay FP8).
 """
 from __future__ import annotations
 
@@ -76,9 +76,12 @@ class Stepper:
             if (self.lengths[r] - 1) % w.P == 0:            # a new page was opened
                 npg = (self.lengths[r] + w.P - 1) // w.P
                 leaving = npg - 1 - w.windows[r]
-                if leaving >= 0 and leaving not in w.anchors[r]:
+                if leaving >= 0:
                     tier, _ = self.pool.page_info(r, leaving)
-                    if tier != S:
+                    if leaving in w.anchors[r]:
+                        if tier == R:
+                            self.pool.set_tier(r, leaving, A)     # protected: stays FP8
+                    elif tier != S:
                         dem_s.append(r)
                         dem_p.append(leaving)
         if dem_s:
