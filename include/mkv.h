@@ -269,6 +269,30 @@ mkv_status mkv_check_device_errors(mkv_pool* pool, mkv_stream_t stream);
  * call's stream, then forgets them.  Lets a caller time that kernel alone. */
 mkv_status mkv_set_timing_events(mkv_pool* pool, void* start, void* stop);
 
+/* Decode attention that allocates nothing (no counterpart in the paper; this
+ * is a convenience of this library).  Same arguments, result and errors as
+ * mkv_decode_attention, but the partial-state scratch of the call lives in a
+ * fixed 8 MiB array compiled into the library (a file-scope __device__ array
+ * that every GPU using the library holds until the process exits) instead of
+ * the pool's workspace.  It is meant for callers that may not allocate device
+ * memory at call time -- for example code running under a framework whose
+ * caching allocator owns the whole device, or code that must not trigger a
+ * cudaMalloc in the middle of a step -- and it calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ * Limit: splits x G x (2 + d) x 4 bytes of partial states must fit in 8 MiB
+ * (1,354 splits at G = 6, d = 256); larger batches return MKV_ERR_CAPACITY
+ * and change nothing.
+ * Set-up: the first call on each device looks the array's device address up
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array, which keeps the
+ * last call's contents; nothing in it needs to start at zero (every partial
+ * state is written in full before it is read).  Calls whose GPU work
+ * overlaps -- on different streams, or from different pools -- race on the
+ * array and must be ordered by the caller. */
+mkv_status mkv_decode_attention_noalloc(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids,
+                                        const void* q, mkv_dtype dtype, float* out, float* lse,
+                                        mkv_stream_t stream);
+
 /* Thread-local text of the last error (never NULL). */
 const char* mkv_last_error(void);
 

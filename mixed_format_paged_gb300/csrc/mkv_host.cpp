@@ -862,6 +862,54 @@ mkv_status mkv_decode_attention(mkv_pool* p, int32_t layer, int32_t n, const int
   return MKV_OK;
 }
 
+// Same as mkv_decode_attention, with the partial states in the library's fixed
+// device scratch instead of the pool workspace; allocates nothing.
+mkv_status mkv_decode_attention_noalloc(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const void* q,
+                                        mkv_dtype dtype, float* out, float* lse, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (dtype != MKV_F32 && dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if (n == 0) return MKV_OK;
+  if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
+  if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no device scratch");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool cached = p->plan_gen == p->generation && p->plan_ids.size() == size_t(n) &&
+                      std::equal(ids, ids + n, p->plan_ids.begin());
+  if (!cached) {
+    if ((st = build_plan(p, n, ids, true, s)) != MKV_OK) {
+      p->plan_gen = 0;
+      return st;
+    }
+    p->plan_gen = p->generation;
+    p->plan_ids.assign(ids, ids + n);
+  }
+  float* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = noalloc_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "device scratch address (cudaGetSymbolAddress)");
+  const size_t need = (p->plan_debug.size() / 6) * size_t(p->G) * (2 + kHeadDim) * sizeof(float);
+  if (need > scratch_bytes)
+    return fail(MKV_ERR_CAPACITY, "batch needs %zu bytes of partial states; the fixed scratch holds %zu",
+                need, scratch_bytes);
+  DecodeParams dp = p->plan_params;
+  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
+  dp.q = q;
+  dp.q_bf16 = dtype == MKV_BF16;
+  dp.part = scratch;
+  e = launch_decode(dp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  MergeParams mp = p->merge_params;
+  mp.part = scratch;
+  mp.out = out;
+  mp.lse = lse;
+  e = launch_merge(mp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return MKV_OK;
+}
+
 mkv_status mkv_pool_stats(const mkv_pool* p, mkv_stats* out) {
   if (!p || !out) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
   mkv_stats st{};

@@ -107,6 +107,10 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 size_t decode_smem_bytes();
+// Device address and size of the library's fixed partial-state scratch (see
+// mkv_decode_attention_noalloc).  The first call on a device looks the address
+// up with that device current; later calls return the cached value.
+cudaError_t noalloc_scratch(float** ptr, size_t* bytes);
 int decode_threads();
 
 }  // namespace mkv

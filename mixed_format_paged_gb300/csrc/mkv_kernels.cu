@@ -20,6 +20,8 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 namespace mkv {
 namespace {
 
@@ -862,6 +864,33 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s) {
 }
 
 size_t decode_smem_bytes() { return kSmemBytes; }
+
+// Fixed scratch for the allocation-free decode entry point: 8 MiB of partial
+// states, compiled into the library so a call never needs to allocate.
+constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchBytes / sizeof(float)];
+
+cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static float* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    // host code must not use the symbol itself as a device address: ask the
+    // runtime for this device's copy (the current device is `dev`)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float*>(p);
+  }
+  *ptr = addr[dev];
+  *bytes = kNoallocScratchBytes;
+  return cudaSuccess;
+}
 int decode_threads() { return kThreads; }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
