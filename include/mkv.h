@@ -231,6 +231,17 @@ mkv_status mkv_decode_attention(mkv_pool* pool, int32_t layer, int32_t n, const 
                                 const void* q, mkv_dtype dtype, float* out, float* lse,
                                 mkv_stream_t stream);
 
+/* One decode step of one layer: append each sequence's newest token (FP8,
+ * as mkv_append_tokens with n_new = 1) and run mixed-format decode attention
+ * over all its tokens (as mkv_decode_attention), in one call and one kernel
+ * launch fewer (the append runs inside the query-preparation kernel).  The
+ * newest token must already be counted by mkv_seq_extend and sit in an FP8
+ * page.  k, v: device [n, H_kv, d] of kv_dtype (row i is seq_ids[i]'s token);
+ * q, out, lse as in mkv_decode_attention.  Errors: those of the two calls. */
+mkv_status mkv_append_decode(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids, const void* k,
+                             const void* v, mkv_dtype kv_dtype, const void* q, mkv_dtype q_dtype, float* out,
+                             float* lse, mkv_stream_t stream);
+
 /* ---------------------------------------------------------------- inspection */
 
 /* Live pages and bytes per tier and KV bytes per live token (the pages'

@@ -179,6 +179,7 @@ struct mkv_pool {
   int demote_cap = 0;
   float* workspace = nullptr;
   size_t workspace_bytes = 0;
+  uint32_t* qfrag = nullptr;
   int* err = nullptr;
   int chunk_cap = 0;
   int entry_cap = 0;
@@ -195,19 +196,24 @@ struct mkv_pool {
   std::vector<int32_t> plan_ids;
   DecodeParams plan_params{};
   MergeParams merge_params{};
+  QprepParams qprep_params{};
+  int plan_parts = 0;
   std::vector<int32_t> plan_debug;   // 6 ints per chunk
   // one-shot timing events around the next decode kernel
   cudaEvent_t t_start = nullptr, t_stop = nullptr;
-  // append cache
+  // append cache (destinations in the append region)
   uint64_t app_gen = 0;
   std::vector<int32_t> app_ids, app_new;
   int app_ntok = 0;
+  // fused append-decode destinations (same region)
+  uint64_t ad_gen = 0;
+  std::vector<int32_t> ad_ids;
 };
 
 namespace {
 
 struct PlanLayout {
-  size_t entries, chunks, cta_chunks, cta_start, merge, total;
+  size_t entries, groups, segs, cta_seg, merge, total;
 };
 
 PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
@@ -215,11 +221,11 @@ PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
   size_t off = 0;
   L.entries = off;
   off += align256(size_t(entry_cap) * sizeof(PageEntry));
-  L.chunks = off;
-  off += align256(size_t(chunk_cap) * sizeof(Chunk));
-  L.cta_chunks = off;
-  off += align256(size_t(chunk_cap) * sizeof(int32_t));
-  L.cta_start = off;
+  L.groups = off;
+  off += align256(size_t(max_batch) * Hkv * 2 * sizeof(Group));
+  L.segs = off;
+  off += align256(size_t(chunk_cap) * sizeof(Segment));
+  L.cta_seg = off;
   off += align256(size_t(kMaxCtas + 1) * sizeof(int32_t));
   L.merge = off;
   off += align256(size_t(max_batch) * Hkv * sizeof(MergeDesc));
@@ -254,7 +260,7 @@ mkv_status validate_config(const mkv_pool_config* c) {
 
 struct Sizes {
   int64_t fp8_page, tq3_page;
-  size_t fp8_arena, tq3_arena, plan, append, demote, workspace, err, total;
+  size_t fp8_arena, tq3_arena, plan, append, demote, workspace, qfrag, err, total;
   int entry_cap, chunk_cap;
 };
 
@@ -273,8 +279,9 @@ Sizes compute_sizes(const mkv_pool_config& c) {
   s.demote = align256(size_t(kDemoteCap) * 8);
   const int G = c.num_q_heads / c.num_kv_heads;
   s.workspace = align256(size_t(s.chunk_cap) * G * (2 + D) * 4);
+  s.qfrag = align256(size_t(mb) * c.num_kv_heads * 2 * kQfragWords * 4);
   s.err = 256;
-  s.total = s.fp8_arena + s.tq3_arena + s.plan + s.append + s.demote + s.workspace + s.err;
+  s.total = s.fp8_arena + s.tq3_arena + s.plan + s.append + s.demote + s.workspace + s.qfrag + s.err;
   return s;
 }
 
@@ -321,10 +328,18 @@ bool valid_seq(const mkv_pool* p, int32_t s) { return s >= 0 && s < p->cfg.max_s
 int npages_for(int len, int P) { return (len + P - 1) / P; }
 
 // ------------------------------------------------------------------ planner
-// Split the batch's pages into partial-state chunks, balanced by bytes, and
-// assign chunks to CTAs (longest first onto the least-loaded CTA).  CTAs
-// [0, n_ctas_fp8) run the FP8 body, the rest the TQ3 body; the CTA split is
-// proportional to each format's bytes.
+// Relative cost of one token of one kv head, per format, plus a fixed cost per
+// 64-token block.  The decode kernel is issue-bound on TQ3 dequantisation and
+// bandwidth-bound on FP8 bytes; these weights balance the two across CTAs.
+constexpr double kCostTq3Token = 1.0;
+constexpr double kCostFp8Token = 1.3;
+constexpr double kCostBlock = 8.0;
+
+// Split the batch's pages into groups (request, kv head, format), lay the
+// groups' 64-token blocks out in one sequence, and cut that sequence into one
+// contiguous piece per CTA of equal estimated cost.  Each (CTA, group) piece
+// writes one partial state; a group's partial states are contiguous, which is
+// what the merge kernel reads.
 mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, cudaStream_t stream) {
   const int P = p->cfg.page_size, H = p->cfg.num_kv_heads;
   const PlanLayout L = plan_layout(p->entry_cap, p->chunk_cap, effective_batch(p->cfg), H);
@@ -332,143 +347,139 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   entries.reserve(size_t(n) * 64);
   struct BatchPages {
     int f_first, f_count, t_first, t_count;
-    int64_t f_tok, t_tok;
   };
   std::vector<BatchPages> bp(n);
-  int64_t fp8_tok = 0, tq3_tok = 0;
   for (int b = 0; b < n; ++b) {
     const SeqRec& s = p->seqs[ids[b]];
     const int np = int(s.pages.size());
     BatchPages& B = bp[b];
     B.f_first = int(entries.size());
-    B.f_tok = B.t_tok = 0;
     for (int i = 0; i < np; ++i) {
       const int nv = (i == np - 1) ? s.len - i * P : P;
-      if (s.pages[i].tier != MKV_TIER_STALE) {
-        entries.push_back({s.pages[i].slot, nv});
-        B.f_tok += nv;
-      }
+      if (s.pages[i].tier != MKV_TIER_STALE)
+        entries.push_back({s.pages[i].slot, int16_t(nv), int16_t(i == np - 1 ? 1 : 0)});
     }
     B.f_count = int(entries.size()) - B.f_first;
     B.t_first = int(entries.size());
-    for (int i = 0; i < np; ++i) {
-      if (s.pages[i].tier == MKV_TIER_STALE) {
-        entries.push_back({s.pages[i].slot, P});
-        B.t_tok += P;
-      }
-    }
+    for (int i = 0; i < np; ++i)
+      if (s.pages[i].tier == MKV_TIER_STALE) entries.push_back({s.pages[i].slot, int16_t(P), int16_t(0)});
     B.t_count = int(entries.size()) - B.t_first;
-    fp8_tok += B.f_tok;
-    tq3_tok += B.t_tok;
   }
   if (int(entries.size()) > p->entry_cap) return fail(MKV_ERR_CAPACITY, "plan entries exceed capacity");
-  const double fbytes = double(fp8_tok) * 2 * (kHeadDim + 2);
-  const double tbytes = double(tq3_tok) * 2 * (3 * kHeadDim / 8 + 2);
-  const int nsm = std::min(p->n_sm, kMaxCtas);
-  int nf = 0, nt = 0;
-  if (fbytes > 0 && tbytes > 0) {
-    nf = int(std::lround(nsm * fbytes / (fbytes + tbytes)));
-    nf = std::max(1, std::min(nf, nsm - 1));
-    nt = nsm - nf;
-  } else if (fbytes > 0) {
-    nf = nsm;
-  } else {
-    nt = nsm;
-  }
-  // chunking
-  std::vector<Chunk> chunks;
-  std::vector<MergeDesc> md(size_t(n) * H);
-  const int per_cta = 2;
-  auto split = [&](int b, int kvh, int fmt, int first, int count, const int64_t target) {
-    if (count == 0) return;
-    int64_t tok = 0;
-    for (int i = 0; i < count; ++i) tok += entries[first + i].nvalid;
-    int nc = int(std::max<int64_t>(1, (tok + target / 2) / std::max<int64_t>(1, target)));
-    nc = std::min(nc, count);
-    for (int c = 0; c < nc; ++c) {
-      const int a = first + int(int64_t(count) * c / nc);
-      const int e = first + int(int64_t(count) * (c + 1) / nc);
-      Chunk ch{};
-      ch.b = b;
-      ch.kvh = kvh;
-      ch.fmt = fmt;
-      ch.entry0 = a;
-      ch.nentry = e - a;
-      int t = 0;
-      for (int i = a; i < e; ++i) t += entries[i].nvalid;
-      ch.tokens = t;
-      chunks.push_back(ch);
+  // groups, TQ3 before FP8 within each (request, kv head)
+  std::vector<Group> groups;
+  for (int b = 0; b < n; ++b)
+    for (int kvh = 0; kvh < H; ++kvh)
+      for (int fmt = 1; fmt >= 0; --fmt) {
+        const int first = fmt ? bp[b].t_first : bp[b].f_first;
+        const int count = fmt ? bp[b].t_count : bp[b].f_count;
+        if (count == 0) continue;
+        Group g{};
+        g.b = b;
+        g.kvh = kvh;
+        g.fmt = fmt;
+        g.entry0 = first;
+        g.nentry = count;
+        for (int i = 0; i < count; ++i) g.tokens += entries[first + i].nvalid;
+        groups.push_back(g);
+      }
+  // block costs and the CTA count
+  double total = 0.0;
+  int64_t nblocks = 0;
+  for (const Group& g : groups)
+    for (int i = 0; i < g.nentry; ++i) {
+      const int nv = entries[g.entry0 + i].nvalid;
+      nblocks += (nv + kStageTokens - 1) / kStageTokens;
+      total += nv * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock * ((nv + kStageTokens - 1) / kStageTokens);
     }
-  };
-  const int64_t ftarget = nf ? std::max<int64_t>(1, fp8_tok * H / (int64_t(nf) * per_cta)) : 1;
-  const int64_t ttarget = nt ? std::max<int64_t>(1, tq3_tok * H / (int64_t(nt) * per_cta)) : 1;
-  for (int b = 0; b < n; ++b) {
-    for (int kvh = 0; kvh < H; ++kvh) {
-      MergeDesc& m = md[size_t(b) * H + kvh];
-      m.tq3_first = int(chunks.size());
-      split(b, kvh, 1, bp[b].t_first, bp[b].t_count, ttarget);
-      m.tq3_count = int(chunks.size()) - m.tq3_first;
-      m.fp8_first = int(chunks.size());
-      split(b, kvh, 0, bp[b].f_first, bp[b].f_count, ftarget);
-      m.fp8_count = int(chunks.size()) - m.fp8_first;
-    }
-  }
-  if (int(chunks.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan chunks exceed capacity");
-  // LPT assignment per format
-  std::vector<std::vector<int32_t>> per_cta_list(size_t(nf + nt));
-  for (int fmt = 0; fmt < 2; ++fmt) {
-    const int c0 = fmt == 0 ? 0 : nf;
-    const int nc = fmt == 0 ? nf : nt;
-    if (nc == 0) continue;
-    std::vector<int32_t> ids_f;
-    for (int i = 0; i < int(chunks.size()); ++i)
-      if (chunks[i].fmt == fmt) ids_f.push_back(i);
-    std::stable_sort(ids_f.begin(), ids_f.end(),
-                     [&](int a, int b) { return chunks[a].tokens > chunks[b].tokens; });
-    using Load = std::pair<int64_t, int>;
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int c = 0; c < nc; ++c) heap.push({0, c});
-    for (int id : ids_f) {
-      Load l = heap.top();
-      heap.pop();
-      per_cta_list[c0 + l.second].push_back(id);
-      l.first += chunks[id].tokens;
-      heap.push(l);
+  const int ncta = int(std::max<int64_t>(1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas),
+                                                                 (nblocks + 1) / 2})));
+  // cut
+  std::vector<Segment> segs;
+  std::vector<int32_t> cta_seg(ncta + 1, 0);
+  const double per_cta = total / ncta;
+  double acc = 0.0;
+  int cur_cta = 0;
+  for (int gi = 0; gi < int(groups.size()); ++gi) {
+    Group& g = groups[gi];
+    bool open = false;
+    for (int i = 0; i < g.nentry; ++i) {
+      const int nv = entries[g.entry0 + i].nvalid;
+      const int nb = (nv + kStageTokens - 1) / kStageTokens;
+      for (int blk = 0; blk < nb; ++blk) {
+        const int tok = std::min(kStageTokens, nv - kStageTokens * blk);
+        int cta = int(acc / per_cta);
+        cta = std::min(std::max(cta, cur_cta), ncta - 1);
+        if (!open || cta != cur_cta) {
+          while (cur_cta < cta) cta_seg[++cur_cta] = int(segs.size());
+          Segment sg{};
+          sg.group = gi;
+          sg.entry = g.entry0 + i;
+          sg.blk = blk;
+          segs.push_back(sg);
+          open = true;
+        }
+        segs.back().nstages += 1;
+        segs.back().tokens += tok;
+        acc += tok * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
+      }
     }
   }
-  // drop empty CTAs at the end of each format range is not needed: empty CTAs exit at once
-  std::vector<int32_t> cta_chunks, cta_start;
-  cta_start.push_back(0);
-  for (auto& l : per_cta_list) {
-    for (int id : l) cta_chunks.push_back(id);
-    cta_start.push_back(int(cta_chunks.size()));
+  while (cur_cta < ncta) cta_seg[++cur_cta] = int(segs.size());
+  if (int(segs.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
+  // partial-state indices: pieces are in group order, so each group's are contiguous
+  for (Group& g : groups) g.nparts = 0;
+  for (int i = 0; i < int(segs.size()); ++i) {
+    Group& g = groups[segs[i].group];
+    if (g.nparts == 0) g.part0 = i;
+    segs[i].part = i;
+    ++g.nparts;
   }
-  // debug record
+  std::vector<MergeDesc> md(size_t(n) * H, MergeDesc{0, 0, 0, 0});
+  for (const Group& g : groups) {
+    MergeDesc& m = md[size_t(g.b) * H + g.kvh];
+    if (g.fmt) {
+      m.tq3_first = g.part0;
+      m.tq3_count = g.nparts;
+    } else {
+      m.fp8_first = g.part0;
+      m.fp8_count = g.nparts;
+    }
+  }
+  // debug record: one line per partial state
   p->plan_debug.clear();
-  for (const Chunk& c : chunks) {
-    const int tier = c.fmt == 0 ? 1 : 3;
-    const int32_t rec[6] = {c.b, c.kvh, tier, c.entry0, c.nentry, c.tokens};
+  for (const Segment& sg : segs) {
+    const Group& g = groups[sg.group];
+    int last = sg.entry, blk = sg.blk;
+    for (int k = 1; k < sg.nstages; ++k) {
+      const int nb = (entries[last].nvalid + kStageTokens - 1) / kStageTokens;
+      if (++blk == nb) {
+        blk = 0;
+        ++last;
+      }
+    }
+    const int32_t rec[6] = {g.b, g.kvh, g.fmt ? 3 : 1, sg.entry, last - sg.entry + 1, sg.tokens};
     p->plan_debug.insert(p->plan_debug.end(), rec, rec + 6);
   }
+  p->plan_parts = int(segs.size());
   // params
   DecodeParams& dp = p->plan_params;
   dp = DecodeParams{};
   dp.entries = reinterpret_cast<const PageEntry*>(p->plan_region + L.entries);
-  dp.chunks = reinterpret_cast<const Chunk*>(p->plan_region + L.chunks);
-  dp.cta_chunks = reinterpret_cast<const int32_t*>(p->plan_region + L.cta_chunks);
-  dp.cta_start = reinterpret_cast<const int32_t*>(p->plan_region + L.cta_start);
-  dp.n_ctas_fp8 = nf;
-  dp.n_ctas = nf + nt;
+  dp.groups = reinterpret_cast<const Group*>(p->plan_region + L.groups);
+  dp.segs = reinterpret_cast<const Segment*>(p->plan_region + L.segs);
+  dp.cta_seg = reinterpret_cast<const int32_t*>(p->plan_region + L.cta_seg);
+  dp.n_ctas = ncta;
   dp.fp8_page_bytes = p->fp8_page_bytes;
   dp.tq3_page_bytes = p->tq3_page_bytes;
   dp.fp8_slots = p->cfg.fp8_slots;
   dp.tq3_slots = p->cfg.tq3_slots;
+  dp.qfrag = p->qfrag;
   dp.Hq = p->cfg.num_q_heads;
   dp.Hkv = H;
   dp.G = p->G;
   dp.P = P;
   dp.part = p->workspace;
-  std::memcpy(dp.signs, p->signs, sizeof dp.signs);
   dp.score_scale = float(1.4426950408889634 / std::sqrt(double(kHeadDim)));
   dp.lut = p->lut;
   dp.err = p->err;
@@ -481,15 +492,22 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   mp.Hkv = H;
   mp.G = p->G;
   std::memcpy(mp.signs, p->signs, sizeof mp.signs);
+  QprepParams& qp = p->qprep_params;
+  qp = QprepParams{};
+  qp.n = n;
+  qp.Hq = p->cfg.num_q_heads;
+  qp.Hkv = H;
+  qp.G = p->G;
+  std::memcpy(qp.signs, p->signs, sizeof qp.signs);
+  qp.qfrag = p->qfrag;
   if (!upload) return MKV_OK;
-  // stage and upload (one copy of the used span)
   mkv_status st = staging_acquire(p->st_plan);
   if (st != MKV_OK) return st;
   uint8_t* h = static_cast<uint8_t*>(p->st_plan.host);
   std::memcpy(h + L.entries, entries.data(), entries.size() * sizeof(PageEntry));
-  std::memcpy(h + L.chunks, chunks.data(), chunks.size() * sizeof(Chunk));
-  std::memcpy(h + L.cta_chunks, cta_chunks.data(), cta_chunks.size() * sizeof(int32_t));
-  std::memcpy(h + L.cta_start, cta_start.data(), cta_start.size() * sizeof(int32_t));
+  std::memcpy(h + L.groups, groups.data(), groups.size() * sizeof(Group));
+  std::memcpy(h + L.segs, segs.data(), segs.size() * sizeof(Segment));
+  std::memcpy(h + L.cta_seg, cta_seg.data(), cta_seg.size() * sizeof(int32_t));
   std::memcpy(h + L.merge, md.data(), md.size() * sizeof(MergeDesc));
   return staging_upload(p->st_plan, p->plan_region, L.total, stream);
 }
@@ -573,6 +591,8 @@ mkv_status mkv_pool_create(const mkv_pool_config* cfg, void* device_buf, size_t 
     off += S.demote;
     p->workspace = reinterpret_cast<float*>(b + off);
     off += S.workspace;
+    p->qfrag = reinterpret_cast<uint32_t*>(b + off);
+    off += S.qfrag;
     p->err = reinterpret_cast<int*>(b + off);
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->n_sm, cudaDevAttrMultiProcessorCount, p->device);
@@ -722,6 +742,7 @@ mkv_status mkv_append_tokens(mkv_pool* p, int32_t layer, int32_t n, const int32_
       if ((st = staging_acquire(p->st_append)) != MKV_OK) return st;
       std::memcpy(p->st_append.host, dest.data() + t0, size_t(cnt) * 4);
       if ((st = staging_upload(p->st_append, p->append_region, size_t(cnt) * 4, s)) != MKV_OK) return st;
+      p->ad_gen = 0;
     }
     ap.dest = p->append_region;
     ap.k = static_cast<const uint8_t*>(k) + t0 * row;
@@ -843,12 +864,14 @@ mkv_status mkv_decode_attention(mkv_pool* p, int32_t layer, int32_t n, const int
     p->plan_ids.assign(ids, ids + n);
   }
   if (p->host_only) return MKV_OK;
+  QprepParams qp = p->qprep_params;
+  qp.q = q;
+  qp.q_bf16 = dtype == MKV_BF16;
+  cudaError_t e = launch_qprep(qp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "q-prep launch");
   DecodeParams dp = p->plan_params;
   dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
   dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
-  dp.q = q;
-  dp.q_bf16 = dtype == MKV_BF16;
-  cudaError_t e = cudaSuccess;
   if (p->t_start) e = cudaEventRecord(p->t_start, s);
   if (e == cudaSuccess) e = launch_decode(dp, s);
   if (e == cudaSuccess && p->t_stop) e = cudaEventRecord(p->t_stop, s);
@@ -889,20 +912,103 @@ mkv_status mkv_decode_attention_noalloc(mkv_pool* p, int32_t layer, int32_t n, c
   size_t scratch_bytes = 0;
   cudaError_t e = noalloc_scratch(&scratch, &scratch_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "device scratch address (cudaGetSymbolAddress)");
-  const size_t need = (p->plan_debug.size() / 6) * size_t(p->G) * (2 + kHeadDim) * sizeof(float);
+  // scratch = [q fragments | partial states]
+  const size_t qf_words = size_t(n) * p->cfg.num_kv_heads * 2 * kQfragWords;
+  const size_t need = qf_words * 4 + size_t(p->plan_parts) * p->G * (2 + kHeadDim) * sizeof(float);
   if (need > scratch_bytes)
-    return fail(MKV_ERR_CAPACITY, "batch needs %zu bytes of partial states; the fixed scratch holds %zu",
-                need, scratch_bytes);
+    return fail(MKV_ERR_CAPACITY, "batch needs %zu bytes of scratch; the fixed scratch holds %zu", need,
+                scratch_bytes);
+  uint32_t* qfrag = reinterpret_cast<uint32_t*>(scratch);
+  float* part = scratch + qf_words;
+  QprepParams qp = p->qprep_params;
+  qp.q = q;
+  qp.q_bf16 = dtype == MKV_BF16;
+  qp.qfrag = qfrag;
+  e = launch_qprep(qp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "q-prep launch");
   DecodeParams dp = p->plan_params;
   dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
   dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
-  dp.q = q;
-  dp.q_bf16 = dtype == MKV_BF16;
-  dp.part = scratch;
+  dp.qfrag = qfrag;
+  dp.part = part;
   e = launch_decode(dp, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   MergeParams mp = p->merge_params;
-  mp.part = scratch;
+  mp.part = part;
+  mp.out = out;
+  mp.lse = lse;
+  e = launch_merge(mp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return MKV_OK;
+}
+
+mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const void* k,
+                             const void* v, mkv_dtype kv_dtype, const void* q, mkv_dtype q_dtype, float* out,
+                             float* lse, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if ((kv_dtype != MKV_F32 && kv_dtype != MKV_BF16) || (q_dtype != MKV_F32 && q_dtype != MKV_BF16))
+    return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if (n == 0) return MKV_OK;
+  if (!k || !v || !q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "k/v/q/out/lse is NULL");
+  const int P = p->cfg.page_size;
+  for (int i = 0; i < n; ++i) {
+    const SeqRec& s = p->seqs[ids[i]];
+    if (s.pages[(s.len - 1) / P].tier == MKV_TIER_STALE)
+      return fail(MKV_ERR_INVALID_STATE, "sequence %d: the newest token's page is TQ3", ids[i]);
+  }
+  if (p->host_only) return MKV_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool cached = p->plan_gen == p->generation && p->plan_ids.size() == size_t(n) &&
+                      std::equal(ids, ids + n, p->plan_ids.begin());
+  if (!cached) {
+    if ((st = build_plan(p, n, ids, true, s)) != MKV_OK) {
+      p->plan_gen = 0;
+      return st;
+    }
+    p->plan_gen = p->generation;
+    p->plan_ids.assign(ids, ids + n);
+  }
+  const bool dest_cached = p->ad_gen == p->generation && p->ad_ids.size() == size_t(n) &&
+                           std::equal(ids, ids + n, p->ad_ids.begin());
+  if (!dest_cached) {
+    if (n > p->append_cap) return fail(MKV_ERR_CAPACITY, "batch larger than the append region");
+    if ((st = staging_acquire(p->st_append)) != MKV_OK) return st;
+    uint32_t* h = static_cast<uint32_t*>(p->st_append.host);
+    for (int i = 0; i < n; ++i) {
+      const SeqRec& sq = p->seqs[ids[i]];
+      const int pos = sq.len - 1;
+      h[i] = (uint32_t(sq.pages[pos / P].slot) << 8) | uint32_t(pos % P);
+    }
+    if ((st = staging_upload(p->st_append, p->append_region, size_t(n) * 4, s)) != MKV_OK) return st;
+    p->app_gen = 0;
+    p->ad_gen = p->generation;
+    p->ad_ids.assign(ids, ids + n);
+  }
+  QprepParams qp = p->qprep_params;
+  qp.q = q;
+  qp.q_bf16 = q_dtype == MKV_BF16;
+  qp.append = 1;
+  qp.kv_bf16 = kv_dtype == MKV_BF16;
+  qp.P = P;
+  qp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  qp.fp8_page_bytes = p->fp8_page_bytes;
+  qp.dest = p->append_region;
+  qp.k = k;
+  qp.v = v;
+  cudaError_t e = launch_qprep(qp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "q-prep/append launch");
+  DecodeParams dp = p->plan_params;
+  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
+  if (p->t_start) e = cudaEventRecord(p->t_start, s);
+  if (e == cudaSuccess) e = launch_decode(dp, s);
+  if (e == cudaSuccess && p->t_stop) e = cudaEventRecord(p->t_stop, s);
+  p->t_start = p->t_stop = nullptr;
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  MergeParams mp = p->merge_params;
   mp.out = out;
   mp.lse = lse;
   e = launch_merge(mp, s);

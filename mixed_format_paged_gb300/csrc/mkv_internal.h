@@ -14,6 +14,7 @@ constexpr int kMaxGroup = 8;       // q heads per kv head held in one MMA tile
 constexpr int kStageTokens = 64;   // tokens per staged page block
 constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
 constexpr int kMaxCtas = 1024;     // upper bound on decode CTAs
+constexpr int kQfragWords = 2048;  // q-prep fragment words per (b, kvh, format)
 
 // Error bits written by kernels into the pool's device error word.
 enum : int {
@@ -23,16 +24,29 @@ enum : int {
 
 struct PageEntry {         // one page of one batch entry in a decode plan
   int32_t slot;            // physical slot in the tier's arena
-  int32_t nvalid;          // tokens written in the page (1..P)
+  int16_t nvalid;          // tokens written in the page (1..P)
+  int16_t tail;            // 1 for a request's last page: it may be written by the
+                           // kernel just before the decode kernel (fused append)
 };
 
-struct Chunk {             // one partial-state split (one CTA work item)
+struct Group {             // one run of pages: (request, kv head, format)
   int32_t b;               // batch index
   int32_t kvh;             // kv head
   int32_t fmt;             // 0 = FP8 (Recent/Anchor), 1 = TQ3 (Stale)
   int32_t entry0;          // first PageEntry
   int32_t nentry;          // number of PageEntry
-  int32_t tokens;          // valid tokens covered (host bookkeeping)
+  int32_t part0;           // first partial-state index of the group
+  int32_t nparts;          // partial states (CTA pieces) of the group
+  int32_t tokens;          // valid tokens (host bookkeeping)
+};
+
+struct Segment {           // one CTA's piece of one group
+  int32_t group;
+  int32_t entry;           // first PageEntry (absolute index)
+  int32_t blk;             // first 64-token block within that entry
+  int32_t nstages;         // 64-token blocks in the piece (a padding block evens odd counts)
+  int32_t part;            // partial-state index the piece writes
+  int32_t tokens;          // valid tokens of the piece (host bookkeeping)
   int32_t pad0, pad1;
 };
 
@@ -56,19 +70,34 @@ struct DecodeParams {
   int64_t fp8_page_bytes, tq3_page_bytes;
   int32_t fp8_slots, tq3_slots;
   const PageEntry* entries;
-  const Chunk* chunks;             // indexed by chunk id (= partial index)
-  const int32_t* cta_chunks;       // chunk ids in per-CTA order
-  const int32_t* cta_start;        // [n_ctas + 1] into cta_chunks
-  int32_t n_ctas_fp8;              // CTAs [0, n_ctas_fp8) run the FP8 body
+  const Group* groups;
+  const Segment* segs;             // per-CTA pieces, CTA by CTA
+  const int32_t* cta_seg;          // [n_ctas + 1] into segs
   int32_t n_ctas;
-  const void* q;                   // [n, Hq, D]
-  int32_t q_bf16;
+  const uint32_t* qfrag;           // q-prep output: [(b*Hkv + kvh)*2 + fmt][32][64]
   int32_t Hq, Hkv, G, P;
-  float* part;                     // [chunks][G][2 + D] (m in log2 units, l, o)
-  uint64_t signs[4];               // bit i set -> sign_i = -1
+  float* part;                     // [parts][G][2 + D] (m in log2 units, l, o)
   float score_scale;               // log2(e) / sqrt(d)
   Lut lut;
   int* err;
+};
+
+struct QprepParams {
+  const void* q;                   // [n, Hq, D]
+  int32_t q_bf16;
+  int32_t n, Hq, Hkv, G;
+  uint64_t signs[4];
+  uint32_t* qfrag;
+  // optional fused single-token append (mkv_append_decode): one new token per
+  // request, rows k/v [n, Hkv, D], destinations as in AppendParams
+  int32_t append;
+  int32_t kv_bf16;
+  int32_t P;
+  uint8_t* fp8_layer;
+  int64_t fp8_page_bytes;
+  const uint32_t* dest;
+  const void* k;
+  const void* v;
 };
 
 struct MergeParams {
@@ -104,6 +133,9 @@ struct DemoteParams {
 // Kernel launchers (mkv_kernels.cu).  Return cudaGetLastError() of the launch.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
+cudaError_t launch_qprep(const QprepParams& p, cudaStream_t s);
+// Launched with programmatic stream serialisation so its copies start while
+// the preceding q-prep kernel finishes; its QK warps wait for q-prep's output.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 size_t decode_smem_bytes();

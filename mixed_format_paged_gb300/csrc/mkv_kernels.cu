@@ -11,8 +11,10 @@
 //   mkv_append_kernel  -- FP8 quantise new K/V rows into their pages
 //   mkv_demote_kernel  -- FP8 page -> TQ3 page (dequantise, rotate, RMS scale,
 //                         Lloyd-Max codes, pack)
-//   mkv_decode_kernel  -- persistent partial-attention kernel; CTAs below
-//                         n_ctas_fp8 run the FP8 body, the rest the TQ3 body
+//   mkv_qprep_kernel   -- per (request, kv head): q rows (and q' = R q) as
+//                         fp16 hi/lo MMA fragments
+//   mkv_decode_kernel  -- persistent, warp-specialised partial-attention
+//                         kernel over both formats
 //   mkv_merge_kernel   -- LSE merge: TQ3 partials in the rotated domain,
 //                         one R^T, then FP8 partials; writes out and lse
 #include "mkv_internal.h"
@@ -55,15 +57,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false when the phase did not complete within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
-  }
-  return true;
-}
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -93,7 +86,10 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 __device__ __forceinline__ bool sign_neg(const uint64_t (&signs)[4], int i) {
-  return (signs[i >> 6] >> (i & 63)) & 1ull;
+  // select the word instead of indexing the parameter array (keeps it out of local memory)
+  const int w = i >> 6;
+  const uint64_t word = w == 0 ? signs[0] : w == 1 ? signs[1] : w == 2 ? signs[2] : signs[3];
+  return (word >> (i & 63)) & 1ull;
 }
 
 // TQ3: four 3-bit codes held as nibbles in sel[15:0] -> two f16x2 registers
@@ -114,22 +110,14 @@ __device__ __forceinline__ void tq3_unit_selectors(uint32_t w0, uint32_t w1, uin
 }
 
 // ============================================================== append
-// One warp per (token, kv head, K|V) row: FP8 scale + codes into the page.
-__global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int nrows = p.ntok * p.Hkv * 2;
-  if (warp >= nrows) return;
-  const int kv = warp & 1;
-  const int h = (warp >> 1) % p.Hkv;
-  const int tok = (warp >> 1) / p.Hkv;
-  const uint32_t dst = p.dest[tok];
-  const int slot = static_cast<int>(dst >> 8), pos = static_cast<int>(dst & 0xff);
-  const size_t row = (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim;
-  const void* src = kv ? p.v : p.k;
+// FP8-quantise one row (one token, kv head, K|V) into its page: the calling
+// warp holds the row; s = fp16(amax / 448), codes = e4m3_rn_satfinite(x / s)
+// with IEEE fp32 divisions.
+__device__ __forceinline__ void fp8_append_row(const void* src_rows, size_t row, int bf16, uint8_t* plane, int P,
+                                               int kv, int pos, int lane) {
   float x[8];
-  if (p.kv_bf16) {
-    const uint4 raw = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + row)[lane];
+  if (bf16) {
+    const uint4 raw = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src_rows) + row)[lane];
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -138,7 +126,7 @@ __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
       x[2 * i + 1] = f.y;
     }
   } else {
-    const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(src) + row) + 2 * lane;
+    const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(src_rows) + row) + 2 * lane;
     const float4 a = f4[0], b = f4[1];
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   }
@@ -160,9 +148,6 @@ __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
     }
     c[i] = two;
   }
-  const int P = p.P;
-  uint8_t* plane = p.fp8_layer + static_cast<int64_t>(slot) * p.fp8_page_bytes +
-                   static_cast<int64_t>(h) * 2 * (P * (kHeadDim + 2)) + kv * (P * (kHeadDim + 2));
   if (kv == 0) {
     uint2 w;
     w.x = c[0] | (c[1] << 16);
@@ -177,6 +162,24 @@ __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
     }
   }
   if (lane == 0) reinterpret_cast<__half*>(plane + P * kHeadDim)[pos] = s16;
+}
+
+// One warp per (token, kv head, K|V) row.
+__global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nrows = p.ntok * p.Hkv * 2;
+  if (warp >= nrows) return;
+  const int kv = warp & 1;
+  const int h = (warp >> 1) % p.Hkv;
+  const int tok = (warp >> 1) / p.Hkv;
+  const uint32_t dst = p.dest[tok];
+  const int slot = static_cast<int>(dst >> 8), pos = static_cast<int>(dst & 0xff);
+  const int P = p.P;
+  uint8_t* plane = p.fp8_layer + static_cast<int64_t>(slot) * p.fp8_page_bytes +
+                   static_cast<int64_t>(h) * 2 * (P * (kHeadDim + 2)) + kv * (P * (kHeadDim + 2));
+  fp8_append_row(kv ? p.v : p.k, (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim, p.kv_bf16, plane, P, kv, pos,
+                 lane);
 }
 
 // ============================================================== demote
@@ -303,198 +306,89 @@ __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
   for (int t = threadIdx.x; t < P; t += blockDim.x) osc[t] = sig[t];
 }
 
-// ============================================================== decode
-// Persistent partial-attention kernel.  Warps 0..7 consume, warp 8 produces.
-//
-// Producer: for every 64-token block of every page of the CTA's chunks, one
-// mbarrier-tracked cp.async.bulk per plane part (K codes, K scales, V codes,
-// V scales) into a ring of kStages(fmt) shared-memory stages.
-// Consumers: warps 0-3 take even blocks and warps 4-7 odd ones; warp w owns
-// tokens [16 (w%4), +16) of its block.  Per 16-token tile:
-//   S^T = Q K^T on mma.sync m16n8k16: A = q rows (hi in rows 0-7, lo
-//   residual in rows 8-15, fp16) from registers, B = dequantised K;
-//   online softmax in log2 units with a lazy rescale;
-//   O^T += V^T P^T: A = dequantised V (token pairs), B = P scaled by the
-//   V row scales (fp16).
-// Epilogue per chunk: the 8 warps' states merge in shared memory into one
-// partial (m, l, o) per q head.
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-
-template <int FMT>
-struct Fmt;
-template <>
-struct Fmt<0> {  // FP8
-  static constexpr int kRowBytes = kHeadDim;            // K row / half V pair-row
-  static constexpr int kStages = 4;
-};
-template <>
-struct Fmt<1> {  // TQ3
-  static constexpr int kRowBytes = 3 * kHeadDim / 8;
-  static constexpr int kStages = 10;
-};
-template <int FMT>
-struct Stage {
-  static constexpr int kCode = kStageTokens * Fmt<FMT>::kRowBytes;    // bytes of K (or V) codes
-  static constexpr int kScale = kStageTokens * 2;
-  static constexpr int kK = 0, kKs = kCode, kV = kCode + kScale, kVs = 2 * kCode + kScale;
-  static constexpr int kBytes = 2 * (kCode + kScale);
-};
-
-constexpr int kEpiFloats = kConsumerWarps * kMaxGroup * kHeadDim;     // O per warp
-constexpr int kSmemRing = 4 * Stage<0>::kBytes > 10 * Stage<1>::kBytes ? 4 * Stage<0>::kBytes
-                                                                       : 10 * Stage<1>::kBytes;
-constexpr int kSmemBytes = kSmemRing + kEpiFloats * 4 + 2 * kConsumerWarps * kMaxGroup * 4 +
-                           kMaxGroup * kHeadDim * 4 + 2 * 16 * 8 + 64;
-
-struct SmemLayout {
-  uint8_t* ring;
-  float* epi_o;   // [warp][head][D]
-  float* epi_m;   // [warp][head]
-  float* epi_l;
-  float* qs;      // [head][D]
-  uint64_t* full;
-  uint64_t* empty;
-  int* abort_flag;
-};
-__device__ __forceinline__ SmemLayout carve(uint8_t* base) {
-  SmemLayout s;
-  s.ring = base;
-  s.epi_o = reinterpret_cast<float*>(base + kSmemRing);
-  s.epi_m = s.epi_o + kEpiFloats;
-  s.epi_l = s.epi_m + kConsumerWarps * kMaxGroup;
-  s.qs = s.epi_l + kConsumerWarps * kMaxGroup;
-  s.full = reinterpret_cast<uint64_t*>(s.qs + kMaxGroup * kHeadDim);
-  s.empty = s.full + 16;
-  s.abort_flag = reinterpret_cast<int*>(s.empty + 16);
-  return s;
-}
-
-// number of 64-token blocks of a page entry that hold valid tokens
-__device__ __forceinline__ int entry_blocks(const PageEntry& e) {
-  return (e.nvalid + kStageTokens - 1) / kStageTokens;
-}
-
-template <int FMT>
-__device__ void producer_loop(const DecodeParams& p, const SmemLayout& sm, int first, int last) {
-  using St = Stage<FMT>;
-  constexpr int NS = Fmt<FMT>::kStages;
-  const uint8_t* arena = FMT == 0 ? p.fp8_layer : p.tq3_layer;
-  const int64_t page_bytes = FMT == 0 ? p.fp8_page_bytes : p.tq3_page_bytes;
-  const int nslots = FMT == 0 ? p.fp8_slots : p.tq3_slots;
-  const int P = p.P;
-  const int plane = P * (Fmt<FMT>::kRowBytes + 2);
-  int gi = 0;   // global block counter
-  bool ok = true;
-  for (int ci = first; ci < last && ok; ++ci) {
-    const Chunk ch = p.chunks[p.cta_chunks[ci]];
-    for (int e = 0; e < ch.nentry && ok; ++e) {
-      const PageEntry pe = p.entries[ch.entry0 + e];
-      if (pe.slot < 0 || pe.slot >= nslots) {
-        atomicOr(p.err, kErrBadPlan);
-        ok = false;
-        break;
-      }
-      const uint8_t* hp = arena + static_cast<int64_t>(pe.slot) * page_bytes +
-                          static_cast<int64_t>(ch.kvh) * 2 * plane;
-      const int nb = entry_blocks(pe);
-      for (int blk = 0; blk < nb; ++blk, ++gi) {
-        const int slot = gi % NS;
-        if (gi >= NS) {
-          if (!mbar_wait(&sm.empty[slot], ((gi / NS) - 1) & 1)) {
-            atomicOr(p.err, kErrWaitTimeout);
-            *sm.abort_flag = 1;
-            ok = false;
-            break;
-          }
-        }
-        if (*reinterpret_cast<volatile int*>(sm.abort_flag)) { ok = false; break; }
-        uint8_t* st = sm.ring + slot * St::kBytes;
-        const int tok0 = blk * kStageTokens;
-        mbar_expect_tx(&sm.full[slot], St::kBytes);
-        bulk_g2s(st + St::kK, hp + tok0 * Fmt<FMT>::kRowBytes, St::kCode, &sm.full[slot]);
-        bulk_g2s(st + St::kKs, hp + P * Fmt<FMT>::kRowBytes + tok0 * 2, St::kScale, &sm.full[slot]);
-        bulk_g2s(st + St::kV, hp + plane + tok0 * Fmt<FMT>::kRowBytes, St::kCode, &sm.full[slot]);
-        bulk_g2s(st + St::kVs, hp + plane + P * Fmt<FMT>::kRowBytes + tok0 * 2, St::kScale, &sm.full[slot]);
-      }
-    }
-  }
-  // drain: wait (bounded) for every issued copy so none lands after exit
-  for (int k = (gi > NS ? gi - NS : 0); k < gi; ++k) {
-    const int slot = k % NS;
-    if (!mbar_wait(&sm.full[slot], (k / NS) & 1)) {
-      atomicOr(p.err, kErrWaitTimeout);
-      break;
-    }
-  }
-}
-
-// Q prologue: q rows of this (b, kvh) -> fp32 in smem (rotated for TQ3) ->
-// per-warp A fragments (hi / lo fp16).
-template <int FMT>
-__device__ __forceinline__ void load_q_frags(const DecodeParams& p, const SmemLayout& sm, int b, int kvh,
-                                             uint32_t (&qa)[16][4]) {
+// ============================================================== q prep
+// Per (request, kv head): the QK warps' MMA A fragments of the group's query
+// rows for both formats -- FP8 pages score against q, TQ3 pages against
+// q' = R q (signs, then H, then 1/16).  Rows 0-7 of the A tile hold fp16(q_h)
+// of heads h = 0..G-1, rows 8-15 the fp16 residual q_h - fp16(q_h), so the
+// two halves of the S accumulator add up to an fp32-accurate score.
+// Fragment layout: [(b*Hkv + kvh)*2 + fmt][lane 32][k-step 16][4 regs], with
+// lane (g, c) = (lane/4, lane%4) covering dims 64c + 4j .. 64c + 4j + 3.
+__global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
+  __shared__ __align__(16) float qs[2][kMaxGroup][kHeadDim];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x % p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // warp w loads head w (zero when w >= G)
-  {
-    float x[8];
-    const int hq = kvh * p.G + warp;
-    if (warp < p.G) {
-      const size_t off = (static_cast<size_t>(b) * p.Hq + hq) * kHeadDim + 8 * lane;
-      if (p.q_bf16) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  if (warp >= kMaxGroup) {
+    // fused single-token append: warp 8 writes the K row, warp 9 the V row
+    if (p.append) {
+      const int kv = warp - kMaxGroup;
+      const uint32_t dst = p.dest[b];
+      const int slot = static_cast<int>(dst >> 8), pos = static_cast<int>(dst & 0xff);
+      uint8_t* plane = p.fp8_layer + static_cast<int64_t>(slot) * p.fp8_page_bytes +
+                       static_cast<int64_t>(kvh) * 2 * (p.P * (kHeadDim + 2)) + kv * (p.P * (kHeadDim + 2));
+      fp8_append_row(kv ? p.v : p.k, (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim, p.kv_bf16, plane, p.P, kv,
+                     pos, lane);
+    }
+    __syncthreads();
+    return;
+  }
+  float x[8];
+  if (warp < p.G) {
+    const size_t off = (static_cast<size_t>(b) * p.Hq + kvh * p.G + warp) * kHeadDim + 8 * lane;
+    if (p.q_bf16) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(b2[i]);
-          x[2 * i] = f.x;
-          x[2 * i + 1] = f.y;
-        }
-      } else {
-        const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + off);
-        const float4 a = f4[0], c = f4[1];
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
       }
     } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.f;
+      const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + off);
+      const float4 a = f4[0], c = f4[1];
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
     }
-    if (FMT == 1) {   // q' = R q = H (signs .* q) / 16
+  } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
-#pragma unroll
-      for (int hs = 1; hs < 8; hs <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if ((i & hs) == 0) {
-            const float a = x[i], c = x[i + hs];
-            x[i] = a + c;
-            x[i + hs] = a - c;
-          }
-      }
-#pragma unroll
-      for (int lm = 1; lm < 32; lm <<= 1) {
-        const bool upper = (lane & lm) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float o = __shfl_xor_sync(kFull, x[i], lm);
-          x[i] = upper ? (o - x[i]) : (x[i] + o);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] *= (1.0f / 16.0f);
-    }
-    float4* dst = reinterpret_cast<float4*>(sm.qs + warp * kHeadDim + 8 * lane);
-    dst[0] = make_float4(x[0], x[1], x[2], x[3]);
-    dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+    for (int i = 0; i < 8; ++i) x[i] = 0.f;
   }
-  named_bar(1, kConsumerWarps * 32);
-  const int g = lane >> 2, c = lane & 3;
-  const float* qr = sm.qs + g * kHeadDim + 64 * c;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float4 v = *reinterpret_cast<const float4*>(qr + 4 * j);
+  for (int i = 0; i < 8; ++i) qs[0][warp][8 * lane + i] = x[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
+#pragma unroll
+  for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & hs) == 0) {
+        const float a = x[i], c = x[i + hs];
+        x[i] = a + c;
+        x[i + hs] = a - c;
+      }
+  }
+#pragma unroll
+  for (int lm = 1; lm < 32; lm <<= 1) {
+    const bool upper = (lane & lm) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float o = __shfl_xor_sync(kFull, x[i], lm);
+      x[i] = upper ? (o - x[i]) : (x[i] + o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) qs[1][warp][8 * lane + i] = x[i] * (1.0f / 16.0f);
+  __syncthreads();
+  if (threadIdx.x >= 256) return;
+  const int fmt = threadIdx.x >> 7, L = (threadIdx.x >> 2) & 31, j0 = 4 * (threadIdx.x & 3);
+  const int g = L >> 2, c = L & 3;
+  uint4* dst = reinterpret_cast<uint4*>(p.qfrag + ((static_cast<size_t>(b) * p.Hkv + kvh) * 2 + fmt) * 2048 +
+                                        L * 64 + 4 * j0);
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const float4 v = *reinterpret_cast<const float4*>(&qs[fmt][g][64 * c + 4 * (j0 + jj)]);
     const float vv[4] = {v.x, v.y, v.z, v.w};
     float hi[4], lo[4];
 #pragma unroll
@@ -502,242 +396,385 @@ __device__ __forceinline__ void load_q_frags(const DecodeParams& p, const SmemLa
       hi[i] = __half2float(__float2half_rn(vv[i]));
       lo[i] = vv[i] - hi[i];
     }
-    qa[j][0] = pack_half2(hi[0], hi[1]);
-    qa[j][1] = pack_half2(lo[0], lo[1]);
-    qa[j][2] = pack_half2(hi[2], hi[3]);
-    qa[j][3] = pack_half2(lo[2], lo[3]);
+    dst[jj] = make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
+                         pack_half2(lo[2], lo[3]));
   }
 }
 
-// S tile (two n8 halves) for one 16-token tile: FP8 K
-__device__ __forceinline__ void qk_fp8(const uint8_t* kbase, int g, int c, const uint32_t (&qa)[16][4],
-                                       float (&s0)[4], float (&s1)[4]) {
-  float a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
+// ============================================================== decode
+// Persistent, warp-specialised partial-attention kernel; one CTA per SM.
+//   warps 0-7   QK warps: S = Q K^T on mma.sync m16n8k16 (A = q rows from the
+//               q-prep fragments, B = K dequantised in registers), online
+//               softmax in log2 units with a lazy rescale, P (scaled by the V
+//               row scales, fp16) handed to the partner PV warp.
+//   warps 8-15  PV warps: O^T += V^T P^T (A = V dequantised in registers).
+// Page blocks (64 tokens of one page and kv head: K codes, K scales, V codes,
+// V scales) move by four cp.async.bulk copies into a ring of kNumStages
+// shared-memory slots whose mbarriers count the bytes.  There is no producer
+// warp: thread 0 issues the first kNumStages blocks and afterwards the last
+// of the eight warps to release a slot (found with a shared-memory counter)
+// issues the block kNumStages further on into it.
+// Pair i = (QK warp i, PV warp 8+i) owns tokens [16 (i%4), +16) of every
+// block whose index has the parity i/4.  The host cut the launch's global
+// sequence of page blocks into one contiguous, cost-balanced piece list per
+// CTA; each (CTA, group) piece is padded to an even number of blocks so every
+// pair sees its last block of the piece, and ends in a merge of the 8 pairs'
+// states into one partial state (m, l, o) per q head.
+constexpr int kPairs = 8;
+constexpr int kDecWarps = 2 * kPairs;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kNumStages = 4;
+constexpr int kSlotBytes = 2 * (kStageTokens * kHeadDim + kStageTokens * 2);   // one FP8 block
+
+template <int FMT>
+struct Blk {                                     // a 64-token block of format FMT in a slot
+  static constexpr int kRow = FMT == 0 ? kHeadDim : 3 * kHeadDim / 8;     // K row bytes
+  static constexpr int kCode = kStageTokens * kRow;
+  static constexpr int kK = 0, kKs = kCode, kV = kCode + 2 * kStageTokens, kVs = 2 * kCode + 2 * kStageTokens;
+};
+
+struct PSlot {                                   // P handoff QK warp -> PV warp
+  uint2 pb[32];                                  // B fragments (fp16 P' pairs) per lane
+  float alpha[kMaxGroup];                        // O rescale factor per head
+  int32_t rescale;
+  int32_t pad[7];
+};
+
+struct DecSmem {
+  uint8_t* ring;
+  PSlot* pslot;                                  // [kPairs][2]
+  float* epi_o;                                  // [kPairs][kMaxGroup][D]
+  float* epi_m;                                  // [kPairs][kMaxGroup]
+  float* epi_l;
+  uint64_t* full;                                // [kNumStages]
+  uint64_t* pfull;                               // [kPairs][2]
+  uint64_t* pempty;                              // [kPairs][2]
+  int* release;                                  // [kNumStages] warps done with the slot
+  int* issued;                                   // blocks issued so far (for the abort drain)
+  int* abort_flag;
+};
+constexpr int kDecSmemRing = kNumStages * kSlotBytes;
+constexpr int kDecSmemP = kPairs * 2 * static_cast<int>(sizeof(PSlot));
+constexpr int kDecSmemEpi = kPairs * kMaxGroup * kHeadDim * 4 + 2 * kPairs * kMaxGroup * 4;
+constexpr int kDecSmemBars = (kNumStages + 4 * kPairs) * 8 + (kNumStages + 2) * 4 + 8;
+constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemP + kDecSmemEpi + kDecSmemBars;
+
+__device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
+  DecSmem s;
+  s.ring = base;
+  s.pslot = reinterpret_cast<PSlot*>(base + kDecSmemRing);
+  s.epi_o = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemP);
+  s.epi_m = s.epi_o + kPairs * kMaxGroup * kHeadDim;
+  s.epi_l = s.epi_m + kPairs * kMaxGroup;
+  s.full = reinterpret_cast<uint64_t*>(s.epi_l + kPairs * kMaxGroup);
+  s.pfull = s.full + kNumStages;
+  s.pempty = s.pfull + 2 * kPairs;
+  s.release = reinterpret_cast<int*>(s.pempty + 2 * kPairs);
+  s.issued = s.release + kNumStages;
+  s.abort_flag = s.issued + 1;
+  return s;
+}
+
+__device__ __forceinline__ bool aborted(const DecSmem& sm) {
+  return *reinterpret_cast<volatile int*>(sm.abort_flag) != 0;
+}
+// Bounded wait that also gives up once any warp of the CTA has aborted.
+__device__ __forceinline__ bool dec_wait(const DecSmem& sm, uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31) == 0) {
+      if (aborted(sm)) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        atomicOr(err, kErrWaitTimeout);
+        *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Walks one CTA's blocks in order: (segment, page entry, 64-token block).
+struct BlockCursor {
+  int seg, seg_end;
+  int k, total;         // block index within the padded piece, padded count
+  int nreal;
+  int e, blk;           // page entry and block within it
+  Segment sg;
+  Group gr;
+  __device__ void load_seg(const DecodeParams& p) {
+    sg = p.segs[seg];
+    gr = p.groups[sg.group];
+    nreal = sg.nstages;
+    total = sg.nstages + (sg.nstages & 1);
+    k = 0;
+    e = sg.entry;
+    blk = sg.blk;
+  }
+  __device__ bool start(const DecodeParams& p, int s0, int s1) {
+    seg = s0;
+    seg_end = s1;
+    if (seg >= seg_end) return false;
+    load_seg(p);
+    return true;
+  }
+  // tokens of the current block (0 for the padding block)
+  __device__ int nvalid(const DecodeParams& p) const {
+    if (k >= nreal) return 0;
+    return min(kStageTokens, p.entries[e].nvalid - kStageTokens * blk);
+  }
+  __device__ bool first() const { return k == 0; }
+  __device__ bool last() const { return k >= total - 2; }
+  __device__ bool next(const DecodeParams& p) {
+    if (k < nreal) {
+      const int nb = (p.entries[e].nvalid + kStageTokens - 1) / kStageTokens;
+      if (++blk == nb) {
+        blk = 0;
+        ++e;
+      }
+    }
+    if (++k < total) return true;
+    if (++seg >= seg_end) return false;
+    load_seg(p);
+    return true;
+  }
+};
+
+// Issue block `gi` (the cursor's current block) into its slot: four bulk
+// copies, or a plain arrive for a padding block.  Returns false on a bad plan.
+__device__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const BlockCursor& cur, int gi) {
+  const int slot = gi % kNumStages;
+  const int nv = cur.nvalid(p);
+  atomicMax(sm.issued, gi + 1);
+  if (nv <= 0) {
+    mbar_arrive(&sm.full[slot]);   // padding block: the phase completes without bytes
+    return true;
+  }
+  const PageEntry pe = p.entries[cur.e];
+  const int fmt = cur.gr.fmt;
+  const int nslots = fmt ? p.tq3_slots : p.fp8_slots;
+  // a request's last page may still be receiving its new token from the
+  // preceding (q-prep + append) kernel: copy it only after that kernel is done
+  if (pe.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (pe.slot < 0 || pe.slot >= nslots) {
+    atomicOr(p.err, kErrBadPlan);
+    *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+    mbar_arrive(&sm.full[slot]);
+    return false;
+  }
+  const int row = fmt ? 3 * kHeadDim / 8 : kHeadDim;
+  const int plane = p.P * (row + 2);
+  const uint8_t* hp = (fmt ? p.tq3_layer : p.fp8_layer) +
+                      static_cast<int64_t>(pe.slot) * (fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
+                      static_cast<int64_t>(cur.gr.kvh) * 2 * plane;
+  const int tok0 = kStageTokens * cur.blk;
+  const uint32_t code = kStageTokens * row;
+  uint8_t* st = sm.ring + slot * kSlotBytes;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(&sm.full[slot], 2 * (code + 2 * kStageTokens));
+  bulk_g2s(st, hp + tok0 * row, code, &sm.full[slot]);
+  bulk_g2s(st + code, hp + p.P * row + 2 * tok0, 2 * kStageTokens, &sm.full[slot]);
+  bulk_g2s(st + code + 2 * kStageTokens, hp + plane + tok0 * row, code, &sm.full[slot]);
+  bulk_g2s(st + 2 * code + 2 * kStageTokens, hp + plane + p.P * row + 2 * tok0, 2 * kStageTokens,
+           &sm.full[slot]);
+  return true;
+}
+
+// A warp is done with block gi's slot.  The eighth (last) warp to say so issues
+// block gi + kNumStages into the slot; `ahead` is that block's cursor (or
+// !ahead_ok when the CTA has no such block).
+__device__ __forceinline__ void dec_release(const DecodeParams& p, const DecSmem& sm, int gi,
+                                            const BlockCursor& ahead, bool ahead_ok) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    __threadfence_block();
+    const int slot = gi % kNumStages;
+    if (atomicAdd(&sm.release[slot], 1) == 2 * 4 - 1) {
+      sm.release[slot] = 0;
+      __threadfence_block();
+      if (ahead_ok && !aborted(sm)) dec_issue(p, sm, ahead, gi + kNumStages);
+    }
+  }
+}
+
+// S for one 16-token tile (two n8 halves, tokens g and 8+g of the tile as B
+// columns); FP8 K rows are row-major, the thread's 64 dims are 64 bytes.
+__device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint32_t (&qa)[16][4],
+                                           float (&s0)[4], float (&s1)[4]) {
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
-    const uint4 w0 = *reinterpret_cast<const uint4*>(kbase + g * kHeadDim + 64 * c + 16 * q4);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(kbase + (8 + g) * kHeadDim + 64 * c + 16 * q4);
+    const uint4 w0 = *reinterpret_cast<const uint4*>(kt + g * kHeadDim + 64 * c + 16 * q4);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(kt + (8 + g) * kHeadDim + 64 * c + 16 * q4);
     const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w};
     const uint32_t x1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int j = 4 * q4 + i;
-      float(&acc0)[4] = (j & 1) ? a0 : s0;
-      float(&acc1)[4] = (j & 1) ? a1 : s1;
-      mma16816(acc0, qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(x0[i]),
-               e4m3x2_to_f16x2(x0[i] >> 16));
-      mma16816(acc1, qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(x1[i]),
-               e4m3x2_to_f16x2(x1[i] >> 16));
+      mma16816(s0, qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(x0[i]), e4m3x2_to_f16x2(x0[i] >> 16));
+      mma16816(s1, qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(x1[i]), e4m3x2_to_f16x2(x1[i] >> 16));
     }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    s0[i] += a0[i];
-    s1[i] += a1[i];
   }
 }
 
-// S tile for TQ3 K: row (u*8 + g) units 2c, 2c+1 (24 bytes at 24c)
-__device__ __forceinline__ void qk_tq3(const uint8_t* kbase, int g, int c, const uint32_t (&qa)[16][4],
-                                       const Lut& lut, float (&s0)[4], float (&s1)[4]) {
-  float a0[4] = {0, 0, 0, 0}, a1[4] = {0, 0, 0, 0};
-  const uint8_t* r0 = kbase + g * 96 + 24 * c;
-  const uint8_t* r1 = kbase + (8 + g) * 96 + 24 * c;
-  const uint2 p0 = *reinterpret_cast<const uint2*>(r0), p1 = *reinterpret_cast<const uint2*>(r0 + 8),
-              p2 = *reinterpret_cast<const uint2*>(r0 + 16);
-  const uint2 q0 = *reinterpret_cast<const uint2*>(r1), q1 = *reinterpret_cast<const uint2*>(r1 + 8),
-              q2 = *reinterpret_cast<const uint2*>(r1 + 16);
-  const uint32_t wa[6] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y};
-  const uint32_t wb[6] = {q0.x, q0.y, q1.x, q1.y, q2.x, q2.y};
+// S for one 16-token tile of TQ3 K: row (8u + g) units 2c, 2c+1 (24 bytes at 24c).
+__device__ __forceinline__ void dec_qk_tq3(const uint8_t* kt, int g, int c, const uint32_t (&qa)[16][4],
+                                           const Lut& lut, float (&s0)[4], float (&s1)[4]) {
+  const uint8_t* r0 = kt + g * 96 + 24 * c;
+  const uint8_t* r1 = kt + (8 + g) * 96 + 24 * c;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
+    const uint2 a01 = *reinterpret_cast<const uint2*>(r0 + 12 * half);
+    const uint32_t a2 = *reinterpret_cast<const uint32_t*>(r0 + 12 * half + 8);
+    const uint2 b01 = *reinterpret_cast<const uint2*>(r1 + 12 * half);
+    const uint32_t b2 = *reinterpret_cast<const uint32_t*>(r1 + 12 * half + 8);
     uint32_t sa[8], sb[8];
-    tq3_unit_selectors(wa[3 * half], wa[3 * half + 1], wa[3 * half + 2], sa);
-    tq3_unit_selectors(wb[3 * half], wb[3 * half + 1], wb[3 * half + 2], sb);
+    tq3_unit_selectors(a01.x, a01.y, a2, sa);
+    tq3_unit_selectors(b01.x, b01.y, b2, sb);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int j = 8 * half + s;
-      uint32_t b0, b1, d0, d1;
-      tq3_lookup4(sa[s], lut, b0, b1);
-      tq3_lookup4(sb[s], lut, d0, d1);
-      float(&acc0)[4] = (j & 1) ? a0 : s0;
-      float(&acc1)[4] = (j & 1) ? a1 : s1;
-      mma16816(acc0, qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
-      mma16816(acc1, qa[j][0], qa[j][1], qa[j][2], qa[j][3], d0, d1);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    s0[i] += a0[i];
-    s1[i] += a1[i];
-  }
-}
-
-// O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32)
-__device__ __forceinline__ void pv_fp8(const uint8_t* vbase, int g, int c, uint32_t pb0, uint32_t pb1,
-                                       float (&o)[16][4]) {
-  const uint8_t* ra = vbase + c * (2 * kHeadDim) + 64 * g;
-  const uint8_t* rb = vbase + (c + 4) * (2 * kHeadDim) + 64 * g;
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    const uint4 wa = *reinterpret_cast<const uint4*>(ra + 16 * q4);
-    const uint4 wb = *reinterpret_cast<const uint4*>(rb + 16 * q4);
-    const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w};
-    const uint32_t xb[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int mt = 4 * q4 + i;
-      mma16816(o[mt], e4m3x2_to_f16x2(xa[i]), e4m3x2_to_f16x2(xa[i] >> 16), e4m3x2_to_f16x2(xb[i]),
-               e4m3x2_to_f16x2(xb[i] >> 16), pb0, pb1);
+      uint32_t x0, x1, y0, y1;
+      tq3_lookup4(sa[s], lut, x0, x1);
+      tq3_lookup4(sb[s], lut, y0, y1);
+      mma16816(s0, qa[j][0], qa[j][1], qa[j][2], qa[j][3], x0, x1);
+      mma16816(s1, qa[j][0], qa[j][1], qa[j][2], qa[j][3], y0, y1);
     }
   }
 }
 
-// O^T += V^T P^T for TQ3 V: pair-rows c and c+4, units 2g, 2g+1 (24 bytes at 24g)
-__device__ __forceinline__ void pv_tq3(const uint8_t* vbase, int g, int c, uint32_t pb0, uint32_t pb1,
-                                       const Lut& lut, float (&o)[16][4]) {
-  const uint8_t* ra = vbase + c * 192 + 24 * g;
-  const uint8_t* rb = vbase + (c + 4) * 192 + 24 * g;
-  const uint2 p0 = *reinterpret_cast<const uint2*>(ra), p1 = *reinterpret_cast<const uint2*>(ra + 8),
-              p2 = *reinterpret_cast<const uint2*>(ra + 16);
-  const uint2 q0 = *reinterpret_cast<const uint2*>(rb), q1 = *reinterpret_cast<const uint2*>(rb + 8),
-              q2 = *reinterpret_cast<const uint2*>(rb + 16);
-  const uint32_t wa[6] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y};
-  const uint32_t wb[6] = {q0.x, q0.y, q1.x, q1.y, q2.x, q2.y};
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint32_t sa[8], sb[8];
-    tq3_unit_selectors(wa[3 * half], wa[3 * half + 1], wa[3 * half + 2], sa);
-    tq3_unit_selectors(wb[3 * half], wb[3 * half + 1], wb[3 * half + 2], sb);
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t a0, a1, a2, a3;
-      tq3_lookup4(sa[s], lut, a0, a1);
-      tq3_lookup4(sb[s], lut, a2, a3);
-      mma16816(o[8 * half + s], a0, a1, a2, a3, pb0, pb1);
-    }
-  }
-}
-
-template <int FMT>
-__device__ void consumer_loop(const DecodeParams& p, const SmemLayout& sm, int first, int last) {
-  using St = Stage<FMT>;
-  constexpr int NS = Fmt<FMT>::kStages;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
+  const int pair = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int grp = warp >> 2, tile = warp & 3;
+  const int grp = pair >> 2, tile = pair & 3;
   const Lut lut = p.lut;
+  const float scale = p.score_scale;
   const int G = p.G;
   uint32_t qa[16][4];
-  float o[16][4];
+  float m_run = -INFINITY, l_run = 0.f;
+  int pj = 0;
+  bool dep_waited = false;
+  BlockCursor cur, ahead;
   int gi = 0;
-  for (int ci = first; ci < last; ++ci) {
-    const int cid = p.cta_chunks[ci];
-    const Chunk ch = p.chunks[cid];
-    load_q_frags<FMT>(p, sm, ch.b, ch.kvh, qa);
+  if (!cur.start(p, s0, s1)) return;
+  bool ahead_ok = ahead.start(p, s0, s1);
+  for (int k = 0; k < kNumStages && ahead_ok; ++k) ahead_ok = ahead.next(p);
+  do {
+    const int fmt = cur.gr.fmt;
+    if (cur.first()) {
+      if (!dep_waited) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        dep_waited = true;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.qfrag + ((static_cast<size_t>(cur.gr.b) * p.Hkv + cur.gr.kvh) * 2 + fmt) * 2048 + lane * 64);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;   // head g, per-thread partial l
-    bool aborted = false;
-    for (int e = 0; e < ch.nentry && !aborted; ++e) {
-      const PageEntry pe = p.entries[ch.entry0 + e];
-      const int nb = entry_blocks(pe);
-      for (int blk = 0; blk < nb; ++blk, ++gi) {
-        if ((gi & 1) != grp) continue;
-        const int slot = gi % NS;
-        if (!mbar_wait(&sm.full[slot], (gi / NS) & 1)) {
-          atomicOr(p.err, kErrWaitTimeout);
-          *sm.abort_flag = 1;
-          aborted = true;
-          break;
+      for (int j = 0; j < 16; ++j) {
+        const uint4 v = src[j];
+        qa[j][0] = v.x;
+        qa[j][1] = v.y;
+        qa[j][2] = v.z;
+        qa[j][3] = v.w;
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+    if ((gi & 1) == grp) {
+      const int slot = gi % kNumStages;
+      const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
+      const int nv = cur.nvalid(p) - kTileTokens * tile;
+      if (ok && nv > 0) {
+        const uint8_t* st = sm.ring + slot * kSlotBytes;
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const __half2* ks;
+        const __half2* vs;
+        if (fmt == 0) {
+          dec_qk_fp8(st + Blk<0>::kK + tile * kTileTokens * kHeadDim, g, c, qa, sa, sb);
+          ks = reinterpret_cast<const __half2*>(st + Blk<0>::kKs + tile * kTileTokens * 2);
+          vs = reinterpret_cast<const __half2*>(st + Blk<0>::kVs + tile * kTileTokens * 2);
+        } else {
+          dec_qk_tq3(st + Blk<1>::kK + tile * kTileTokens * 96, g, c, qa, lut, sa, sb);
+          ks = reinterpret_cast<const __half2*>(st + Blk<1>::kKs + tile * kTileTokens * 2);
+          vs = reinterpret_cast<const __half2*>(st + Blk<1>::kVs + tile * kTileTokens * 2);
         }
-        const int base = blk * kStageTokens + tile * kTileTokens;   // first token of this tile in the page
-        const int nv = pe.nvalid - base;
-        if (nv > 0) {
-          const uint8_t* st = sm.ring + slot * St::kBytes;
-          float s0[4] = {0, 0, 0, 0}, s1[4] = {0, 0, 0, 0};
-          if (FMT == 0)
-            qk_fp8(st + St::kK + tile * kTileTokens * kHeadDim, g, c, qa, s0, s1);
-          else
-            qk_tq3(st + St::kK + tile * kTileTokens * 96, g, c, qa, lut, s0, s1);
-          // scores of head g at tokens 2c, 2c+1, 8+2c, 9+2c (log2 units)
-          const __half2* ks = reinterpret_cast<const __half2*>(st + St::kKs + tile * kTileTokens * 2);
-          const __half2* vs = reinterpret_cast<const __half2*>(st + St::kVs + tile * kTileTokens * 2);
-          const float2 k01 = __half22float2(ks[c]), k89 = __half22float2(ks[4 + c]);
-          const float2 v01 = __half22float2(vs[c]), v89 = __half22float2(vs[4 + c]);
-          float sc[4];
-          sc[0] = (s0[0] + s0[2]) * k01.x * p.score_scale;
-          sc[1] = (s0[1] + s0[3]) * k01.y * p.score_scale;
-          sc[2] = (s1[0] + s1[2]) * k89.x * p.score_scale;
-          sc[3] = (s1[1] + s1[3]) * k89.y * p.score_scale;
-          const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (tk[i] >= nv || g >= G) sc[i] = -INFINITY;
-          float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-          mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
-          mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-          const bool need = mt > m_run + kLazyRescale;
-          if (__any_sync(kFull, need)) {
-            const float m_new = fmaxf(m_run, mt);
-            const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-            m_run = m_new;
-            l_run *= alpha;
-            const float a0 = __shfl_sync(kFull, alpha, (2 * c) * 4);
-            const float a1 = __shfl_sync(kFull, alpha, (2 * c + 1) * 4);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              o[i][0] *= a0;
-              o[i][1] *= a1;
-              o[i][2] *= a0;
-              o[i][3] *= a1;
-            }
-          }
-          float pr[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) pr[i] = (sc[i] == -INFINITY) ? 0.f : exp2f(sc[i] - m_run);
-          l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-          const float vsc = FMT == 0 ? kFp8PScale : 1.0f;
-          const uint32_t pb0 = pack_half2(pr[0] * v01.x * vsc, pr[1] * v01.y * vsc);
-          const uint32_t pb1 = pack_half2(pr[2] * v89.x * vsc, pr[3] * v89.y * vsc);
-          if (FMT == 0)
-            pv_fp8(st + St::kV + tile * (kTileTokens / 2) * (2 * kHeadDim), g, c, pb0, pb1, o);
-          else
-            pv_tq3(st + St::kV + tile * (kTileTokens / 2) * 192, g, c, pb0, pb1, lut, o);
+        const float2 k01 = __half22float2(ks[c]), k89 = __half22float2(ks[4 + c]);
+        const float2 v01 = __half22float2(vs[c]), v89 = __half22float2(vs[4 + c]);
+        float sc[4];
+        sc[0] = (sa[0] + sa[2]) * (k01.x * scale);
+        sc[1] = (sa[1] + sa[3]) * (k01.y * scale);
+        sc[2] = (sb[0] + sb[2]) * (k89.x * scale);
+        sc[3] = (sb[1] + sb[3]) * (k89.y * scale);
+        if (g >= G) {
+          sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;
+        } else if (nv < kTileTokens) {
+          if (2 * c >= nv) sc[0] = -INFINITY;
+          if (2 * c + 1 >= nv) sc[1] = -INFINITY;
+          if (8 + 2 * c >= nv) sc[2] = -INFINITY;
+          if (9 + 2 * c >= nv) sc[3] = -INFINITY;
+        }
+        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+        float alpha = 1.f;
+        const bool rescale = __any_sync(kFull, mt > m_run + kLazyRescale);
+        if (rescale) {
+          const float m_new = fmaxf(m_run, mt);
+          alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        // m_run = -inf only for heads g >= G (all scores -inf): keep p = 0 there
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+        const float p0 = ex2(sc[0] - mref), p1 = ex2(sc[1] - mref), p2 = ex2(sc[2] - mref), p3 = ex2(sc[3] - mref);
+        l_run += (p0 + p1) + (p2 + p3);
+        const float vsc = fmt == 0 ? kFp8PScale : 1.f;
+        const uint2 pb = make_uint2(pack_half2(p0 * (v01.x * vsc), p1 * (v01.y * vsc)),
+                                    pack_half2(p2 * (v89.x * vsc), p3 * (v89.y * vsc)));
+        const int ps = pj & 1;
+        PSlot& slotp = sm.pslot[2 * pair + ps];
+        bool okp = true;
+        if (pj >= 2) okp = dec_wait(sm, &sm.pempty[2 * pair + ps], ((pj >> 1) - 1) & 1, p.err);
+        if (okp) {
+          slotp.pb[lane] = pb;
+          if (c == 0) slotp.alpha[g] = alpha;
+          if (lane == 0) slotp.rescale = rescale ? 1 : 0;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+        if (lane == 0) mbar_arrive(&sm.pfull[2 * pair + ps]);
+        ++pj;
       }
+      dec_release(p, sm, gi, ahead, ahead_ok);
     }
-    // ---- epilogue: merge the 8 warps' states into one partial
-    l_run += __shfl_xor_sync(kFull, l_run, 1);
-    l_run += __shfl_xor_sync(kFull, l_run, 2);
-    if (c == 0) {
-      sm.epi_m[warp * kMaxGroup + g] = m_run;
-      sm.epi_l[warp * kMaxGroup + g] = l_run;
-    }
-    const float osc = FMT == 0 ? 1.0f / kFp8PScale : 1.0f;
-    float* ow = sm.epi_o + warp * kMaxGroup * kHeadDim;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int d = 32 * g + 2 * i;
-      *reinterpret_cast<float2*>(ow + (2 * c) * kHeadDim + d) = make_float2(o[i][0] * osc, o[i][2] * osc);
-      *reinterpret_cast<float2*>(ow + (2 * c + 1) * kHeadDim + d) = make_float2(o[i][1] * osc, o[i][3] * osc);
-    }
-    named_bar(1, kConsumerWarps * 32);
-    {
-      const int d = threadIdx.x;   // 0..255
-      float* dst = p.part + static_cast<size_t>(cid) * G * (2 + kHeadDim);
-      for (int h = 0; h < G; ++h) {
+    if (cur.last() && ((gi & 1) == grp)) {
+      // end of this CTA's piece of the group: publish (m, l) of head g
+      float l = l_run;
+      l += __shfl_xor_sync(kFull, l, 1);
+      l += __shfl_xor_sync(kFull, l, 2);
+      if (c == 0) {
+        sm.epi_m[pair * kMaxGroup + g] = m_run;
+        sm.epi_l[pair * kMaxGroup + g] = l;
+      }
+      named_bar(1, 2 * kPairs * 32);
+      // combine: QK threads take even heads, PV threads odd heads (see dec_pv_warp)
+      const int d = threadIdx.x & 255;
+      const int hbase = (threadIdx.x >> 8);   // 0 for QK warps 0..7
+      float* dst = p.part + static_cast<size_t>(cur.sg.part) * G * (2 + kHeadDim);
+      for (int h = hbase; h < G; h += 2) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
+        for (int w = 0; w < kPairs; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
         float L = 0.f, acc = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
+          for (int w = 0; w < kPairs; ++w) {
             const float mw = sm.epi_m[w * kMaxGroup + h];
-            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
             L += f * sm.epi_l[w * kMaxGroup + h];
             acc += f * sm.epi_o[(w * kMaxGroup + h) * kHeadDim + d];
           }
@@ -748,103 +785,287 @@ __device__ void consumer_loop(const DecodeParams& p, const SmemLayout& sm, int f
           dst[h * (2 + kHeadDim) + 1] = L;
         }
       }
+      named_bar(1, 2 * kPairs * 32);
     }
-    named_bar(1, kConsumerWarps * 32);
-    if (aborted || *reinterpret_cast<volatile int*>(sm.abort_flag)) return;
+    ++gi;
+    if (ahead_ok) ahead_ok = ahead.next(p);
+  } while (cur.next(p));
+}
+
+// O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32)
+__device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, uint2 pb, float (&o)[16][4]) {
+  const uint8_t* ra = vt + c * (2 * kHeadDim) + 64 * g;
+  const uint8_t* rb = vt + (c + 4) * (2 * kHeadDim) + 64 * g;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint4 wa = *reinterpret_cast<const uint4*>(ra + 16 * q4);
+    const uint4 wb = *reinterpret_cast<const uint4*>(rb + 16 * q4);
+    const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t xb[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      mma16816(o[4 * q4 + i], e4m3x2_to_f16x2(xa[i]), e4m3x2_to_f16x2(xa[i] >> 16), e4m3x2_to_f16x2(xb[i]),
+               e4m3x2_to_f16x2(xb[i] >> 16), pb.x, pb.y);
   }
 }
 
-template <int FMT>
-__device__ void decode_body(const DecodeParams& p, const SmemLayout& sm, int first, int last) {
-  const int warp = threadIdx.x >> 5;
-  if (warp == kConsumerWarps) {
-    if ((threadIdx.x & 31) == 0) producer_loop<FMT>(p, sm, first, last);
-  } else {
-    consumer_loop<FMT>(p, sm, first, last);
+// O^T += V^T P^T for TQ3 V: pair-rows c and c+4, units 2g, 2g+1 (24 bytes at 24g)
+__device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint2 pb, const Lut& lut,
+                                           float (&o)[16][4]) {
+  const uint8_t* ra = vt + c * 192 + 24 * g;
+  const uint8_t* rb = vt + (c + 4) * 192 + 24 * g;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint2 a01 = *reinterpret_cast<const uint2*>(ra + 12 * half);
+    const uint32_t a2 = *reinterpret_cast<const uint32_t*>(ra + 12 * half + 8);
+    const uint2 b01 = *reinterpret_cast<const uint2*>(rb + 12 * half);
+    const uint32_t b2 = *reinterpret_cast<const uint32_t*>(rb + 12 * half + 8);
+    uint32_t sa[8], sb[8];
+    tq3_unit_selectors(a01.x, a01.y, a2, sa);
+    tq3_unit_selectors(b01.x, b01.y, b2, sb);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t x0, x1, y0, y1;
+      tq3_lookup4(sa[s], lut, x0, x1);
+      tq3_lookup4(sb[s], lut, y0, y1);
+      mma16816(o[8 * half + s], x0, x1, y0, y1, pb.x, pb.y);
+    }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mkv_decode_kernel(DecodeParams p) {
+__device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
+  const int pair = (threadIdx.x >> 5) - kPairs, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int grp = pair >> 2, tile = pair & 3;
+  const Lut lut = p.lut;
+  const int G = p.G;
+  float o[16][4];
+  int pj = 0;
+  BlockCursor cur, ahead;
+  int gi = 0;
+  if (!cur.start(p, s0, s1)) return;
+  bool ahead_ok = ahead.start(p, s0, s1);
+  for (int k = 0; k < kNumStages && ahead_ok; ++k) ahead_ok = ahead.next(p);
+  do {
+    const int fmt = cur.gr.fmt;
+    if (cur.first()) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+    if ((gi & 1) == grp) {
+      const int slot = gi % kNumStages;
+      const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
+      const int nv = cur.nvalid(p) - kTileTokens * tile;
+      if (ok && nv > 0) {
+        const int ps = pj & 1;
+        const PSlot& slotp = sm.pslot[2 * pair + ps];
+        const bool okp = dec_wait(sm, &sm.pfull[2 * pair + ps], (pj >> 1) & 1, p.err);
+        const uint2 pb = slotp.pb[lane];
+        const int rescale = slotp.rescale;
+        float a0 = 1.f, a1 = 1.f;
+        if (rescale) {
+          a0 = slotp.alpha[2 * c];
+          a1 = slotp.alpha[2 * c + 1];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.pempty[2 * pair + ps]);
+        ++pj;
+        if (okp) {
+          if (rescale) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              o[i][0] *= a0;
+              o[i][1] *= a1;
+              o[i][2] *= a0;
+              o[i][3] *= a1;
+            }
+          }
+          const uint8_t* st = sm.ring + slot * kSlotBytes;
+          if (fmt == 0)
+            dec_pv_fp8(st + Blk<0>::kV + tile * (kTileTokens / 2) * (2 * kHeadDim), g, c, pb, o);
+          else
+            dec_pv_tq3(st + Blk<1>::kV + tile * (kTileTokens / 2) * 192, g, c, pb, lut, o);
+        }
+      }
+      dec_release(p, sm, gi, ahead, ahead_ok);
+    }
+    if (cur.last() && ((gi & 1) == grp)) {
+      const float osc = fmt == 0 ? 1.f / kFp8PScale : 1.f;
+      float* ow = sm.epi_o + pair * kMaxGroup * kHeadDim;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int d = 32 * g + 2 * i;
+        if (2 * c < G)
+          *reinterpret_cast<float2*>(ow + (2 * c) * kHeadDim + d) = make_float2(o[i][0] * osc, o[i][2] * osc);
+        if (2 * c + 1 < G)
+          *reinterpret_cast<float2*>(ow + (2 * c + 1) * kHeadDim + d) = make_float2(o[i][1] * osc, o[i][3] * osc);
+      }
+      named_bar(1, 2 * kPairs * 32);
+      const int d = threadIdx.x & 255;
+      float* dst = p.part + static_cast<size_t>(cur.sg.part) * G * (2 + kHeadDim);
+      for (int h = 1; h < G; h += 2) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kPairs; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
+        float L = 0.f, acc = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kPairs; ++w) {
+            const float mw = sm.epi_m[w * kMaxGroup + h];
+            const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+            L += f * sm.epi_l[w * kMaxGroup + h];
+            acc += f * sm.epi_o[(w * kMaxGroup + h) * kHeadDim + d];
+          }
+        }
+        dst[h * (2 + kHeadDim) + 2 + d] = acc;
+        if (d == 0) {
+          dst[h * (2 + kHeadDim)] = M;
+          dst[h * (2 + kHeadDim) + 1] = L;
+        }
+      }
+      named_bar(1, 2 * kPairs * 32);
+    }
+    ++gi;
+    if (ahead_ok) ahead_ok = ahead.next(p);
+  } while (cur.next(p));
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const SmemLayout sm = carve(smem);
-  const int cta = blockIdx.x;
-  const int first = p.cta_start[cta], last = p.cta_start[cta + 1];
-  const bool fp8 = cta < p.n_ctas_fp8;
+  const DecSmem sm = dec_carve(smem);
+  const int s0 = p.cta_seg[blockIdx.x], s1 = p.cta_seg[blockIdx.x + 1];
+  // the merge kernel that follows waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
-    const int ns = fp8 ? Fmt<0>::kStages : Fmt<1>::kStages;
-    for (int i = 0; i < ns; ++i) {
+    for (int i = 0; i < kNumStages; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], 4);
+      sm.release[i] = 0;
     }
+    for (int i = 0; i < 2 * kPairs; ++i) {
+      mbar_init(&sm.pfull[i], 1);
+      mbar_init(&sm.pempty[i], 1);
+    }
+    *sm.issued = 0;
     *sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the first kNumStages blocks
+    BlockCursor cur;
+    if (cur.start(p, s0, s1)) {
+      int gi = 0;
+      do {
+        if (!dec_issue(p, sm, cur, gi)) break;
+      } while (++gi < kNumStages && cur.next(p));
+    }
   }
   __syncthreads();
-  if (first >= last) return;
-  if (fp8)
-    decode_body<0>(p, sm, first, last);
-  else
-    decode_body<1>(p, sm, first, last);
+  if (s0 < s1) {
+    if (threadIdx.x < kPairs * 32)
+      dec_qk_warp(p, sm, s0, s1);
+    else
+      dec_pv_warp(p, sm, s0, s1);
+  }
+  // every issued block is consumed on the normal path; after an abort, wait
+  // (bounded) for copies still in flight before the CTA exits
+  __syncthreads();
+  if (threadIdx.x == 0 && aborted(sm)) {
+    const int n = *sm.issued;
+    for (int k = n > kNumStages ? n - kNumStages : 0; k < n; ++k) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&sm.full[k % kNumStages], (k / kNumStages) & 1))
+        if (clock64() - t0 > kWaitCycles) break;
+    }
+  }
 }
 
 // ============================================================== merge
-// One block (256 threads, thread = dim) per (b, kvh).  TQ3 partials merge in
-// the rotated domain, R^T is applied once (FWHT across the block), then the
-// FP8 partials join; out = O / L, lse = (M + log2 L) ln 2.
+// One block (256 threads, thread = dim) per (request, kv head, q head).  The
+// partial states' (m, l) are staged in shared memory; the TQ3 partials merge
+// in the rotated domain, R^T is applied once (FWHT across the block, then the
+// signs and 1/16), the FP8 partials join, and out = O / L,
+// lse = (M + log2 L) ln 2.
+constexpr int kMergeStage = 256;   // partial states staged per pass
+
+// Merge partial states [first, first + count) of head h at dim d.
+__device__ __forceinline__ void merge_range(const float* part, int stride, int h, int first, int count, int d,
+                                            float* sm_m, float* sm_l, float& Mout, float& Lout, float& oout) {
+  float M = -INFINITY;
+  for (int base = 0; base < count; base += kMergeStage) {
+    const int cnt = min(kMergeStage, count - base);
+    __syncthreads();
+    if (d < cnt) {
+      const float* pj = part + static_cast<size_t>(first + base + d) * stride + h * (2 + kHeadDim);
+      sm_m[d] = pj[0];
+      sm_l[d] = pj[1];
+    }
+    __syncthreads();
+    for (int j = 0; j < cnt; ++j) M = fmaxf(M, sm_m[j]);
+  }
+  float L = 0.f, o = 0.f;
+  if (M != -INFINITY) {
+    for (int base = 0; base < count; base += kMergeStage) {
+      const int cnt = min(kMergeStage, count - base);
+      __syncthreads();
+      if (d < cnt) {
+        const float* pj = part + static_cast<size_t>(first + base + d) * stride + h * (2 + kHeadDim);
+        const float mj = pj[0];
+        sm_m[d] = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
+        sm_l[d] = pj[1];
+      }
+      __syncthreads();
+      const float* col = part + static_cast<size_t>(first + base) * stride + h * (2 + kHeadDim) + 2 + d;
+      int j = 0;
+      for (; j + 4 <= cnt; j += 4) {
+        const float v0 = col[static_cast<size_t>(j) * stride], v1 = col[static_cast<size_t>(j + 1) * stride];
+        const float v2 = col[static_cast<size_t>(j + 2) * stride], v3 = col[static_cast<size_t>(j + 3) * stride];
+        o += sm_m[j] * v0 + sm_m[j + 1] * v1 + sm_m[j + 2] * v2 + sm_m[j + 3] * v3;
+      }
+      for (; j < cnt; ++j) o += sm_m[j] * col[static_cast<size_t>(j) * stride];
+      for (int jj = 0; jj < cnt; ++jj) L += sm_m[jj] * sm_l[jj];
+    }
+  }
+  Mout = M;
+  Lout = L;
+  oout = o;
+}
+
 __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   __shared__ float xs[kHeadDim];
-  const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x % p.Hkv;
-  const MergeDesc md = p.desc[blockIdx.x];
+  __shared__ float sm_m[kMergeStage], sm_l[kMergeStage];
+  // launched as a programmatic dependent of the decode kernel: wait for its
+  // partial states before reading them
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int h = blockIdx.x % p.G;
+  const int bk = blockIdx.x / p.G;
+  const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  const MergeDesc md = p.desc[bk];
   const int d = threadIdx.x, lane = d & 31;
   const int stride = p.G * (2 + kHeadDim);
-  for (int h = 0; h < p.G; ++h) {
-    // TQ3 partials
-    float Ms = -INFINITY, Ls = 0.f, os = 0.f;
-    for (int j = 0; j < md.tq3_count; ++j) Ms = fmaxf(Ms, p.part[(md.tq3_first + j) * stride + h * (2 + kHeadDim)]);
-    if (Ms != -INFINITY) {
-      for (int j = 0; j < md.tq3_count; ++j) {
-        const float* pj = p.part + (md.tq3_first + j) * stride + h * (2 + kHeadDim);
-        const float f = (pj[0] == -INFINITY) ? 0.f : exp2f(pj[0] - Ms);
-        Ls += f * pj[1];
-        os += f * pj[2 + d];
-      }
-    }
-    // o_S = R^T o'_S = signs .* (H o'_S) / 16: butterflies over lane bits by
-    // shuffle, over warp bits through shared memory
+  float Ms, Ls, os, Mf, Lf, of;
+  merge_range(p.part, stride, h, md.tq3_first, md.tq3_count, d, sm_m, sm_l, Ms, Ls, os);
+  // o_S = R^T o'_S = signs .* (H o'_S) / 16: butterflies over lane bits by
+  // shuffle, over warp bits through shared memory
 #pragma unroll
-    for (int lm = 1; lm < 32; lm <<= 1) {
-      const float other = __shfl_xor_sync(kFull, os, lm);
-      os = (lane & lm) ? (other - os) : (os + other);
-    }
-    for (int bm = 32; bm < kHeadDim; bm <<= 1) {
-      __syncthreads();
-      xs[d] = os;
-      __syncthreads();
-      const float other = xs[d ^ bm];
-      os = (d & bm) ? (other - os) : (os + other);
-    }
-    os *= (1.0f / 16.0f);
-    if (sign_neg(p.signs, d)) os = -os;
-    // FP8 partials
-    float Mf = -INFINITY, Lf = 0.f, of = 0.f;
-    for (int j = 0; j < md.fp8_count; ++j) Mf = fmaxf(Mf, p.part[(md.fp8_first + j) * stride + h * (2 + kHeadDim)]);
-    if (Mf != -INFINITY) {
-      for (int j = 0; j < md.fp8_count; ++j) {
-        const float* pj = p.part + (md.fp8_first + j) * stride + h * (2 + kHeadDim);
-        const float f = (pj[0] == -INFINITY) ? 0.f : exp2f(pj[0] - Mf);
-        Lf += f * pj[1];
-        of += f * pj[2 + d];
-      }
-    }
-    const float M = fmaxf(Ms, Mf);
-    const float fs = (Ms == -INFINITY) ? 0.f : exp2f(Ms - M);
-    const float ff = (Mf == -INFINITY) ? 0.f : exp2f(Mf - M);
-    const float L = Ls * fs + Lf * ff;
-    const int hq = kvh * p.G + h;
-    p.out[(static_cast<size_t>(b) * p.Hq + hq) * kHeadDim + d] = (os * fs + of * ff) / L;
-    if (d == 0) p.lse[b * p.Hq + hq] = (M + log2f(L)) * 0.69314718055994530942f;
-    __syncthreads();
+  for (int lm = 1; lm < 32; lm <<= 1) {
+    const float other = __shfl_xor_sync(kFull, os, lm);
+    os = (lane & lm) ? (other - os) : (os + other);
   }
+  for (int bm = 32; bm < kHeadDim; bm <<= 1) {
+    __syncthreads();
+    xs[d] = os;
+    __syncthreads();
+    const float other = xs[d ^ bm];
+    os = (d & bm) ? (other - os) : (os + other);
+  }
+  os *= (1.0f / 16.0f);
+  if (sign_neg(p.signs, d)) os = -os;
+  merge_range(p.part, stride, h, md.fp8_first, md.fp8_count, d, sm_m, sm_l, Mf, Lf, of);
+  const float M = fmaxf(Ms, Mf);
+  const float fs = (Ms == -INFINITY) ? 0.f : exp2f(Ms - M);
+  const float ff = (Mf == -INFINITY) ? 0.f : exp2f(Mf - M);
+  const float L = Ls * fs + Lf * ff;
+  const int hq = kvh * p.G + h;
+  p.out[(static_cast<size_t>(b) * p.Hq + hq) * kHeadDim + d] = (os * fs + of * ff) / L;
+  if (d == 0) p.lse[b * p.Hq + hq] = (M + log2f(L)) * 0.69314718055994530942f;
 }
 
 }  // namespace
@@ -863,7 +1084,7 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-size_t decode_smem_bytes() { return kSmemBytes; }
+size_t decode_smem_bytes() { return kDecSmemBytes; }
 
 // Fixed scratch for the allocation-free decode entry point: 8 MiB of partial
 // states, compiled into the library so a call never needs to allocate.
@@ -891,23 +1112,48 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
   *bytes = kNoallocScratchBytes;
   return cudaSuccess;
 }
-int decode_threads() { return kThreads; }
+int decode_threads() { return kDecThreads; }
+
+cudaError_t launch_qprep(const QprepParams& p, cudaStream_t s) {
+  if (p.n * p.Hkv > 0) mkv_qprep_kernel<<<p.n * p.Hkv, 320, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (p.n_ctas > 0) mkv_decode_kernel<<<p.n_ctas, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  if (p.n_ctas <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_ctas);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mkv_decode_kernel, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
-  if (p.n * p.Hkv > 0) mkv_merge_kernel<<<p.n * p.Hkv, kHeadDim, 0, s>>>(p);
-  return cudaGetLastError();
+  if (p.n * p.Hkv <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n * p.Hkv * p.G);
+  cfg.blockDim = dim3(kHeadDim);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mkv_merge_kernel, p);
 }
 
 }  // namespace mkv

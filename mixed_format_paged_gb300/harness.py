@@ -88,5 +88,10 @@ class Stepper:
             self.pool.demote(dem_s, dem_p)
 
     def layer(self, layer: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, out=None, lse=None):
+        """Append the step's token and decode, in one library call."""
+        return self.pool.append_decode(layer, self.ids, k, v, q, out, lse)
+
+    def layer_separate(self, layer: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, out=None, lse=None):
+        """The same through the two separate calls (append, then decode)."""
         self.pool.append(layer, self.ids, [1] * len(self.ids), k, v)
         return self.pool.decode(layer, self.ids, q, out, lse)

@@ -86,6 +86,19 @@ class MkvPool:
         B.mkv_decode_attention(self.handle, layer, seq_ids, q, dtype, out, lse, self._stream(stream))
         return out, lse
 
+    def append_decode(self, layer: int, seq_ids, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
+                      out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+        """Append each sequence's newest token (k, v: [n, H_kv, d]) and decode (q: [n, H_q, d])."""
+        n = len(seq_ids)
+        if out is None:
+            out = torch.empty((n, self.num_q_heads, self.head_dim), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((n, self.num_q_heads), dtype=torch.float32, device=q.device)
+        kvd = B.MKV_BF16 if k.dtype == torch.bfloat16 else B.MKV_F32
+        qd = B.MKV_BF16 if q.dtype == torch.bfloat16 else B.MKV_F32
+        B.mkv_append_decode(self.handle, layer, seq_ids, k, v, kvd, q, qd, out, lse, self._stream(stream))
+        return out, lse
+
     def stats(self):
         return B.mkv_pool_stats(self.handle)
 

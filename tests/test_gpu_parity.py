@@ -309,3 +309,49 @@ def test_full_size_sampled(mkv, name):
     s = pool.stats()
     assert s.live_tokens == sum(st.lengths)
     assert s.workspace_bytes < 64 * 2 ** 20
+
+
+# ------------------------------------------------------------------ fused append + decode
+def test_append_decode_matches_separate_calls(mkv):
+    """mkv_append_decode (append fused into the q-preparation kernel) gives the
+    same page bytes and the same outputs as mkv_append_tokens + mkv_decode_attention."""
+    g = torch.Generator().manual_seed(21)
+    pools = [_small_pool(mkv, P=64, layers=2, fp8=64, tq3=64, maxp=24, seed=77) for _ in range(2)]
+    lens = [64 * 6 + 63, 64 * 3, 1]
+    data = [(torch.randn(n, 4, 256, generator=g).to(torch.bfloat16), torch.randn(n, 4, 256, generator=g).to(torch.bfloat16))
+            for n in lens]
+    for pool in pools:
+        for r, n in enumerate(lens):
+            pool.extend([r], [n])
+            for layer in range(2):
+                pool.append(layer, [r], [n], data[r][0].to(DEV), data[r][1].to(DEV))
+        pool.demote([0, 0, 0], [1, 2, 3])
+    ids = [0, 1, 2]
+    for step in range(3):
+        k = torch.randn(3, 4, 256, generator=g).to(torch.bfloat16).to(DEV)
+        v = torch.randn(3, 4, 256, generator=g).to(torch.bfloat16).to(DEV)
+        q = torch.randn(3, 24, 256, generator=g).to(torch.bfloat16).to(DEV)
+        outs = []
+        for i, pool in enumerate(pools):
+            pool.extend(ids, [1, 1, 1])
+            res = []
+            for layer in range(2):
+                if i == 0:
+                    o, l_ = pool.append_decode(layer, ids, k, v, q)
+                else:
+                    pool.append(layer, ids, [1, 1, 1], k, v)
+                    o, l_ = pool.decode(layer, ids, q)
+                res.append((o.clone(), l_.clone()))
+            outs.append(res)
+        torch.cuda.synchronize()
+        for layer in range(2):
+            assert torch.equal(outs[0][layer][0], outs[1][layer][0])
+            assert torch.equal(outs[0][layer][1], outs[1][layer][1])
+    for layer in range(2):
+        for r in ids:
+            a = _export(pools[0], layer, r)
+            b = _export(pools[1], layer, r)
+            assert all(np.array_equal(x[1], y[1]) for x, y in zip(a, b))
+    _check_decode(pools[0], 1, ids, q.float(), outs[0][1][0], outs[0][1][1], 77)
+    for pool in pools:
+        pool.check_device_errors()
