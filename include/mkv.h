@@ -242,6 +242,16 @@ mkv_status mkv_append_decode(mkv_pool* pool, int32_t layer, int32_t n, const int
                              const void* v, mkv_dtype kv_dtype, const void* q, mkv_dtype q_dtype, float* out,
                              float* lse, mkv_stream_t stream);
 
+/* Materialising export: dequantise pages [page0, page0 + npages) of one
+ * sequence and layer into dense rows -- the "materializing quality profile"
+ * of the pages (abstract, mlsanity.com) as a debugging and quality tool, not
+ * part of decode.  FP8 rows give x_hat (exact), TQ3 rows x_tilde = R^T (sigma
+ * L[code]) (fp32 FWHT).  k_out, v_out: device [npages * P, H_kv, d] of
+ * out_dtype (MKV_F32 or MKV_BF16, round-to-nearest-even); token slots past
+ * the sequence length are written as 0.  Enqueued on `stream`. */
+mkv_status mkv_dequantize_pages(mkv_pool* pool, int32_t layer, int32_t seq, int32_t page0, int32_t npages,
+                                void* k_out, void* v_out, mkv_dtype out_dtype, mkv_stream_t stream);
+
 /* ---------------------------------------------------------------- inspection */
 
 /* Live pages and bytes per tier and KV bytes per live token (the pages'

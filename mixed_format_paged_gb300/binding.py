@@ -27,7 +27,7 @@ MKV_POOL_HOST_ONLY = 1
 EXPORTED = [
     "mkv_pool_required_bytes", "mkv_pool_create", "mkv_pool_destroy", "mkv_seq_extend", "mkv_seq_release",
     "mkv_seq_info", "mkv_page_info", "mkv_append_tokens", "mkv_set_tier", "mkv_demote_pages",
-    "mkv_decode_attention", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
+    "mkv_decode_attention", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
     "mkv_plan_decode", "mkv_check_device_errors", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
 ]
 
@@ -86,6 +86,7 @@ def lib() -> ctypes.CDLL:
         "mkv_decode_attention": [P, I32, I32, I32P, P, ctypes.c_int, P, P, P],
         "mkv_decode_attention_noalloc": [P, I32, I32, I32P, P, ctypes.c_int, P, P, P],
         "mkv_append_decode": [P, I32, I32, I32P, P, P, ctypes.c_int, P, ctypes.c_int, P, P, P],
+        "mkv_dequantize_pages": [P, I32, I32, I32, I32, P, P, ctypes.c_int, P],
         "mkv_pool_stats": [P, ctypes.POINTER(Stats)],
         "mkv_export_page": [P, I32, I32, I32, P, ctypes.c_size_t, I32P, I32P, P],
         "mkv_rotation_signs": [P, ctypes.POINTER(ctypes.c_int8), I32],
@@ -218,6 +219,12 @@ def mkv_append_decode(pool, layer: int, seq_ids, k, v, kv_dtype: int, q, q_dtype
     a, n = _i32(seq_ids)
     check(lib().mkv_append_decode(pool, layer, n, a, _ptr(k), _ptr(v), kv_dtype, _ptr(q), q_dtype, _ptr(out),
                                   _ptr(lse), _stream(stream)), "mkv_append_decode")
+
+
+def mkv_dequantize_pages(pool, layer: int, seq: int, page0: int, npages: int, k_out, v_out, out_dtype: int,
+                         stream=None) -> None:
+    check(lib().mkv_dequantize_pages(pool, layer, seq, page0, npages, _ptr(k_out), _ptr(v_out), out_dtype,
+                                     _stream(stream)), "mkv_dequantize_pages")
 
 
 def mkv_pool_stats(pool) -> Stats:

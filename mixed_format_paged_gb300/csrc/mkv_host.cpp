@@ -1016,6 +1016,51 @@ mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_
   return MKV_OK;
 }
 
+mkv_status mkv_dequantize_pages(mkv_pool* p, int32_t layer, int32_t seq, int32_t page0, int32_t npages,
+                                void* k_out, void* v_out, mkv_dtype out_dtype, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (!valid_seq(p, seq)) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence id %d out of range", seq);
+  if (out_dtype != MKV_F32 && out_dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  const SeqRec& s = p->seqs[seq];
+  if (npages < 0 || page0 < 0 || page0 + npages > int(s.pages.size()))
+    return fail(MKV_ERR_INVALID_ARGUMENT, "page range [%d, %d) outside the sequence's %zu pages", page0,
+                page0 + npages, s.pages.size());
+  if (npages == 0) return MKV_OK;
+  if (!k_out || !v_out) return fail(MKV_ERR_INVALID_ARGUMENT, "k_out/v_out is NULL");
+  if (npages > p->demote_cap) return fail(MKV_ERR_CAPACITY, "at most %d pages per call", p->demote_cap);
+  if (p->host_only) return MKV_OK;
+  const int P = p->cfg.page_size;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  mkv_status r = staging_acquire(p->st_demote);
+  if (r != MKV_OK) return r;
+  int2* h = static_cast<int2*>(p->st_demote.host);
+  for (int i = 0; i < npages; ++i) {
+    const PageRec& rec = s.pages[page0 + i];
+    const int nv = std::min(P, s.len - (page0 + i) * P);
+    h[i].x = rec.slot;
+    h[i].y = (int(rec.tier) << 16) | nv;
+  }
+  if ((r = staging_upload(p->st_demote, p->demote_region, size_t(npages) * sizeof(int2), st)) != MKV_OK) return r;
+  DequantParams dq{};
+  dq.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  dq.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
+  dq.fp8_page_bytes = p->fp8_page_bytes;
+  dq.tq3_page_bytes = p->tq3_page_bytes;
+  dq.pages = p->demote_region;
+  dq.npages = npages;
+  dq.Hkv = p->cfg.num_kv_heads;
+  dq.P = P;
+  dq.out_bf16 = out_dtype == MKV_BF16;
+  dq.k_out = k_out;
+  dq.v_out = v_out;
+  std::memcpy(dq.signs, p->signs, sizeof dq.signs);
+  std::memcpy(dq.level, codebook().level, sizeof dq.level);
+  const cudaError_t e = launch_dequant(dq, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dequantise launch");
+  return MKV_OK;
+}
+
 mkv_status mkv_pool_stats(const mkv_pool* p, mkv_stats* out) {
   if (!p || !out) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
   mkv_stats st{};

@@ -130,6 +130,19 @@ struct DemoteParams {
   float thr[7];
 };
 
+struct DequantParams {
+  const uint8_t* fp8_layer;
+  const uint8_t* tq3_layer;
+  int64_t fp8_page_bytes, tq3_page_bytes;
+  const int2* pages;               // (slot, tier << 16 | valid tokens) per page
+  int32_t npages, Hkv, P;
+  int32_t out_bf16;
+  void* k_out;                     // [npages * P, Hkv, D]
+  void* v_out;
+  uint64_t signs[4];
+  float level[8];
+};
+
 // Kernel launchers (mkv_kernels.cu).  Return cudaGetLastError() of the launch.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
@@ -138,6 +151,7 @@ cudaError_t launch_qprep(const QprepParams& p, cudaStream_t s);
 // the preceding q-prep kernel finishes; its QK warps wait for q-prep's output.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
+cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s);
 size_t decode_smem_bytes();
 // Device address and size of the library's fixed partial-state scratch (see
 // mkv_decode_attention_noalloc).  The first call on a device looks the address

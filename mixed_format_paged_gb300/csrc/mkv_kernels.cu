@@ -306,6 +306,123 @@ __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
   for (int t = threadIdx.x; t < P; t += blockDim.x) osc[t] = sig[t];
 }
 
+// ============================================================== dequantise (export)
+// One warp per (token, kv head, K|V) row of the requested pages: FP8 rows are
+// e4m3 * s; TQ3 rows are unpacked from their 12-byte units, scaled by the
+// stored levels and sigma, and rotated back (H, then the signs, then 1/16).
+__global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int P = p.P;
+  const int nrows = p.npages * P * p.Hkv * 2;
+  if (warp >= nrows) return;
+  const int kv = warp & 1;
+  const int h = (warp >> 1) % p.Hkv;
+  const int t_all = (warp >> 1) / p.Hkv;          // token index in the output
+  const int pg = t_all / P, t = t_all % P;
+  const int2 pe = p.pages[pg];
+  const int tier = pe.y >> 16, nvalid = pe.y & 0xffff;
+  float x[8];
+  if (t >= nvalid) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = 0.f;
+  } else if (tier != 3) {
+    const int plane = P * (kHeadDim + 2);
+    const uint8_t* base = p.fp8_layer + static_cast<int64_t>(pe.x) * p.fp8_page_bytes +
+                          static_cast<int64_t>(h) * 2 * plane + kv * plane;
+    const float s = __half2float(reinterpret_cast<const __half*>(base + P * kHeadDim)[t]);
+    uint8_t b[8];
+    if (kv == 0) {
+      const uint2 w = *reinterpret_cast<const uint2*>(base + t * kHeadDim + 8 * lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        b[i] = (w.x >> (8 * i)) & 0xff;
+        b[4 + i] = (w.y >> (8 * i)) & 0xff;
+      }
+    } else {
+      const uint8_t* r = base + (t >> 1) * (2 * kHeadDim) + (t & 1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = r[2 * (8 * lane + i)];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t f2 = e4m3x2_to_f16x2(b[2 * i] | (b[2 * i + 1] << 8));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f2));
+      x[2 * i] = f.x * s;
+      x[2 * i + 1] = f.y * s;
+    }
+  } else {
+    const int plane = P * (3 * kHeadDim / 8 + 2);
+    const uint8_t* base = p.tq3_layer + static_cast<int64_t>(pe.x) * p.tq3_page_bytes +
+                          static_cast<int64_t>(h) * 2 * plane + kv * plane;
+    const float sg = __half2float(reinterpret_cast<const __half*>(base + P * (3 * kHeadDim / 8))[t]);
+    // lane holds dims 8*lane .. 8*lane+7
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = 8 * lane + i;
+      int unit, e;
+      if (kv == 0) {
+        unit = t * (kHeadDim / 32) + j / 32;
+        e = j % 32;
+      } else {
+        unit = (t >> 1) * (kHeadDim / 16) + j / 16;
+        e = 2 * (j % 16) + (t & 1);
+      }
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(base + 12 * unit);
+      int code;
+      if (e < 24) {
+        code = (w[e >> 3] >> (4 * (e & 7))) & 7;
+      } else {
+        const int i2 = e - 24;
+        code = ((w[0] >> (4 * i2 + 3)) & 1) | (((w[1] >> (4 * i2 + 3)) & 1) << 1) | (((w[2] >> (4 * i2 + 3)) & 1) << 2);
+      }
+      x[i] = sg * p.level[code];
+    }
+    // x <- H x (natural order), then signs and 1/16
+#pragma unroll
+    for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((i & hs) == 0) {
+          const float a = x[i], c = x[i + hs];
+          x[i] = a + c;
+          x[i + hs] = a - c;
+        }
+    }
+#pragma unroll
+    for (int lm = 1; lm < 32; lm <<= 1) {
+      const bool upper = (lane & lm) != 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_xor_sync(kFull, x[i], lm);
+        x[i] = upper ? (o - x[i]) : (x[i] + o);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[i] *= (1.0f / 16.0f);
+      if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
+    }
+  }
+  const size_t off = (static_cast<size_t>(t_all) * p.Hkv + h) * kHeadDim + 8 * lane;
+  void* dst = kv ? p.v_out : p.k_out;
+  if (p.out_bf16) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(dst) + off;
+    uint4 pk;
+    __nv_bfloat162 q0 = __floats2bfloat162_rn(x[0], x[1]), q1 = __floats2bfloat162_rn(x[2], x[3]);
+    __nv_bfloat162 q2 = __floats2bfloat162_rn(x[4], x[5]), q3 = __floats2bfloat162_rn(x[6], x[7]);
+    pk.x = *reinterpret_cast<uint32_t*>(&q0);
+    pk.y = *reinterpret_cast<uint32_t*>(&q1);
+    pk.z = *reinterpret_cast<uint32_t*>(&q2);
+    pk.w = *reinterpret_cast<uint32_t*>(&q3);
+    *reinterpret_cast<uint4*>(o) = pk;
+  } else {
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(dst) + off);
+    o[0] = make_float4(x[0], x[1], x[2], x[3]);
+    o[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+}
+
 // ============================================================== q prep
 // Per (request, kv head): the QK warps' MMA A fragments of the group's query
 // rows for both formats -- FP8 pages score against q, TQ3 pages against
@@ -501,63 +618,67 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Walks one CTA's blocks in order: (segment, page entry, 64-token block).
-struct BlockCursor {
-  int seg, seg_end;
-  int k, total;         // block index within the padded piece, padded count
-  int nreal;
-  int e, blk;           // page entry and block within it
+// Finds blocks of one CTA's piece list by global block index gi.  Pieces are
+// padded to an even block count, so a warp can step through one parity
+// (gi += 2) and index a block directly: every page before a group's last has
+// P/64 blocks.
+struct PieceCursor {
+  int si, s1;           // current piece, end of the CTA's list
+  int pstart, ptotal;   // first global block index of the piece, padded block count
+  int bshift;           // log2(blocks per page)
   Segment sg;
   Group gr;
-  __device__ void load_seg(const DecodeParams& p) {
-    sg = p.segs[seg];
+  __device__ void load(const DecodeParams& p) {
+    sg = p.segs[si];
     gr = p.groups[sg.group];
-    nreal = sg.nstages;
-    total = sg.nstages + (sg.nstages & 1);
-    k = 0;
-    e = sg.entry;
-    blk = sg.blk;
+    ptotal = sg.nstages + (sg.nstages & 1);
   }
-  __device__ bool start(const DecodeParams& p, int s0, int s1) {
-    seg = s0;
-    seg_end = s1;
-    if (seg >= seg_end) return false;
-    load_seg(p);
+  __device__ bool start(const DecodeParams& p, int s0, int s1_) {
+    si = s0;
+    s1 = s1_;
+    pstart = 0;
+    bshift = p.P == 128 ? 1 : 0;
+    if (si >= s1) return false;
+    load(p);
     return true;
   }
-  // tokens of the current block (0 for the padding block)
-  __device__ int nvalid(const DecodeParams& p) const {
-    if (k >= nreal) return 0;
-    return min(kStageTokens, p.entries[e].nvalid - kStageTokens * blk);
-  }
-  __device__ bool first() const { return k == 0; }
-  __device__ bool last() const { return k >= total - 2; }
-  __device__ bool next(const DecodeParams& p) {
-    if (k < nreal) {
-      const int nb = (p.entries[e].nvalid + kStageTokens - 1) / kStageTokens;
-      if (++blk == nb) {
-        blk = 0;
-        ++e;
-      }
+  // move forward to the piece holding block gi; false past the end
+  __device__ bool seek(const DecodeParams& p, int gi) {
+    while (gi >= pstart + ptotal) {
+      pstart += ptotal;
+      if (++si >= s1) return false;
+      load(p);
     }
-    if (++k < total) return true;
-    if (++seg >= seg_end) return false;
-    load_seg(p);
     return true;
+  }
+  // page entry and block within the page of piece block k < nstages
+  __device__ void locate(int k, int& e, int& blk) const {
+    const int b = sg.blk + k;
+    e = sg.entry + (b >> bshift);
+    blk = b & ((1 << bshift) - 1);
+  }
+  // tokens of piece block k (0 for the padding block)
+  __device__ int nvalid(const DecodeParams& p, int k) const {
+    if (k >= sg.nstages) return 0;
+    int e, blk;
+    locate(k, e, blk);
+    return min(kStageTokens, p.entries[e].nvalid - kStageTokens * blk);
   }
 };
 
-// Issue block `gi` (the cursor's current block) into its slot: four bulk
-// copies, or a plain arrive for a padding block.  Returns false on a bad plan.
-__device__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const BlockCursor& cur, int gi) {
+// Issue global block gi (cursor positioned on its piece) into its slot: four
+// bulk copies, or a plain arrive for a padding block.  False on a bad plan.
+__device__ __noinline__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const PieceCursor& cur, int gi) {
   const int slot = gi % kNumStages;
-  const int nv = cur.nvalid(p);
+  const int k = gi - cur.pstart;
   atomicMax(sm.issued, gi + 1);
-  if (nv <= 0) {
+  if (k >= cur.sg.nstages) {
     mbar_arrive(&sm.full[slot]);   // padding block: the phase completes without bytes
     return true;
   }
-  const PageEntry pe = p.entries[cur.e];
+  int e, blk;
+  cur.locate(k, e, blk);
+  const PageEntry pe = p.entries[e];
   const int fmt = cur.gr.fmt;
   const int nslots = fmt ? p.tq3_slots : p.fp8_slots;
   // a request's last page may still be receiving its new token from the
@@ -574,7 +695,7 @@ __device__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const BlockC
   const uint8_t* hp = (fmt ? p.tq3_layer : p.fp8_layer) +
                       static_cast<int64_t>(pe.slot) * (fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
                       static_cast<int64_t>(cur.gr.kvh) * 2 * plane;
-  const int tok0 = kStageTokens * cur.blk;
+  const int tok0 = kStageTokens * blk;
   const uint32_t code = kStageTokens * row;
   uint8_t* st = sm.ring + slot * kSlotBytes;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -587,11 +708,15 @@ __device__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const BlockC
   return true;
 }
 
+// Issue block gi + kNumStages if it exists (cursor positioned at or before it).
+__device__ __noinline__ void dec_issue_ahead(const DecodeParams& p, const DecSmem& sm, PieceCursor cur, int gi) {
+  if (cur.seek(p, gi + kNumStages)) dec_issue(p, sm, cur, gi + kNumStages);
+}
+
 // A warp is done with block gi's slot.  The eighth (last) warp to say so issues
-// block gi + kNumStages into the slot; `ahead` is that block's cursor (or
-// !ahead_ok when the CTA has no such block).
+// block gi + kNumStages into the slot.
 __device__ __forceinline__ void dec_release(const DecodeParams& p, const DecSmem& sm, int gi,
-                                            const BlockCursor& ahead, bool ahead_ok) {
+                                            const PieceCursor& cur) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) {
     __threadfence_block();
@@ -599,7 +724,7 @@ __device__ __forceinline__ void dec_release(const DecodeParams& p, const DecSmem
     if (atomicAdd(&sm.release[slot], 1) == 2 * 4 - 1) {
       sm.release[slot] = 0;
       __threadfence_block();
-      if (ahead_ok && !aborted(sm)) dec_issue(p, sm, ahead, gi + kNumStages);
+      if (!aborted(sm)) dec_issue_ahead(p, sm, cur, gi);
     }
   }
 }
@@ -660,14 +785,12 @@ __device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
   float m_run = -INFINITY, l_run = 0.f;
   int pj = 0;
   bool dep_waited = false;
-  BlockCursor cur, ahead;
-  int gi = 0;
+  PieceCursor cur;
   if (!cur.start(p, s0, s1)) return;
-  bool ahead_ok = ahead.start(p, s0, s1);
-  for (int k = 0; k < kNumStages && ahead_ok; ++k) ahead_ok = ahead.next(p);
-  do {
+  for (int gi = grp; cur.seek(p, gi); gi += 2) {
     const int fmt = cur.gr.fmt;
-    if (cur.first()) {
+    const int kb = gi - cur.pstart;
+    if (kb < 2) {
       if (!dep_waited) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         dep_waited = true;
@@ -685,10 +808,10 @@ __device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
       m_run = -INFINITY;
       l_run = 0.f;
     }
-    if ((gi & 1) == grp) {
+    {
       const int slot = gi % kNumStages;
       const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
-      const int nv = cur.nvalid(p) - kTileTokens * tile;
+      const int nv = cur.nvalid(p, kb) - kTileTokens * tile;
       if (ok && nv > 0) {
         const uint8_t* st = sm.ring + slot * kSlotBytes;
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -749,9 +872,9 @@ __device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
         if (lane == 0) mbar_arrive(&sm.pfull[2 * pair + ps]);
         ++pj;
       }
-      dec_release(p, sm, gi, ahead, ahead_ok);
+      dec_release(p, sm, gi, cur);
     }
-    if (cur.last() && ((gi & 1) == grp)) {
+    if (kb >= cur.ptotal - 2) {
       // end of this CTA's piece of the group: publish (m, l) of head g
       float l = l_run;
       l += __shfl_xor_sync(kFull, l, 1);
@@ -787,9 +910,7 @@ __device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
       }
       named_bar(1, 2 * kPairs * 32);
     }
-    ++gi;
-    if (ahead_ok) ahead_ok = ahead.next(p);
-  } while (cur.next(p));
+  }
 }
 
 // O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32)
@@ -841,21 +962,19 @@ __device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
   const int G = p.G;
   float o[16][4];
   int pj = 0;
-  BlockCursor cur, ahead;
-  int gi = 0;
+  PieceCursor cur;
   if (!cur.start(p, s0, s1)) return;
-  bool ahead_ok = ahead.start(p, s0, s1);
-  for (int k = 0; k < kNumStages && ahead_ok; ++k) ahead_ok = ahead.next(p);
-  do {
+  for (int gi = grp; cur.seek(p, gi); gi += 2) {
     const int fmt = cur.gr.fmt;
-    if (cur.first()) {
+    const int kb = gi - cur.pstart;
+    if (kb < 2) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
-    if ((gi & 1) == grp) {
+    {
       const int slot = gi % kNumStages;
       const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
-      const int nv = cur.nvalid(p) - kTileTokens * tile;
+      const int nv = cur.nvalid(p, kb) - kTileTokens * tile;
       if (ok && nv > 0) {
         const int ps = pj & 1;
         const PSlot& slotp = sm.pslot[2 * pair + ps];
@@ -887,9 +1006,9 @@ __device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
             dec_pv_tq3(st + Blk<1>::kV + tile * (kTileTokens / 2) * 192, g, c, pb, lut, o);
         }
       }
-      dec_release(p, sm, gi, ahead, ahead_ok);
+      dec_release(p, sm, gi, cur);
     }
-    if (cur.last() && ((gi & 1) == grp)) {
+    if (kb >= cur.ptotal - 2) {
       const float osc = fmt == 0 ? 1.f / kFp8PScale : 1.f;
       float* ow = sm.epi_o + pair * kMaxGroup * kHeadDim;
 #pragma unroll
@@ -925,9 +1044,7 @@ __device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
       }
       named_bar(1, 2 * kPairs * 32);
     }
-    ++gi;
-    if (ahead_ok) ahead_ok = ahead.next(p);
-  } while (cur.next(p));
+  }
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams p) {
@@ -949,12 +1066,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     *sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the first kNumStages blocks
-    BlockCursor cur;
+    PieceCursor cur;
     if (cur.start(p, s0, s1)) {
-      int gi = 0;
-      do {
+      for (int gi = 0; gi < kNumStages && cur.seek(p, gi); ++gi)
         if (!dec_issue(p, sm, cur, gi)) break;
-      } while (++gi < kNumStages && cur.next(p));
     }
   }
   __syncthreads();
@@ -1113,6 +1228,12 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
   return cudaSuccess;
 }
 int decode_threads() { return kDecThreads; }
+
+cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
+  const int rows = p.npages * p.P * p.Hkv * 2;
+  if (rows > 0) mkv_dequant_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_qprep(const QprepParams& p, cudaStream_t s) {
   if (p.n * p.Hkv > 0) mkv_qprep_kernel<<<p.n * p.Hkv, 320, 0, s>>>(p);

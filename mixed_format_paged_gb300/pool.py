@@ -99,6 +99,15 @@ class MkvPool:
         B.mkv_append_decode(self.handle, layer, seq_ids, k, v, kvd, q, qd, out, lse, self._stream(stream))
         return out, lse
 
+    def dequantize(self, layer: int, seq: int, page0: int, npages: int, dtype=torch.float32, stream=None):
+        """Dense K, V [npages * P, H_kv, d] of pages [page0, page0 + npages)."""
+        shape = (npages * self.page_size, self.num_kv_heads, self.head_dim)
+        k = torch.empty(shape, dtype=dtype, device=self.buf.device)
+        v = torch.empty(shape, dtype=dtype, device=self.buf.device)
+        od = B.MKV_BF16 if dtype == torch.bfloat16 else B.MKV_F32
+        B.mkv_dequantize_pages(self.handle, layer, seq, page0, npages, k, v, od, self._stream(stream))
+        return k, v
+
     def stats(self):
         return B.mkv_pool_stats(self.handle)
 

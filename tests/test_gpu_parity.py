@@ -182,11 +182,15 @@ def test_decode_mixed_layouts(mkv, P, qdtype):
     torch.cuda.synchronize()
     pool.check_device_errors()
     _check_decode(pool, 0, ids, q.float(), out, lse, 4321)
-    # a sub-batch in another order gives the same rows
+    # a sub-batch in another order gives the same rows (up to the parity
+    # tolerance: another batch is split differently, and P is rounded to fp16
+    # relative to each split's running max)
     out2, lse2 = pool.decode(0, [5, 2], q[[5, 2]].to(DEV).contiguous())
     torch.cuda.synchronize()
-    assert torch.allclose(out2, out[[5, 2]], atol=1e-5, rtol=0)
-    assert torch.allclose(lse2, lse[[5, 2]], atol=1e-5, rtol=0)
+    for i, r in enumerate([5, 2]):
+        ref = out[r].double()
+        assert (out2[i].double() - ref).abs().max() <= OUT_TOL * ref.abs().max()
+        assert (lse2[i].double() - lse[r].double()).abs().max() <= LSE_TOL
 
 
 def test_decode_repeatable(mkv):
@@ -355,3 +359,37 @@ def test_append_decode_matches_separate_calls(mkv):
     _check_decode(pools[0], 1, ids, q.float(), outs[0][1][0], outs[0][1][1], 77)
     for pool in pools:
         pool.check_device_errors()
+
+
+# ------------------------------------------------------------------ materialising export
+@pytest.mark.parametrize("P", [64, 128])
+def test_dequantize_pages_matches_oracle(mkv, P):
+    from oracle.paged import TIER_STALE, fp8_page_dequant, tq3_page_dequant
+    g = torch.Generator().manual_seed(31)
+    pool = _small_pool(mkv, P=P, layers=2, seed=555)
+    n = 5 * P + 19
+    pool.extend([0], [n])
+    for layer in range(2):
+        K, V = _kv(n, torch.bfloat16, g)
+        pool.append(layer, [0], [n], K.to(DEV), V.to(DEV))
+    pool.set_tier(0, 4, 2)
+    pool.demote([0, 0, 0], [0, 2, 3])
+    k32, v32 = pool.dequantize(1, 0, 0, 6)
+    kb, vb = pool.dequantize(1, 0, 1, 4, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    pages = _export(pool, 1, 0)
+    for pg, (tier, b, nv) in enumerate(pages):
+        if tier == TIER_STALE:
+            Kr, Vr = tq3_page_dequant(b, P, 4, 256, 555)
+            tol = 1e-5
+        else:
+            Kr, Vr = fp8_page_dequant(b, P, 4, 256)
+            tol = 0.0
+        kg = k32[pg * P:(pg + 1) * P].double().cpu().numpy()
+        vg = v32[pg * P:(pg + 1) * P].double().cpu().numpy()
+        for got, ref in ((kg, Kr), (vg, Vr)):
+            assert np.abs(got[:nv] - ref[:nv]).max() <= tol * max(1.0, np.abs(ref[:nv]).max())
+            assert np.all(got[nv:] == 0.0)
+    # bf16 output is the fp32 result rounded to nearest even
+    assert torch.equal(kb, k32[P:5 * P].to(torch.bfloat16)) and torch.equal(vb, v32[P:5 * P].to(torch.bfloat16))
+    pool.check_device_errors()
