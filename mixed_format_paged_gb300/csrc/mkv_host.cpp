@@ -383,47 +383,55 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
         for (int i = 0; i < count; ++i) g.tokens += entries[first + i].nvalid;
         groups.push_back(g);
       }
-  // block costs and the CTA count
-  double total = 0.0;
-  int64_t nblocks = 0;
-  for (const Group& g : groups)
-    for (int i = 0; i < g.nentry; ++i) {
-      const int nv = entries[g.entry0 + i].nvalid;
-      nblocks += (nv + kStageTokens - 1) / kStageTokens;
-      total += nv * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock * ((nv + kStageTokens - 1) / kStageTokens);
+  // Blocks: an FP8 block is 64 tokens (one page at P = 64, half a page at
+  // P = 128); a TQ3 block is 128 tokens (two pages at P = 64, one at P = 128).
+  // Block list: (group, first entry, block within the entry, tokens).
+  struct Blk {
+    int group, entry, half, tokens;
+  };
+  std::vector<Blk> blocks;
+  for (int gi = 0; gi < int(groups.size()); ++gi) {
+    const Group& g = groups[gi];
+    if (g.fmt == 0) {
+      for (int i = 0; i < g.nentry; ++i) {
+        const int nv = entries[g.entry0 + i].nvalid;
+        for (int h = 0; h * kStageTokens < nv; ++h)
+          blocks.push_back({gi, g.entry0 + i, h, std::min(kStageTokens, nv - h * kStageTokens)});
+      }
+    } else {
+      const int ppb = 128 / P;
+      for (int i = 0; i < g.nentry; i += ppb)
+        blocks.push_back({gi, g.entry0 + i, 0, std::min(ppb, g.nentry - i) * P});
     }
-  const int ncta = int(std::max<int64_t>(1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas),
-                                                                 (nblocks + 1) / 2})));
-  // cut
+  }
+  auto cost = [&](const Blk& b) {
+    return b.tokens * (groups[b.group].fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
+  };
+  double total = 0.0;
+  for (const Blk& b : blocks) total += cost(b);
+  const int ncta = int(std::max<int64_t>(
+      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), (int64_t(blocks.size()) + 1) / 2})));
+  // cut the block sequence into ncta pieces lists of equal cost
   std::vector<Segment> segs;
   std::vector<int32_t> cta_seg(ncta + 1, 0);
   const double per_cta = total / ncta;
   double acc = 0.0;
-  int cur_cta = 0;
-  for (int gi = 0; gi < int(groups.size()); ++gi) {
-    Group& g = groups[gi];
-    bool open = false;
-    for (int i = 0; i < g.nentry; ++i) {
-      const int nv = entries[g.entry0 + i].nvalid;
-      const int nb = (nv + kStageTokens - 1) / kStageTokens;
-      for (int blk = 0; blk < nb; ++blk) {
-        const int tok = std::min(kStageTokens, nv - kStageTokens * blk);
-        int cta = int(acc / per_cta);
-        cta = std::min(std::max(cta, cur_cta), ncta - 1);
-        if (!open || cta != cur_cta) {
-          while (cur_cta < cta) cta_seg[++cur_cta] = int(segs.size());
-          Segment sg{};
-          sg.group = gi;
-          sg.entry = g.entry0 + i;
-          sg.blk = blk;
-          segs.push_back(sg);
-          open = true;
-        }
-        segs.back().nstages += 1;
-        segs.back().tokens += tok;
-        acc += tok * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
-      }
+  int cur_cta = 0, cur_group = -1;
+  for (const Blk& b : blocks) {
+    int cta = int(acc / per_cta);
+    cta = std::min(std::max(cta, cur_cta), ncta - 1);
+    if (b.group != cur_group || cta != cur_cta) {
+      while (cur_cta < cta) cta_seg[++cur_cta] = int(segs.size());
+      Segment sg{};
+      sg.group = b.group;
+      sg.entry = b.entry;
+      sg.blk = b.half;
+      segs.push_back(sg);
+      cur_group = b.group;
     }
+    segs.back().nstages += 1;
+    segs.back().tokens += b.tokens;
+    acc += cost(b);
   }
   while (cur_cta < ncta) cta_seg[++cur_cta] = int(segs.size());
   if (int(segs.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
@@ -450,13 +458,12 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   p->plan_debug.clear();
   for (const Segment& sg : segs) {
     const Group& g = groups[sg.group];
-    int last = sg.entry, blk = sg.blk;
-    for (int k = 1; k < sg.nstages; ++k) {
-      const int nb = (entries[last].nvalid + kStageTokens - 1) / kStageTokens;
-      if (++blk == nb) {
-        blk = 0;
-        ++last;
-      }
+    int last;
+    if (g.fmt == 0) {
+      const int bpp = P / kStageTokens;
+      last = sg.entry + (sg.blk + sg.nstages - 1) / bpp;
+    } else {
+      last = std::min(g.entry0 + g.nentry, sg.entry + sg.nstages * (128 / P)) - 1;
     }
     const int32_t rec[6] = {g.b, g.kvh, g.fmt ? 3 : 1, sg.entry, last - sg.entry + 1, sg.tokens};
     p->plan_debug.insert(p->plan_debug.end(), rec, rec + 6);

@@ -525,30 +525,36 @@ __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
 //               softmax in log2 units with a lazy rescale, P (scaled by the V
 //               row scales, fp16) handed to the partner PV warp.
 //   warps 8-15  PV warps: O^T += V^T P^T (A = V dequantised in registers).
-// Page blocks (64 tokens of one page and kv head: K codes, K scales, V codes,
-// V scales) move by four cp.async.bulk copies into a ring of kNumStages
-// shared-memory slots whose mbarriers count the bytes.  There is no producer
-// warp: thread 0 issues the first kNumStages blocks and afterwards the last
-// of the eight warps to release a slot (found with a shared-memory counter)
-// issues the block kNumStages further on into it.
-// Pair i = (QK warp i, PV warp 8+i) owns tokens [16 (i%4), +16) of every
-// block whose index has the parity i/4.  The host cut the launch's global
-// sequence of page blocks into one contiguous, cost-balanced piece list per
-// CTA; each (CTA, group) piece is padded to an even number of blocks so every
-// pair sees its last block of the piece, and ends in a merge of the 8 pairs'
-// states into one partial state (m, l, o) per q head.
+// Page blocks move by cp.async.bulk copies (K codes, K scales, V codes, V
+// scales of each page) into a ring of kNumStages shared-memory slots whose
+// mbarriers count the bytes.  A TQ3 block is 128 tokens (8 tiles of 16: pair
+// i takes tile i); an FP8 block is 64 tokens (4 tiles: pair i takes tile i%4
+// of the blocks with parity i/4, and FP8 pieces are padded to an even number
+// of blocks so every pair sees the last one).  There is no producer warp:
+// thread 0 issues the first kNumStages blocks and afterwards the last warp to
+// release a slot (found with a shared-memory counter) issues the block
+// kNumStages further on into it.
+// The host cut the launch's global sequence of blocks into one contiguous,
+// cost-balanced piece list per CTA; each (CTA, group) piece ends with the 8
+// pairs' states merged into one partial state (m, l, o) per q head.
 constexpr int kPairs = 8;
 constexpr int kDecWarps = 2 * kPairs;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kNumStages = 4;
-constexpr int kSlotBytes = 2 * (kStageTokens * kHeadDim + kStageTokens * 2);   // one FP8 block
+constexpr int kNumStages = 5;
+constexpr int kFp8Tokens = 64;            // tokens per FP8 block
+constexpr int kTq3Tokens = 128;           // tokens per TQ3 block
+constexpr int kSlotBytes = 2 * (kFp8Tokens * kHeadDim + 2 * kFp8Tokens);   // an FP8 block; a TQ3 block fits
+constexpr uint32_t kWaitHintNs = 20000;   // try_wait suspend hint
 
 template <int FMT>
-struct Blk {                                     // a 64-token block of format FMT in a slot
-  static constexpr int kRow = FMT == 0 ? kHeadDim : 3 * kHeadDim / 8;     // K row bytes
-  static constexpr int kCode = kStageTokens * kRow;
-  static constexpr int kK = 0, kKs = kCode, kV = kCode + 2 * kStageTokens, kVs = 2 * kCode + 2 * kStageTokens;
+struct Blk {                               // a block of format FMT in a slot
+  static constexpr int kTokens = FMT == 0 ? kFp8Tokens : kTq3Tokens;
+  static constexpr int kRow = FMT == 0 ? kHeadDim : 3 * kHeadDim / 8;      // K row bytes
+  static constexpr int kCode = kTokens * kRow;
+  static constexpr int kK = 0, kKs = kCode, kV = kCode + 2 * kTokens, kVs = 2 * kCode + 2 * kTokens;
+  static constexpr int kBytes = 2 * (kCode + 2 * kTokens);
 };
+static_assert(Blk<1>::kBytes <= kSlotBytes, "a TQ3 block must fit a slot");
 
 struct PSlot {                                   // P handoff QK warp -> PV warp
   uint2 pb[32];                                  // B fragments (fp16 P' pairs) per lane
@@ -560,7 +566,7 @@ struct PSlot {                                   // P handoff QK warp -> PV warp
 struct DecSmem {
   uint8_t* ring;
   PSlot* pslot;                                  // [kPairs][2]
-  float* epi_o;                                  // [kPairs][kMaxGroup][D]
+  float* acc;                                    // [4][kMaxGroup][D]: pair sums of a piece's O
   float* epi_m;                                  // [kPairs][kMaxGroup]
   float* epi_l;
   uint64_t* full;                                // [kNumStages]
@@ -572,7 +578,7 @@ struct DecSmem {
 };
 constexpr int kDecSmemRing = kNumStages * kSlotBytes;
 constexpr int kDecSmemP = kPairs * 2 * static_cast<int>(sizeof(PSlot));
-constexpr int kDecSmemEpi = kPairs * kMaxGroup * kHeadDim * 4 + 2 * kPairs * kMaxGroup * 4;
+constexpr int kDecSmemEpi = 4 * kMaxGroup * kHeadDim * 4 + 2 * kPairs * kMaxGroup * 4;
 constexpr int kDecSmemBars = (kNumStages + 4 * kPairs) * 8 + (kNumStages + 2) * 4 + 8;
 constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemP + kDecSmemEpi + kDecSmemBars;
 
@@ -580,8 +586,8 @@ __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   DecSmem s;
   s.ring = base;
   s.pslot = reinterpret_cast<PSlot*>(base + kDecSmemRing);
-  s.epi_o = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemP);
-  s.epi_m = s.epi_o + kPairs * kMaxGroup * kHeadDim;
+  s.acc = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemP);
+  s.epi_m = s.acc + 4 * kMaxGroup * kHeadDim;
   s.epi_l = s.epi_m + kPairs * kMaxGroup;
   s.full = reinterpret_cast<uint64_t*>(s.epi_l + kPairs * kMaxGroup);
   s.pfull = s.full + kNumStages;
@@ -595,19 +601,29 @@ __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
 __device__ __forceinline__ bool aborted(const DecSmem& sm) {
   return *reinterpret_cast<volatile int*>(sm.abort_flag) != 0;
 }
-// Bounded wait that also gives up once any warp of the CTA has aborted.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitHintNs)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (kWaitCycles) that also gives up once any warp of the CTA has
+// aborted; the thread sleeps in try_wait until the phase completes.
 __device__ __forceinline__ bool dec_wait(const DecSmem& sm, uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_hint(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31) == 0) {
-      if (aborted(sm)) return false;
-      if (clock64() - t0 > kWaitCycles) {
-        atomicOr(err, kErrWaitTimeout);
-        *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity)) return true;
+    if (aborted(sm)) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, kErrWaitTimeout);
+      *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+      return false;
     }
   }
 }
@@ -618,93 +634,124 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Finds blocks of one CTA's piece list by global block index gi.  Pieces are
-// padded to an even block count, so a warp can step through one parity
-// (gi += 2) and index a block directly: every page before a group's last has
-// P/64 blocks.
+// One CTA's piece list: piece si covers global blocks [pstart, pstart + ptotal).
+// Holds only the fields the loops use.
 struct PieceCursor {
-  int si, s1;           // current piece, end of the CTA's list
-  int pstart, ptotal;   // first global block index of the piece, padded block count
-  int bshift;           // log2(blocks per page)
-  Segment sg;
-  Group gr;
+  int si, s1;
+  int pstart, ptotal;
+  int entry, blk, nstages, part;   // from the Segment
+  int fmt, b, kvh, gend;           // from the Group (gend: one past its last entry)
   __device__ void load(const DecodeParams& p) {
-    sg = p.segs[si];
-    gr = p.groups[sg.group];
-    ptotal = sg.nstages + (sg.nstages & 1);
+    const Segment* sp = p.segs + si;
+    const int grp = sp->group;
+    entry = sp->entry;
+    blk = sp->blk;
+    nstages = sp->nstages;
+    part = sp->part;
+    const Group* gp = p.groups + grp;
+    fmt = gp->fmt;
+    b = gp->b;
+    kvh = gp->kvh;
+    gend = gp->entry0 + gp->nentry;
+    ptotal = fmt ? nstages : nstages + (nstages & 1);
   }
   __device__ bool start(const DecodeParams& p, int s0, int s1_) {
     si = s0;
     s1 = s1_;
     pstart = 0;
-    bshift = p.P == 128 ? 1 : 0;
     if (si >= s1) return false;
     load(p);
     return true;
   }
-  // move forward to the piece holding block gi; false past the end
-  __device__ bool seek(const DecodeParams& p, int gi) {
-    while (gi >= pstart + ptotal) {
-      pstart += ptotal;
-      if (++si >= s1) return false;
-      load(p);
-    }
+  __device__ bool next_piece(const DecodeParams& p) {
+    pstart += ptotal;
+    if (++si >= s1) return false;
+    load(p);
     return true;
   }
-  // page entry and block within the page of piece block k < nstages
-  __device__ void locate(int k, int& e, int& blk) const {
-    const int b = sg.blk + k;
-    e = sg.entry + (b >> bshift);
-    blk = b & ((1 << bshift) - 1);
+  __device__ bool seek(const DecodeParams& p, int gi) {
+    while (gi >= pstart + ptotal)
+      if (!next_piece(p)) return false;
+    return true;
   }
-  // tokens of piece block k (0 for the padding block)
-  __device__ int nvalid(const DecodeParams& p, int k) const {
-    if (k >= sg.nstages) return 0;
-    int e, blk;
-    locate(k, e, blk);
-    return min(kStageTokens, p.entries[e].nvalid - kStageTokens * blk);
+  // Block k of the piece: first page entry, block within that page (FP8 at
+  // P = 128 has two blocks per page), pages (TQ3 at P = 64 has two pages per
+  // block), and valid tokens (0 for an FP8 padding block).
+  __device__ int block(const DecodeParams& p, int k, int& e, int& half, int& npages) const {
+    if (k >= nstages) return 0;
+    if (fmt == 0) {
+      const int bpp = p.P / kFp8Tokens;                // blocks per page: 1 or 2
+      const int bb = blk + k;
+      e = entry + bb / bpp;
+      half = bb % bpp;
+      npages = 1;
+      return min(kFp8Tokens, p.entries[e].nvalid - kFp8Tokens * half);
+    }
+    const int ppb = kTq3Tokens / p.P;                  // pages per block: 2 or 1
+    e = entry + k * ppb;
+    half = 0;
+    npages = min(ppb, gend - e);
+    return npages * p.P;
+  }
+  // valid tokens of block k only (consumers)
+  __device__ int tokens(const DecodeParams& p, int k) const {
+    if (k >= nstages) return 0;
+    if (fmt == 0) {
+      const int bpp = p.P / kFp8Tokens;
+      const int bb = blk + k;
+      return min(kFp8Tokens, p.entries[entry + bb / bpp].nvalid - kFp8Tokens * (bb % bpp));
+    }
+    const int ppb = kTq3Tokens / p.P;
+    return min(ppb, gend - (entry + k * ppb)) * p.P;
   }
 };
 
 // Issue global block gi (cursor positioned on its piece) into its slot: four
-// bulk copies, or a plain arrive for a padding block.  False on a bad plan.
+// bulk copies per page, or a plain arrive for a padding block.  False on a
+// bad plan.
 __device__ __noinline__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const PieceCursor& cur, int gi) {
   const int slot = gi % kNumStages;
-  const int k = gi - cur.pstart;
   atomicMax(sm.issued, gi + 1);
-  if (k >= cur.sg.nstages) {
+  int e = 0, half = 0, npages = 0;
+  if (cur.block(p, gi - cur.pstart, e, half, npages) <= 0) {
     mbar_arrive(&sm.full[slot]);   // padding block: the phase completes without bytes
     return true;
   }
-  int e, blk;
-  cur.locate(k, e, blk);
-  const PageEntry pe = p.entries[e];
-  const int fmt = cur.gr.fmt;
+  const int fmt = cur.fmt;
   const int nslots = fmt ? p.tq3_slots : p.fp8_slots;
-  // a request's last page may still be receiving its new token from the
-  // preceding (q-prep + append) kernel: copy it only after that kernel is done
-  if (pe.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (pe.slot < 0 || pe.slot >= nslots) {
-    atomicOr(p.err, kErrBadPlan);
-    *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
-    mbar_arrive(&sm.full[slot]);
-    return false;
-  }
   const int row = fmt ? 3 * kHeadDim / 8 : kHeadDim;
   const int plane = p.P * (row + 2);
-  const uint8_t* hp = (fmt ? p.tq3_layer : p.fp8_layer) +
-                      static_cast<int64_t>(pe.slot) * (fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
-                      static_cast<int64_t>(cur.gr.kvh) * 2 * plane;
-  const int tok0 = kStageTokens * blk;
-  const uint32_t code = kStageTokens * row;
+  const int btok = fmt ? kTq3Tokens : kFp8Tokens;          // tokens per block in the slot layout
+  const int ptok = fmt ? p.P : kFp8Tokens;                 // tokens copied per page
+  for (int i = 0; i < npages; ++i) {
+    const PageEntry pe = p.entries[e + i];
+    // a request's last page may still be receiving its new token from the
+    // preceding (q-prep + append) kernel: copy it only after that kernel is done
+    if (pe.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (pe.slot < 0 || pe.slot >= nslots) {
+      atomicOr(p.err, kErrBadPlan);
+      *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+      mbar_arrive(&sm.full[slot]);
+      return false;
+    }
+  }
   uint8_t* st = sm.ring + slot * kSlotBytes;
+  const uint32_t code = ptok * row;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(&sm.full[slot], 2 * (code + 2 * kStageTokens));
-  bulk_g2s(st, hp + tok0 * row, code, &sm.full[slot]);
-  bulk_g2s(st + code, hp + p.P * row + 2 * tok0, 2 * kStageTokens, &sm.full[slot]);
-  bulk_g2s(st + code + 2 * kStageTokens, hp + plane + tok0 * row, code, &sm.full[slot]);
-  bulk_g2s(st + 2 * code + 2 * kStageTokens, hp + plane + p.P * row + 2 * tok0, 2 * kStageTokens,
-           &sm.full[slot]);
+  mbar_expect_tx(&sm.full[slot], npages * 2 * (code + 2 * ptok));
+  for (int i = 0; i < npages; ++i) {
+    const PageEntry pe = p.entries[e + i];
+    const uint8_t* hp = (fmt ? p.tq3_layer : p.fp8_layer) +
+                        static_cast<int64_t>(pe.slot) * (fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
+                        static_cast<int64_t>(cur.kvh) * 2 * plane;
+    const int tok0 = ptok * half;                          // first token of the copy within its page
+    const int t = ptok * i;                                // first token of the copy within the block
+    bulk_g2s(st + t * row, hp + tok0 * row, code, &sm.full[slot]);
+    bulk_g2s(st + btok * row + 2 * t, hp + p.P * row + 2 * tok0, 2 * ptok, &sm.full[slot]);
+    bulk_g2s(st + btok * row + 2 * btok + t * row, hp + plane + tok0 * row, code, &sm.full[slot]);
+    bulk_g2s(st + 2 * btok * row + 2 * btok + 2 * t, hp + plane + p.P * row + 2 * tok0, 2 * ptok,
+             &sm.full[slot]);
+  }
   return true;
 }
 
@@ -713,15 +760,15 @@ __device__ __noinline__ void dec_issue_ahead(const DecodeParams& p, const DecSme
   if (cur.seek(p, gi + kNumStages)) dec_issue(p, sm, cur, gi + kNumStages);
 }
 
-// A warp is done with block gi's slot.  The eighth (last) warp to say so issues
-// block gi + kNumStages into the slot.
-__device__ __forceinline__ void dec_release(const DecodeParams& p, const DecSmem& sm, int gi,
+// A warp is done with block gi's slot (`users` warps use a block of this
+// format).  The last one to say so issues block gi + kNumStages into the slot.
+__device__ __forceinline__ void dec_release(const DecodeParams& p, const DecSmem& sm, int gi, int users,
                                             const PieceCursor& cur) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) {
     __threadfence_block();
     const int slot = gi % kNumStages;
-    if (atomicAdd(&sm.release[slot], 1) == 2 * 4 - 1) {
+    if (atomicAdd(&sm.release[slot], 1) == users - 1) {
       sm.release[slot] = 0;
       __threadfence_block();
       if (!aborted(sm)) dec_issue_ahead(p, sm, cur, gi);
@@ -774,145 +821,6 @@ __device__ __forceinline__ void dec_qk_tq3(const uint8_t* kt, int g, int c, cons
   }
 }
 
-__device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
-  const int pair = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int grp = pair >> 2, tile = pair & 3;
-  const Lut lut = p.lut;
-  const float scale = p.score_scale;
-  const int G = p.G;
-  uint32_t qa[16][4];
-  float m_run = -INFINITY, l_run = 0.f;
-  int pj = 0;
-  bool dep_waited = false;
-  PieceCursor cur;
-  if (!cur.start(p, s0, s1)) return;
-  for (int gi = grp; cur.seek(p, gi); gi += 2) {
-    const int fmt = cur.gr.fmt;
-    const int kb = gi - cur.pstart;
-    if (kb < 2) {
-      if (!dep_waited) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        dep_waited = true;
-      }
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.qfrag + ((static_cast<size_t>(cur.gr.b) * p.Hkv + cur.gr.kvh) * 2 + fmt) * 2048 + lane * 64);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint4 v = src[j];
-        qa[j][0] = v.x;
-        qa[j][1] = v.y;
-        qa[j][2] = v.z;
-        qa[j][3] = v.w;
-      }
-      m_run = -INFINITY;
-      l_run = 0.f;
-    }
-    {
-      const int slot = gi % kNumStages;
-      const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
-      const int nv = cur.nvalid(p, kb) - kTileTokens * tile;
-      if (ok && nv > 0) {
-        const uint8_t* st = sm.ring + slot * kSlotBytes;
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        const __half2* ks;
-        const __half2* vs;
-        if (fmt == 0) {
-          dec_qk_fp8(st + Blk<0>::kK + tile * kTileTokens * kHeadDim, g, c, qa, sa, sb);
-          ks = reinterpret_cast<const __half2*>(st + Blk<0>::kKs + tile * kTileTokens * 2);
-          vs = reinterpret_cast<const __half2*>(st + Blk<0>::kVs + tile * kTileTokens * 2);
-        } else {
-          dec_qk_tq3(st + Blk<1>::kK + tile * kTileTokens * 96, g, c, qa, lut, sa, sb);
-          ks = reinterpret_cast<const __half2*>(st + Blk<1>::kKs + tile * kTileTokens * 2);
-          vs = reinterpret_cast<const __half2*>(st + Blk<1>::kVs + tile * kTileTokens * 2);
-        }
-        const float2 k01 = __half22float2(ks[c]), k89 = __half22float2(ks[4 + c]);
-        const float2 v01 = __half22float2(vs[c]), v89 = __half22float2(vs[4 + c]);
-        float sc[4];
-        sc[0] = (sa[0] + sa[2]) * (k01.x * scale);
-        sc[1] = (sa[1] + sa[3]) * (k01.y * scale);
-        sc[2] = (sb[0] + sb[2]) * (k89.x * scale);
-        sc[3] = (sb[1] + sb[3]) * (k89.y * scale);
-        if (g >= G) {
-          sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;
-        } else if (nv < kTileTokens) {
-          if (2 * c >= nv) sc[0] = -INFINITY;
-          if (2 * c + 1 >= nv) sc[1] = -INFINITY;
-          if (8 + 2 * c >= nv) sc[2] = -INFINITY;
-          if (9 + 2 * c >= nv) sc[3] = -INFINITY;
-        }
-        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-        float alpha = 1.f;
-        const bool rescale = __any_sync(kFull, mt > m_run + kLazyRescale);
-        if (rescale) {
-          const float m_new = fmaxf(m_run, mt);
-          alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
-          m_run = m_new;
-          l_run *= alpha;
-        }
-        // m_run = -inf only for heads g >= G (all scores -inf): keep p = 0 there
-        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-        const float p0 = ex2(sc[0] - mref), p1 = ex2(sc[1] - mref), p2 = ex2(sc[2] - mref), p3 = ex2(sc[3] - mref);
-        l_run += (p0 + p1) + (p2 + p3);
-        const float vsc = fmt == 0 ? kFp8PScale : 1.f;
-        const uint2 pb = make_uint2(pack_half2(p0 * (v01.x * vsc), p1 * (v01.y * vsc)),
-                                    pack_half2(p2 * (v89.x * vsc), p3 * (v89.y * vsc)));
-        const int ps = pj & 1;
-        PSlot& slotp = sm.pslot[2 * pair + ps];
-        bool okp = true;
-        if (pj >= 2) okp = dec_wait(sm, &sm.pempty[2 * pair + ps], ((pj >> 1) - 1) & 1, p.err);
-        if (okp) {
-          slotp.pb[lane] = pb;
-          if (c == 0) slotp.alpha[g] = alpha;
-          if (lane == 0) slotp.rescale = rescale ? 1 : 0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.pfull[2 * pair + ps]);
-        ++pj;
-      }
-      dec_release(p, sm, gi, cur);
-    }
-    if (kb >= cur.ptotal - 2) {
-      // end of this CTA's piece of the group: publish (m, l) of head g
-      float l = l_run;
-      l += __shfl_xor_sync(kFull, l, 1);
-      l += __shfl_xor_sync(kFull, l, 2);
-      if (c == 0) {
-        sm.epi_m[pair * kMaxGroup + g] = m_run;
-        sm.epi_l[pair * kMaxGroup + g] = l;
-      }
-      named_bar(1, 2 * kPairs * 32);
-      // combine: QK threads take even heads, PV threads odd heads (see dec_pv_warp)
-      const int d = threadIdx.x & 255;
-      const int hbase = (threadIdx.x >> 8);   // 0 for QK warps 0..7
-      float* dst = p.part + static_cast<size_t>(cur.sg.part) * G * (2 + kHeadDim);
-      for (int h = hbase; h < G; h += 2) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kPairs; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
-        float L = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kPairs; ++w) {
-            const float mw = sm.epi_m[w * kMaxGroup + h];
-            const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-            L += f * sm.epi_l[w * kMaxGroup + h];
-            acc += f * sm.epi_o[(w * kMaxGroup + h) * kHeadDim + d];
-          }
-        }
-        dst[h * (2 + kHeadDim) + 2 + d] = acc;
-        if (d == 0) {
-          dst[h * (2 + kHeadDim)] = M;
-          dst[h * (2 + kHeadDim) + 1] = L;
-        }
-      }
-      named_bar(1, 2 * kPairs * 32);
-    }
-  }
-}
-
 // O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32)
 __device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, uint2 pb, float (&o)[16][4]) {
   const uint8_t* ra = vt + c * (2 * kHeadDim) + 64 * g;
@@ -954,27 +862,176 @@ __device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint
   }
 }
 
+// The piece's partial state.  QK warps have published (m, l) per pair and
+// head; PV warps have left O rescaled to the common max in four buffers
+// (pair i + pair i+4 in buffer i).  Every thread writes its share, summing the
+// buffers in a fixed order so the result does not depend on timing.
+__device__ __forceinline__ void dec_piece_write(const DecodeParams& p, const DecSmem& sm, int part, int G) {
+  const int t = threadIdx.x, d = t & 255;
+  float* dst = p.part + static_cast<size_t>(part) * G * (2 + kHeadDim);
+  for (int h = t >> 8; h < G; h += 2) {
+    const float* a = sm.acc + h * kHeadDim + d;
+    constexpr int kBuf = kMaxGroup * kHeadDim;
+    dst[h * (2 + kHeadDim) + 2 + d] = (a[0] + a[kBuf]) + (a[2 * kBuf] + a[3 * kBuf]);
+    if (d == 0) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kPairs; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kPairs; ++w) {
+          const float mw = sm.epi_m[w * kMaxGroup + h];
+          if (mw != -INFINITY) L += ex2(mw - M) * sm.epi_l[w * kMaxGroup + h];
+        }
+      }
+      dst[h * (2 + kHeadDim)] = M;
+      dst[h * (2 + kHeadDim) + 1] = L;
+    }
+  }
+}
+
+__device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
+  const int pair = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const Lut lut = p.lut;
+  const float scale = p.score_scale;
+  const int G = p.G;
+  uint32_t qa[16][4];
+  int pj = 0;
+  bool dep_waited = false;
+  PieceCursor cur;
+  for (bool more = cur.start(p, s0, s1); more; more = cur.next_piece(p)) {
+    const int fmt = cur.fmt;
+    if (!dep_waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      dep_waited = true;
+    }
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.qfrag + ((static_cast<size_t>(cur.b) * p.Hkv + cur.kvh) * 2 + fmt) * kQfragWords + lane * 64);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint4 v = src[j];
+        qa[j][0] = v.x;
+        qa[j][1] = v.y;
+        qa[j][2] = v.z;
+        qa[j][3] = v.w;
+      }
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    const int tile = fmt ? pair : (pair & 3);
+    const int step = fmt ? 1 : 2;
+    const int users = fmt ? 2 * kPairs : kPairs;
+    for (int k = fmt ? 0 : (pair >> 2); k < cur.ptotal; k += step) {
+      const int gi = cur.pstart + k;
+      const int slot = gi % kNumStages;
+      const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
+      const int nv = cur.tokens(p, k) - kTileTokens * tile;
+      if (ok && nv > 0) {
+        const uint8_t* st = sm.ring + slot * kSlotBytes;
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const __half2* ks;
+        const __half2* vs;
+        if (fmt == 0) {
+          dec_qk_fp8(st + Blk<0>::kK + tile * kTileTokens * kHeadDim, g, c, qa, sa, sb);
+          ks = reinterpret_cast<const __half2*>(st + Blk<0>::kKs + tile * kTileTokens * 2);
+          vs = reinterpret_cast<const __half2*>(st + Blk<0>::kVs + tile * kTileTokens * 2);
+        } else {
+          dec_qk_tq3(st + Blk<1>::kK + tile * kTileTokens * 96, g, c, qa, lut, sa, sb);
+          ks = reinterpret_cast<const __half2*>(st + Blk<1>::kKs + tile * kTileTokens * 2);
+          vs = reinterpret_cast<const __half2*>(st + Blk<1>::kVs + tile * kTileTokens * 2);
+        }
+        const float2 k01 = __half22float2(ks[c]), k89 = __half22float2(ks[4 + c]);
+        const float2 v01 = __half22float2(vs[c]), v89 = __half22float2(vs[4 + c]);
+        float sc[4];
+        sc[0] = (sa[0] + sa[2]) * (k01.x * scale);
+        sc[1] = (sa[1] + sa[3]) * (k01.y * scale);
+        sc[2] = (sb[0] + sb[2]) * (k89.x * scale);
+        sc[3] = (sb[1] + sb[3]) * (k89.y * scale);
+        if (g >= G) {
+          sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;
+        } else if (nv < kTileTokens) {
+          if (2 * c >= nv) sc[0] = -INFINITY;
+          if (2 * c + 1 >= nv) sc[1] = -INFINITY;
+          if (8 + 2 * c >= nv) sc[2] = -INFINITY;
+          if (9 + 2 * c >= nv) sc[3] = -INFINITY;
+        }
+        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+        float alpha = 1.f;
+        const bool rescale = __any_sync(kFull, mt > m_run + kLazyRescale);
+        if (rescale) {
+          const float m_new = fmaxf(m_run, mt);
+          alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        // m_run stays -inf only for heads g >= G (all their scores -inf)
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[i] = (sc[i] == -INFINITY) ? 0.f : ex2(sc[i] - mref);
+        l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+        // masked tokens give exactly 0 (their scale bytes may be stale)
+        const float vsc = fmt == 0 ? kFp8PScale : 1.f;
+        const float w0 = pr[0] == 0.f ? 0.f : pr[0] * (v01.x * vsc);
+        const float w1 = pr[1] == 0.f ? 0.f : pr[1] * (v01.y * vsc);
+        const float w2 = pr[2] == 0.f ? 0.f : pr[2] * (v89.x * vsc);
+        const float w3 = pr[3] == 0.f ? 0.f : pr[3] * (v89.y * vsc);
+        const uint2 pb = make_uint2(pack_half2(w0, w1), pack_half2(w2, w3));
+        const int ps = pj & 1;
+        PSlot& slotp = sm.pslot[2 * pair + ps];
+        bool okp = true;
+        if (pj >= 2) okp = dec_wait(sm, &sm.pempty[2 * pair + ps], ((pj >> 1) - 1) & 1, p.err);
+        if (okp) {
+          slotp.pb[lane] = pb;
+          if (c == 0) slotp.alpha[g] = alpha;
+          if (lane == 0) slotp.rescale = rescale ? 1 : 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.pfull[2 * pair + ps]);
+        ++pj;
+      }
+      dec_release(p, sm, gi, users, cur);
+    }
+    // end of the piece: publish (m, l) of head g, then merge with the PV warps
+    float l = l_run;
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (c == 0) {
+      sm.epi_m[pair * kMaxGroup + g] = (g < G) ? m_run : -INFINITY;
+      sm.epi_l[pair * kMaxGroup + g] = (g < G) ? l : 0.f;
+    }
+    named_bar(1, kDecThreads);   // (m, l) published
+    named_bar(1, kDecThreads);   // pairs 4-7 stored their O
+    named_bar(1, kDecThreads);   // pairs 0-3 added theirs
+    dec_piece_write(p, sm, cur.part, G);
+    named_bar(1, kDecThreads);   // buffers and (m, l) free again
+  }
+}
+
 __device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
   const int pair = (threadIdx.x >> 5) - kPairs, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int grp = pair >> 2, tile = pair & 3;
   const Lut lut = p.lut;
   const int G = p.G;
   float o[16][4];
   int pj = 0;
   PieceCursor cur;
-  if (!cur.start(p, s0, s1)) return;
-  for (int gi = grp; cur.seek(p, gi); gi += 2) {
-    const int fmt = cur.gr.fmt;
-    const int kb = gi - cur.pstart;
-    if (kb < 2) {
+  for (bool more = cur.start(p, s0, s1); more; more = cur.next_piece(p)) {
+    const int fmt = cur.fmt;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    }
-    {
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const int tile = fmt ? pair : (pair & 3);
+    const int step = fmt ? 1 : 2;
+    const int users = fmt ? 2 * kPairs : kPairs;
+    for (int k = fmt ? 0 : (pair >> 2); k < cur.ptotal; k += step) {
+      const int gi = cur.pstart + k;
       const int slot = gi % kNumStages;
       const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
-      const int nv = cur.nvalid(p, kb) - kTileTokens * tile;
+      const int nv = cur.tokens(p, k) - kTileTokens * tile;
       if (ok && nv > 0) {
         const int ps = pj & 1;
         const PSlot& slotp = sm.pslot[2 * pair + ps];
@@ -1006,44 +1063,55 @@ __device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, in
             dec_pv_tq3(st + Blk<1>::kV + tile * (kTileTokens / 2) * 192, g, c, pb, lut, o);
         }
       }
-      dec_release(p, sm, gi, cur);
+      dec_release(p, sm, gi, users, cur);
     }
-    if (kb >= cur.ptotal - 2) {
-      const float osc = fmt == 0 ? 1.f / kFp8PScale : 1.f;
-      float* ow = sm.epi_o + pair * kMaxGroup * kHeadDim;
+    // end of the piece: wait for the QK warps' (m, l), rescale O to the common
+    // max of each head, and combine pairs i and i+4 into buffer i (i < 4)
+    named_bar(1, kDecThreads);
+    const float osc = fmt == 0 ? 1.f / kFp8PScale : 1.f;
+    float f0, f1;
+    {
+      float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kPairs; ++w) {
+        M0 = fmaxf(M0, sm.epi_m[w * kMaxGroup + 2 * c]);
+        M1 = fmaxf(M1, sm.epi_m[w * kMaxGroup + 2 * c + 1]);
+      }
+      const float m0 = sm.epi_m[pair * kMaxGroup + 2 * c], m1 = sm.epi_m[pair * kMaxGroup + 2 * c + 1];
+      f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0) * osc;
+      f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1) * osc;
+    }
+    float* buf = sm.acc + (pair & 3) * kMaxGroup * kHeadDim;
+    if (pair >= 4) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int d = 32 * g + 2 * i;
         if (2 * c < G)
-          *reinterpret_cast<float2*>(ow + (2 * c) * kHeadDim + d) = make_float2(o[i][0] * osc, o[i][2] * osc);
+          *reinterpret_cast<float2*>(buf + (2 * c) * kHeadDim + d) = make_float2(o[i][0] * f0, o[i][2] * f0);
         if (2 * c + 1 < G)
-          *reinterpret_cast<float2*>(ow + (2 * c + 1) * kHeadDim + d) = make_float2(o[i][1] * osc, o[i][3] * osc);
+          *reinterpret_cast<float2*>(buf + (2 * c + 1) * kHeadDim + d) = make_float2(o[i][1] * f1, o[i][3] * f1);
       }
-      named_bar(1, 2 * kPairs * 32);
-      const int d = threadIdx.x & 255;
-      float* dst = p.part + static_cast<size_t>(cur.sg.part) * G * (2 + kHeadDim);
-      for (int h = 1; h < G; h += 2) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kPairs; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
-        float L = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kPairs; ++w) {
-            const float mw = sm.epi_m[w * kMaxGroup + h];
-            const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-            L += f * sm.epi_l[w * kMaxGroup + h];
-            acc += f * sm.epi_o[(w * kMaxGroup + h) * kHeadDim + d];
-          }
-        }
-        dst[h * (2 + kHeadDim) + 2 + d] = acc;
-        if (d == 0) {
-          dst[h * (2 + kHeadDim)] = M;
-          dst[h * (2 + kHeadDim) + 1] = L;
-        }
-      }
-      named_bar(1, 2 * kPairs * 32);
     }
+    named_bar(1, kDecThreads);
+    if (pair < 4) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int d = 32 * g + 2 * i;
+        if (2 * c < G) {
+          float2* q = reinterpret_cast<float2*>(buf + (2 * c) * kHeadDim + d);
+          const float2 v = *q;
+          *q = make_float2(o[i][0] * f0 + v.x, o[i][2] * f0 + v.y);
+        }
+        if (2 * c + 1 < G) {
+          float2* q = reinterpret_cast<float2*>(buf + (2 * c + 1) * kHeadDim + d);
+          const float2 v = *q;
+          *q = make_float2(o[i][1] * f1 + v.x, o[i][3] * f1 + v.y);
+        }
+      }
+    }
+    named_bar(1, kDecThreads);
+    dec_piece_write(p, sm, cur.part, G);
+    named_bar(1, kDecThreads);
   }
 }
 
