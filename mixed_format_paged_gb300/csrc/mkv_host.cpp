@@ -329,14 +329,15 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 
 // ------------------------------------------------------------------ planner
 // Relative cost of one token of one kv head, per format, plus a fixed cost per
-// 64-token block.  The decode kernel is issue-bound on TQ3 dequantisation and
+// block.  The decode kernel is ALU-bound on TQ3 dequantisation and closer to
 // bandwidth-bound on FP8 bytes; these weights balance the two across CTAs.
 constexpr double kCostTq3Token = 1.0;
 constexpr double kCostFp8Token = 1.3;
 constexpr double kCostBlock = 8.0;
+constexpr int kMinBlocksPerCta = 16;   // two blocks per warp at least
 
 // Split the batch's pages into groups (request, kv head, format), lay the
-// groups' 64-token blocks out in one sequence, and cut that sequence into one
+// groups' blocks out in one sequence, and cut that sequence into one
 // contiguous piece per CTA of equal estimated cost.  Each (CTA, group) piece
 // writes one partial state; a group's partial states are contiguous, which is
 // what the merge kernel reads.
@@ -383,25 +384,23 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
         for (int i = 0; i < count; ++i) g.tokens += entries[first + i].nvalid;
         groups.push_back(g);
       }
-  // Blocks: an FP8 block is 64 tokens (one page at P = 64, half a page at
-  // P = 128); a TQ3 block is 128 tokens (two pages at P = 64, one at P = 128).
-  // Block list: (group, first entry, block within the entry, tokens).
+  // Blocks: an FP8 block is kFp8Blk tokens and a TQ3 block kTq3Blk tokens
+  // of one page; a group's blocks are numbered page by page, bpp = P / bt per
+  // page, up to the last valid token (a block past a page's valid tokens is
+  // empty and only costs its overhead).
   struct Blk {
-    int group, entry, half, tokens;
+    int group, index, tokens;
   };
   std::vector<Blk> blocks;
   for (int gi = 0; gi < int(groups.size()); ++gi) {
     const Group& g = groups[gi];
-    if (g.fmt == 0) {
-      for (int i = 0; i < g.nentry; ++i) {
-        const int nv = entries[g.entry0 + i].nvalid;
-        for (int h = 0; h * kStageTokens < nv; ++h)
-          blocks.push_back({gi, g.entry0 + i, h, std::min(kStageTokens, nv - h * kStageTokens)});
-      }
-    } else {
-      const int ppb = 128 / P;
-      for (int i = 0; i < g.nentry; i += ppb)
-        blocks.push_back({gi, g.entry0 + i, 0, std::min(ppb, g.nentry - i) * P});
+    const int bt = g.fmt ? kTq3Blk : kFp8Blk;
+    const int bpp = P / bt;
+    const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
+    const int nblk = (g.nentry - 1) * bpp + (last_nv + bt - 1) / bt;
+    for (int k = 0; k < nblk; ++k) {
+      const int nv = entries[g.entry0 + k / bpp].nvalid - (k % bpp) * bt;
+      blocks.push_back({gi, k, std::max(0, std::min(bt, nv))});
     }
   }
   auto cost = [&](const Blk& b) {
@@ -409,8 +408,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   };
   double total = 0.0;
   for (const Blk& b : blocks) total += cost(b);
+  // one CTA per SM, each with at least kMinBlocksPerCta blocks
   const int ncta = int(std::max<int64_t>(
-      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), (int64_t(blocks.size()) + 1) / 2})));
+      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), int64_t(blocks.size()) / kMinBlocksPerCta})));
   // cut the block sequence into ncta pieces lists of equal cost
   std::vector<Segment> segs;
   std::vector<int32_t> cta_seg(ncta + 1, 0);
@@ -422,10 +422,11 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
     cta = std::min(std::max(cta, cur_cta), ncta - 1);
     if (b.group != cur_group || cta != cur_cta) {
       while (cur_cta < cta) cta_seg[++cur_cta] = int(segs.size());
+      const Group& g = groups[b.group];
       Segment sg{};
       sg.group = b.group;
-      sg.entry = b.entry;
-      sg.blk = b.half;
+      sg.entry = g.entry0 + b.index / (P / (g.fmt ? kTq3Blk : kFp8Blk));
+      sg.blk = b.index;
       segs.push_back(sg);
       cur_group = b.group;
     }
@@ -458,13 +459,8 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   p->plan_debug.clear();
   for (const Segment& sg : segs) {
     const Group& g = groups[sg.group];
-    int last;
-    if (g.fmt == 0) {
-      const int bpp = P / kStageTokens;
-      last = sg.entry + (sg.blk + sg.nstages - 1) / bpp;
-    } else {
-      last = std::min(g.entry0 + g.nentry, sg.entry + sg.nstages * (128 / P)) - 1;
-    }
+    const int bpp = P / (g.fmt ? kTq3Blk : kFp8Blk);
+    const int last = g.entry0 + (sg.blk + sg.nstages - 1) / bpp;
     const int32_t rec[6] = {g.b, g.kvh, g.fmt ? 3 : 1, sg.entry, last - sg.entry + 1, sg.tokens};
     p->plan_debug.insert(p->plan_debug.end(), rec, rec + 6);
   }

@@ -11,7 +11,8 @@ namespace mkv {
 
 constexpr int kHeadDim = 256;      // head_dim the kernels are written for
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one MMA tile
-constexpr int kStageTokens = 64;   // tokens per staged page block
+constexpr int kFp8Blk = 16;        // tokens per FP8 decode block (one MMA tile)
+constexpr int kTq3Blk = 32;        // tokens per TQ3 decode block (two MMA tiles)
 constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
 constexpr int kMaxCtas = 1024;     // upper bound on decode CTAs
 constexpr int kQfragWords = 2048;  // q-prep fragment words per (b, kvh, format)
@@ -42,9 +43,11 @@ struct Group {             // one run of pages: (request, kv head, format)
 
 struct Segment {           // one CTA's piece of one group
   int32_t group;
-  int32_t entry;           // first PageEntry (absolute index)
-  int32_t blk;             // first 64-token block within that entry
-  int32_t nstages;         // 64-token blocks in the piece (a padding block evens odd counts)
+  int32_t entry;           // first PageEntry (absolute index; host bookkeeping)
+  int32_t blk;             // first block of the piece, counted within the group:
+                           // block k covers tokens [bt (k % bpp), +bt) of page
+                           // entry0 + k / bpp (bt = kFp8Blk or kTq3Blk, bpp = P / bt)
+  int32_t nstages;         // blocks in the piece
   int32_t part;            // partial-state index the piece writes
   int32_t tokens;          // valid tokens of the piece (host bookkeeping)
   int32_t pad0, pad1;

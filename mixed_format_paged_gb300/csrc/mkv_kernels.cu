@@ -13,8 +13,9 @@
 //                         Lloyd-Max codes, pack)
 //   mkv_qprep_kernel   -- per (request, kv head): q rows (and q' = R q) as
 //                         fp16 hi/lo MMA fragments
-//   mkv_decode_kernel  -- persistent, warp-specialised partial-attention
-//                         kernel over both formats
+//   mkv_decode_kernel  -- persistent partial-attention kernel over both
+//                         formats: 8 independent warps per CTA, each with its
+//                         own ring of bulk-copied page blocks
 //   mkv_merge_kernel   -- LSE merge: TQ3 partials in the rotated domain,
 //                         one R^T, then FP8 partials; writes out and lse
 #include "mkv_internal.h"
@@ -519,107 +520,82 @@ __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
 }
 
 // ============================================================== decode
-// Persistent, warp-specialised partial-attention kernel; one CTA per SM.
-//   warps 0-7   QK warps: S = Q K^T on mma.sync m16n8k16 (A = q rows from the
-//               q-prep fragments, B = K dequantised in registers), online
-//               softmax in log2 units with a lazy rescale, P (scaled by the V
-//               row scales, fp16) handed to the partner PV warp.
-//   warps 8-15  PV warps: O^T += V^T P^T (A = V dequantised in registers).
-// Page blocks move by cp.async.bulk copies (K codes, K scales, V codes, V
-// scales of each page) into a ring of kNumStages shared-memory slots whose
-// mbarriers count the bytes.  A TQ3 block is 128 tokens (8 tiles of 16: pair
-// i takes tile i); an FP8 block is 64 tokens (4 tiles: pair i takes tile i%4
-// of the blocks with parity i/4, and FP8 pieces are padded to an even number
-// of blocks so every pair sees the last one).  There is no producer warp:
-// thread 0 issues the first kNumStages blocks and afterwards the last warp to
-// release a slot (found with a shared-memory counter) issues the block
-// kNumStages further on into it.
-// The host cut the launch's global sequence of blocks into one contiguous,
-// cost-balanced piece list per CTA; each (CTA, group) piece ends with the 8
-// pairs' states merged into one partial state (m, l, o) per q head.
-constexpr int kPairs = 8;
-constexpr int kDecWarps = 2 * kPairs;
+// Persistent partial-attention kernel; one CTA of 8 warps per SM.
+// The host cut the launch's blocks into one contiguous, cost-balanced piece
+// list per CTA (a piece is a run of blocks of one (request, kv head, format)
+// group).  Within a piece, warp w takes blocks w, w + 8, w + 16, ... and runs
+// the whole of attention on them by itself:
+//   S = Q K^T on mma.sync m16n8k16: A = q rows (hi in rows 0-7, lo residual
+//     in rows 8-15, fp16) from the q-prep fragments, B = K dequantised in
+//     registers (TQ3: PRMT byte-table lookups; FP8: cvt e4m3x2);
+//   online softmax in log2 units with a lazy rescale (per warp);
+//   O^T += V^T P^T: A = V dequantised in registers (token pairs), B = P
+//     scaled by the V row scales (fp16), the S accumulator layout itself.
+// Each warp owns a ring of kSlots shared-memory slots; its lane 0 moves a
+// block in with four cp.async.bulk copies (K codes, K scales, V codes, V
+// scales) counted by the slot's mbarrier, and refills the slot with the
+// warp's block kSlots further on as soon as the warp is done with it.  No
+// warp waits for another except at the end of a piece, where the 8 warps'
+// states merge, in a fixed order, into one partial state (m, l, o) per q head.
+constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kNumStages = 5;
-constexpr int kFp8Tokens = 64;            // tokens per FP8 block
-constexpr int kTq3Tokens = 128;           // tokens per TQ3 block
-constexpr int kSlotBytes = 2 * (kFp8Tokens * kHeadDim + 2 * kFp8Tokens);   // an FP8 block; a TQ3 block fits
-constexpr uint32_t kWaitHintNs = 20000;   // try_wait suspend hint
+constexpr int kSlots = 3;                 // staging slots per warp
+constexpr int kSlotBytes = 2 * (kFp8Blk * kHeadDim + 2 * kFp8Blk);   // an FP8 block; a TQ3 block fits
 
 template <int FMT>
-struct Blk {                               // a block of format FMT in a slot
-  static constexpr int kTokens = FMT == 0 ? kFp8Tokens : kTq3Tokens;
+struct Blk {                              // a block of format FMT in a slot
+  static constexpr int kTokens = FMT == 0 ? kFp8Blk : kTq3Blk;
+  static constexpr int kTiles = kTokens / kTileTokens;
   static constexpr int kRow = FMT == 0 ? kHeadDim : 3 * kHeadDim / 8;      // K row bytes
+  static constexpr int kPairRow = 2 * kRow;                                 // V pair-row bytes
   static constexpr int kCode = kTokens * kRow;
   static constexpr int kK = 0, kKs = kCode, kV = kCode + 2 * kTokens, kVs = 2 * kCode + 2 * kTokens;
   static constexpr int kBytes = 2 * (kCode + 2 * kTokens);
 };
-static_assert(Blk<1>::kBytes <= kSlotBytes, "a TQ3 block must fit a slot");
+static_assert(Blk<0>::kBytes <= kSlotBytes && Blk<1>::kBytes <= kSlotBytes, "a block must fit a slot");
+static_assert(kSlotBytes % 16 == 0 && Blk<0>::kV % 16 == 0 && Blk<1>::kV % 16 == 0 && Blk<0>::kVs % 16 == 0 &&
+                  Blk<1>::kVs % 16 == 0 && Blk<1>::kKs % 16 == 0,
+              "bulk copies need 16-byte aligned destinations");
 
-struct PSlot {                                   // P handoff QK warp -> PV warp
-  uint2 pb[32];                                  // B fragments (fp16 P' pairs) per lane
-  float alpha[kMaxGroup];                        // O rescale factor per head
-  int32_t rescale;
-  int32_t pad[7];
-};
+constexpr int kRedBufs = 4;                    // O buffers of the piece-end reduction tree
+constexpr int kRedFloats = 16 * 4 * 32;        // one warp's O fragments, lane-major
 
 struct DecSmem {
-  uint8_t* ring;
-  PSlot* pslot;                                  // [kPairs][2]
-  float* acc;                                    // [4][kMaxGroup][D]: pair sums of a piece's O
-  float* epi_m;                                  // [kPairs][kMaxGroup]
+  uint8_t* ring;                               // [warp][slot] kSlotBytes
+  float* red;                                  // [kRedBufs][kRedFloats]
+  float* epi_m;                                // [warp][kMaxGroup]
   float* epi_l;
-  uint64_t* full;                                // [kNumStages]
-  uint64_t* pfull;                               // [kPairs][2]
-  uint64_t* pempty;                              // [kPairs][2]
-  int* release;                                  // [kNumStages] warps done with the slot
-  int* issued;                                   // blocks issued so far (for the abort drain)
+  uint64_t* full;                              // [warp][slot]
   int* abort_flag;
 };
-constexpr int kDecSmemRing = kNumStages * kSlotBytes;
-constexpr int kDecSmemP = kPairs * 2 * static_cast<int>(sizeof(PSlot));
-constexpr int kDecSmemEpi = 4 * kMaxGroup * kHeadDim * 4 + 2 * kPairs * kMaxGroup * 4;
-constexpr int kDecSmemBars = (kNumStages + 4 * kPairs) * 8 + (kNumStages + 2) * 4 + 8;
-constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemP + kDecSmemEpi + kDecSmemBars;
+constexpr int kDecSmemRing = kDecWarps * kSlots * kSlotBytes;
+constexpr int kDecSmemRed = kRedBufs * kRedFloats * 4;
+constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
+constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
+constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
+static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 
 __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   DecSmem s;
   s.ring = base;
-  s.pslot = reinterpret_cast<PSlot*>(base + kDecSmemRing);
-  s.acc = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemP);
-  s.epi_m = s.acc + 4 * kMaxGroup * kHeadDim;
-  s.epi_l = s.epi_m + kPairs * kMaxGroup;
-  s.full = reinterpret_cast<uint64_t*>(s.epi_l + kPairs * kMaxGroup);
-  s.pfull = s.full + kNumStages;
-  s.pempty = s.pfull + 2 * kPairs;
-  s.release = reinterpret_cast<int*>(s.pempty + 2 * kPairs);
-  s.issued = s.release + kNumStages;
-  s.abort_flag = s.issued + 1;
+  s.red = reinterpret_cast<float*>(base + kDecSmemRing);
+  s.epi_m = s.red + kRedBufs * kRedFloats;
+  s.epi_l = s.epi_m + kDecWarps * kMaxGroup;
+  s.full = reinterpret_cast<uint64_t*>(s.epi_l + kDecWarps * kMaxGroup);
+  s.abort_flag = reinterpret_cast<int*>(s.full + kDecWarps * kSlots);
   return s;
 }
 
 __device__ __forceinline__ bool aborted(const DecSmem& sm) {
   return *reinterpret_cast<volatile int*>(sm.abort_flag) != 0;
 }
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitHintNs)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait (kWaitCycles) that also gives up once any warp of the CTA has
-// aborted; the thread sleeps in try_wait until the phase completes.
+// Bounded wait (kWaitCycles); gives up at once when the CTA has aborted.
 __device__ __forceinline__ bool dec_wait(const DecSmem& sm, uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait_hint(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait_hint(bar, parity)) return true;
     if (aborted(sm)) return false;
+    if (mbar_try_wait(bar, parity)) return true;
     if (clock64() - t0 > kWaitCycles) {
       atomicOr(err, kErrWaitTimeout);
       *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
@@ -634,150 +610,93 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// One CTA's piece list: piece si covers global blocks [pstart, pstart + ptotal).
-// Holds only the fields the loops use.
-struct PieceCursor {
-  int si, s1;
-  int pstart, ptotal;
-  int entry, blk, nstages, part;   // from the Segment
-  int fmt, b, kvh, gend;           // from the Group (gend: one past its last entry)
-  __device__ void load(const DecodeParams& p) {
-    const Segment* sp = p.segs + si;
-    const int grp = sp->group;
-    entry = sp->entry;
-    blk = sp->blk;
-    nstages = sp->nstages;
-    part = sp->part;
-    const Group* gp = p.groups + grp;
-    fmt = gp->fmt;
-    b = gp->b;
-    kvh = gp->kvh;
-    gend = gp->entry0 + gp->nentry;
-    ptotal = fmt ? nstages : nstages + (nstages & 1);
-  }
-  __device__ bool start(const DecodeParams& p, int s0, int s1_) {
+struct Piece {                                 // one CTA piece (a Segment and its Group)
+  int fmt, b, kvh, entry0, blk0, nblk, part;
+};
+__device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
+  const Segment s = p.segs[si];
+  const Group g = p.groups[s.group];
+  return Piece{g.fmt, g.b, g.kvh, g.entry0, s.blk, s.nstages, s.part};
+}
+
+// Block k of a piece: page entry, first token within the page, valid tokens
+// (<= 0: the block is empty).
+__device__ __forceinline__ int block_locate(const DecodeParams& p, const Piece& pc, int k, int& e, int& tok0) {
+  const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
+  const int bpp = p.P / bt;
+  const int bb = pc.blk0 + k;
+  e = pc.entry0 + bb / bpp;
+  tok0 = (bb % bpp) * bt;
+  return min(bt, static_cast<int>(p.entries[e].nvalid) - tok0);
+}
+
+// The warp's sequence of blocks over the CTA's pieces (block k of piece si,
+// k = warp, warp + 8, ...).  Every lane keeps the same cursor.
+struct BlockCursor {
+  int si, s1, k;
+  int issued;              // lane 0: blocks copied in so far
+  Piece pc;
+  __device__ void start(const DecodeParams& p, int s0, int s1_, int warp) {
+    issued = 0;
     si = s0;
     s1 = s1_;
-    pstart = 0;
-    if (si >= s1) return false;
-    load(p);
-    return true;
+    k = warp;
+    if (si < s1) pc = load_piece(p, si);
+    settle(p, warp);
   }
-  __device__ bool next_piece(const DecodeParams& p) {
-    pstart += ptotal;
-    if (++si >= s1) return false;
-    load(p);
-    return true;
-  }
-  __device__ bool seek(const DecodeParams& p, int gi) {
-    while (gi >= pstart + ptotal)
-      if (!next_piece(p)) return false;
-    return true;
-  }
-  // Block k of the piece: first page entry, block within that page (FP8 at
-  // P = 128 has two blocks per page), pages (TQ3 at P = 64 has two pages per
-  // block), and valid tokens (0 for an FP8 padding block).
-  __device__ int block(const DecodeParams& p, int k, int& e, int& half, int& npages) const {
-    if (k >= nstages) return 0;
-    if (fmt == 0) {
-      const int bpp = p.P / kFp8Tokens;                // blocks per page: 1 or 2
-      const int bb = blk + k;
-      e = entry + bb / bpp;
-      half = bb % bpp;
-      npages = 1;
-      return min(kFp8Tokens, p.entries[e].nvalid - kFp8Tokens * half);
+  __device__ void settle(const DecodeParams& p, int warp) {
+    while (si < s1 && k >= pc.nblk) {
+      if (++si < s1) pc = load_piece(p, si);
+      k = warp;
     }
-    const int ppb = kTq3Tokens / p.P;                  // pages per block: 2 or 1
-    e = entry + k * ppb;
-    half = 0;
-    npages = min(ppb, gend - e);
-    return npages * p.P;
   }
-  // valid tokens of block k only (consumers)
-  __device__ int tokens(const DecodeParams& p, int k) const {
-    if (k >= nstages) return 0;
-    if (fmt == 0) {
-      const int bpp = p.P / kFp8Tokens;
-      const int bb = blk + k;
-      return min(kFp8Tokens, p.entries[entry + bb / bpp].nvalid - kFp8Tokens * (bb % bpp));
-    }
-    const int ppb = kTq3Tokens / p.P;
-    return min(ppb, gend - (entry + k * ppb)) * p.P;
+  __device__ bool valid() const { return si < s1; }
+  __device__ void advance(const DecodeParams& p, int warp) {
+    k += kDecWarps;
+    settle(p, warp);
   }
 };
 
-// Issue global block gi (cursor positioned on its piece) into its slot: four
-// bulk copies per page, or a plain arrive for a padding block.  False on a
-// bad plan.
-__device__ __noinline__ bool dec_issue(const DecodeParams& p, const DecSmem& sm, const PieceCursor& cur, int gi) {
-  const int slot = gi % kNumStages;
-  atomicMax(sm.issued, gi + 1);
-  int e = 0, half = 0, npages = 0;
-  if (cur.block(p, gi - cur.pstart, e, half, npages) <= 0) {
-    mbar_arrive(&sm.full[slot]);   // padding block: the phase completes without bytes
-    return true;
+// Lane 0: copy block k of piece pc into the warp's slot, or complete the
+// slot's phase without bytes for an empty block or a bad plan entry.
+__device__ __noinline__ void dec_issue(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int k, int warp,
+                                       int slot) {
+  uint64_t* bar = sm.full + warp * kSlots + slot;
+  int e = 0, tok0 = 0;
+  const int nv = block_locate(p, pc, k, e, tok0);
+  const PageEntry pe = p.entries[e];
+  const int nslots = pc.fmt ? p.tq3_slots : p.fp8_slots;
+  if (nv <= 0) {
+    mbar_arrive(bar);
+    return;
   }
-  const int fmt = cur.fmt;
-  const int nslots = fmt ? p.tq3_slots : p.fp8_slots;
-  const int row = fmt ? 3 * kHeadDim / 8 : kHeadDim;
+  if (pe.slot < 0 || pe.slot >= nslots) {
+    atomicOr(p.err, kErrBadPlan);
+    *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+    mbar_arrive(bar);
+    return;
+  }
+  // a request's last page may still be receiving its new token from the
+  // preceding (q-prep + append) kernel: copy it only once that kernel is done
+  if (pe.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int row = pc.fmt ? 3 * kHeadDim / 8 : kHeadDim;
+  const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
   const int plane = p.P * (row + 2);
-  const int btok = fmt ? kTq3Tokens : kFp8Tokens;          // tokens per block in the slot layout
-  const int ptok = fmt ? p.P : kFp8Tokens;                 // tokens copied per page
-  for (int i = 0; i < npages; ++i) {
-    const PageEntry pe = p.entries[e + i];
-    // a request's last page may still be receiving its new token from the
-    // preceding (q-prep + append) kernel: copy it only after that kernel is done
-    if (pe.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (pe.slot < 0 || pe.slot >= nslots) {
-      atomicOr(p.err, kErrBadPlan);
-      *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
-      mbar_arrive(&sm.full[slot]);
-      return false;
-    }
-  }
-  uint8_t* st = sm.ring + slot * kSlotBytes;
-  const uint32_t code = ptok * row;
+  const uint8_t* hp = (pc.fmt ? p.tq3_layer : p.fp8_layer) +
+                      static_cast<int64_t>(pe.slot) * (pc.fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
+                      static_cast<int64_t>(pc.kvh) * 2 * plane;
+  uint8_t* st = sm.ring + (warp * kSlots + slot) * kSlotBytes;
+  const uint32_t code = bt * row;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(&sm.full[slot], npages * 2 * (code + 2 * ptok));
-  for (int i = 0; i < npages; ++i) {
-    const PageEntry pe = p.entries[e + i];
-    const uint8_t* hp = (fmt ? p.tq3_layer : p.fp8_layer) +
-                        static_cast<int64_t>(pe.slot) * (fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
-                        static_cast<int64_t>(cur.kvh) * 2 * plane;
-    const int tok0 = ptok * half;                          // first token of the copy within its page
-    const int t = ptok * i;                                // first token of the copy within the block
-    bulk_g2s(st + t * row, hp + tok0 * row, code, &sm.full[slot]);
-    bulk_g2s(st + btok * row + 2 * t, hp + p.P * row + 2 * tok0, 2 * ptok, &sm.full[slot]);
-    bulk_g2s(st + btok * row + 2 * btok + t * row, hp + plane + tok0 * row, code, &sm.full[slot]);
-    bulk_g2s(st + 2 * btok * row + 2 * btok + 2 * t, hp + plane + p.P * row + 2 * tok0, 2 * ptok,
-             &sm.full[slot]);
-  }
-  return true;
+  mbar_expect_tx(bar, 2 * (code + 2 * bt));
+  bulk_g2s(st, hp + tok0 * row, code, bar);
+  bulk_g2s(st + code, hp + p.P * row + 2 * tok0, 2 * bt, bar);
+  bulk_g2s(st + code + 2 * bt, hp + plane + tok0 * row, code, bar);
+  bulk_g2s(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar);
 }
 
-// Issue block gi + kNumStages if it exists (cursor positioned at or before it).
-__device__ __noinline__ void dec_issue_ahead(const DecodeParams& p, const DecSmem& sm, PieceCursor cur, int gi) {
-  if (cur.seek(p, gi + kNumStages)) dec_issue(p, sm, cur, gi + kNumStages);
-}
-
-// A warp is done with block gi's slot (`users` warps use a block of this
-// format).  The last one to say so issues block gi + kNumStages into the slot.
-__device__ __forceinline__ void dec_release(const DecodeParams& p, const DecSmem& sm, int gi, int users,
-                                            const PieceCursor& cur) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
-    __threadfence_block();
-    const int slot = gi % kNumStages;
-    if (atomicAdd(&sm.release[slot], 1) == users - 1) {
-      sm.release[slot] = 0;
-      __threadfence_block();
-      if (!aborted(sm)) dec_issue_ahead(p, sm, cur, gi);
-    }
-  }
-}
-
-// S for one 16-token tile (two n8 halves, tokens g and 8+g of the tile as B
-// columns); FP8 K rows are row-major, the thread's 64 dims are 64 bytes.
+// S for one 16-token tile of FP8 K (two n8 halves: tokens g and 8+g of the
+// tile as B columns); rows are row-major, the thread's 64 dims are 64 bytes.
 __device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint32_t (&qa)[16][4],
                                            float (&s0)[4], float (&s1)[4]) {
 #pragma unroll
@@ -795,20 +714,26 @@ __device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, cons
   }
 }
 
+// The two 12-byte units at p (8-byte aligned): words of unit 0 in u[0..2],
+// unit 1 in u[3..5], read as three aligned 8-byte loads.
+__device__ __forceinline__ void load_unit_pair(const uint8_t* p, uint32_t (&u)[6]) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p);
+  const uint2 b = *reinterpret_cast<const uint2*>(p + 8);
+  const uint2 c = *reinterpret_cast<const uint2*>(p + 16);
+  u[0] = a.x; u[1] = a.y; u[2] = b.x; u[3] = b.y; u[4] = c.x; u[5] = c.y;
+}
+
 // S for one 16-token tile of TQ3 K: row (8u + g) units 2c, 2c+1 (24 bytes at 24c).
 __device__ __forceinline__ void dec_qk_tq3(const uint8_t* kt, int g, int c, const uint32_t (&qa)[16][4],
                                            const Lut& lut, float (&s0)[4], float (&s1)[4]) {
-  const uint8_t* r0 = kt + g * 96 + 24 * c;
-  const uint8_t* r1 = kt + (8 + g) * 96 + 24 * c;
+  uint32_t ua[6], ub[6];
+  load_unit_pair(kt + g * 96 + 24 * c, ua);
+  load_unit_pair(kt + (8 + g) * 96 + 24 * c, ub);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    const uint2 a01 = *reinterpret_cast<const uint2*>(r0 + 12 * half);
-    const uint32_t a2 = *reinterpret_cast<const uint32_t*>(r0 + 12 * half + 8);
-    const uint2 b01 = *reinterpret_cast<const uint2*>(r1 + 12 * half);
-    const uint32_t b2 = *reinterpret_cast<const uint32_t*>(r1 + 12 * half + 8);
     uint32_t sa[8], sb[8];
-    tq3_unit_selectors(a01.x, a01.y, a2, sa);
-    tq3_unit_selectors(b01.x, b01.y, b2, sb);
+    tq3_unit_selectors(ua[3 * half], ua[3 * half + 1], ua[3 * half + 2], sa);
+    tq3_unit_selectors(ub[3 * half], ub[3 * half + 1], ub[3 * half + 2], sb);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       const int j = 8 * half + s;
@@ -841,17 +766,14 @@ __device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, uint
 // O^T += V^T P^T for TQ3 V: pair-rows c and c+4, units 2g, 2g+1 (24 bytes at 24g)
 __device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint2 pb, const Lut& lut,
                                            float (&o)[16][4]) {
-  const uint8_t* ra = vt + c * 192 + 24 * g;
-  const uint8_t* rb = vt + (c + 4) * 192 + 24 * g;
+  uint32_t ua[6], ub[6];
+  load_unit_pair(vt + c * 192 + 24 * g, ua);
+  load_unit_pair(vt + (c + 4) * 192 + 24 * g, ub);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    const uint2 a01 = *reinterpret_cast<const uint2*>(ra + 12 * half);
-    const uint32_t a2 = *reinterpret_cast<const uint32_t*>(ra + 12 * half + 8);
-    const uint2 b01 = *reinterpret_cast<const uint2*>(rb + 12 * half);
-    const uint32_t b2 = *reinterpret_cast<const uint32_t*>(rb + 12 * half + 8);
     uint32_t sa[8], sb[8];
-    tq3_unit_selectors(a01.x, a01.y, a2, sa);
-    tq3_unit_selectors(b01.x, b01.y, b2, sb);
+    tq3_unit_selectors(ua[3 * half], ua[3 * half + 1], ua[3 * half + 2], sa);
+    tq3_unit_selectors(ub[3 * half], ub[3 * half + 1], ub[3 * half + 2], sb);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       uint32_t x0, x1, y0, y1;
@@ -862,256 +784,221 @@ __device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint
   }
 }
 
-// The piece's partial state.  QK warps have published (m, l) per pair and
-// head; PV warps have left O rescaled to the common max in four buffers
-// (pair i + pair i+4 in buffer i).  Every thread writes its share, summing the
-// buffers in a fixed order so the result does not depend on timing.
-__device__ __forceinline__ void dec_piece_write(const DecodeParams& p, const DecSmem& sm, int part, int G) {
-  const int t = threadIdx.x, d = t & 255;
-  float* dst = p.part + static_cast<size_t>(part) * G * (2 + kHeadDim);
-  for (int h = t >> 8; h < G; h += 2) {
-    const float* a = sm.acc + h * kHeadDim + d;
-    constexpr int kBuf = kMaxGroup * kHeadDim;
-    dst[h * (2 + kHeadDim) + 2 + d] = (a[0] + a[kBuf]) + (a[2 * kBuf] + a[3 * kBuf]);
-    if (d == 0) {
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kPairs; ++w) M = fmaxf(M, sm.epi_m[w * kMaxGroup + h]);
-      float L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kPairs; ++w) {
-          const float mw = sm.epi_m[w * kMaxGroup + h];
-          if (mw != -INFINITY) L += ex2(mw - M) * sm.epi_l[w * kMaxGroup + h];
-        }
-      }
-      dst[h * (2 + kHeadDim)] = M;
-      dst[h * (2 + kHeadDim) + 1] = L;
-    }
-  }
-}
+// Per-warp running state of a piece.
+struct WarpState {
+  float o[16][4];          // O^T fragments: m-tile i rows (dims) 32g+2i, 32g+2i+1; columns heads 2c, 2c+1
+  float m_run, l_run;      // head g: running max (log2 units) and this lane's share of the sum
+};
 
-__device__ void dec_qk_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
-  const int pair = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const Lut lut = p.lut;
+// One block of format FMT at st (nv valid tokens): scores, online softmax, PV.
+template <int FMT>
+__device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* st, int nv,
+                                          const uint32_t (&qa)[16][4], WarpState& ws) {
+  using B = Blk<FMT>;
+  constexpr int NT = B::kTiles;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const Lut& lut = p.lut;
+  float sacc[NT][2][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) sacc[t][h][0] = sacc[t][h][1] = sacc[t][h][2] = sacc[t][h][3] = 0.f;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    if (FMT == 0)
+      dec_qk_fp8(st + B::kK + t * kTileTokens * B::kRow, g, c, qa, sacc[t][0], sacc[t][1]);
+    else
+      dec_qk_tq3(st + B::kK + t * kTileTokens * B::kRow, g, c, qa, lut, sacc[t][0], sacc[t][1]);
+  }
+  const __half2* ks = reinterpret_cast<const __half2*>(st + B::kKs);
+  const __half2* vs = reinterpret_cast<const __half2*>(st + B::kVs);
   const float scale = p.score_scale;
-  const int G = p.G;
-  uint32_t qa[16][4];
-  int pj = 0;
-  bool dep_waited = false;
-  PieceCursor cur;
-  for (bool more = cur.start(p, s0, s1); more; more = cur.next_piece(p)) {
-    const int fmt = cur.fmt;
-    if (!dep_waited) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      dep_waited = true;
-    }
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.qfrag + ((static_cast<size_t>(cur.b) * p.Hkv + cur.kvh) * 2 + fmt) * kQfragWords + lane * 64);
+  // lane's tokens in tile t: 16t + 2c + {0, 1} (half 0) and 16t + 8 + 2c + {0, 1} (half 1)
+  float sc[NT][4];
+  float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint4 v = src[j];
-        qa[j][0] = v.x;
-        qa[j][1] = v.y;
-        qa[j][2] = v.z;
-        qa[j][3] = v.w;
-      }
+  for (int t = 0; t < NT; ++t) {
+    const float2 k0 = __half22float2(ks[8 * t + c]), k1 = __half22float2(ks[8 * t + 4 + c]);
+    sc[t][0] = (sacc[t][0][0] + sacc[t][0][2]) * (k0.x * scale);
+    sc[t][1] = (sacc[t][0][1] + sacc[t][0][3]) * (k0.y * scale);
+    sc[t][2] = (sacc[t][1][0] + sacc[t][1][2]) * (k1.x * scale);
+    sc[t][3] = (sacc[t][1][1] + sacc[t][1][3]) * (k1.y * scale);
+    if (g >= p.G) {
+      sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = -INFINITY;
+    } else if (nv < B::kTokens) {
+      const int tb = 16 * t + 2 * c;
+      if (tb >= nv) sc[t][0] = -INFINITY;
+      if (tb + 1 >= nv) sc[t][1] = -INFINITY;
+      if (tb + 8 >= nv) sc[t][2] = -INFINITY;
+      if (tb + 9 >= nv) sc[t][3] = -INFINITY;
     }
-    float m_run = -INFINITY, l_run = 0.f;
-    const int tile = fmt ? pair : (pair & 3);
-    const int step = fmt ? 1 : 2;
-    const int users = fmt ? 2 * kPairs : kPairs;
-    for (int k = fmt ? 0 : (pair >> 2); k < cur.ptotal; k += step) {
-      const int gi = cur.pstart + k;
-      const int slot = gi % kNumStages;
-      const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
-      const int nv = cur.tokens(p, k) - kTileTokens * tile;
-      if (ok && nv > 0) {
-        const uint8_t* st = sm.ring + slot * kSlotBytes;
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        const __half2* ks;
-        const __half2* vs;
-        if (fmt == 0) {
-          dec_qk_fp8(st + Blk<0>::kK + tile * kTileTokens * kHeadDim, g, c, qa, sa, sb);
-          ks = reinterpret_cast<const __half2*>(st + Blk<0>::kKs + tile * kTileTokens * 2);
-          vs = reinterpret_cast<const __half2*>(st + Blk<0>::kVs + tile * kTileTokens * 2);
-        } else {
-          dec_qk_tq3(st + Blk<1>::kK + tile * kTileTokens * 96, g, c, qa, lut, sa, sb);
-          ks = reinterpret_cast<const __half2*>(st + Blk<1>::kKs + tile * kTileTokens * 2);
-          vs = reinterpret_cast<const __half2*>(st + Blk<1>::kVs + tile * kTileTokens * 2);
-        }
-        const float2 k01 = __half22float2(ks[c]), k89 = __half22float2(ks[4 + c]);
-        const float2 v01 = __half22float2(vs[c]), v89 = __half22float2(vs[4 + c]);
-        float sc[4];
-        sc[0] = (sa[0] + sa[2]) * (k01.x * scale);
-        sc[1] = (sa[1] + sa[3]) * (k01.y * scale);
-        sc[2] = (sb[0] + sb[2]) * (k89.x * scale);
-        sc[3] = (sb[1] + sb[3]) * (k89.y * scale);
-        if (g >= G) {
-          sc[0] = sc[1] = sc[2] = sc[3] = -INFINITY;
-        } else if (nv < kTileTokens) {
-          if (2 * c >= nv) sc[0] = -INFINITY;
-          if (2 * c + 1 >= nv) sc[1] = -INFINITY;
-          if (8 + 2 * c >= nv) sc[2] = -INFINITY;
-          if (9 + 2 * c >= nv) sc[3] = -INFINITY;
-        }
-        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
-        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-        float alpha = 1.f;
-        const bool rescale = __any_sync(kFull, mt > m_run + kLazyRescale);
-        if (rescale) {
-          const float m_new = fmaxf(m_run, mt);
-          alpha = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_new);
-          m_run = m_new;
-          l_run *= alpha;
-        }
-        // m_run stays -inf only for heads g >= G (all their scores -inf)
-        const float mref = (m_run == -INFINITY) ? 0.f : m_run;
-        float pr[4];
+    mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
+  }
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+  if (__any_sync(kFull, mt > ws.m_run + kLazyRescale)) {
+    const float m_new = fmaxf(ws.m_run, mt);
+    const float alpha = (ws.m_run == -INFINITY) ? 0.f : ex2(ws.m_run - m_new);
+    ws.m_run = m_new;
+    ws.l_run *= alpha;
+    // O columns are heads 2c and 2c+1: their factors live in lanes 8c and 8c+4
+    const float a0 = __shfl_sync(kFull, alpha, 8 * c), a1 = __shfl_sync(kFull, alpha, 8 * c + 4);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = (sc[i] == -INFINITY) ? 0.f : ex2(sc[i] - mref);
-        l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-        // masked tokens give exactly 0 (their scale bytes may be stale)
-        const float vsc = fmt == 0 ? kFp8PScale : 1.f;
-        const float w0 = pr[0] == 0.f ? 0.f : pr[0] * (v01.x * vsc);
-        const float w1 = pr[1] == 0.f ? 0.f : pr[1] * (v01.y * vsc);
-        const float w2 = pr[2] == 0.f ? 0.f : pr[2] * (v89.x * vsc);
-        const float w3 = pr[3] == 0.f ? 0.f : pr[3] * (v89.y * vsc);
-        const uint2 pb = make_uint2(pack_half2(w0, w1), pack_half2(w2, w3));
-        const int ps = pj & 1;
-        PSlot& slotp = sm.pslot[2 * pair + ps];
-        bool okp = true;
-        if (pj >= 2) okp = dec_wait(sm, &sm.pempty[2 * pair + ps], ((pj >> 1) - 1) & 1, p.err);
-        if (okp) {
-          slotp.pb[lane] = pb;
-          if (c == 0) slotp.alpha[g] = alpha;
-          if (lane == 0) slotp.rescale = rescale ? 1 : 0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.pfull[2 * pair + ps]);
-        ++pj;
-      }
-      dec_release(p, sm, gi, users, cur);
+    for (int i = 0; i < 16; ++i) {
+      ws.o[i][0] *= a0;
+      ws.o[i][1] *= a1;
+      ws.o[i][2] *= a0;
+      ws.o[i][3] *= a1;
     }
-    // end of the piece: publish (m, l) of head g, then merge with the PV warps
-    float l = l_run;
-    l += __shfl_xor_sync(kFull, l, 1);
-    l += __shfl_xor_sync(kFull, l, 2);
-    if (c == 0) {
-      sm.epi_m[pair * kMaxGroup + g] = (g < G) ? m_run : -INFINITY;
-      sm.epi_l[pair * kMaxGroup + g] = (g < G) ? l : 0.f;
-    }
-    named_bar(1, kDecThreads);   // (m, l) published
-    named_bar(1, kDecThreads);   // pairs 4-7 stored their O
-    named_bar(1, kDecThreads);   // pairs 0-3 added theirs
-    dec_piece_write(p, sm, cur.part, G);
-    named_bar(1, kDecThreads);   // buffers and (m, l) free again
+  }
+  // m_run stays -inf only for heads g >= G (all their scores -inf)
+  const float mref = (ws.m_run == -INFINITY) ? 0.f : ws.m_run;
+  const float vsc = FMT == 0 ? kFp8PScale : 1.f;
+  uint2 pb[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    float pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = (sc[t][i] == -INFINITY) ? 0.f : ex2(sc[t][i] - mref);
+    ws.l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    const float2 v0 = __half22float2(vs[8 * t + c]), v1 = __half22float2(vs[8 * t + 4 + c]);
+    // masked tokens give exactly 0 (their scale bytes may be stale)
+    const float w0 = pr[0] == 0.f ? 0.f : pr[0] * (v0.x * vsc);
+    const float w1 = pr[1] == 0.f ? 0.f : pr[1] * (v0.y * vsc);
+    const float w2 = pr[2] == 0.f ? 0.f : pr[2] * (v1.x * vsc);
+    const float w3 = pr[3] == 0.f ? 0.f : pr[3] * (v1.y * vsc);
+    pb[t] = make_uint2(pack_half2(w0, w1), pack_half2(w2, w3));
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    if (FMT == 0)
+      dec_pv_fp8(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], ws.o);
+    else
+      dec_pv_tq3(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], lut, ws.o);
   }
 }
 
-__device__ void dec_pv_warp(const DecodeParams& p, const DecSmem& sm, int s0, int s1) {
-  const int pair = (threadIdx.x >> 5) - kPairs, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const Lut lut = p.lut;
+// End of a piece: the 8 warps' states merge into the piece's partial state.
+// Each warp rescales its O to the common max of each head; O then sums up a
+// fixed tree (warps 4-7 into 0-3, 2-3 into 0-1, 1 into 0) so the result does
+// not depend on timing; warp 0 writes (m, l, o) per q head.
+__device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
+                                              WarpState& ws, int warp) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int G = p.G;
-  float o[16][4];
-  int pj = 0;
-  PieceCursor cur;
-  for (bool more = cur.start(p, s0, s1); more; more = cur.next_piece(p)) {
-    const int fmt = cur.fmt;
+  float l = ws.l_run;
+  l += __shfl_xor_sync(kFull, l, 1);
+  l += __shfl_xor_sync(kFull, l, 2);
+  if (c == 0) {
+    sm.epi_m[warp * kMaxGroup + g] = (g < G) ? ws.m_run : -INFINITY;
+    sm.epi_l[warp * kMaxGroup + g] = (g < G) ? l : 0.f;
+  }
+  named_bar(1, kDecThreads);
+  const float osc = pc.fmt == 0 ? 1.f / kFp8PScale : 1.f;
+  float f0, f1, Mg = -INFINITY, Lg = 0.f;
+  {
+    float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    const int tile = fmt ? pair : (pair & 3);
-    const int step = fmt ? 1 : 2;
-    const int users = fmt ? 2 * kPairs : kPairs;
-    for (int k = fmt ? 0 : (pair >> 2); k < cur.ptotal; k += step) {
-      const int gi = cur.pstart + k;
-      const int slot = gi % kNumStages;
-      const bool ok = dec_wait(sm, &sm.full[slot], (gi / kNumStages) & 1, p.err);
-      const int nv = cur.tokens(p, k) - kTileTokens * tile;
-      if (ok && nv > 0) {
-        const int ps = pj & 1;
-        const PSlot& slotp = sm.pslot[2 * pair + ps];
-        const bool okp = dec_wait(sm, &sm.pfull[2 * pair + ps], (pj >> 1) & 1, p.err);
-        const uint2 pb = slotp.pb[lane];
-        const int rescale = slotp.rescale;
-        float a0 = 1.f, a1 = 1.f;
-        if (rescale) {
-          a0 = slotp.alpha[2 * c];
-          a1 = slotp.alpha[2 * c + 1];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.pempty[2 * pair + ps]);
-        ++pj;
-        if (okp) {
-          if (rescale) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              o[i][0] *= a0;
-              o[i][1] *= a1;
-              o[i][2] *= a0;
-              o[i][3] *= a1;
-            }
-          }
-          const uint8_t* st = sm.ring + slot * kSlotBytes;
-          if (fmt == 0)
-            dec_pv_fp8(st + Blk<0>::kV + tile * (kTileTokens / 2) * (2 * kHeadDim), g, c, pb, o);
-          else
-            dec_pv_tq3(st + Blk<1>::kV + tile * (kTileTokens / 2) * 192, g, c, pb, lut, o);
-        }
-      }
-      dec_release(p, sm, gi, users, cur);
+    for (int w = 0; w < kDecWarps; ++w) {
+      M0 = fmaxf(M0, sm.epi_m[w * kMaxGroup + 2 * c]);
+      M1 = fmaxf(M1, sm.epi_m[w * kMaxGroup + 2 * c + 1]);
+      Mg = fmaxf(Mg, sm.epi_m[w * kMaxGroup + g]);
     }
-    // end of the piece: wait for the QK warps' (m, l), rescale O to the common
-    // max of each head, and combine pairs i and i+4 into buffer i (i < 4)
-    named_bar(1, kDecThreads);
-    const float osc = fmt == 0 ? 1.f / kFp8PScale : 1.f;
-    float f0, f1;
-    {
-      float M0 = -INFINITY, M1 = -INFINITY;
+    const float m0 = sm.epi_m[warp * kMaxGroup + 2 * c], m1 = sm.epi_m[warp * kMaxGroup + 2 * c + 1];
+    f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0) * osc;
+    f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1) * osc;
+    if (warp == 0 && Mg != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kPairs; ++w) {
-        M0 = fmaxf(M0, sm.epi_m[w * kMaxGroup + 2 * c]);
-        M1 = fmaxf(M1, sm.epi_m[w * kMaxGroup + 2 * c + 1]);
-      }
-      const float m0 = sm.epi_m[pair * kMaxGroup + 2 * c], m1 = sm.epi_m[pair * kMaxGroup + 2 * c + 1];
-      f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0) * osc;
-      f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1) * osc;
-    }
-    float* buf = sm.acc + (pair & 3) * kMaxGroup * kHeadDim;
-    if (pair >= 4) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int d = 32 * g + 2 * i;
-        if (2 * c < G)
-          *reinterpret_cast<float2*>(buf + (2 * c) * kHeadDim + d) = make_float2(o[i][0] * f0, o[i][2] * f0);
-        if (2 * c + 1 < G)
-          *reinterpret_cast<float2*>(buf + (2 * c + 1) * kHeadDim + d) = make_float2(o[i][1] * f1, o[i][3] * f1);
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = sm.epi_m[w * kMaxGroup + g];
+        if (mw != -INFINITY) Lg += ex2(mw - Mg) * sm.epi_l[w * kMaxGroup + g];
       }
     }
-    named_bar(1, kDecThreads);
-    if (pair < 4) {
+  }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int d = 32 * g + 2 * i;
-        if (2 * c < G) {
-          float2* q = reinterpret_cast<float2*>(buf + (2 * c) * kHeadDim + d);
-          const float2 v = *q;
-          *q = make_float2(o[i][0] * f0 + v.x, o[i][2] * f0 + v.y);
-        }
-        if (2 * c + 1 < G) {
-          float2* q = reinterpret_cast<float2*>(buf + (2 * c + 1) * kHeadDim + d);
-          const float2 v = *q;
-          *q = make_float2(o[i][1] * f1 + v.x, o[i][3] * f1 + v.y);
-        }
-      }
+  for (int i = 0; i < 16; ++i) {
+    ws.o[i][0] *= f0;
+    ws.o[i][1] *= f1;
+    ws.o[i][2] *= f0;
+    ws.o[i][3] *= f1;
+  }
+  // the tree: at each level the upper half stores, the lower half adds
+#pragma unroll
+  for (int half = kDecWarps / 2; half >= 1; half >>= 1) {
+    if (warp >= half && warp < 2 * half) {
+      float* buf = sm.red + (warp - half) * kRedFloats + lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) buf[(4 * i + k) * 32] = ws.o[i][k];
     }
     named_bar(1, kDecThreads);
-    dec_piece_write(p, sm, cur.part, G);
-    named_bar(1, kDecThreads);
+    if (warp < half) {
+      const float* buf = sm.red + warp * kRedFloats + lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ws.o[i][k] += buf[(4 * i + k) * 32];
+    }
+    if (half > 1) named_bar(1, kDecThreads);
+  }
+  if (warp == 0) {
+    float* dst = p.part + static_cast<size_t>(pc.part) * G * (2 + kHeadDim);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int d = 32 * g + 2 * i;
+      if (2 * c < G)
+        *reinterpret_cast<float2*>(dst + (2 * c) * (2 + kHeadDim) + 2 + d) = make_float2(ws.o[i][0], ws.o[i][2]);
+      if (2 * c + 1 < G)
+        *reinterpret_cast<float2*>(dst + (2 * c + 1) * (2 + kHeadDim) + 2 + d) =
+            make_float2(ws.o[i][1], ws.o[i][3]);
+    }
+    if (c == 0 && g < G) {
+      dst[g * (2 + kHeadDim)] = Mg;
+      dst[g * (2 + kHeadDim) + 1] = Lg;
+    }
+  }
+}
+
+// The warp's blocks of one piece.  `q` counts the warp's blocks over the
+// launch (slot q % kSlots, phase q / kSlots); `ic` is the cursor of the next
+// block to copy in.
+template <int FMT>
+__device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
+                                          BlockCursor& ic, int& q, int warp, WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+  if (warp >= pc.nblk) return;
+  uint32_t qa[16][4];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        p.qfrag + ((static_cast<size_t>(pc.b) * p.Hkv + pc.kvh) * 2 + FMT) * kQfragWords + lane * 64);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint4 v = src[j];
+      qa[j][0] = v.x;
+      qa[j][1] = v.y;
+      qa[j][2] = v.z;
+      qa[j][3] = v.w;
+    }
+  }
+  for (int k = warp; k < pc.nblk; k += kDecWarps, ++q) {
+    const int slot = q % kSlots;
+    int nv = Blk<FMT>::kTokens;
+    if (FMT == 0) {
+      int e, tok0;
+      nv = block_locate(p, pc, k, e, tok0);
+    }
+    const bool ok = dec_wait(sm, sm.full + warp * kSlots + slot, (q / kSlots) & 1, p.err);
+    if (ok && nv > 0) dec_block<FMT>(p, sm.ring + (warp * kSlots + slot) * kSlotBytes, nv, qa, ws);
+    __syncwarp();
+    // the slot is free again: copy in the warp's block kSlots further on
+    if (ic.valid()) {
+      if (lane == 0 && !aborted(sm)) {
+        dec_issue(p, sm, ic.pc, ic.k, warp, slot);
+        ++ic.issued;
+      }
+      ic.advance(p, warp);
+    }
   }
 }
 
@@ -1119,42 +1006,49 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   extern __shared__ __align__(128) uint8_t smem[];
   const DecSmem sm = dec_carve(smem);
   const int s0 = p.cta_seg[blockIdx.x], s1 = p.cta_seg[blockIdx.x + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the merge kernel that follows waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumStages; ++i) {
-      mbar_init(&sm.full[i], 1);
-      sm.release[i] = 0;
-    }
-    for (int i = 0; i < 2 * kPairs; ++i) {
-      mbar_init(&sm.pfull[i], 1);
-      mbar_init(&sm.pempty[i], 1);
-    }
-    *sm.issued = 0;
-    *sm.abort_flag = 0;
+  if (lane == 0) {
+    for (int i = 0; i < kSlots; ++i) mbar_init(sm.full + warp * kSlots + i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the first kNumStages blocks
-    PieceCursor cur;
-    if (cur.start(p, s0, s1)) {
-      for (int gi = 0; gi < kNumStages && cur.seek(p, gi); ++gi)
-        if (!dec_issue(p, sm, cur, gi)) break;
+  }
+  if (threadIdx.x == 0) *sm.abort_flag = 0;
+  __syncthreads();
+  // the warp's first kSlots blocks (their copies do not depend on q-prep,
+  // except a request's last page, which dec_issue orders after it)
+  BlockCursor ic;
+  ic.start(p, s0, s1, warp);
+  for (int i = 0; i < kSlots && ic.valid(); ++i) {
+    if (lane == 0) {
+      dec_issue(p, sm, ic.pc, ic.k, warp, i);
+      ++ic.issued;
     }
+    ic.advance(p, warp);
   }
-  __syncthreads();
-  if (s0 < s1) {
-    if (threadIdx.x < kPairs * 32)
-      dec_qk_warp(p, sm, s0, s1);
+  // q fragments come from the preceding q-prep kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int q = 0;
+  WarpState ws;
+  for (int si = s0; si < s1; ++si) {
+    const Piece pc = load_piece(p, si);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ws.o[i][0] = ws.o[i][1] = ws.o[i][2] = ws.o[i][3] = 0.f;
+    ws.m_run = -INFINITY;
+    ws.l_run = 0.f;
+    if (pc.fmt)
+      dec_piece<1>(p, sm, pc, ic, q, warp, ws);
     else
-      dec_pv_warp(p, sm, s0, s1);
+      dec_piece<0>(p, sm, pc, ic, q, warp, ws);
+    dec_piece_end(p, sm, pc, ws, warp);
   }
-  // every issued block is consumed on the normal path; after an abort, wait
-  // (bounded) for copies still in flight before the CTA exits
-  __syncthreads();
-  if (threadIdx.x == 0 && aborted(sm)) {
-    const int n = *sm.issued;
-    for (int k = n > kNumStages ? n - kNumStages : 0; k < n; ++k) {
+  // on the normal path every block copied in was consumed; after an abort,
+  // wait (bounded) for the warp's copies still in flight before exiting
+  __syncwarp();
+  if (lane == 0 && aborted(sm)) {
+    for (int j = ic.issued > kSlots ? ic.issued - kSlots : 0; j < ic.issued; ++j) {
       const long long t0 = clock64();
-      while (!mbar_try_wait(&sm.full[k % kNumStages], (k / kNumStages) & 1))
+      while (!mbar_try_wait(sm.full + warp * kSlots + j % kSlots, (j / kSlots) & 1))
         if (clock64() - t0 > kWaitCycles) break;
     }
   }

@@ -184,14 +184,19 @@ def _check_plan_covers(mkv, pool, ids, lengths, tiers_of):
             mine = [c for c in plan if c[0] == b and c[1] == kvh]
             f = sorted((c[3], c[4]) for c in mine if c[2] == 1)
             t = sorted((c[3], c[4]) for c in mine if c[2] == 3)
-            # chunk entry ranges tile each tier's page list exactly once
+            # chunk entry ranges cover each tier's page list in order; a page
+            # may be cut between two consecutive chunks (block granularity)
             for ranges, pages in ((f, fp8_pages), (t, tq3_pages)):
-                covered = sum(n for _, n in ranges)
-                assert covered == len(pages)
+                if not pages:
+                    assert not ranges
+                    continue
                 pos = [a for a, _ in ranges]
                 assert pos == sorted(pos)
+                assert all(n >= 1 for _, n in ranges)
                 for (a, n), (a2, _) in zip(ranges, ranges[1:]):
-                    assert a + n == a2
+                    assert a2 in (a + n - 1, a + n)
+                first, (la, ln) = ranges[0][0], ranges[-1]
+                assert la + ln - first == len(pages)
             assert sum(c[5] for c in mine) == lengths[b]
     return plan
 
