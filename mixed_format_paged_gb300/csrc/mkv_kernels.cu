@@ -14,7 +14,7 @@
 //   mkv_qprep_kernel   -- per (request, kv head): q rows (and q' = R q) as
 //                         fp16 hi/lo MMA fragments
 //   mkv_decode_kernel  -- persistent partial-attention kernel over both
-//                         formats: 8 independent warps per CTA, each with its
+//                         formats: 12 independent warps per CTA, each with its
 //                         own ring of bulk-copied page blocks
 //   mkv_merge_kernel   -- LSE merge: TQ3 partials in the rotated domain,
 //                         one R^T, then FP8 partials; writes out and lse
@@ -102,7 +102,10 @@ __device__ __forceinline__ void tq3_lookup4(uint32_t sel, const Lut& t, uint32_t
   h01 = __byte_perm(lo, hi, 0x5140);
   h23 = __byte_perm(lo, hi, 0x7362);
 }
-// One 12-byte unit (32 codes) -> eight nibble selectors (4 codes each).
+// One 12-byte unit (32 codes) -> eight nibble selectors (4 codes each):
+// codes 8k+i sit in nibbles of word k already (mask off bit 3); codes 24+i
+// gather bit 3 of nibble i of the three words.  PRMT reads selector bits
+// [15:0] only, so the upper four codes of a word take a 16-bit right shift.
 __device__ __forceinline__ void tq3_unit_selectors(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&s)[8]) {
   const uint32_t m0 = w0 & 0x77777777u, m1 = w1 & 0x77777777u, m2 = w2 & 0x77777777u;
   const uint32_t e = ((w0 >> 3) & 0x11111111u) | ((w1 >> 2) & 0x22222222u) | ((w2 >> 1) & 0x44444444u);
@@ -430,8 +433,9 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
 // q' = R q (signs, then H, then 1/16).  Rows 0-7 of the A tile hold fp16(q_h)
 // of heads h = 0..G-1, rows 8-15 the fp16 residual q_h - fp16(q_h), so the
 // two halves of the S accumulator add up to an fp32-accurate score.
-// Fragment layout: [(b*Hkv + kvh)*2 + fmt][lane 32][k-step 16][4 regs], with
-// lane (g, c) = (lane/4, lane%4) covering dims 64c + 4j .. 64c + 4j + 3.
+// Fragment layout: [(b*Hkv + kvh)*2 + fmt][k-step 16][lane 32][4 regs], with
+// lane (g, c) = (lane/4, lane%4) covering dims 64c + 4j .. 64c + 4j + 3 at
+// k-step j (k-step-major, so a warp reads one k-step as 512 contiguous bytes).
 __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
   __shared__ __align__(16) float qs[2][kMaxGroup][kHeadDim];
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -502,8 +506,8 @@ __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
   if (threadIdx.x >= 256) return;
   const int fmt = threadIdx.x >> 7, L = (threadIdx.x >> 2) & 31, j0 = 4 * (threadIdx.x & 3);
   const int g = L >> 2, c = L & 3;
-  uint4* dst = reinterpret_cast<uint4*>(p.qfrag + ((static_cast<size_t>(b) * p.Hkv + kvh) * 2 + fmt) * 2048 +
-                                        L * 64 + 4 * j0);
+  uint4* dst = reinterpret_cast<uint4*>(p.qfrag + ((static_cast<size_t>(b) * p.Hkv + kvh) * 2 + fmt) * kQfragWords) +
+              j0 * 32 + L;
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const float4 v = *reinterpret_cast<const float4*>(&qs[fmt][g][64 * c + 4 * (j0 + jj)]);
@@ -514,16 +518,16 @@ __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
       hi[i] = __half2float(__float2half_rn(vv[i]));
       lo[i] = vv[i] - hi[i];
     }
-    dst[jj] = make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
-                         pack_half2(lo[2], lo[3]));
+    dst[jj * 32] = make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
+                              pack_half2(lo[2], lo[3]));
   }
 }
 
 // ============================================================== decode
-// Persistent partial-attention kernel; one CTA of 8 warps per SM.
+// Persistent partial-attention kernel; one CTA of kDecWarps (12) warps per SM.
 // The host cut the launch's blocks into one contiguous, cost-balanced piece
 // list per CTA (a piece is a run of blocks of one (request, kv head, format)
-// group).  Within a piece, warp w takes blocks w, w + 8, w + 16, ... and runs
+// group).  Within a piece, warp w takes blocks w, w + 12, w + 24, ... and runs
 // the whole of attention on them by itself:
 //   S = Q K^T on mma.sync m16n8k16: A = q rows (hi in rows 0-7, lo residual
 //     in rows 8-15, fp16) from the q-prep fragments, B = K dequantised in
@@ -535,11 +539,11 @@ __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
 // block in with four cp.async.bulk copies (K codes, K scales, V codes, V
 // scales) counted by the slot's mbarrier, and refills the slot with the
 // warp's block kSlots further on as soon as the warp is done with it.  No
-// warp waits for another except at the end of a piece, where the 8 warps'
+// warp waits for another except at the end of a piece, where the warps'
 // states merge, in a fixed order, into one partial state (m, l, o) per q head.
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 12;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kSlots = 3;                 // staging slots per warp
+constexpr int kSlots = 2;                 // staging slots per warp
 constexpr int kSlotBytes = 2 * (kFp8Blk * kHeadDim + 2 * kFp8Blk);   // an FP8 block; a TQ3 block fits
 
 template <int FMT>
@@ -557,32 +561,38 @@ static_assert(kSlotBytes % 16 == 0 && Blk<0>::kV % 16 == 0 && Blk<1>::kV % 16 ==
                   Blk<1>::kVs % 16 == 0 && Blk<1>::kKs % 16 == 0,
               "bulk copies need 16-byte aligned destinations");
 
-constexpr int kRedBufs = 4;                    // O buffers of the piece-end reduction tree
+constexpr int kRedBufs = 2;                    // O buffers of the piece-end reduction
 constexpr int kRedFloats = 16 * 4 * 32;        // one warp's O fragments, lane-major
+constexpr int kQBytes = kQfragWords * 4;       // one piece's q fragments
 
 struct DecSmem {
   uint8_t* ring;                               // [warp][slot] kSlotBytes
+  uint4* qbuf;                                 // [2][k-step 16][lane 32]: q fragments of pieces i, i+1
   float* red;                                  // [kRedBufs][kRedFloats]
   float* epi_m;                                // [warp][kMaxGroup]
   float* epi_l;
   uint64_t* full;                              // [warp][slot]
+  uint64_t* qbar;                              // [2]
   int* abort_flag;
 };
 constexpr int kDecSmemRing = kDecWarps * kSlots * kSlotBytes;
+constexpr int kDecSmemQ = 2 * kQBytes;
 constexpr int kDecSmemRed = kRedBufs * kRedFloats * 4;
 constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
-constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
-constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
+constexpr int kDecSmemBars = (kDecWarps * kSlots + 2) * 8 + 16;
+constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
 static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 
 __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   DecSmem s;
   s.ring = base;
-  s.red = reinterpret_cast<float*>(base + kDecSmemRing);
+  s.qbuf = reinterpret_cast<uint4*>(base + kDecSmemRing);
+  s.red = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemQ);
   s.epi_m = s.red + kRedBufs * kRedFloats;
   s.epi_l = s.epi_m + kDecWarps * kMaxGroup;
   s.full = reinterpret_cast<uint64_t*>(s.epi_l + kDecWarps * kMaxGroup);
-  s.abort_flag = reinterpret_cast<int*>(s.full + kDecWarps * kSlots);
+  s.qbar = s.full + kDecWarps * kSlots;
+  s.abort_flag = reinterpret_cast<int*>(s.qbar + 2);
   return s;
 }
 
@@ -631,7 +641,7 @@ __device__ __forceinline__ int block_locate(const DecodeParams& p, const Piece& 
 }
 
 // The warp's sequence of blocks over the CTA's pieces (block k of piece si,
-// k = warp, warp + 8, ...).  Every lane keeps the same cursor.
+// k = warp, warp + kDecWarps, ...).  Every lane keeps the same cursor.
 struct BlockCursor {
   int si, s1, k;
   int issued;              // lane 0: blocks copied in so far
@@ -657,11 +667,10 @@ struct BlockCursor {
   }
 };
 
-// Lane 0: copy block k of piece pc into the warp's slot, or complete the
-// slot's phase without bytes for an empty block or a bad plan entry.
-__device__ __noinline__ void dec_issue(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int k, int warp,
-                                       int slot) {
-  uint64_t* bar = sm.full + warp * kSlots + slot;
+// Lane 0: copy block k of piece pc into slot st (mbarrier bar), or complete
+// the slot's phase without bytes for an empty block or a bad plan entry.
+__device__ __noinline__ void dec_issue(const DecodeParams& p, Piece pc, int k, uint8_t* st, uint64_t* bar,
+                                       int* abort_flag) {
   int e = 0, tok0 = 0;
   const int nv = block_locate(p, pc, k, e, tok0);
   const PageEntry pe = p.entries[e];
@@ -672,7 +681,7 @@ __device__ __noinline__ void dec_issue(const DecodeParams& p, const DecSmem& sm,
   }
   if (pe.slot < 0 || pe.slot >= nslots) {
     atomicOr(p.err, kErrBadPlan);
-    *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+    *reinterpret_cast<volatile int*>(abort_flag) = 1;
     mbar_arrive(bar);
     return;
   }
@@ -685,7 +694,6 @@ __device__ __noinline__ void dec_issue(const DecodeParams& p, const DecSmem& sm,
   const uint8_t* hp = (pc.fmt ? p.tq3_layer : p.fp8_layer) +
                       static_cast<int64_t>(pe.slot) * (pc.fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
                       static_cast<int64_t>(pc.kvh) * 2 * plane;
-  uint8_t* st = sm.ring + (warp * kSlots + slot) * kSlotBytes;
   const uint32_t code = bt * row;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, 2 * (code + 2 * bt));
@@ -695,23 +703,13 @@ __device__ __noinline__ void dec_issue(const DecodeParams& p, const DecSmem& sm,
   bulk_g2s(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar);
 }
 
-// S for one 16-token tile of FP8 K (two n8 halves: tokens g and 8+g of the
-// tile as B columns); rows are row-major, the thread's 64 dims are 64 bytes.
-__device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint32_t (&qa)[16][4],
-                                           float (&s0)[4], float (&s1)[4]) {
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    const uint4 w0 = *reinterpret_cast<const uint4*>(kt + g * kHeadDim + 64 * c + 16 * q4);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(kt + (8 + g) * kHeadDim + 64 * c + 16 * q4);
-    const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w};
-    const uint32_t x1[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int j = 4 * q4 + i;
-      mma16816(s0, qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(x0[i]), e4m3x2_to_f16x2(x0[i] >> 16));
-      mma16816(s1, qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(x1[i]), e4m3x2_to_f16x2(x1[i] >> 16));
-    }
-  }
+// Thread 0: copy piece pc's q fragments (8 KB, written by the q-prep kernel)
+// into q buffer `buf`.
+__device__ __forceinline__ void dec_issue_q(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int buf) {
+  const uint32_t* src = p.qfrag + ((static_cast<size_t>(pc.b) * p.Hkv + pc.kvh) * 2 + pc.fmt) * kQfragWords;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(sm.qbar + buf, kQBytes);
+  bulk_g2s(sm.qbuf + buf * (kQBytes / 16), src, kQBytes, sm.qbar + buf);
 }
 
 // The two 12-byte units at p (8-byte aligned): words of unit 0 in u[0..2],
@@ -723,25 +721,57 @@ __device__ __forceinline__ void load_unit_pair(const uint8_t* p, uint32_t (&u)[6
   u[0] = a.x; u[1] = a.y; u[2] = b.x; u[3] = b.y; u[4] = c.x; u[5] = c.y;
 }
 
-// S for one 16-token tile of TQ3 K: row (8u + g) units 2c, 2c+1 (24 bytes at 24c).
-__device__ __forceinline__ void dec_qk_tq3(const uint8_t* kt, int g, int c, const uint32_t (&qa)[16][4],
-                                           const Lut& lut, float (&s0)[4], float (&s1)[4]) {
-  uint32_t ua[6], ub[6];
-  load_unit_pair(kt + g * 96 + 24 * c, ua);
-  load_unit_pair(kt + (8 + g) * 96 + 24 * c, ub);
+// S for the one 16-token tile of an FP8 block (two n8 halves: tokens g and
+// 8+g as B columns); K rows are row-major, the thread's 64 dims are 64 bytes.
+// A (q) comes k-step by k-step from shared memory.
+__device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint4* qs, float (&s0)[4],
+                                           float (&s1)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint4 w0 = *reinterpret_cast<const uint4*>(kt + g * kHeadDim + 64 * c + 16 * q4);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(kt + (8 + g) * kHeadDim + 64 * c + 16 * q4);
+    const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w};
+    const uint32_t x1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = qs[(4 * q4 + i) * 32 + lane];
+      mma16816(s0, a.x, a.y, a.z, a.w, e4m3x2_to_f16x2(x0[i]), e4m3x2_to_f16x2(x0[i] >> 16));
+      mma16816(s1, a.x, a.y, a.z, a.w, e4m3x2_to_f16x2(x1[i]), e4m3x2_to_f16x2(x1[i] >> 16));
+    }
+  }
+}
+
+// S for the two 16-token tiles of a TQ3 block: tile t, row (16t + 8r + g),
+// units 2c, 2c+1 (24 bytes at 24c).  Each k-step's A fragment is read once
+// and feeds the four MMAs (two tiles x two n8 halves).
+__device__ __forceinline__ void dec_qk_tq3(const uint8_t* kb, int g, int c, const uint4* qs, const Lut& lut,
+                                           float (&s)[2][2][4]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t u[2][2][6];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) load_unit_pair(kb + (16 * t + 8 * r + g) * 96 + 24 * c, u[t][r]);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
-    uint32_t sa[8], sb[8];
-    tq3_unit_selectors(ua[3 * half], ua[3 * half + 1], ua[3 * half + 2], sa);
-    tq3_unit_selectors(ub[3 * half], ub[3 * half + 1], ub[3 * half + 2], sb);
+    uint32_t sel[2][2][8];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int j = 8 * half + s;
-      uint32_t x0, x1, y0, y1;
-      tq3_lookup4(sa[s], lut, x0, x1);
-      tq3_lookup4(sb[s], lut, y0, y1);
-      mma16816(s0, qa[j][0], qa[j][1], qa[j][2], qa[j][3], x0, x1);
-      mma16816(s1, qa[j][0], qa[j][1], qa[j][2], qa[j][3], y0, y1);
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        tq3_unit_selectors(u[t][r][3 * half], u[t][r][3 * half + 1], u[t][r][3 * half + 2], sel[t][r]);
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      const uint4 a = qs[(8 * half + st) * 32 + lane];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          uint32_t x0, x1;
+          tq3_lookup4(sel[t][r][st], lut, x0, x1);
+          mma16816(s[t][r], a.x, a.y, a.z, a.w, x0, x1);
+        }
     }
   }
 }
@@ -792,24 +822,21 @@ struct WarpState {
 
 // One block of format FMT at st (nv valid tokens): scores, online softmax, PV.
 template <int FMT>
-__device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* st, int nv,
-                                          const uint32_t (&qa)[16][4], WarpState& ws) {
+__device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* st, int nv, const uint4* qs,
+                                          WarpState& ws) {
   using B = Blk<FMT>;
   constexpr int NT = B::kTiles;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const Lut& lut = p.lut;
-  float sacc[NT][2][4];
+  float sacc[2][2][4];
 #pragma unroll
-  for (int t = 0; t < NT; ++t)
+  for (int t = 0; t < 2; ++t)
 #pragma unroll
     for (int h = 0; h < 2; ++h) sacc[t][h][0] = sacc[t][h][1] = sacc[t][h][2] = sacc[t][h][3] = 0.f;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    if (FMT == 0)
-      dec_qk_fp8(st + B::kK + t * kTileTokens * B::kRow, g, c, qa, sacc[t][0], sacc[t][1]);
-    else
-      dec_qk_tq3(st + B::kK + t * kTileTokens * B::kRow, g, c, qa, lut, sacc[t][0], sacc[t][1]);
-  }
+  if (FMT == 0)
+    dec_qk_fp8(st + B::kK, g, c, qs, sacc[0][0], sacc[0][1]);
+  else
+    dec_qk_tq3(st + B::kK, g, c, qs, lut, sacc);
   const __half2* ks = reinterpret_cast<const __half2*>(st + B::kKs);
   const __half2* vs = reinterpret_cast<const __half2*>(st + B::kVs);
   const float scale = p.score_scale;
@@ -851,7 +878,8 @@ __device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* 
       ws.o[i][3] *= a1;
     }
   }
-  // m_run stays -inf only for heads g >= G (all their scores -inf)
+  // m_run stays -inf only for heads g >= G (all their scores -inf); a masked
+  // score gives ex2(-inf) = 0, and 0 times a (finite, possibly stale) scale is 0
   const float mref = (ws.m_run == -INFINITY) ? 0.f : ws.m_run;
   const float vsc = FMT == 0 ? kFp8PScale : 1.f;
   uint2 pb[NT];
@@ -859,15 +887,11 @@ __device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* 
   for (int t = 0; t < NT; ++t) {
     float pr[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = (sc[t][i] == -INFINITY) ? 0.f : ex2(sc[t][i] - mref);
+    for (int i = 0; i < 4; ++i) pr[i] = ex2(sc[t][i] - mref);
     ws.l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
     const float2 v0 = __half22float2(vs[8 * t + c]), v1 = __half22float2(vs[8 * t + 4 + c]);
-    // masked tokens give exactly 0 (their scale bytes may be stale)
-    const float w0 = pr[0] == 0.f ? 0.f : pr[0] * (v0.x * vsc);
-    const float w1 = pr[1] == 0.f ? 0.f : pr[1] * (v0.y * vsc);
-    const float w2 = pr[2] == 0.f ? 0.f : pr[2] * (v1.x * vsc);
-    const float w3 = pr[3] == 0.f ? 0.f : pr[3] * (v1.y * vsc);
-    pb[t] = make_uint2(pack_half2(w0, w1), pack_half2(w2, w3));
+    pb[t] = make_uint2(pack_half2(pr[0] * (v0.x * vsc), pr[1] * (v0.y * vsc)),
+                       pack_half2(pr[2] * (v1.x * vsc), pr[3] * (v1.y * vsc)));
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
@@ -878,10 +902,26 @@ __device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* 
   }
 }
 
-// End of a piece: the 8 warps' states merge into the piece's partial state.
-// Each warp rescales its O to the common max of each head; O then sums up a
-// fixed tree (warps 4-7 into 0-3, 2-3 into 0-1, 1 into 0) so the result does
-// not depend on timing; warp 0 writes (m, l, o) per q head.
+// Store / add one warp's O fragments to / from a reduction buffer (lane-major).
+__device__ __forceinline__ void red_store(float* buf, const WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) buf[(4 * i + k) * 32 + lane] = ws.o[i][k];
+}
+__device__ __forceinline__ void red_add(const float* buf, WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ws.o[i][k] += buf[(4 * i + k) * 32 + lane];
+}
+
+// End of a piece: the CTA's warps' states merge into the
+// piece's partial state.  Each warp rescales its O to the common max of each
+// head; O then sums up a fixed tree (two buffers) so the result does not
+// depend on timing; warp 0 writes (m, l, o) per q head.
 __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
                                               WarpState& ws, int warp) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
@@ -922,25 +962,20 @@ __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSm
     ws.o[i][2] *= f0;
     ws.o[i][3] *= f1;
   }
-  // the tree: at each level the upper half stores, the lower half adds
+  // the tree: with n warps holding sums, warps [ceil(n/2), n) add into warps
+  // [0, n - ceil(n/2)), kRedBufs at a time
 #pragma unroll
-  for (int half = kDecWarps / 2; half >= 1; half >>= 1) {
-    if (warp >= half && warp < 2 * half) {
-      float* buf = sm.red + (warp - half) * kRedFloats + lane;
+  for (int n = kDecWarps; n > 1; n = (n + 1) / 2) {
+    const int lo = (n + 1) / 2;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) buf[(4 * i + k) * 32] = ws.o[i][k];
+    for (int i0 = 0; i0 < n - lo; i0 += kRedBufs) {
+      const int i = warp - lo - i0;                      // this warp as a source
+      if (i >= 0 && i < kRedBufs && lo + i0 + i < n) red_store(sm.red + i * kRedFloats, ws);
+      named_bar(1, kDecThreads);
+      const int j = warp - i0;                           // this warp as a destination
+      if (j >= 0 && j < kRedBufs && lo + i0 + j < n) red_add(sm.red + j * kRedFloats, ws);
+      if (n > 2) named_bar(1, kDecThreads);
     }
-    named_bar(1, kDecThreads);
-    if (warp < half) {
-      const float* buf = sm.red + warp * kRedFloats + lane;
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ws.o[i][k] += buf[(4 * i + k) * 32];
-    }
-    if (half > 1) named_bar(1, kDecThreads);
   }
   if (warp == 0) {
     float* dst = p.part + static_cast<size_t>(pc.part) * G * (2 + kHeadDim);
@@ -960,45 +995,47 @@ __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSm
   }
 }
 
-// The warp's blocks of one piece.  `q` counts the warp's blocks over the
-// launch (slot q % kSlots, phase q / kSlots); `ic` is the cursor of the next
-// block to copy in.
-template <int FMT>
-__device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
-                                          BlockCursor& ic, int& q, int warp, WarpState& ws) {
-  const int lane = threadIdx.x & 31;
-  if (warp >= pc.nblk) return;
-  uint32_t qa[16][4];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        p.qfrag + ((static_cast<size_t>(pc.b) * p.Hkv + pc.kvh) * 2 + FMT) * kQfragWords + lane * 64);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint4 v = src[j];
-      qa[j][0] = v.x;
-      qa[j][1] = v.y;
-      qa[j][2] = v.z;
-      qa[j][3] = v.w;
+// The warp's position in its own ring: slot and phase parity of the next
+// block it consumes.
+struct RingPos {
+  int slot, phase;
+  __device__ void step() {
+    if (++slot == kSlots) {
+      slot = 0;
+      phase ^= 1;
     }
   }
-  for (int k = warp; k < pc.nblk; k += kDecWarps, ++q) {
-    const int slot = q % kSlots;
+};
+
+// The warp's blocks of piece number pi (piece pc); `ic` is the cursor of the
+// next block to copy in.
+template <int FMT>
+__device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int pi,
+                                          BlockCursor& ic, RingPos& rp, int warp, WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+  if (warp >= pc.nblk) return;
+  const uint4* qs = sm.qbuf + (pi & 1) * (kQBytes / 16);
+  bool ok = dec_wait(sm, sm.qbar + (pi & 1), (pi >> 1) & 1, p.err);
+  for (int k = warp; k < pc.nblk; k += kDecWarps) {
     int nv = Blk<FMT>::kTokens;
     if (FMT == 0) {
       int e, tok0;
       nv = block_locate(p, pc, k, e, tok0);
     }
-    const bool ok = dec_wait(sm, sm.full + warp * kSlots + slot, (q / kSlots) & 1, p.err);
-    if (ok && nv > 0) dec_block<FMT>(p, sm.ring + (warp * kSlots + slot) * kSlotBytes, nv, qa, ws);
+    const bool okb = dec_wait(sm, sm.full + warp * kSlots + rp.slot, rp.phase, p.err);
+    if (ok && okb && nv > 0) dec_block<FMT>(p, sm.ring + (warp * kSlots + rp.slot) * kSlotBytes, nv, qs, ws);
+    ok = ok && okb;
     __syncwarp();
     // the slot is free again: copy in the warp's block kSlots further on
     if (ic.valid()) {
       if (lane == 0 && !aborted(sm)) {
-        dec_issue(p, sm, ic.pc, ic.k, warp, slot);
+        dec_issue(p, ic.pc, ic.k, sm.ring + (warp * kSlots + rp.slot) * kSlotBytes, sm.full + warp * kSlots + rp.slot,
+                  sm.abort_flag);
         ++ic.issued;
       }
       ic.advance(p, warp);
     }
+    rp.step();
   }
 }
 
@@ -1011,9 +1048,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(sm.full + warp * kSlots + i, 1);
+    if (warp == 0) {
+      mbar_init(sm.qbar, 1);
+      mbar_init(sm.qbar + 1, 1);
+      *sm.abort_flag = 0;
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (threadIdx.x == 0) *sm.abort_flag = 0;
   __syncthreads();
   // the warp's first kSlots blocks (their copies do not depend on q-prep,
   // except a request's last page, which dec_issue orders after it)
@@ -1021,35 +1062,54 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   ic.start(p, s0, s1, warp);
   for (int i = 0; i < kSlots && ic.valid(); ++i) {
     if (lane == 0) {
-      dec_issue(p, sm, ic.pc, ic.k, warp, i);
+      dec_issue(p, ic.pc, ic.k, sm.ring + (warp * kSlots + i) * kSlotBytes, sm.full + warp * kSlots + i,
+                sm.abort_flag);
       ++ic.issued;
     }
     ic.advance(p, warp);
   }
   // q fragments come from the preceding q-prep kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  int q = 0;
+  int qissued = 0;   // thread 0: pieces whose q fragments were copied in
+  if (threadIdx.x == 0)
+    for (; qissued < 2 && s0 + qissued < s1; ++qissued) dec_issue_q(p, sm, load_piece(p, s0 + qissued), qissued);
+  RingPos rp{0, 0};
   WarpState ws;
   for (int si = s0; si < s1; ++si) {
+    const int pi = si - s0;
     const Piece pc = load_piece(p, si);
 #pragma unroll
     for (int i = 0; i < 16; ++i) ws.o[i][0] = ws.o[i][1] = ws.o[i][2] = ws.o[i][3] = 0.f;
     ws.m_run = -INFINITY;
     ws.l_run = 0.f;
     if (pc.fmt)
-      dec_piece<1>(p, sm, pc, ic, q, warp, ws);
+      dec_piece<1>(p, sm, pc, pi, ic, rp, warp, ws);
     else
-      dec_piece<0>(p, sm, pc, ic, q, warp, ws);
+      dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
     dec_piece_end(p, sm, pc, ws, warp);
+    // every warp is past piece pi's QK work: its q buffer takes piece pi + 2
+    if (threadIdx.x == 0 && si + 2 < s1 && !aborted(sm)) {
+      dec_issue_q(p, sm, load_piece(p, si + 2), pi & 1);
+      ++qissued;
+    }
   }
-  // on the normal path every block copied in was consumed; after an abort,
-  // wait (bounded) for the warp's copies still in flight before exiting
-  __syncwarp();
-  if (lane == 0 && aborted(sm)) {
-    for (int j = ic.issued > kSlots ? ic.issued - kSlots : 0; j < ic.issued; ++j) {
-      const long long t0 = clock64();
-      while (!mbar_try_wait(sm.full + warp * kSlots + j % kSlots, (j / kSlots) & 1))
-        if (clock64() - t0 > kWaitCycles) break;
+  // on the normal path every copy issued was waited for; after an abort, wait
+  // (bounded) for copies still in flight before the CTA exits
+  __syncthreads();
+  if (aborted(sm)) {
+    if (lane == 0) {
+      for (int j = ic.issued > kSlots ? ic.issued - kSlots : 0; j < ic.issued; ++j) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(sm.full + warp * kSlots + j % kSlots, (j / kSlots) & 1))
+          if (clock64() - t0 > kWaitCycles) break;
+      }
+    }
+    if (threadIdx.x == 0) {
+      for (int j = qissued > 2 ? qissued - 2 : 0; j < qissued; ++j) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(sm.qbar + (j & 1), (j >> 1) & 1))
+          if (clock64() - t0 > kWaitCycles) break;
+      }
     }
   }
 }
