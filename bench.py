@@ -331,7 +331,8 @@ def run_mkv(args):
     kernel_bytes = [b / L for b, _ in bytes_acc for _ in range(L)]
     achieved = (sum(kernel_bytes) / len(kernel_bytes)) / (sum(kernel_ms) / len(kernel_ms) * 1e-3) / 1e9
     peak, peak_src = measured_peaks()
-    gpu_launches = args.steps * L * 3 + timed_demotes
+    # per layer and step: the decode kernel (with the fused append) and the merge
+    gpu_launches = args.steps * L * 2 + timed_demotes
     # ---------------- e2e through host buffers
     e2e = None
     if e2e_steps:

@@ -179,7 +179,6 @@ struct mkv_pool {
   int demote_cap = 0;
   float* workspace = nullptr;
   size_t workspace_bytes = 0;
-  uint32_t* qfrag = nullptr;
   int* err = nullptr;
   int chunk_cap = 0;
   int entry_cap = 0;
@@ -196,7 +195,6 @@ struct mkv_pool {
   std::vector<int32_t> plan_ids;
   DecodeParams plan_params{};
   MergeParams merge_params{};
-  QprepParams qprep_params{};
   int plan_parts = 0;
   std::vector<int32_t> plan_debug;   // 6 ints per chunk
   // one-shot timing events around the next decode kernel
@@ -206,8 +204,6 @@ struct mkv_pool {
   std::vector<int32_t> app_ids, app_new;
   int app_ntok = 0;
   // fused append-decode destinations (same region)
-  uint64_t ad_gen = 0;
-  std::vector<int32_t> ad_ids;
 };
 
 namespace {
@@ -260,7 +256,7 @@ mkv_status validate_config(const mkv_pool_config* c) {
 
 struct Sizes {
   int64_t fp8_page, tq3_page;
-  size_t fp8_arena, tq3_arena, plan, append, demote, workspace, qfrag, err, total;
+  size_t fp8_arena, tq3_arena, plan, append, demote, workspace, err, total;
   int entry_cap, chunk_cap;
 };
 
@@ -279,9 +275,8 @@ Sizes compute_sizes(const mkv_pool_config& c) {
   s.demote = align256(size_t(kDemoteCap) * 8);
   const int G = c.num_q_heads / c.num_kv_heads;
   s.workspace = align256(size_t(s.chunk_cap) * G * (2 + D) * 4);
-  s.qfrag = align256(size_t(mb) * c.num_kv_heads * 2 * kQfragWords * 4);
   s.err = 256;
-  s.total = s.fp8_arena + s.tq3_arena + s.plan + s.append + s.demote + s.workspace + s.qfrag + s.err;
+  s.total = s.fp8_arena + s.tq3_arena + s.plan + s.append + s.demote + s.workspace + s.err;
   return s;
 }
 
@@ -329,12 +324,15 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 
 // ------------------------------------------------------------------ planner
 // Relative cost of one token of one kv head, per format, plus a fixed cost per
-// block.  The decode kernel is ALU-bound on TQ3 dequantisation and closer to
-// bandwidth-bound on FP8 bytes; these weights balance the two across CTAs.
+// block and per piece, in units of one TQ3 token.  Fitted to per-CTA times of
+// the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.37 us of CTA
+// time, a 16-token FP8 block ~0.29 us, a piece ~5 us (its end-of-piece merge
+// and the warps left idle in its last round of blocks).
 constexpr double kCostTq3Token = 1.0;
-constexpr double kCostFp8Token = 1.3;
+constexpr double kCostFp8Token = 1.45;
 constexpr double kCostBlock = 8.0;
-constexpr int kMinBlocksPerCta = 16;   // two blocks per warp at least
+constexpr double kCostPiece = 540.0;
+constexpr int kMinBlocksPerCta = 24;   // two blocks per warp at least
 
 // Split the batch's pages into groups (request, kv head, format), lay the
 // groups' blocks out in one sequence, and cut that sequence into one
@@ -406,33 +404,50 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   auto cost = [&](const Blk& b) {
     return b.tokens * (groups[b.group].fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
   };
-  double total = 0.0;
-  for (const Blk& b : blocks) total += cost(b);
+  double blocks_cost = 0.0;
+  for (const Blk& b : blocks) blocks_cost += cost(b);
   // one CTA per SM, each with at least kMinBlocksPerCta blocks
   const int ncta = int(std::max<int64_t>(
       1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), int64_t(blocks.size()) / kMinBlocksPerCta})));
-  // cut the block sequence into ncta pieces lists of equal cost
+  // Cut the block sequence into ncta piece lists of equal cost, a piece
+  // costing kCostPiece on top of its blocks (the end-of-piece merge and the
+  // warps left idle in its last round).  Within a group, a cut falls only
+  // where the piece before it holds a multiple of kDecWarps blocks, so
+  // every warp of the CTA gets the same number of them.  Two passes: the
+  // second uses the piece count of the first.
   std::vector<Segment> segs;
   std::vector<int32_t> cta_seg(ncta + 1, 0);
-  const double per_cta = total / ncta;
-  double acc = 0.0;
-  int cur_cta = 0, cur_group = -1;
-  for (const Blk& b : blocks) {
-    int cta = int(acc / per_cta);
-    cta = std::min(std::max(cta, cur_cta), ncta - 1);
-    if (b.group != cur_group || cta != cur_cta) {
-      while (cur_cta < cta) cta_seg[++cur_cta] = int(segs.size());
-      const Group& g = groups[b.group];
-      Segment sg{};
-      sg.group = b.group;
-      sg.entry = g.entry0 + b.index / (P / (g.fmt ? kTq3Blk : kFp8Blk));
-      sg.blk = b.index;
-      segs.push_back(sg);
-      cur_group = b.group;
+  int npieces = ncta + int(groups.size());
+  int cur_cta = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    segs.clear();
+    std::fill(cta_seg.begin(), cta_seg.end(), 0);
+    const double per_cta = (blocks_cost + kCostPiece * npieces) / ncta;
+    double acc = 0.0;
+    int cur_group = -1, in_piece = 0;
+    cur_cta = 0;
+    for (const Blk& b : blocks) {
+      const bool new_group = b.group != cur_group;
+      const bool may_cut = new_group || in_piece % kDecWarps == 0;
+      const bool cut = may_cut && cur_cta < ncta - 1 && acc >= (cur_cta + 1) * per_cta;
+      if (new_group || cut) {
+        if (cut) cta_seg[++cur_cta] = int(segs.size());
+        const Group& g = groups[b.group];
+        Segment sg{};
+        sg.group = b.group;
+        sg.entry = g.entry0 + b.index / (P / (g.fmt ? kTq3Blk : kFp8Blk));
+        sg.blk = b.index;
+        segs.push_back(sg);
+        cur_group = b.group;
+        in_piece = 0;
+        acc += kCostPiece;
+      }
+      segs.back().nstages += 1;
+      segs.back().tokens += b.tokens;
+      acc += cost(b);
+      ++in_piece;
     }
-    segs.back().nstages += 1;
-    segs.back().tokens += b.tokens;
-    acc += cost(b);
+    npieces = int(segs.size());
   }
   while (cur_cta < ncta) cta_seg[++cur_cta] = int(segs.size());
   if (int(segs.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
@@ -477,7 +492,7 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   dp.tq3_page_bytes = p->tq3_page_bytes;
   dp.fp8_slots = p->cfg.fp8_slots;
   dp.tq3_slots = p->cfg.tq3_slots;
-  dp.qfrag = p->qfrag;
+  std::memcpy(dp.signs, p->signs, sizeof dp.signs);
   dp.Hq = p->cfg.num_q_heads;
   dp.Hkv = H;
   dp.G = p->G;
@@ -495,14 +510,6 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   mp.Hkv = H;
   mp.G = p->G;
   std::memcpy(mp.signs, p->signs, sizeof mp.signs);
-  QprepParams& qp = p->qprep_params;
-  qp = QprepParams{};
-  qp.n = n;
-  qp.Hq = p->cfg.num_q_heads;
-  qp.Hkv = H;
-  qp.G = p->G;
-  std::memcpy(qp.signs, p->signs, sizeof qp.signs);
-  qp.qfrag = p->qfrag;
   if (!upload) return MKV_OK;
   mkv_status st = staging_acquire(p->st_plan);
   if (st != MKV_OK) return st;
@@ -594,8 +601,6 @@ mkv_status mkv_pool_create(const mkv_pool_config* cfg, void* device_buf, size_t 
     off += S.demote;
     p->workspace = reinterpret_cast<float*>(b + off);
     off += S.workspace;
-    p->qfrag = reinterpret_cast<uint32_t*>(b + off);
-    off += S.qfrag;
     p->err = reinterpret_cast<int*>(b + off);
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->n_sm, cudaDevAttrMultiProcessorCount, p->device);
@@ -745,7 +750,6 @@ mkv_status mkv_append_tokens(mkv_pool* p, int32_t layer, int32_t n, const int32_
       if ((st = staging_acquire(p->st_append)) != MKV_OK) return st;
       std::memcpy(p->st_append.host, dest.data() + t0, size_t(cnt) * 4);
       if ((st = staging_upload(p->st_append, p->append_region, size_t(cnt) * 4, s)) != MKV_OK) return st;
-      p->ad_gen = 0;
     }
     ap.dest = p->append_region;
     ap.k = static_cast<const uint8_t*>(k) + t0 * row;
@@ -846,6 +850,35 @@ mkv_status mkv_demote_pages(mkv_pool* p, int32_t n, const int32_t* ids, const in
   return MKV_OK;
 }
 
+// Enqueue the decode kernel (with the fused append when k is non-NULL) and
+// the merge for the pool's current plan; partial states go to `part`.
+mkv_status enqueue_decode(mkv_pool* p, int32_t layer, const void* q, mkv_dtype q_dtype, float* part, const void* k,
+                          const void* v, mkv_dtype kv_dtype, float* out, float* lse, cudaStream_t s) {
+  DecodeParams dp = p->plan_params;
+  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
+  dp.q = q;
+  dp.q_bf16 = q_dtype == MKV_BF16;
+  dp.part = part;
+  dp.append = k != nullptr;
+  dp.kv_bf16 = kv_dtype == MKV_BF16;
+  dp.k = k;
+  dp.v = v;
+  cudaError_t e = cudaSuccess;
+  if (p->t_start) e = cudaEventRecord(p->t_start, s);
+  if (e == cudaSuccess) e = launch_decode(dp, s);
+  if (e == cudaSuccess && p->t_stop) e = cudaEventRecord(p->t_stop, s);
+  p->t_start = p->t_stop = nullptr;
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  MergeParams mp = p->merge_params;
+  mp.part = part;
+  mp.out = out;
+  mp.lse = lse;
+  e = launch_merge(mp, s);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return MKV_OK;
+}
+
 mkv_status mkv_decode_attention(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const void* q,
                                 mkv_dtype dtype, float* out, float* lse, mkv_stream_t stream) {
   if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
@@ -867,25 +900,7 @@ mkv_status mkv_decode_attention(mkv_pool* p, int32_t layer, int32_t n, const int
     p->plan_ids.assign(ids, ids + n);
   }
   if (p->host_only) return MKV_OK;
-  QprepParams qp = p->qprep_params;
-  qp.q = q;
-  qp.q_bf16 = dtype == MKV_BF16;
-  cudaError_t e = launch_qprep(qp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "q-prep launch");
-  DecodeParams dp = p->plan_params;
-  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
-  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
-  if (p->t_start) e = cudaEventRecord(p->t_start, s);
-  if (e == cudaSuccess) e = launch_decode(dp, s);
-  if (e == cudaSuccess && p->t_stop) e = cudaEventRecord(p->t_stop, s);
-  p->t_start = p->t_stop = nullptr;
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  MergeParams mp = p->merge_params;
-  mp.out = out;
-  mp.lse = lse;
-  e = launch_merge(mp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return MKV_OK;
+  return enqueue_decode(p, layer, q, dtype, p->workspace, nullptr, nullptr, MKV_F32, out, lse, s);
 }
 
 // Same as mkv_decode_attention, with the partial states in the library's fixed
@@ -915,34 +930,12 @@ mkv_status mkv_decode_attention_noalloc(mkv_pool* p, int32_t layer, int32_t n, c
   size_t scratch_bytes = 0;
   cudaError_t e = noalloc_scratch(&scratch, &scratch_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "device scratch address (cudaGetSymbolAddress)");
-  // scratch = [q fragments | partial states]
-  const size_t qf_words = size_t(n) * p->cfg.num_kv_heads * 2 * kQfragWords;
-  const size_t need = qf_words * 4 + size_t(p->plan_parts) * p->G * (2 + kHeadDim) * sizeof(float);
+  // scratch = the partial states
+  const size_t need = size_t(p->plan_parts) * p->G * (2 + kHeadDim) * sizeof(float);
   if (need > scratch_bytes)
     return fail(MKV_ERR_CAPACITY, "batch needs %zu bytes of scratch; the fixed scratch holds %zu", need,
                 scratch_bytes);
-  uint32_t* qfrag = reinterpret_cast<uint32_t*>(scratch);
-  float* part = scratch + qf_words;
-  QprepParams qp = p->qprep_params;
-  qp.q = q;
-  qp.q_bf16 = dtype == MKV_BF16;
-  qp.qfrag = qfrag;
-  e = launch_qprep(qp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "q-prep launch");
-  DecodeParams dp = p->plan_params;
-  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
-  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
-  dp.qfrag = qfrag;
-  dp.part = part;
-  e = launch_decode(dp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  MergeParams mp = p->merge_params;
-  mp.part = part;
-  mp.out = out;
-  mp.lse = lse;
-  e = launch_merge(mp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return MKV_OK;
+  return enqueue_decode(p, layer, q, dtype, scratch, nullptr, nullptr, MKV_F32, out, lse, s);
 }
 
 mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const void* k,
@@ -974,49 +967,7 @@ mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_
     p->plan_gen = p->generation;
     p->plan_ids.assign(ids, ids + n);
   }
-  const bool dest_cached = p->ad_gen == p->generation && p->ad_ids.size() == size_t(n) &&
-                           std::equal(ids, ids + n, p->ad_ids.begin());
-  if (!dest_cached) {
-    if (n > p->append_cap) return fail(MKV_ERR_CAPACITY, "batch larger than the append region");
-    if ((st = staging_acquire(p->st_append)) != MKV_OK) return st;
-    uint32_t* h = static_cast<uint32_t*>(p->st_append.host);
-    for (int i = 0; i < n; ++i) {
-      const SeqRec& sq = p->seqs[ids[i]];
-      const int pos = sq.len - 1;
-      h[i] = (uint32_t(sq.pages[pos / P].slot) << 8) | uint32_t(pos % P);
-    }
-    if ((st = staging_upload(p->st_append, p->append_region, size_t(n) * 4, s)) != MKV_OK) return st;
-    p->app_gen = 0;
-    p->ad_gen = p->generation;
-    p->ad_ids.assign(ids, ids + n);
-  }
-  QprepParams qp = p->qprep_params;
-  qp.q = q;
-  qp.q_bf16 = q_dtype == MKV_BF16;
-  qp.append = 1;
-  qp.kv_bf16 = kv_dtype == MKV_BF16;
-  qp.P = P;
-  qp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
-  qp.fp8_page_bytes = p->fp8_page_bytes;
-  qp.dest = p->append_region;
-  qp.k = k;
-  qp.v = v;
-  cudaError_t e = launch_qprep(qp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "q-prep/append launch");
-  DecodeParams dp = p->plan_params;
-  dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
-  dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
-  if (p->t_start) e = cudaEventRecord(p->t_start, s);
-  if (e == cudaSuccess) e = launch_decode(dp, s);
-  if (e == cudaSuccess && p->t_stop) e = cudaEventRecord(p->t_stop, s);
-  p->t_start = p->t_stop = nullptr;
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  MergeParams mp = p->merge_params;
-  mp.out = out;
-  mp.lse = lse;
-  e = launch_merge(mp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-  return MKV_OK;
+  return enqueue_decode(p, layer, q, q_dtype, p->workspace, k, v, kv_dtype, out, lse, s);
 }
 
 mkv_status mkv_dequantize_pages(mkv_pool* p, int32_t layer, int32_t seq, int32_t page0, int32_t npages,

@@ -11,11 +11,12 @@ namespace mkv {
 
 constexpr int kHeadDim = 256;      // head_dim the kernels are written for
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one MMA tile
+constexpr int kDecWarps = 12;     // warps of a decode CTA (a piece's blocks go round-robin)
 constexpr int kFp8Blk = 16;        // tokens per FP8 decode block (one MMA tile)
 constexpr int kTq3Blk = 32;        // tokens per TQ3 decode block (two MMA tiles)
 constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
 constexpr int kMaxCtas = 1024;     // upper bound on decode CTAs
-constexpr int kQfragWords = 2048;  // q-prep fragment words per (b, kvh, format)
+constexpr int kQfragWords = 2048;  // A-fragment words of one piece's q rows (16 x 256 fp16)
 
 // Error bits written by kernels into the pool's device error word.
 enum : int {
@@ -68,7 +69,7 @@ struct Lut {               // byte tables for the PRMT level lookup
 };
 
 struct DecodeParams {
-  const uint8_t* fp8_layer;        // FP8 arena base of this layer
+  uint8_t* fp8_layer;              // FP8 arena base of this layer (written by the fused append)
   const uint8_t* tq3_layer;        // TQ3 arena base of this layer
   int64_t fp8_page_bytes, tq3_page_bytes;
   int32_t fp8_slots, tq3_slots;
@@ -77,30 +78,20 @@ struct DecodeParams {
   const Segment* segs;             // per-CTA pieces, CTA by CTA
   const int32_t* cta_seg;          // [n_ctas + 1] into segs
   int32_t n_ctas;
-  const uint32_t* qfrag;           // q-prep output: [(b*Hkv + kvh)*2 + fmt][32][64]
+  const void* q;                   // [n, Hq, D], fp32 or bf16
+  int32_t q_bf16;
+  uint64_t signs[4];               // rotation signs (bit i set: negative)
   int32_t Hq, Hkv, G, P;
   float* part;                     // [parts][G][2 + D] (m in log2 units, l, o)
   float score_scale;               // log2(e) / sqrt(d)
   Lut lut;
-  int* err;
-};
-
-struct QprepParams {
-  const void* q;                   // [n, Hq, D]
-  int32_t q_bf16;
-  int32_t n, Hq, Hkv, G;
-  uint64_t signs[4];
-  uint32_t* qfrag;
-  // optional fused single-token append (mkv_append_decode): one new token per
-  // request, rows k/v [n, Hkv, D], destinations as in AppendParams
+  // fused single-token append (mkv_append_decode): each request's newest
+  // token (the last valid one of its tail page), rows k/v [n, Hkv, D]
   int32_t append;
   int32_t kv_bf16;
-  int32_t P;
-  uint8_t* fp8_layer;
-  int64_t fp8_page_bytes;
-  const uint32_t* dest;
   const void* k;
   const void* v;
+  int* err;
 };
 
 struct MergeParams {
@@ -149,9 +140,9 @@ struct DequantParams {
 // Kernel launchers (mkv_kernels.cu).  Return cudaGetLastError() of the launch.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
-cudaError_t launch_qprep(const QprepParams& p, cudaStream_t s);
-// Launched with programmatic stream serialisation so its copies start while
-// the preceding q-prep kernel finishes; its QK warps wait for q-prep's output.
+// Launched with programmatic stream serialisation: its first page copies start
+// while the preceding kernel finishes; it waits for that kernel before reading
+// q or writing partial states.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s);

@@ -11,8 +11,6 @@
 //   mkv_append_kernel  -- FP8 quantise new K/V rows into their pages
 //   mkv_demote_kernel  -- FP8 page -> TQ3 page (dequantise, rotate, RMS scale,
 //                         Lloyd-Max codes, pack)
-//   mkv_qprep_kernel   -- per (request, kv head): q rows (and q' = R q) as
-//                         fp16 hi/lo MMA fragments
 //   mkv_decode_kernel  -- persistent partial-attention kernel over both
 //                         formats: 12 independent warps per CTA, each with its
 //                         own ring of bulk-copied page blocks
@@ -114,11 +112,11 @@ __device__ __forceinline__ void tq3_unit_selectors(uint32_t w0, uint32_t w1, uin
 }
 
 // ============================================================== append
-// FP8-quantise one row (one token, kv head, K|V) into its page: the calling
-// warp holds the row; s = fp16(amax / 448), codes = e4m3_rn_satfinite(x / s)
-// with IEEE fp32 divisions.
-__device__ __forceinline__ void fp8_append_row(const void* src_rows, size_t row, int bf16, uint8_t* plane, int P,
-                                               int kv, int pos, int lane) {
+// FP8-quantise one row (one token, kv head, K|V) held by the calling warp:
+// s = fp16(amax / 448), codes = e4m3_rn_satfinite(x / s) with IEEE fp32
+// divisions.  Lane l gets the codes of dims 8l .. 8l+7 (two per c[i]).
+__device__ __forceinline__ void fp8_quantize_row(const void* src_rows, size_t row, int bf16, int lane,
+                                                 uint32_t (&c)[4], __half& s16) {
   float x[8];
   if (bf16) {
     const uint4 raw = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src_rows) + row)[lane];
@@ -139,9 +137,8 @@ __device__ __forceinline__ void fp8_append_row(const void* src_rows, size_t row,
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-  const __half s16 = __float2half_rn(__fdiv_rn(amax, 448.0f));
+  s16 = __float2half_rn(__fdiv_rn(amax, 448.0f));
   const float s = __half2float(s16);
-  uint32_t c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint16_t two = 0;
@@ -152,6 +149,13 @@ __device__ __forceinline__ void fp8_append_row(const void* src_rows, size_t row,
     }
     c[i] = two;
   }
+}
+// Store a quantised row at position pos of a K (kv = 0) or V (kv = 1) plane
+// of P tokens: K codes row-major, V codes pair-interleaved, then P fp16 scales.
+// Works on a page plane in global memory and on a staged block in shared
+// memory alike (a staged FP8 block has the layout of a 16-token page).
+__device__ __forceinline__ void fp8_store_row(uint8_t* plane, int P, int kv, int pos, int lane,
+                                              const uint32_t (&c)[4], __half s16) {
   if (kv == 0) {
     uint2 w;
     w.x = c[0] | (c[1] << 16);
@@ -182,8 +186,10 @@ __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
   const int P = p.P;
   uint8_t* plane = p.fp8_layer + static_cast<int64_t>(slot) * p.fp8_page_bytes +
                    static_cast<int64_t>(h) * 2 * (P * (kHeadDim + 2)) + kv * (P * (kHeadDim + 2));
-  fp8_append_row(kv ? p.v : p.k, (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim, p.kv_bf16, plane, P, kv, pos,
-                 lane);
+  uint32_t c[4];
+  __half s16;
+  fp8_quantize_row(kv ? p.v : p.k, (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim, p.kv_bf16, lane, c, s16);
+  fp8_store_row(plane, P, kv, pos, lane, c, s16);
 }
 
 // ============================================================== demote
@@ -427,102 +433,6 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
   }
 }
 
-// ============================================================== q prep
-// Per (request, kv head): the QK warps' MMA A fragments of the group's query
-// rows for both formats -- FP8 pages score against q, TQ3 pages against
-// q' = R q (signs, then H, then 1/16).  Rows 0-7 of the A tile hold fp16(q_h)
-// of heads h = 0..G-1, rows 8-15 the fp16 residual q_h - fp16(q_h), so the
-// two halves of the S accumulator add up to an fp32-accurate score.
-// Fragment layout: [(b*Hkv + kvh)*2 + fmt][k-step 16][lane 32][4 regs], with
-// lane (g, c) = (lane/4, lane%4) covering dims 64c + 4j .. 64c + 4j + 3 at
-// k-step j (k-step-major, so a warp reads one k-step as 512 contiguous bytes).
-__global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
-  __shared__ __align__(16) float qs[2][kMaxGroup][kHeadDim];
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.x / p.Hkv, kvh = blockIdx.x % p.Hkv;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp >= kMaxGroup) {
-    // fused single-token append: warp 8 writes the K row, warp 9 the V row
-    if (p.append) {
-      const int kv = warp - kMaxGroup;
-      const uint32_t dst = p.dest[b];
-      const int slot = static_cast<int>(dst >> 8), pos = static_cast<int>(dst & 0xff);
-      uint8_t* plane = p.fp8_layer + static_cast<int64_t>(slot) * p.fp8_page_bytes +
-                       static_cast<int64_t>(kvh) * 2 * (p.P * (kHeadDim + 2)) + kv * (p.P * (kHeadDim + 2));
-      fp8_append_row(kv ? p.v : p.k, (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim, p.kv_bf16, plane, p.P, kv,
-                     pos, lane);
-    }
-    __syncthreads();
-    return;
-  }
-  float x[8];
-  if (warp < p.G) {
-    const size_t off = (static_cast<size_t>(b) * p.Hq + kvh * p.G + warp) * kHeadDim + 8 * lane;
-    if (p.q_bf16) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(b2[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-      }
-    } else {
-      const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + off);
-      const float4 a = f4[0], c = f4[1];
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = 0.f;
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) qs[0][warp][8 * lane + i] = x[i];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
-#pragma unroll
-  for (int hs = 1; hs < 8; hs <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((i & hs) == 0) {
-        const float a = x[i], c = x[i + hs];
-        x[i] = a + c;
-        x[i + hs] = a - c;
-      }
-  }
-#pragma unroll
-  for (int lm = 1; lm < 32; lm <<= 1) {
-    const bool upper = (lane & lm) != 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float o = __shfl_xor_sync(kFull, x[i], lm);
-      x[i] = upper ? (o - x[i]) : (x[i] + o);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) qs[1][warp][8 * lane + i] = x[i] * (1.0f / 16.0f);
-  __syncthreads();
-  if (threadIdx.x >= 256) return;
-  const int fmt = threadIdx.x >> 7, L = (threadIdx.x >> 2) & 31, j0 = 4 * (threadIdx.x & 3);
-  const int g = L >> 2, c = L & 3;
-  uint4* dst = reinterpret_cast<uint4*>(p.qfrag + ((static_cast<size_t>(b) * p.Hkv + kvh) * 2 + fmt) * kQfragWords) +
-              j0 * 32 + L;
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const float4 v = *reinterpret_cast<const float4*>(&qs[fmt][g][64 * c + 4 * (j0 + jj)]);
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-    float hi[4], lo[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      hi[i] = __half2float(__float2half_rn(vv[i]));
-      lo[i] = vv[i] - hi[i];
-    }
-    dst[jj * 32] = make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
-                              pack_half2(lo[2], lo[3]));
-  }
-}
-
 // ============================================================== decode
 // Persistent partial-attention kernel; one CTA of kDecWarps (12) warps per SM.
 // The host cut the launch's blocks into one contiguous, cost-balanced piece
@@ -541,7 +451,6 @@ __global__ void __launch_bounds__(320) mkv_qprep_kernel(QprepParams p) {
 // warp's block kSlots further on as soon as the warp is done with it.  No
 // warp waits for another except at the end of a piece, where the warps'
 // states merge, in a fixed order, into one partial state (m, l, o) per q head.
-constexpr int kDecWarps = 12;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kSlots = 2;                 // staging slots per warp
 constexpr int kSlotBytes = 2 * (kFp8Blk * kHeadDim + 2 * kFp8Blk);   // an FP8 block; a TQ3 block fits
@@ -572,14 +481,13 @@ struct DecSmem {
   float* epi_m;                                // [warp][kMaxGroup]
   float* epi_l;
   uint64_t* full;                              // [warp][slot]
-  uint64_t* qbar;                              // [2]
   int* abort_flag;
 };
 constexpr int kDecSmemRing = kDecWarps * kSlots * kSlotBytes;
 constexpr int kDecSmemQ = 2 * kQBytes;
 constexpr int kDecSmemRed = kRedBufs * kRedFloats * 4;
 constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
-constexpr int kDecSmemBars = (kDecWarps * kSlots + 2) * 8 + 16;
+constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
 constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
 static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 
@@ -591,8 +499,7 @@ __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   s.epi_m = s.red + kRedBufs * kRedFloats;
   s.epi_l = s.epi_m + kDecWarps * kMaxGroup;
   s.full = reinterpret_cast<uint64_t*>(s.epi_l + kDecWarps * kMaxGroup);
-  s.qbar = s.full + kDecWarps * kSlots;
-  s.abort_flag = reinterpret_cast<int*>(s.qbar + 2);
+  s.abort_flag = reinterpret_cast<int*>(s.full + kDecWarps * kSlots);
   return s;
 }
 
@@ -685,9 +592,6 @@ __device__ __noinline__ void dec_issue(const DecodeParams& p, Piece pc, int k, u
     mbar_arrive(bar);
     return;
   }
-  // a request's last page may still be receiving its new token from the
-  // preceding (q-prep + append) kernel: copy it only once that kernel is done
-  if (pe.tail) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = pc.fmt ? 3 * kHeadDim / 8 : kHeadDim;
   const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
   const int plane = p.P * (row + 2);
@@ -703,13 +607,106 @@ __device__ __noinline__ void dec_issue(const DecodeParams& p, Piece pc, int k, u
   bulk_g2s(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar);
 }
 
-// Thread 0: copy piece pc's q fragments (8 KB, written by the q-prep kernel)
-// into q buffer `buf`.
-__device__ __forceinline__ void dec_issue_q(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int buf) {
-  const uint32_t* src = p.qfrag + ((static_cast<size_t>(pc.b) * p.Hkv + pc.kvh) * 2 + pc.fmt) * kQfragWords;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_tx(sm.qbar + buf, kQBytes);
-  bulk_g2s(sm.qbuf + buf * (kQBytes / 16), src, kQBytes, sm.qbar + buf);
+// Raw q row h of piece pc (8 dims per lane, bf16 in r[0] or fp32 in r[0..1]);
+// zeros for h >= G.  Split from dec_build_q_row so the load can be issued a
+// piece ahead.
+struct QRow {
+  uint4 r[2];
+};
+__device__ __forceinline__ QRow dec_load_q_row(const DecodeParams& p, const Piece& pc, int h, int lane) {
+  QRow q{};
+  if (h < p.G) {
+    const size_t off = (static_cast<size_t>(pc.b) * p.Hq + pc.kvh * p.G + h) * kHeadDim + 8 * lane;
+    if (p.q_bf16) {
+      q.r[0] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
+    } else {
+      const uint4* f4 = reinterpret_cast<const uint4*>(static_cast<const float*>(p.q) + off);
+      q.r[0] = f4[0];
+      q.r[1] = f4[1];
+    }
+  } else {
+    q.r[0] = q.r[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  return q;
+}
+
+// Row h of piece pc's A fragments from its raw q row, written by one warp
+// into q buffer qb: rows 0-7 hold fp16(x), rows 8-15 the fp16 residual
+// x - fp16(x), where x is q (FP8 pieces) or q' = R q = (H D q)/16 (TQ3
+// pieces; signs, then the Walsh-Hadamard butterflies, 8 dims per lane in
+// registers and across lanes by shuffles).  Fragment layout [k-step 16]
+// [lane 32][4 regs]: lane (g, c) at k-step j covers dims 64c + 4j .. +3 of
+// row g, so lane l of this warp (dims 8l .. 8l+7) fills fragment lane
+// 4h + l/8 at k-steps 2(l%8) and 2(l%8) + 1.
+__device__ __forceinline__ void dec_build_q_row(const DecodeParams& p, uint4* qb, const Piece& pc, int h, int lane,
+                                                const QRow& q) {
+  float x[8];
+  if (p.q_bf16) {
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&q.r[0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b2[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else {
+    const float* f = reinterpret_cast<const float*>(&q.r[0]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = f[i];
+  }
+  if (pc.fmt) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
+#pragma unroll
+    for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((i & hs) == 0) {
+          const float a = x[i], c = x[i + hs];
+          x[i] = a + c;
+          x[i + hs] = a - c;
+        }
+    }
+#pragma unroll
+    for (int lm = 1; lm < 32; lm <<= 1) {
+      const bool upper = (lane & lm) != 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_xor_sync(kFull, x[i], lm);
+        x[i] = upper ? (o - x[i]) : (x[i] + o);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] *= (1.0f / 16.0f);
+  }
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    float hi[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      hi[i] = __half2float(__float2half_rn(x[4 * jj + i]));
+      lo[i] = x[4 * jj + i] - hi[i];
+    }
+    qb[(2 * (lane & 7) + jj) * 32 + 4 * h + (lane >> 3)] =
+        make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
+                   pack_half2(lo[2], lo[3]));
+  }
+}
+
+// The first two pieces' q fragments (into buffers 0 and 1): the CTA's warps
+// share the 2 x kMaxGroup rows.  Ends with a CTA barrier.
+__device__ __forceinline__ void dec_prep_q_first(const DecodeParams& p, const DecSmem& sm, int s0, int s1, int warp,
+                                                 int lane) {
+  for (int task = warp; task < 2 * kMaxGroup; task += kDecWarps) {
+    const int i = task / kMaxGroup;
+    if (s0 + i < s1) {
+      const Piece pc = load_piece(p, s0 + i);
+      dec_build_q_row(p, sm.qbuf + i * (kQBytes / 16), pc, task % kMaxGroup,
+                      lane, dec_load_q_row(p, pc, task % kMaxGroup, lane));
+    }
+  }
+  named_bar(1, kDecThreads);
 }
 
 // The two 12-byte units at p (8-byte aligned): words of unit 0 in u[0..2],
@@ -1007,24 +1004,46 @@ struct RingPos {
   }
 };
 
+// Fused append (mkv_append_decode): the warp whose FP8 block holds a
+// request's newest token quantises the token's K and V rows, stores them into
+// the page (global memory, for later steps) and into the staged block it has
+// just received (whose copy predates them).
+__device__ __forceinline__ void dec_append_tail(const DecodeParams& p, const Piece& pc, const PageEntry& pe, int tok0,
+                                                uint8_t* st, int lane) {
+  const int pos = pe.nvalid - 1;
+  const size_t row = (static_cast<size_t>(pc.b) * p.Hkv + pc.kvh) * kHeadDim;
+  const int plane = p.P * (kHeadDim + 2);
+  uint8_t* hp = p.fp8_layer + static_cast<int64_t>(pe.slot) * p.fp8_page_bytes + static_cast<int64_t>(pc.kvh) * 2 * plane;
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    uint32_t c[4];
+    __half s16;
+    fp8_quantize_row(kv ? p.v : p.k, row, p.kv_bf16, lane, c, s16);
+    fp8_store_row(hp + kv * plane, p.P, kv, pos, lane, c, s16);
+    fp8_store_row(st + kv * (Blk<0>::kBytes / 2), kFp8Blk, kv, pos - tok0, lane, c, s16);
+  }
+  __syncwarp();
+}
+
 // The warp's blocks of piece number pi (piece pc); `ic` is the cursor of the
 // next block to copy in.
 template <int FMT>
 __device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int pi,
                                           BlockCursor& ic, RingPos& rp, int warp, WarpState& ws) {
   const int lane = threadIdx.x & 31;
-  if (warp >= pc.nblk) return;
   const uint4* qs = sm.qbuf + (pi & 1) * (kQBytes / 16);
-  bool ok = dec_wait(sm, sm.qbar + (pi & 1), (pi >> 1) & 1, p.err);
   for (int k = warp; k < pc.nblk; k += kDecWarps) {
-    int nv = Blk<FMT>::kTokens;
-    if (FMT == 0) {
-      int e, tok0;
-      nv = block_locate(p, pc, k, e, tok0);
+    int nv = Blk<FMT>::kTokens, e = 0, tok0 = 0;
+    if (FMT == 0) nv = block_locate(p, pc, k, e, tok0);
+    const bool ok = dec_wait(sm, sm.full + warp * kSlots + rp.slot, rp.phase, p.err);
+    uint8_t* st = sm.ring + (warp * kSlots + rp.slot) * kSlotBytes;
+    if (ok && nv > 0) {
+      if (FMT == 0 && p.append) {
+        const PageEntry pe = p.entries[e];
+        if (pe.tail && pe.nvalid - 1 >= tok0 && pe.nvalid - 1 < tok0 + kFp8Blk) dec_append_tail(p, pc, pe, tok0, st, lane);
+      }
+      dec_block<FMT>(p, st, nv, qs, ws);
     }
-    const bool okb = dec_wait(sm, sm.full + warp * kSlots + rp.slot, rp.phase, p.err);
-    if (ok && okb && nv > 0) dec_block<FMT>(p, sm.ring + (warp * kSlots + rp.slot) * kSlotBytes, nv, qs, ws);
-    ok = ok && okb;
     __syncwarp();
     // the slot is free again: copy in the warp's block kSlots further on
     if (ic.valid()) {
@@ -1048,16 +1067,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(sm.full + warp * kSlots + i, 1);
-    if (warp == 0) {
-      mbar_init(sm.qbar, 1);
-      mbar_init(sm.qbar + 1, 1);
-      *sm.abort_flag = 0;
-    }
+    if (warp == 0) *sm.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // the warp's first kSlots blocks (their copies do not depend on q-prep,
-  // except a request's last page, which dec_issue orders after it)
+  // the warp's first kSlots blocks: pages are written only by kernels that
+  // finish before this one starts
   BlockCursor ic;
   ic.start(p, s0, s1, warp);
   for (int i = 0; i < kSlots && ic.valid(); ++i) {
@@ -1068,16 +1083,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     }
     ic.advance(p, warp);
   }
-  // q fragments come from the preceding q-prep kernel
+  // q, and the partial-state workspace the previous launch's merge may still
+  // read, belong to the preceding kernels: wait for them, then build the first
+  // two pieces' q fragments while the first blocks arrive
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  int qissued = 0;   // thread 0: pieces whose q fragments were copied in
-  if (threadIdx.x == 0)
-    for (; qissued < 2 && s0 + qissued < s1; ++qissued) dec_issue_q(p, sm, load_piece(p, s0 + qissued), qissued);
+  dec_prep_q_first(p, sm, s0, s1, warp, lane);
   RingPos rp{0, 0};
   WarpState ws;
   for (int si = s0; si < s1; ++si) {
     const int pi = si - s0;
     const Piece pc = load_piece(p, si);
+    // warp h < kMaxGroup builds row h of piece si + 2's q fragments at the end
+    // of this piece; its q row load goes out now
+    const bool prep_next = si + 2 < s1 && warp < kMaxGroup;
+    Piece pn{};
+    QRow qn{};
+    if (prep_next) {
+      pn = load_piece(p, si + 2);
+      qn = dec_load_q_row(p, pn, warp, lane);
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) ws.o[i][0] = ws.o[i][1] = ws.o[i][2] = ws.o[i][3] = 0.f;
     ws.m_run = -INFINITY;
@@ -1087,29 +1111,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     else
       dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
     dec_piece_end(p, sm, pc, ws, warp);
-    // every warp is past piece pi's QK work: its q buffer takes piece pi + 2
-    if (threadIdx.x == 0 && si + 2 < s1 && !aborted(sm)) {
-      dec_issue_q(p, sm, load_piece(p, si + 2), pi & 1);
-      ++qissued;
+    // every warp is past piece pi: its q buffer takes piece pi + 2
+    if (si + 2 < s1) {
+      if (prep_next) dec_build_q_row(p, sm.qbuf + (pi & 1) * (kQBytes / 16), pn, warp, lane, qn);
+      named_bar(1, kDecThreads);
     }
   }
   // on the normal path every copy issued was waited for; after an abort, wait
   // (bounded) for copies still in flight before the CTA exits
   __syncthreads();
-  if (aborted(sm)) {
-    if (lane == 0) {
-      for (int j = ic.issued > kSlots ? ic.issued - kSlots : 0; j < ic.issued; ++j) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(sm.full + warp * kSlots + j % kSlots, (j / kSlots) & 1))
-          if (clock64() - t0 > kWaitCycles) break;
-      }
-    }
-    if (threadIdx.x == 0) {
-      for (int j = qissued > 2 ? qissued - 2 : 0; j < qissued; ++j) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(sm.qbar + (j & 1), (j >> 1) & 1))
-          if (clock64() - t0 > kWaitCycles) break;
-      }
+  if (aborted(sm) && lane == 0) {
+    for (int j = ic.issued > kSlots ? ic.issued - kSlots : 0; j < ic.issued; ++j) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(sm.full + warp * kSlots + j % kSlots, (j / kSlots) & 1))
+        if (clock64() - t0 > kWaitCycles) break;
     }
   }
 }
@@ -1254,11 +1269,6 @@ int decode_threads() { return kDecThreads; }
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
   const int rows = p.npages * p.P * p.Hkv * 2;
   if (rows > 0) mkv_dequant_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_qprep(const QprepParams& p, cudaStream_t s) {
-  if (p.n * p.Hkv > 0) mkv_qprep_kernel<<<p.n * p.Hkv, 320, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -219,11 +219,17 @@ def test_plan_covers_every_page_once(mkv):
                 pool.demote([r] * len(stale), stale)
         ids = list(range(w.n))
         plan = _check_plan_covers(mkv, pool, ids, w.lengths, w.tiers)
-        # byte balance: no TQ3 chunk is more than ~3x the mean (LPT assignment
-        # handles the rest); there are at most a few chunks per CTA
-        tq = [c[5] for c in plan if c[2] == 3]
-        if tq:
-            assert max(tq) <= 3 * np.mean(tq) + 64
+        # balance: a host-only pool plans for up to 152 CTAs (24 blocks each at
+        # least); no chunk is larger than
+        # one CTA's share of the estimated work (blocks of 32 TQ3 / 16 FP8
+        # tokens with a fixed cost each, and a fixed cost per chunk) plus one
+        # warp-round of blocks; there are at most a few chunks per CTA
+        def cost(c):
+            bt, per_tok = (32, 1.0) if c[2] == 3 else (16, 1.45)
+            return c[5] * per_tok + 8.0 * -(-c[5] // bt) + 540.0
+        nblk = sum(-(-c[5] // (32 if c[2] == 3 else 16)) for c in plan)
+        share = sum(cost(c) for c in plan) / max(1, min(152, nblk // 24))
+        assert max(cost(c) for c in plan) <= share + 12 * 40.0
         assert len(plan) <= w.n * 4 * 2 + 4 * 1024
 
 

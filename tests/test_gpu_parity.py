@@ -317,7 +317,7 @@ def test_full_size_sampled(mkv, name):
 
 # ------------------------------------------------------------------ fused append + decode
 def test_append_decode_matches_separate_calls(mkv):
-    """mkv_append_decode (append fused into the q-preparation kernel) gives the
+    """mkv_append_decode (append fused into the decode kernel) gives the
     same page bytes and the same outputs as mkv_append_tokens + mkv_decode_attention."""
     g = torch.Generator().manual_seed(21)
     pools = [_small_pool(mkv, P=64, layers=2, fp8=64, tq3=64, maxp=24, seed=77) for _ in range(2)]
