@@ -416,11 +416,14 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   // every warp of the CTA gets the same number of them.  Two passes: the
   // second uses the piece count of the first.
   std::vector<Segment> segs;
+  std::vector<int32_t> seg_entry, seg_tokens;   // first page entry and valid tokens of each piece
   std::vector<int32_t> cta_seg(ncta + 1, 0);
   int npieces = ncta + int(groups.size());
   int cur_cta = 0;
   for (int pass = 0; pass < 2; ++pass) {
     segs.clear();
+    seg_entry.clear();
+    seg_tokens.clear();
     std::fill(cta_seg.begin(), cta_seg.end(), 0);
     const double per_cta = (blocks_cost + kCostPiece * npieces) / ncta;
     double acc = 0.0;
@@ -434,16 +437,21 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
         if (cut) cta_seg[++cur_cta] = int(segs.size());
         const Group& g = groups[b.group];
         Segment sg{};
+        sg.fmt = g.fmt;
+        sg.b = g.b;
+        sg.kvh = g.kvh;
+        sg.entry0 = g.entry0;
         sg.group = b.group;
-        sg.entry = g.entry0 + b.index / (P / (g.fmt ? kTq3Blk : kFp8Blk));
         sg.blk = b.index;
         segs.push_back(sg);
+        seg_entry.push_back(g.entry0 + b.index / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
+        seg_tokens.push_back(0);
         cur_group = b.group;
         in_piece = 0;
         acc += kCostPiece;
       }
-      segs.back().nstages += 1;
-      segs.back().tokens += b.tokens;
+      segs.back().nblk += 1;
+      seg_tokens.back() += b.tokens;
       acc += cost(b);
       ++in_piece;
     }
@@ -475,8 +483,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   for (const Segment& sg : segs) {
     const Group& g = groups[sg.group];
     const int bpp = P / (g.fmt ? kTq3Blk : kFp8Blk);
-    const int last = g.entry0 + (sg.blk + sg.nstages - 1) / bpp;
-    const int32_t rec[6] = {g.b, g.kvh, g.fmt ? 3 : 1, sg.entry, last - sg.entry + 1, sg.tokens};
+    const size_t i = size_t(&sg - segs.data());
+    const int last = g.entry0 + (sg.blk + sg.nblk - 1) / bpp;
+    const int32_t rec[6] = {g.b, g.kvh, g.fmt ? 3 : 1, seg_entry[i], last - seg_entry[i] + 1, seg_tokens[i]};
     p->plan_debug.insert(p->plan_debug.end(), rec, rec + 6);
   }
   p->plan_parts = int(segs.size());

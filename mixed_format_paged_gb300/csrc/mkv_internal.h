@@ -42,16 +42,17 @@ struct Group {             // one run of pages: (request, kv head, format)
   int32_t tokens;          // valid tokens (host bookkeeping)
 };
 
-struct Segment {           // one CTA's piece of one group
-  int32_t group;
-  int32_t entry;           // first PageEntry (absolute index; host bookkeeping)
+struct Segment {           // one CTA's piece of one group: all the decode kernel reads about it
+  int32_t fmt;             // 0 = FP8 (Recent/Anchor), 1 = TQ3 (Stale)
+  int32_t b;               // batch index
+  int32_t kvh;             // kv head
+  int32_t entry0;          // the group's first PageEntry
   int32_t blk;             // first block of the piece, counted within the group:
                            // block k covers tokens [bt (k % bpp), +bt) of page
                            // entry0 + k / bpp (bt = kFp8Blk or kTq3Blk, bpp = P / bt)
-  int32_t nstages;         // blocks in the piece
+  int32_t nblk;            // blocks in the piece
   int32_t part;            // partial-state index the piece writes
-  int32_t tokens;          // valid tokens of the piece (host bookkeeping)
-  int32_t pad0, pad1;
+  int32_t group;           // the group (host bookkeeping)
 };
 
 struct MergeDesc {         // partial-state index ranges of one (b, kvh)

@@ -490,6 +490,8 @@ constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
 constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
 constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
 static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+static_assert(kQBytes == kRedFloats * 4, "a q buffer doubles as a reduction buffer");
+static_assert(2 * kDecWarps >= 2 * kMaxGroup, "the prologue builds two pieces' q rows in two rounds");
 
 __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   DecSmem s;
@@ -527,13 +529,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-struct Piece {                                 // one CTA piece (a Segment and its Group)
+struct Piece {                                 // one CTA piece (its Segment)
   int fmt, b, kvh, entry0, blk0, nblk, part;
 };
 __device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
   const Segment s = p.segs[si];
-  const Group g = p.groups[s.group];
-  return Piece{g.fmt, g.b, g.kvh, g.entry0, s.blk, s.nstages, s.part};
+  return Piece{s.fmt, s.b, s.kvh, s.entry0, s.blk, s.nblk, s.part};
 }
 
 // Block k of a piece: page entry, first token within the page, valid tokens
@@ -692,21 +693,6 @@ __device__ __forceinline__ void dec_build_q_row(const DecodeParams& p, uint4* qb
         make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
                    pack_half2(lo[2], lo[3]));
   }
-}
-
-// The first two pieces' q fragments (into buffers 0 and 1): the CTA's warps
-// share the 2 x kMaxGroup rows.  Ends with a CTA barrier.
-__device__ __forceinline__ void dec_prep_q_first(const DecodeParams& p, const DecSmem& sm, int s0, int s1, int warp,
-                                                 int lane) {
-  for (int task = warp; task < 2 * kMaxGroup; task += kDecWarps) {
-    const int i = task / kMaxGroup;
-    if (s0 + i < s1) {
-      const Piece pc = load_piece(p, s0 + i);
-      dec_build_q_row(p, sm.qbuf + i * (kQBytes / 16), pc, task % kMaxGroup,
-                      lane, dec_load_q_row(p, pc, task % kMaxGroup, lane));
-    }
-  }
-  named_bar(1, kDecThreads);
 }
 
 // The two 12-byte units at p (8-byte aligned): words of unit 0 in u[0..2],
@@ -899,28 +885,33 @@ __device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* 
   }
 }
 
-// Store / add one warp's O fragments to / from a reduction buffer (lane-major).
+// Store / add one warp's O fragments to / from a reduction buffer: m-tile i
+// of lane l as one float4 at [i][l] (conflict-free 16-byte accesses).
 __device__ __forceinline__ void red_store(float* buf, const WarpState& ws) {
   const int lane = threadIdx.x & 31;
+  float4* b4 = reinterpret_cast<float4*>(buf) + lane;
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) buf[(4 * i + k) * 32 + lane] = ws.o[i][k];
+  for (int i = 0; i < 16; ++i) b4[i * 32] = make_float4(ws.o[i][0], ws.o[i][1], ws.o[i][2], ws.o[i][3]);
 }
 __device__ __forceinline__ void red_add(const float* buf, WarpState& ws) {
   const int lane = threadIdx.x & 31;
+  const float4* b4 = reinterpret_cast<const float4*>(buf) + lane;
 #pragma unroll
-  for (int i = 0; i < 16; ++i)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) ws.o[i][k] += buf[(4 * i + k) * 32 + lane];
+  for (int i = 0; i < 16; ++i) {
+    const float4 v = b4[i * 32];
+    ws.o[i][0] += v.x;
+    ws.o[i][1] += v.y;
+    ws.o[i][2] += v.z;
+    ws.o[i][3] += v.w;
+  }
 }
 
 // End of a piece: the CTA's warps' states merge into the
 // piece's partial state.  Each warp rescales its O to the common max of each
-// head; O then sums up a fixed tree (two buffers) so the result does not
+// head; O then sums up a fixed tree (three buffers) so the result does not
 // depend on timing; warp 0 writes (m, l, o) per q head.
 __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
-                                              WarpState& ws, int warp) {
+                                              WarpState& ws, int warp, int pi) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int G = p.G;
   float l = ws.l_run;
@@ -960,17 +951,20 @@ __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSm
     ws.o[i][3] *= f1;
   }
   // the tree: with n warps holding sums, warps [ceil(n/2), n) add into warps
-  // [0, n - ceil(n/2)), kRedBufs at a time
+  // [0, n - ceil(n/2)), three at a time: the two reduction buffers and the
+  // q buffer of this piece, which every warp is done with
+  float* const qb = reinterpret_cast<float*>(sm.qbuf + (pi & 1) * (kQBytes / 16));
+  auto buf = [&](int i) { return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : qb; };
 #pragma unroll
   for (int n = kDecWarps; n > 1; n = (n + 1) / 2) {
     const int lo = (n + 1) / 2;
 #pragma unroll
-    for (int i0 = 0; i0 < n - lo; i0 += kRedBufs) {
+    for (int i0 = 0; i0 < n - lo; i0 += 3) {
       const int i = warp - lo - i0;                      // this warp as a source
-      if (i >= 0 && i < kRedBufs && lo + i0 + i < n) red_store(sm.red + i * kRedFloats, ws);
+      if (i >= 0 && i < 3 && lo + i0 + i < n) red_store(buf(i), ws);
       named_bar(1, kDecThreads);
       const int j = warp - i0;                           // this warp as a destination
-      if (j >= 0 && j < kRedBufs && lo + i0 + j < n) red_add(sm.red + j * kRedFloats, ws);
+      if (j >= 0 && j < 3 && lo + i0 + j < n) red_add(buf(j), ws);
       if (n > 2) named_bar(1, kDecThreads);
     }
   }
@@ -1071,8 +1065,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // the warp's first kSlots blocks: pages are written only by kernels that
-  // finish before this one starts
+  // q and the partial-state workspace belong to the preceding kernels (the
+  // previous launch's merge reads the workspace): wait for them first
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the q rows of the first two pieces (rows warp and warp + kDecWarps of the
+  // 2 x kMaxGroup) go out now and are built once the first copies are issued
+  constexpr int kQTasks = 2 * kMaxGroup;
+  Piece pq[2];
+  QRow qr[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int task = warp + t * kDecWarps;
+    if (task < kQTasks && s0 + task / kMaxGroup < s1) {
+      pq[t] = load_piece(p, s0 + task / kMaxGroup);
+      qr[t] = dec_load_q_row(p, pq[t], task % kMaxGroup, lane);
+    }
+  }
+  // the warp's first kSlots blocks
   BlockCursor ic;
   ic.start(p, s0, s1, warp);
   for (int i = 0; i < kSlots && ic.valid(); ++i) {
@@ -1083,11 +1092,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     }
     ic.advance(p, warp);
   }
-  // q, and the partial-state workspace the previous launch's merge may still
-  // read, belong to the preceding kernels: wait for them, then build the first
-  // two pieces' q fragments while the first blocks arrive
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  dec_prep_q_first(p, sm, s0, s1, warp, lane);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int task = warp + t * kDecWarps;
+    if (task < kQTasks && s0 + task / kMaxGroup < s1)
+      dec_build_q_row(p, sm.qbuf + (task / kMaxGroup) * (kQBytes / 16), pq[t], task % kMaxGroup, lane, qr[t]);
+  }
+  named_bar(1, kDecThreads);
   RingPos rp{0, 0};
   WarpState ws;
   for (int si = s0; si < s1; ++si) {
@@ -1110,7 +1121,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
       dec_piece<1>(p, sm, pc, pi, ic, rp, warp, ws);
     else
       dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
-    dec_piece_end(p, sm, pc, ws, warp);
+    dec_piece_end(p, sm, pc, ws, warp, pi);
     // every warp is past piece pi: its q buffer takes piece pi + 2
     if (si + 2 < s1) {
       if (prep_next) dec_build_q_row(p, sm.qbuf + (pi & 1) * (kQBytes / 16), pn, warp, lane, qn);
