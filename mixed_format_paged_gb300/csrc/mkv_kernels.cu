@@ -1141,59 +1141,64 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
 }
 
 // ============================================================== merge
-// One block (256 threads, thread = dim) per (request, kv head, q head).  The
-// partial states' (m, l) are staged in shared memory; the TQ3 partials merge
-// in the rotated domain, R^T is applied once (FWHT across the block, then the
-// signs and 1/16), the FP8 partials join, and out = O / L,
+// One block (256 threads, thread = dim) per (request, kv head, q head).  Each
+// format's partial states merge in one pass with a running (M, L, O) -- the
+// online-softmax recurrence, in partial-state order, so the result does not
+// depend on timing -- loading eight partials at a time.  The TQ3 partials
+// merge in the rotated domain, R^T is applied once (FWHT across the block,
+// then the signs and 1/16), the FP8 partials join, and out = O / L,
 // lse = (M + log2 L) ln 2.
-constexpr int kMergeStage = 256;   // partial states staged per pass
+constexpr int kMergeBatch = 8;
 
-// Merge partial states [first, first + count) of head h at dim d.
-__device__ __forceinline__ void merge_range(const float* part, int stride, int h, int first, int count, int d,
-                                            float* sm_m, float* sm_l, float& Mout, float& Lout, float& oout) {
-  float M = -INFINITY;
-  for (int base = 0; base < count; base += kMergeStage) {
-    const int cnt = min(kMergeStage, count - base);
-    __syncthreads();
-    if (d < cnt) {
-      const float* pj = part + static_cast<size_t>(first + base + d) * stride + h * (2 + kHeadDim);
-      sm_m[d] = pj[0];
-      sm_l[d] = pj[1];
-    }
-    __syncthreads();
-    for (int j = 0; j < cnt; ++j) M = fmaxf(M, sm_m[j]);
-  }
-  float L = 0.f, o = 0.f;
-  if (M != -INFINITY) {
-    for (int base = 0; base < count; base += kMergeStage) {
-      const int cnt = min(kMergeStage, count - base);
-      __syncthreads();
-      if (d < cnt) {
-        const float* pj = part + static_cast<size_t>(first + base + d) * stride + h * (2 + kHeadDim);
-        const float mj = pj[0];
-        sm_m[d] = (mj == -INFINITY) ? 0.f : exp2f(mj - M);
-        sm_l[d] = pj[1];
-      }
-      __syncthreads();
-      const float* col = part + static_cast<size_t>(first + base) * stride + h * (2 + kHeadDim) + 2 + d;
-      int j = 0;
-      for (; j + 4 <= cnt; j += 4) {
-        const float v0 = col[static_cast<size_t>(j) * stride], v1 = col[static_cast<size_t>(j + 1) * stride];
-        const float v2 = col[static_cast<size_t>(j + 2) * stride], v3 = col[static_cast<size_t>(j + 3) * stride];
-        o += sm_m[j] * v0 + sm_m[j + 1] * v1 + sm_m[j + 2] * v2 + sm_m[j + 3] * v3;
-      }
-      for (; j < cnt; ++j) o += sm_m[j] * col[static_cast<size_t>(j) * stride];
-      for (int jj = 0; jj < cnt; ++jj) L += sm_m[jj] * sm_l[jj];
+// Loads of partial states [first + base, + kMergeBatch) of head h at dim d.
+struct MergeBatch {
+  float m[kMergeBatch], l[kMergeBatch], o[kMergeBatch];
+};
+__device__ __forceinline__ void merge_load(const float* part, int stride, int h, int first, int base, int count,
+                                           int d, MergeBatch& mb) {
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) {
+    if (base + u < count) {
+      const float* pj = part + static_cast<size_t>(first + base + u) * stride + h * (2 + kHeadDim);
+      mb.m[u] = pj[0];
+      mb.l[u] = pj[1];
+      mb.o[u] = pj[2 + d];
+    } else {
+      mb.m[u] = -INFINITY;
+      mb.l[u] = 0.f;
+      mb.o[u] = 0.f;
     }
   }
-  Mout = M;
-  Lout = L;
-  oout = o;
+}
+__device__ __forceinline__ void merge_fold(const MergeBatch& mb, float& M, float& L, float& O) {
+#pragma unroll
+  for (int u = 0; u < kMergeBatch; ++u) {
+    if (mb.m[u] == -INFINITY) continue;   // an empty head (the same for every thread)
+    const float Mn = fmaxf(M, mb.m[u]);
+    const float a = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+    const float w = exp2f(mb.m[u] - Mn);
+    L = L * a + mb.l[u] * w;
+    O = O * a + mb.o[u] * w;
+    M = Mn;
+  }
+}
+// Partial states [first, first + count) of head h merged at dim d; the first
+// batch is passed in already loaded.
+__device__ __forceinline__ void merge_run(const float* part, int stride, int h, int first, int count, int d,
+                                          const MergeBatch& first_batch, float& M, float& L, float& O) {
+  M = -INFINITY;
+  L = 0.f;
+  O = 0.f;
+  merge_fold(first_batch, M, L, O);
+  for (int base = kMergeBatch; base < count; base += kMergeBatch) {
+    MergeBatch mb;
+    merge_load(part, stride, h, first, base, count, d, mb);
+    merge_fold(mb, M, L, O);
+  }
 }
 
 __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   __shared__ float xs[kHeadDim];
-  __shared__ float sm_m[kMergeStage], sm_l[kMergeStage];
   // launched as a programmatic dependent of the decode kernel: wait for its
   // partial states before reading them
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1203,8 +1208,12 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   const MergeDesc md = p.desc[bk];
   const int d = threadIdx.x, lane = d & 31;
   const int stride = p.G * (2 + kHeadDim);
+  // the first batch of both formats goes out at once
+  MergeBatch bs, bf;
+  merge_load(p.part, stride, h, md.tq3_first, 0, md.tq3_count, d, bs);
+  merge_load(p.part, stride, h, md.fp8_first, 0, md.fp8_count, d, bf);
   float Ms, Ls, os, Mf, Lf, of;
-  merge_range(p.part, stride, h, md.tq3_first, md.tq3_count, d, sm_m, sm_l, Ms, Ls, os);
+  merge_run(p.part, stride, h, md.tq3_first, md.tq3_count, d, bs, Ms, Ls, os);
   // o_S = R^T o'_S = signs .* (H o'_S) / 16: butterflies over lane bits by
   // shuffle, over warp bits through shared memory
 #pragma unroll
@@ -1221,7 +1230,7 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   }
   os *= (1.0f / 16.0f);
   if (sign_neg(p.signs, d)) os = -os;
-  merge_range(p.part, stride, h, md.fp8_first, md.fp8_count, d, sm_m, sm_l, Mf, Lf, of);
+  merge_run(p.part, stride, h, md.fp8_first, md.fp8_count, d, bf, Mf, Lf, of);
   const float M = fmaxf(Ms, Mf);
   const float fs = (Ms == -INFINITY) ? 0.f : exp2f(Ms - M);
   const float ff = (Mf == -INFINITY) ? 0.f : exp2f(Mf - M);
