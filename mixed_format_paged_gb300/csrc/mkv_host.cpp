@@ -209,7 +209,7 @@ struct mkv_pool {
 namespace {
 
 struct PlanLayout {
-  size_t entries, groups, segs, cta_seg, merge, total;
+  size_t entries, groups, segs, merge, total;
 };
 
 PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
@@ -221,8 +221,6 @@ PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
   off += align256(size_t(max_batch) * Hkv * 2 * sizeof(Group));
   L.segs = off;
   off += align256(size_t(chunk_cap) * sizeof(Segment));
-  L.cta_seg = off;
-  off += align256(size_t(kMaxCtas + 1) * sizeof(int32_t));
   L.merge = off;
   off += align256(size_t(max_batch) * Hkv * sizeof(MergeDesc));
   L.total = off;
@@ -495,7 +493,8 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   dp.entries = reinterpret_cast<const PageEntry*>(p->plan_region + L.entries);
   dp.groups = reinterpret_cast<const Group*>(p->plan_region + L.groups);
   dp.segs = reinterpret_cast<const Segment*>(p->plan_region + L.segs);
-  dp.cta_seg = reinterpret_cast<const int32_t*>(p->plan_region + L.cta_seg);
+  for (int i = 0; i <= ncta; ++i) dp.cta_seg[i] = cta_seg[i];
+  for (int i = 0; i < ncta; ++i) dp.first[i] = cta_seg[i] < cta_seg[i + 1] ? segs[cta_seg[i]] : Segment{};
   dp.n_ctas = ncta;
   dp.fp8_page_bytes = p->fp8_page_bytes;
   dp.tq3_page_bytes = p->tq3_page_bytes;
@@ -526,7 +525,6 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   std::memcpy(h + L.entries, entries.data(), entries.size() * sizeof(PageEntry));
   std::memcpy(h + L.groups, groups.data(), groups.size() * sizeof(Group));
   std::memcpy(h + L.segs, segs.data(), segs.size() * sizeof(Segment));
-  std::memcpy(h + L.cta_seg, cta_seg.data(), cta_seg.size() * sizeof(int32_t));
   std::memcpy(h + L.merge, md.data(), md.size() * sizeof(MergeDesc));
   return staging_upload(p->st_plan, p->plan_region, L.total, stream);
 }

@@ -15,7 +15,7 @@ constexpr int kDecWarps = 12;     // warps of a decode CTA (a piece's blocks go 
 constexpr int kFp8Blk = 16;        // tokens per FP8 decode block (one MMA tile)
 constexpr int kTq3Blk = 32;        // tokens per TQ3 decode block (two MMA tiles)
 constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
-constexpr int kMaxCtas = 1024;     // upper bound on decode CTAs
+constexpr int kMaxCtas = 160;      // upper bound on decode CTAs (their plan heads travel as kernel parameters)
 constexpr int kQfragWords = 2048;  // A-fragment words of one piece's q rows (16 x 256 fp16)
 
 // Error bits written by kernels into the pool's device error word.
@@ -77,8 +77,9 @@ struct DecodeParams {
   const PageEntry* entries;
   const Group* groups;
   const Segment* segs;             // per-CTA pieces, CTA by CTA
-  const int32_t* cta_seg;          // [n_ctas + 1] into segs
   int32_t n_ctas;
+  int32_t cta_seg[kMaxCtas + 1];   // CTA i's pieces: segs[cta_seg[i] .. cta_seg[i + 1])
+  Segment first[kMaxCtas];         // each CTA's first piece (a copy of segs[cta_seg[i]])
   const void* q;                   // [n, Hq, D], fp32 or bf16
   int32_t q_bf16;
   uint64_t signs[4];               // rotation signs (bit i set: negative)

@@ -491,7 +491,7 @@ constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
 constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
 static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 static_assert(kQBytes == kRedFloats * 4, "a q buffer doubles as a reduction buffer");
-static_assert(2 * kDecWarps >= 2 * kMaxGroup, "the prologue builds two pieces' q rows in two rounds");
+static_assert(kDecWarps >= kMaxGroup, "warp h builds row h of a piece's q fragments");
 
 __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   DecSmem s;
@@ -532,9 +532,12 @@ __device__ __forceinline__ float ex2(float x) {
 struct Piece {                                 // one CTA piece (its Segment)
   int fmt, b, kvh, entry0, blk0, nblk, part;
 };
-__device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
-  const Segment s = p.segs[si];
+__device__ __forceinline__ Piece piece_of(const Segment& s) {
   return Piece{s.fmt, s.b, s.kvh, s.entry0, s.blk, s.nblk, s.part};
+}
+// Piece si of this CTA: the first one travels in the kernel parameters.
+__device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
+  return si == p.cta_seg[blockIdx.x] ? piece_of(p.first[blockIdx.x]) : piece_of(p.segs[si]);
 }
 
 // Block k of a piece: page entry, first token within the page, valid tokens
@@ -575,13 +578,11 @@ struct BlockCursor {
   }
 };
 
-// Lane 0: copy block k of piece pc into slot st (mbarrier bar), or complete
-// the slot's phase without bytes for an empty block or a bad plan entry.
-__device__ __noinline__ void dec_issue(const DecodeParams& p, Piece pc, int k, uint8_t* st, uint64_t* bar,
-                                       int* abort_flag) {
-  int e = 0, tok0 = 0;
-  const int nv = block_locate(p, pc, k, e, tok0);
-  const PageEntry pe = p.entries[e];
+// Lane 0: copy a block (page entry pe, first token tok0, nv valid tokens) of
+// piece pc into slot st (mbarrier bar), or complete the slot's phase without
+// bytes for an empty block or a bad plan entry.
+__device__ __noinline__ void dec_issue_entry(const DecodeParams& p, Piece pc, PageEntry pe, int tok0, int nv,
+                                             uint8_t* st, uint64_t* bar, int* abort_flag) {
   const int nslots = pc.fmt ? p.tq3_slots : p.fp8_slots;
   if (nv <= 0) {
     mbar_arrive(bar);
@@ -606,6 +607,14 @@ __device__ __noinline__ void dec_issue(const DecodeParams& p, Piece pc, int k, u
   bulk_g2s(st + code, hp + p.P * row + 2 * tok0, 2 * bt, bar);
   bulk_g2s(st + code + 2 * bt, hp + plane + tok0 * row, code, bar);
   bulk_g2s(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar);
+}
+
+// Lane 0: locate block k of piece pc and copy it into slot st.
+__device__ __forceinline__ void dec_issue(const DecodeParams& p, const Piece& pc, int k, uint8_t* st, uint64_t* bar,
+                                          int* abort_flag) {
+  int e = 0, tok0 = 0;
+  const int nv = block_locate(p, pc, k, e, tok0);
+  dec_issue_entry(p, pc, p.entries[e], tok0, nv, st, bar, abort_flag);
 }
 
 // Raw q row h of piece pc (8 dims per lane, bf16 in r[0] or fp32 in r[0..1]);
@@ -1068,49 +1077,57 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   // q and the partial-state workspace belong to the preceding kernels (the
   // previous launch's merge reads the workspace): wait for them first
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the q rows of the first two pieces (rows warp and warp + kDecWarps of the
-  // 2 x kMaxGroup) go out now and are built once the first copies are issued
-  constexpr int kQTasks = 2 * kMaxGroup;
-  Piece pq[2];
-  QRow qr[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int task = warp + t * kDecWarps;
-    if (task < kQTasks && s0 + task / kMaxGroup < s1) {
-      pq[t] = load_piece(p, s0 + task / kMaxGroup);
-      qr[t] = dec_load_q_row(p, pq[t], task % kMaxGroup, lane);
-    }
-  }
-  // the warp's first kSlots blocks
+  // warp h < kMaxGroup builds row h of each piece's q fragments; piece s0's
+  // row load goes out now, the next piece's at the start of each piece
+  const bool q_warp = warp < kMaxGroup;
   BlockCursor ic;
-  ic.start(p, s0, s1, warp);
-  for (int i = 0; i < kSlots && ic.valid(); ++i) {
-    if (lane == 0) {
-      dec_issue(p, ic.pc, ic.k, sm.ring + (warp * kSlots + i) * kSlotBytes, sm.full + warp * kSlots + i,
-                sm.abort_flag);
-      ++ic.issued;
+  {
+    QRow qr{};
+    Piece p0{};
+    if (q_warp && s0 < s1) {
+      p0 = load_piece(p, s0);
+      qr = dec_load_q_row(p, p0, warp, lane);
     }
-    ic.advance(p, warp);
-  }
+    // the warp's first kSlots blocks: their page-entry loads go out together
+    ic.start(p, s0, s1, warp);
+    Piece fp[kSlots];
+    int fk[kSlots];
+    int nfirst = 0;
+    for (; nfirst < kSlots && ic.valid(); ++nfirst) {
+      fp[nfirst] = ic.pc;
+      fk[nfirst] = ic.k;
+      ic.advance(p, warp);
+    }
+    if (lane == 0) {
+      PageEntry pe[kSlots];
+      int tok0[kSlots], nv[kSlots];
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int task = warp + t * kDecWarps;
-    if (task < kQTasks && s0 + task / kMaxGroup < s1)
-      dec_build_q_row(p, sm.qbuf + (task / kMaxGroup) * (kQBytes / 16), pq[t], task % kMaxGroup, lane, qr[t]);
+      for (int i = 0; i < kSlots; ++i)
+        if (i < nfirst) {
+          int e = 0;
+          nv[i] = block_locate(p, fp[i], fk[i], e, tok0[i]);
+          pe[i] = p.entries[e];
+        }
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i)
+        if (i < nfirst)
+          dec_issue_entry(p, fp[i], pe[i], tok0[i], nv[i], sm.ring + (warp * kSlots + i) * kSlotBytes,
+                          sm.full + warp * kSlots + i, sm.abort_flag);
+      ic.issued = nfirst;
+    }
+    if (q_warp && s0 < s1) dec_build_q_row(p, sm.qbuf, p0, warp, lane, qr);
+    named_bar(1, kDecThreads);
   }
-  named_bar(1, kDecThreads);
   RingPos rp{0, 0};
   WarpState ws;
   for (int si = s0; si < s1; ++si) {
     const int pi = si - s0;
     const Piece pc = load_piece(p, si);
-    // warp h < kMaxGroup builds row h of piece si + 2's q fragments at the end
-    // of this piece; its q row load goes out now
-    const bool prep_next = si + 2 < s1 && warp < kMaxGroup;
+    const bool prep_next = si + 1 < s1 && q_warp;
     Piece pn{};
     QRow qn{};
     if (prep_next) {
-      pn = load_piece(p, si + 2);
+      pn = load_piece(p, si + 1);
       qn = dec_load_q_row(p, pn, warp, lane);
     }
 #pragma unroll
@@ -1122,9 +1139,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     else
       dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
     dec_piece_end(p, sm, pc, ws, warp, pi);
-    // every warp is past piece pi: its q buffer takes piece pi + 2
-    if (si + 2 < s1) {
-      if (prep_next) dec_build_q_row(p, sm.qbuf + (pi & 1) * (kQBytes / 16), pn, warp, lane, qn);
+    // every warp is past piece pi; the other q buffer (piece pi - 1's, free
+    // since its end) takes piece pi + 1
+    if (si + 1 < s1) {
+      if (prep_next) dec_build_q_row(p, sm.qbuf + ((pi + 1) & 1) * (kQBytes / 16), pn, warp, lane, qn);
       named_bar(1, kDecThreads);
     }
   }
