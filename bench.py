@@ -22,6 +22,7 @@ are independent; no collective on the data path); value sums all ranks.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -85,21 +86,27 @@ def committed_traffic(workload):
 
 
 class ClockSampler:
+    """nvidia-smi clock and throttle samples (every 10 ms, timestamped).  Start
+    it before the warm-up; `stop(t0, t1)` keeps the samples taken inside the
+    timed region [t0, t1] (host wall clock), padded by one sampling period."""
+
+    PERIOD_S = 0.010
+
     def __init__(self, gpu_index: int):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                       "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
-                                      stderr=subprocess.DEVNULL)
+                                       "-lms", str(int(self.PERIOD_S * 1000)), "-i", str(gpu_index)],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
 
-    def stop(self):
+    def stop(self, t0: float, t1: float):
         if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.p.terminate()
         try:
             self.p.wait(timeout=5)
@@ -107,23 +114,30 @@ class ClockSampler:
             self.p.kill()
         self.f.flush()
         self.f.seek(0)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in self.f.read().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
+        os.unlink(self.f.name)
+        pad = self.PERIOD_S
+        inside = [r for r in rows if t0 - pad <= r[0] <= t1 + pad]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        os.unlink(self.f.name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [r[1] for r in inside]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window_ms": round((t1 - t0) * 1e3, 2), "period_ms": int(self.PERIOD_S * 1000)}
 
 
 def job_totals(local_ms: float, local_bytes: float, world: int, device=None):
@@ -297,6 +311,9 @@ def run_mkv(args):
                 B.mkv_set_timing_events(pool.handle, *ev_pairs[layer])
             stepper.layer(layer, k, v, q, *outs[layer])
 
+    # clocks are sampled from before the warm-up on; only samples inside the
+    # timed region count (nvidia-smi takes a while to start)
+    sampler = ClockSampler(local)
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
@@ -311,16 +328,17 @@ def run_mkv(args):
     bytes_acc = []
     barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
     demotes[0] = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
     e0.record()
     for i in range(args.steps):
         step(args.warmup + i, ev[i], bytes_acc)
     e1.record()
     torch.cuda.synchronize()
+    t_wall1 = time.time()
     barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(t_wall0, t_wall1)
     pool.check_device_errors()
     ms = e0.elapsed_time(e1)
     timed_demotes = demotes[0]

@@ -917,10 +917,10 @@ __device__ __forceinline__ void red_add(const float* buf, WarpState& ws) {
 
 // End of a piece: the CTA's warps' states merge into the
 // piece's partial state.  Each warp rescales its O to the common max of each
-// head; O then sums up a fixed tree (three buffers) so the result does not
+// head; O then sums up a fixed tree (four buffers) so the result does not
 // depend on timing; warp 0 writes (m, l, o) per q head.
 __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
-                                              WarpState& ws, int warp, int pi) {
+                                              WarpState& ws, int warp) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int G = p.G;
   float l = ws.l_run;
@@ -959,23 +959,22 @@ __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSm
     ws.o[i][2] *= f0;
     ws.o[i][3] *= f1;
   }
-  // the tree: with n warps holding sums, warps [ceil(n/2), n) add into warps
-  // [0, n - ceil(n/2)), three at a time: the two reduction buffers and the
-  // q buffer of this piece, which every warp is done with
-  float* const qb = reinterpret_cast<float*>(sm.qbuf + (pi & 1) * (kQBytes / 16));
-  auto buf = [&](int i) { return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : qb; };
+  // the tree: with n warps holding sums, warps [n - h, n) add into warps
+  // [0, h), h = min(4, n / 2): one round per level through four 8 KB buffers
+  // (the two reduction buffers and both q buffers: the next piece's q
+  // fragments are built only after this merge)
+  float* const q0 = reinterpret_cast<float*>(sm.qbuf);
+  float* const q1 = reinterpret_cast<float*>(sm.qbuf + kQBytes / 16);
+  auto buf = [&](int i) { return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : i == 2 ? q0 : q1; };
 #pragma unroll
-  for (int n = kDecWarps; n > 1; n = (n + 1) / 2) {
-    const int lo = (n + 1) / 2;
-#pragma unroll
-    for (int i0 = 0; i0 < n - lo; i0 += 3) {
-      const int i = warp - lo - i0;                      // this warp as a source
-      if (i >= 0 && i < 3 && lo + i0 + i < n) red_store(buf(i), ws);
-      named_bar(1, kDecThreads);
-      const int j = warp - i0;                           // this warp as a destination
-      if (j >= 0 && j < 3 && lo + i0 + j < n) red_add(buf(j), ws);
-      if (n > 2) named_bar(1, kDecThreads);
-    }
+  for (int n = kDecWarps; n > 1;) {
+    const int h = min(4, n / 2), lo = n - h;
+    const int i = warp - lo;                             // this warp as a source
+    if (i >= 0 && i < h) red_store(buf(i), ws);
+    named_bar(1, kDecThreads);
+    if (warp < h) red_add(buf(warp), ws);
+    n = lo;
+    if (n > 1) named_bar(1, kDecThreads);
   }
   if (warp == 0) {
     float* dst = p.part + static_cast<size_t>(pc.part) * G * (2 + kHeadDim);
@@ -1138,7 +1137,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
       dec_piece<1>(p, sm, pc, pi, ic, rp, warp, ws);
     else
       dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
-    dec_piece_end(p, sm, pc, ws, warp, pi);
+    dec_piece_end(p, sm, pc, ws, warp);
     // every warp is past piece pi; the other q buffer (piece pi - 1's, free
     // since its end) takes piece pi + 1
     if (si + 1 < s1) {
