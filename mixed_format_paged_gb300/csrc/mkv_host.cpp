@@ -323,8 +323,8 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 // ------------------------------------------------------------------ planner
 // Relative cost of one token of one kv head, per format, plus a fixed cost per
 // block and per piece, in units of one TQ3 token.  Fitted to per-CTA times of
-// the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.37 us of CTA
-// time, a 16-token FP8 block ~0.29 us, a piece ~5 us (its end-of-piece merge
+// the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.31 us of CTA
+// time, a 16-token FP8 block ~0.25 us, a piece ~4 us (its end-of-piece merge
 // and the warps left idle in its last round of blocks).
 constexpr double kCostTq3Token = 1.0;
 constexpr double kCostFp8Token = 1.45;
