@@ -63,6 +63,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// The same copy with an L2 cache policy (createpolicy): KV page data is read
+// once per launch and should not push the small, reused data (plan tables, q,
+// partial states) out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -603,10 +619,11 @@ __device__ __noinline__ void dec_issue_entry(const DecodeParams& p, Piece pc, Pa
   const uint32_t code = bt * row;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, 2 * (code + 2 * bt));
-  bulk_g2s(st, hp + tok0 * row, code, bar);
-  bulk_g2s(st + code, hp + p.P * row + 2 * tok0, 2 * bt, bar);
-  bulk_g2s(st + code + 2 * bt, hp + plane + tok0 * row, code, bar);
-  bulk_g2s(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar);
+  const uint64_t pol = l2_evict_first_policy();
+  bulk_g2s_hint(st, hp + tok0 * row, code, bar, pol);
+  bulk_g2s_hint(st + code, hp + p.P * row + 2 * tok0, 2 * bt, bar, pol);
+  bulk_g2s_hint(st + code + 2 * bt, hp + plane + tok0 * row, code, bar, pol);
+  bulk_g2s_hint(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar, pol);
 }
 
 // Lane 0: locate block k of piece pc and copy it into slot st.
