@@ -1104,7 +1104,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
       p0 = load_piece(p, s0);
       qr = dec_load_q_row(p, p0, warp, lane);
     }
-    // the warp's first kSlots blocks: their page-entry loads go out together
+    // the warp's first kSlots blocks
     ic.start(p, s0, s1, warp);
     Piece fp[kSlots];
     int fk[kSlots];
@@ -1114,9 +1114,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
       fk[nfirst] = ic.k;
       ic.advance(p, warp);
     }
+    // page-entry loads of the first blocks go out together
+    PageEntry pe[kSlots];
+    int tok0[kSlots], nv[kSlots];
     if (lane == 0) {
-      PageEntry pe[kSlots];
-      int tok0[kSlots], nv[kSlots];
 #pragma unroll
       for (int i = 0; i < kSlots; ++i)
         if (i < nfirst) {
@@ -1124,14 +1125,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
           nv[i] = block_locate(p, fp[i], fk[i], e, tok0[i]);
           pe[i] = p.entries[e];
         }
-#pragma unroll
-      for (int i = 0; i < kSlots; ++i)
-        if (i < nfirst)
-          dec_issue_entry(p, fp[i], pe[i], tok0[i], nv[i], sm.ring + (warp * kSlots + i) * kSlotBytes,
-                          sm.full + warp * kSlots + i, sm.abort_flag);
+      // the first block now; the rest after the q fragments, so that a full
+      // copy queue does not hold the warp's q build back
+      if (nfirst > 0)
+        dec_issue_entry(p, fp[0], pe[0], tok0[0], nv[0], sm.ring + warp * kSlots * kSlotBytes, sm.full + warp * kSlots,
+                        sm.abort_flag);
       ic.issued = nfirst;
     }
     if (q_warp && s0 < s1) dec_build_q_row(p, sm.qbuf, p0, warp, lane, qr);
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 1; i < kSlots; ++i)
+        if (i < nfirst)
+          dec_issue_entry(p, fp[i], pe[i], tok0[i], nv[i], sm.ring + (warp * kSlots + i) * kSlotBytes,
+                          sm.full + warp * kSlots + i, sm.abort_flag);
+    }
     named_bar(1, kDecThreads);
   }
   RingPos rp{0, 0};
