@@ -294,11 +294,20 @@ def run_mkv(args):
         ins.append(row)
     outs = [(torch.empty((w.n, w.Hq, w.D), device=dev), torch.empty((w.n, w.Hq), device=dev)) for _ in range(L)]
     demotes = [0]
+    demote_events = []                # (start, stop) CUDA events of the timed region's demotions
+    timing_demotes = [False]
     orig_demote = pool.demote
 
     def counting_demote(*a, **kw):
         demotes[0] += 1
-        return orig_demote(*a, **kw)
+        if not timing_demotes[0]:
+            return orig_demote(*a, **kw)
+        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        e[0].record()
+        r = orig_demote(*a, **kw)
+        e[1].record()
+        demote_events.append(e)
+        return r
     pool.demote = counting_demote
 
     # The decode kernel is timed on the last layer of every timed step: events
@@ -334,6 +343,7 @@ def run_mkv(args):
     barrier()
     torch.cuda.synchronize()
     demotes[0] = 0
+    timing_demotes[0] = True
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record()
@@ -342,8 +352,10 @@ def run_mkv(args):
     e1.record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
+    timing_demotes[0] = False
     barrier()
     clocks = sampler.stop(t_wall0, t_wall1)
+    demote_ms = [a.elapsed_time(b) for a, b in demote_events]
     pool.check_device_errors()
     ms = e0.elapsed_time(e1)
     timed_demotes = demotes[0]
@@ -441,6 +453,10 @@ def run_mkv(args):
                                      "pool_kv_bytes_per_live_token": st.kv_bytes_per_live_token,
                                      "pages_reported_kib_per_token": 18.3},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks,
+        "append": "fused into the decode kernel (one launch per layer appends the step's token and decodes)",
+        "demote": {"calls": len(demote_ms), "ms_total": round(sum(demote_ms), 4),
+                   "ms_per_step": round(sum(demote_ms) / args.steps, 4),
+                   "share_of_step": round(sum(demote_ms) / ms, 4) if ms > 0 else None},
     }
     print(json.dumps(line), flush=True)
     if world > 1:
