@@ -330,7 +330,8 @@ constexpr double kCostTq3Token = 1.0;
 constexpr double kCostFp8Token = 1.45;
 constexpr double kCostBlock = 8.0;
 constexpr double kCostPiece = 540.0;
-constexpr int kMinBlocksPerCta = 24;   // two blocks per warp at least
+constexpr double kShortRoundBase = 0.4;  // a round with one busy warp costs 0.4 + 0.6/12 of a full one
+constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
 
 // Split the batch's pages into groups (request, kv head, format), lay the
 // groups' blocks out in one sequence, and cut that sequence into one
@@ -402,60 +403,90 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   auto cost = [&](const Blk& b) {
     return b.tokens * (groups[b.group].fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
   };
-  double blocks_cost = 0.0;
-  for (const Blk& b : blocks) blocks_cost += cost(b);
-  // one CTA per SM, each with at least kMinBlocksPerCta blocks
-  const int ncta = int(std::max<int64_t>(
+  // Rounds: runs of up to kDecWarps consecutive blocks of one group, from the
+  // group's first block on.  A CTA's warps take one round together, so a cut
+  // inside a group falls only between rounds and every warp of a piece gets
+  // the same number of blocks (one fewer for some in a group's last round).
+  // A round costs its slowest block on every warp; a short round, with warps
+  // idle, runs its blocks faster and is priced between the two.
+  struct Round {
+    int group, first, nblk;
+    double cost;
+  };
+  std::vector<Round> rounds;
+  for (size_t i = 0; i < blocks.size();) {
+    const int g = blocks[i].group;
+    size_t j = i;
+    double worst = 0.0;
+    while (j < blocks.size() && blocks[j].group == g && int(j - i) < kDecWarps) worst = std::max(worst, cost(blocks[j++]));
+    const double busy = double(j - i) / kDecWarps;
+    rounds.push_back({g, int(i), int(j - i), worst * kDecWarps * (kShortRoundBase + (1.0 - kShortRoundBase) * busy)});
+    i = j;
+  }
+  // one CTA per SM at most, each with at least kMinBlocksPerCta blocks
+  const int max_cta = int(std::max<int64_t>(
       1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), int64_t(blocks.size()) / kMinBlocksPerCta})));
-  // Cut the block sequence into ncta piece lists of equal cost, a piece
-  // costing kCostPiece on top of its blocks (the end-of-piece merge and the
-  // warps left idle in its last round).  Within a group, a cut falls only
-  // where the piece before it holds a multiple of kDecWarps blocks, so
-  // every warp of the CTA gets the same number of them.  Two passes: the
-  // second uses the piece count of the first.
+  // Contiguous split of the rounds into at most max_cta CTAs that minimises
+  // the largest CTA cost, a piece costing kCostPiece on top of its rounds (its
+  // end-of-piece merge): the greedy fill below needs the fewest CTAs for a
+  // given bound, so a bisection on the bound finds the smallest feasible one.
+  auto fill = [&](double bound, std::vector<int>* starts) {
+    int n_cta = 0, last_group = -1;
+    double acc = 0.0;
+    for (int r = 0; r < int(rounds.size()); ++r) {
+      const double add = rounds[r].cost + (rounds[r].group != last_group ? kCostPiece : 0.0);
+      if (n_cta == 0 || acc + add > bound) {
+        ++n_cta;
+        if (starts) starts->push_back(r);
+        acc = kCostPiece + rounds[r].cost;
+      } else {
+        acc += add;
+      }
+      last_group = rounds[r].group;
+    }
+    return n_cta;
+  };
+  double lo = 0.0, hi = 0.0;
+  for (const Round& r : rounds) {
+    lo = std::max(lo, kCostPiece + r.cost);
+    hi += kCostPiece + r.cost;
+  }
+  if (fill(lo, nullptr) > max_cta) {
+    while (hi - lo > 1e-4 * hi) {
+      const double mid = 0.5 * (lo + hi);
+      (fill(mid, nullptr) <= max_cta ? hi : lo) = mid;
+    }
+    lo = hi;
+  }
+  std::vector<int> starts;
+  const int ncta = rounds.empty() ? 0 : fill(lo, &starts);
+  starts.push_back(int(rounds.size()));
   std::vector<Segment> segs;
   std::vector<int32_t> seg_entry, seg_tokens;   // first page entry and valid tokens of each piece
   std::vector<int32_t> cta_seg(ncta + 1, 0);
-  int npieces = ncta + int(groups.size());
-  int cur_cta = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    segs.clear();
-    seg_entry.clear();
-    seg_tokens.clear();
-    std::fill(cta_seg.begin(), cta_seg.end(), 0);
-    const double per_cta = (blocks_cost + kCostPiece * npieces) / ncta;
-    double acc = 0.0;
-    int cur_group = -1, in_piece = 0;
-    cur_cta = 0;
-    for (const Blk& b : blocks) {
-      const bool new_group = b.group != cur_group;
-      const bool may_cut = new_group || in_piece % kDecWarps == 0;
-      const bool cut = may_cut && cur_cta < ncta - 1 && acc >= (cur_cta + 1) * per_cta;
-      if (new_group || cut) {
-        if (cut) cta_seg[++cur_cta] = int(segs.size());
-        const Group& g = groups[b.group];
+  for (int c = 0; c < ncta; ++c) {
+    cta_seg[c] = int(segs.size());
+    for (int r = starts[c]; r < starts[c + 1]; ++r) {
+      const Round& rd = rounds[r];
+      if (r == starts[c] || rd.group != rounds[r - 1].group) {
+        const Group& g = groups[rd.group];
+        const int blk = blocks[rd.first].index;
         Segment sg{};
         sg.fmt = g.fmt;
         sg.b = g.b;
         sg.kvh = g.kvh;
         sg.entry0 = g.entry0;
-        sg.group = b.group;
-        sg.blk = b.index;
+        sg.group = rd.group;
+        sg.blk = blk;
         segs.push_back(sg);
-        seg_entry.push_back(g.entry0 + b.index / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
+        seg_entry.push_back(g.entry0 + blk / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
         seg_tokens.push_back(0);
-        cur_group = b.group;
-        in_piece = 0;
-        acc += kCostPiece;
       }
-      segs.back().nblk += 1;
-      seg_tokens.back() += b.tokens;
-      acc += cost(b);
-      ++in_piece;
+      segs.back().nblk += rd.nblk;
+      for (int k = rd.first; k < rd.first + rd.nblk; ++k) seg_tokens.back() += blocks[k].tokens;
     }
-    npieces = int(segs.size());
   }
-  while (cur_cta < ncta) cta_seg[++cur_cta] = int(segs.size());
+  cta_seg[ncta] = int(segs.size());
   if (int(segs.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
   // partial-state indices: pieces are in group order, so each group's are contiguous
   for (Group& g : groups) g.nparts = 0;
