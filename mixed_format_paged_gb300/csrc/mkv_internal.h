@@ -70,30 +70,32 @@ struct Lut {               // byte tables for the PRMT level lookup
 };
 
 struct DecodeParams {
+  // scalars first, so that the kernel's first parameter loads bring them in together
   uint8_t* fp8_layer;              // FP8 arena base of this layer (written by the fused append)
   const uint8_t* tq3_layer;        // TQ3 arena base of this layer
   int64_t fp8_page_bytes, tq3_page_bytes;
-  int32_t fp8_slots, tq3_slots;
   const PageEntry* entries;
   const Group* groups;
   const Segment* segs;             // per-CTA pieces, CTA by CTA
-  int32_t n_ctas;
-  int32_t cta_seg[kMaxCtas + 1];   // CTA i's pieces: segs[cta_seg[i] .. cta_seg[i + 1])
-  Segment first[kMaxCtas];         // each CTA's first piece (a copy of segs[cta_seg[i]])
   const void* q;                   // [n, Hq, D], fp32 or bf16
-  int32_t q_bf16;
-  uint64_t signs[4];               // rotation signs (bit i set: negative)
-  int32_t Hq, Hkv, G, P;
   float* part;                     // [parts][G][2 + D] (m in log2 units, l, o)
-  float score_scale;               // log2(e) / sqrt(d)
-  Lut lut;
   // fused single-token append (mkv_append_decode): each request's newest
   // token (the last valid one of its tail page), rows k/v [n, Hkv, D]
-  int32_t append;
-  int32_t kv_bf16;
   const void* k;
   const void* v;
   int* err;
+  uint64_t signs[4];               // rotation signs (bit i set: negative)
+  Lut lut;
+  int32_t fp8_slots, tq3_slots;
+  int32_t n_ctas;
+  int32_t q_bf16;
+  int32_t Hq, Hkv, G, P;
+  float score_scale;               // log2(e) / sqrt(d)
+  int32_t append;
+  int32_t kv_bf16;
+  // per CTA
+  int32_t cta_seg[kMaxCtas + 1];   // CTA i's pieces: segs[cta_seg[i] .. cta_seg[i + 1])
+  Segment first[kMaxCtas];         // each CTA's first piece (a copy of segs[cta_seg[i]])
 };
 
 struct MergeParams {

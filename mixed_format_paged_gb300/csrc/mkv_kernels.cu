@@ -666,7 +666,7 @@ __device__ __forceinline__ QRow dec_load_q_row(const DecodeParams& p, const Piec
 // row g, so lane l of this warp (dims 8l .. 8l+7) fills fragment lane
 // 4h + l/8 at k-steps 2(l%8) and 2(l%8) + 1.
 __device__ __forceinline__ void dec_build_q_row(const DecodeParams& p, uint4* qb, const Piece& pc, int h, int lane,
-                                                const QRow& q) {
+                                                const QRow& q, uint32_t qsign) {
   float x[8];
   if (p.q_bf16) {
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&q.r[0]);
@@ -684,7 +684,7 @@ __device__ __forceinline__ void dec_build_q_row(const DecodeParams& p, uint4* qb
   if (pc.fmt) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
+      if ((qsign >> i) & 1u) x[i] = -x[i];
 #pragma unroll
     for (int hs = 1; hs < 8; hs <<= 1) {
 #pragma unroll
@@ -1084,6 +1084,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the merge kernel that follows waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the rotation signs of this lane's q dims 8 lane .. 8 lane + 7, loaded
+  // before the barrier so that the q build does not wait for them
+  const uint32_t qsign = static_cast<uint32_t>(
+      (lane < 8 ? p.signs[0] : lane < 16 ? p.signs[1] : lane < 24 ? p.signs[2] : p.signs[3]) >> (8 * (lane & 7))) & 0xFFu;
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(sm.full + warp * kSlots + i, 1);
     if (warp == 0) *sm.abort_flag = 0;
@@ -1132,7 +1136,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
                         sm.abort_flag);
       ic.issued = nfirst;
     }
-    if (q_warp && s0 < s1) dec_build_q_row(p, sm.qbuf, p0, warp, lane, qr);
+    if (q_warp && s0 < s1) dec_build_q_row(p, sm.qbuf, p0, warp, lane, qr, qsign);
     if (lane == 0) {
 #pragma unroll
       for (int i = 1; i < kSlots; ++i)
@@ -1166,7 +1170,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
     // every warp is past piece pi; the other q buffer (piece pi - 1's, free
     // since its end) takes piece pi + 1
     if (si + 1 < s1) {
-      if (prep_next) dec_build_q_row(p, sm.qbuf + ((pi + 1) & 1) * (kQBytes / 16), pn, warp, lane, qn);
+      if (prep_next) dec_build_q_row(p, sm.qbuf + ((pi + 1) & 1) * (kQBytes / 16), pn, warp, lane, qn, qsign);
       named_bar(1, kDecThreads);
     }
   }
