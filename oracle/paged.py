@@ -155,3 +155,28 @@ def decode_attention_streaming(q: np.ndarray, pages, P: int, Hkv: int, D: int, s
         out[kv * G:(kv + 1) * G] = o
         lse[kv * G:(kv + 1) * G] = l
     return out, lse
+
+
+def decode_attention_multi(q: np.ndarray, pages, P: int, Hkv: int, D: int, seed: int):
+    """Several query tokens per request with a causal mask: q [nq, Hq, D]
+    are the request's last nq tokens, and query token i (position
+    T - nq + i, T the valid tokens of all pages) attends to tokens
+    0 .. T - nq + i of the dequantised cache.  Returns out [nq, Hq, D] and
+    lse [nq, Hq].
+
+    The pages describe one query per decode step; a chunk of queries (prefill
+    of a chunk, or verification of speculative tokens) is the same softmax
+    attention under the decoder's causal mask: each token sees itself and
+    every earlier token."""
+    K, V = dequant_pages(pages, P, Hkv, D, seed)
+    q = np.asarray(q, dtype=np.float64)
+    nq, T = q.shape[0], K.shape[0]
+    if nq > T:
+        raise ValueError("more query tokens than cached tokens")
+    outs, lses = [], []
+    for i in range(nq):
+        visible = T - nq + i + 1
+        o, l = attention_dense(q[i], K[:visible], V[:visible])
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)

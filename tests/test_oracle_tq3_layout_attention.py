@@ -268,3 +268,63 @@ def test_streaming_equals_dense():
     assert np.allclose(a[0], b[0], atol=1e-12) and np.allclose(a[1], b[1], atol=1e-12)
     c = decode_attention_streaming(q, pages, P, Hkv, D, SEED, kv_heads=[1])
     assert np.allclose(c[0][3:], a[0][3:], atol=1e-12) and np.all(np.isnan(c[0][:3]))
+
+
+# ----------------------------------------------------------------- several query tokens
+def _masked_matrix_attention(q, K, V):
+    """Causal attention written as one masked score matrix: S = Q K^T / sqrt(d)
+    with S[i, t] = -inf for t > T - nq + i, row-wise softmax, times V."""
+    nq, T = q.shape[0], K.shape[0]
+    S = (q @ K.T) / np.sqrt(q.shape[1])
+    mask = np.arange(T)[None, :] > (T - nq + np.arange(nq))[:, None]
+    S = np.where(mask, -np.inf, S)
+    m = S.max(axis=1, keepdims=True)
+    E = np.exp(S - m)
+    return (E @ V) / E.sum(axis=1, keepdims=True), m[:, 0] + np.log(E.sum(axis=1))
+
+
+def test_multi_query_equals_masked_matrix():
+    from oracle.paged import decode_attention_multi, dequant_pages
+    rng = np.random.default_rng(19)
+    P, Hkv, D = 16, 2, 64
+    tiers = [TIER_ANCHOR, TIER_STALE, TIER_STALE, TIER_RECENT, TIER_RECENT]
+    pages = _pages(rng, P, Hkv, D, tiers, 5)          # tail page: 5 tokens
+    K, V = dequant_pages(pages, P, Hkv, D, SEED)
+    for nq in (1, 3, 5, 9):                            # 9 reaches into the page before the tail
+        q = rng.standard_normal((nq, 6, D))
+        out, lse = decode_attention_multi(q, pages, P, Hkv, D, SEED)
+        for h in range(6):
+            kv = h // 3
+            ro, rl = _masked_matrix_attention(q[:, h], K[:, kv], V[:, kv])
+            assert np.allclose(out[:, h], ro, atol=1e-12) and np.allclose(lse[:, h], rl, atol=1e-12)
+
+
+def test_multi_query_token_is_decode_over_its_prefix():
+    from oracle.paged import decode_attention_multi
+    rng = np.random.default_rng(20)
+    P, Hkv, D = 16, 2, 64
+    tiers = [TIER_STALE, TIER_ANCHOR, TIER_RECENT, TIER_RECENT]
+    pages = _pages(rng, P, Hkv, D, tiers, 3)
+    T = 3 * P + 3
+    nq = 7
+    q = rng.standard_normal((nq, 6, D))
+    out, lse = decode_attention_multi(q, pages, P, Hkv, D, SEED)
+    # nq = 1 is the decode step itself
+    o1, l1 = decode_attention_multi(q[-1:], pages, P, Hkv, D, SEED)
+    d1 = decode_attention(q[-1], pages, P, Hkv, D, SEED)
+    assert np.allclose(o1[0], d1[0], atol=1e-12) and np.allclose(l1[0], d1[1], atol=1e-12)
+    # query i equals a single decode over the cache cut after its own token:
+    # the page list truncated and its last page's valid count lowered
+    for i in range(nq):
+        visible = T - nq + i + 1
+        cut = []
+        for t, pg, n in pages:
+            start = sum(x[2] for x in cut)
+            if start >= visible:
+                break
+            cut.append((t, pg, min(n, visible - start)))
+        ref = decode_attention(q[i], cut, P, Hkv, D, SEED)
+        assert np.allclose(out[i], ref[0], atol=1e-12) and np.allclose(lse[i], ref[1], atol=1e-12)
+    # more query tokens than cached tokens is an error
+    with pytest.raises(ValueError):
+        decode_attention_multi(rng.standard_normal((T + 1, 6, D)), pages, P, Hkv, D, SEED)
