@@ -231,10 +231,28 @@ mkv_status mkv_decode_attention(mkv_pool* pool, int32_t layer, int32_t n, const 
                                 const void* q, mkv_dtype dtype, float* out, float* lse,
                                 mkv_stream_t stream);
 
+/* Several query tokens per request over the mixed-format cache (chunked
+ * prefill, or verifying speculative tokens).  The pages describe one query
+ * token per step; this call extends the same attention, partial states and
+ * merge causally: the last nq tokens of each sequence (already appended, so
+ * the sequence holds len >= nq tokens) are the queries, and query token i
+ * (position len - nq + i) attends to tokens 0 .. len - nq + i.  The result
+ * is exactly mkv_decode_attention run nq times over the growing prefix.
+ * q: device [n, nq, H_q, d] of `dtype`; out: device fp32 [n, nq, H_q, d];
+ * lse: device fp32 [n, nq, H_q].  The pages that hold the query tokens must
+ * be FP8 (they are the newest, so Recent).  The plan holds n * nq batch
+ * entries (query token i of request b is entry b * nq + i), each reading its
+ * own prefix.  Errors: those of mkv_decode_attention; INVALID_ARGUMENT for
+ * nq < 1, n * nq > max_batch or a sequence shorter than nq; INVALID_STATE
+ * when a query token sits in a TQ3 page. */
+mkv_status mkv_decode_attention_multi(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids,
+                                      int32_t nq, const void* q, mkv_dtype dtype, float* out, float* lse,
+                                      mkv_stream_t stream);
+
 /* One decode step of one layer: append each sequence's newest token (FP8,
  * as mkv_append_tokens with n_new = 1) and run mixed-format decode attention
  * over all its tokens (as mkv_decode_attention), in one call and one kernel
- * launch fewer (the append runs inside the query-preparation kernel).  The
+ * launch fewer (the append runs inside the partial-attention kernel).  The
  * newest token must already be counted by mkv_seq_extend and sit in an FP8
  * page.  k, v: device [n, H_kv, d] of kv_dtype (row i is seq_ids[i]'s token);
  * q, out, lse as in mkv_decode_attention.  Errors: those of the two calls. */

@@ -27,7 +27,7 @@ MKV_POOL_HOST_ONLY = 1
 EXPORTED = [
     "mkv_pool_required_bytes", "mkv_pool_create", "mkv_pool_destroy", "mkv_seq_extend", "mkv_seq_release",
     "mkv_seq_info", "mkv_page_info", "mkv_append_tokens", "mkv_set_tier", "mkv_demote_pages",
-    "mkv_decode_attention", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
+    "mkv_decode_attention", "mkv_decode_attention_multi", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
     "mkv_plan_decode", "mkv_check_device_errors", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
 ]
 
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
         "mkv_set_tier": [P, I32, I32, ctypes.c_int],
         "mkv_demote_pages": [P, I32, I32P, I32P, P],
         "mkv_decode_attention": [P, I32, I32, I32P, P, ctypes.c_int, P, P, P],
+        "mkv_decode_attention_multi": [P, I32, I32, I32P, I32, P, ctypes.c_int, P, P, P],
         "mkv_decode_attention_noalloc": [P, I32, I32, I32P, P, ctypes.c_int, P, P, P],
         "mkv_append_decode": [P, I32, I32, I32P, P, P, ctypes.c_int, P, ctypes.c_int, P, P, P],
         "mkv_dequantize_pages": [P, I32, I32, I32, I32, P, P, ctypes.c_int, P],
@@ -204,6 +205,12 @@ def mkv_decode_attention(pool, layer: int, seq_ids, q, dtype: int, out, lse, str
     a, n = _i32(seq_ids)
     check(lib().mkv_decode_attention(pool, layer, n, a, _ptr(q), dtype, _ptr(out), _ptr(lse), _stream(stream)),
           "mkv_decode_attention")
+
+
+def mkv_decode_attention_multi(pool, layer: int, seq_ids, nq: int, q, dtype: int, out, lse, stream=None) -> None:
+    a, n = _i32(seq_ids)
+    check(lib().mkv_decode_attention_multi(pool, layer, n, a, nq, _ptr(q), dtype, _ptr(out), _ptr(lse),
+                                           _stream(stream)), "mkv_decode_attention_multi")
 
 
 def mkv_decode_attention_noalloc(pool, layer: int, seq_ids, q, dtype: int, out, lse, stream=None) -> None:

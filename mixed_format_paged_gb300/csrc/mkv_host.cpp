@@ -193,6 +193,7 @@ struct mkv_pool {
   // plan cache
   uint64_t plan_gen = 0;
   std::vector<int32_t> plan_ids;
+  int32_t plan_nq = 1;             // query tokens per request of the cached plan
   DecodeParams plan_params{};
   MergeParams merge_params{};
   int plan_parts = 0;
@@ -338,9 +339,14 @@ constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
 // contiguous piece per CTA of equal estimated cost.  Each (CTA, group) piece
 // writes one partial state; a group's partial states are contiguous, which is
 // what the merge kernel reads.
-mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, cudaStream_t stream) {
+mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq, bool upload, cudaStream_t stream) {
   const int P = p->cfg.page_size, H = p->cfg.num_kv_heads;
   const PlanLayout L = plan_layout(p->entry_cap, p->chunk_cap, effective_batch(p->cfg), H);
+  // With nq query tokens per request the plan holds n_req * nq batch
+  // entries: entry b * nq + i is request ids[b] cut after its token
+  // len - nq + i (query token i sees that prefix).
+  const int n = n_req * nq;
+  if (n > effective_batch(p->cfg)) return fail(MKV_ERR_CAPACITY, "%d requests x %d query tokens > max_batch", n_req, nq);
   std::vector<PageEntry> entries;
   entries.reserve(size_t(n) * 64);
   struct BatchPages {
@@ -348,14 +354,15 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   };
   std::vector<BatchPages> bp(n);
   for (int b = 0; b < n; ++b) {
-    const SeqRec& s = p->seqs[ids[b]];
-    const int np = int(s.pages.size());
+    const SeqRec& s = p->seqs[ids[b / nq]];
+    const int len = s.len - (nq - 1 - b % nq);
+    const int np = npages_for(len, P);
     BatchPages& B = bp[b];
     B.f_first = int(entries.size());
     for (int i = 0; i < np; ++i) {
-      const int nv = (i == np - 1) ? s.len - i * P : P;
+      const int nv = (i == np - 1) ? len - i * P : P;
       if (s.pages[i].tier != MKV_TIER_STALE)
-        entries.push_back({s.pages[i].slot, int16_t(nv), int16_t(i == np - 1 ? 1 : 0)});
+        entries.push_back({s.pages[i].slot, int16_t(nv), int16_t(i == np - 1 && nq == 1 ? 1 : 0)});
     }
     B.f_count = int(entries.size()) - B.f_first;
     B.t_first = int(entries.size());
@@ -558,6 +565,23 @@ mkv_status build_plan(mkv_pool* p, int32_t n, const int32_t* ids, bool upload, c
   std::memcpy(h + L.segs, segs.data(), segs.size() * sizeof(Segment));
   std::memcpy(h + L.merge, md.data(), md.size() * sizeof(MergeDesc));
   return staging_upload(p->st_plan, p->plan_region, L.total, stream);
+}
+
+// The decode plan of (ids, nq query tokens per request), rebuilt only when
+// the pool changed or another batch was planned since.
+mkv_status ensure_plan(mkv_pool* p, int32_t n, const int32_t* ids, int32_t nq, bool upload, cudaStream_t s) {
+  const bool cached = p->plan_gen == p->generation && p->plan_nq == nq && p->plan_ids.size() == size_t(n) &&
+                      std::equal(ids, ids + n, p->plan_ids.begin());
+  if (cached) return MKV_OK;
+  const mkv_status st = build_plan(p, n, ids, nq, upload, s);
+  if (st != MKV_OK) {
+    p->plan_gen = 0;
+    return st;
+  }
+  p->plan_gen = p->generation;
+  p->plan_nq = nq;
+  p->plan_ids.assign(ids, ids + n);
+  return MKV_OK;
 }
 
 mkv_status check_batch(const mkv_pool* p, int32_t n, const int32_t* ids, bool need_nonempty) {
@@ -927,16 +951,33 @@ mkv_status mkv_decode_attention(mkv_pool* p, int32_t layer, int32_t n, const int
   if (n == 0) return MKV_OK;
   if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool cached = p->plan_gen == p->generation && p->plan_ids.size() == size_t(n) &&
-                      std::equal(ids, ids + n, p->plan_ids.begin());
-  if (!cached) {
-    if ((st = build_plan(p, n, ids, !p->host_only, s)) != MKV_OK) {
-      p->plan_gen = 0;
-      return st;
-    }
-    p->plan_gen = p->generation;
-    p->plan_ids.assign(ids, ids + n);
+  if ((st = ensure_plan(p, n, ids, 1, !p->host_only, s)) != MKV_OK) return st;
+  if (p->host_only) return MKV_OK;
+  return enqueue_decode(p, layer, q, dtype, p->workspace, nullptr, nullptr, MKV_F32, out, lse, s);
+}
+
+mkv_status mkv_decode_attention_multi(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, int32_t nq,
+                                      const void* q, mkv_dtype dtype, float* out, float* lse, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (dtype != MKV_F32 && dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if (nq < 1 || nq > effective_batch(p->cfg)) return fail(MKV_ERR_INVALID_ARGUMENT, "nq = %d", nq);
+  if (int64_t(n) * nq > effective_batch(p->cfg))
+    return fail(MKV_ERR_INVALID_ARGUMENT, "%d requests x %d query tokens > max_batch", n, nq);
+  if (n == 0) return MKV_OK;
+  if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
+  const int P = p->cfg.page_size;
+  for (int i = 0; i < n; ++i) {
+    const SeqRec& sr = p->seqs[ids[i]];
+    if (sr.len < nq) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence %d holds %d < nq tokens", ids[i], sr.len);
+    for (int pg = (sr.len - nq) / P; pg <= (sr.len - 1) / P; ++pg)
+      if (sr.pages[pg].tier == MKV_TIER_STALE)
+        return fail(MKV_ERR_INVALID_STATE, "sequence %d: a query token's page %d is TQ3", ids[i], pg);
   }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = ensure_plan(p, n, ids, nq, !p->host_only, s)) != MKV_OK) return st;
   if (p->host_only) return MKV_OK;
   return enqueue_decode(p, layer, q, dtype, p->workspace, nullptr, nullptr, MKV_F32, out, lse, s);
 }
@@ -954,16 +995,7 @@ mkv_status mkv_decode_attention_noalloc(mkv_pool* p, int32_t layer, int32_t n, c
   if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
   if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no device scratch");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool cached = p->plan_gen == p->generation && p->plan_ids.size() == size_t(n) &&
-                      std::equal(ids, ids + n, p->plan_ids.begin());
-  if (!cached) {
-    if ((st = build_plan(p, n, ids, true, s)) != MKV_OK) {
-      p->plan_gen = 0;
-      return st;
-    }
-    p->plan_gen = p->generation;
-    p->plan_ids.assign(ids, ids + n);
-  }
+  if ((st = ensure_plan(p, n, ids, 1, true, s)) != MKV_OK) return st;
   float* scratch = nullptr;
   size_t scratch_bytes = 0;
   cudaError_t e = noalloc_scratch(&scratch, &scratch_bytes);
@@ -995,16 +1027,7 @@ mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_
   }
   if (p->host_only) return MKV_OK;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool cached = p->plan_gen == p->generation && p->plan_ids.size() == size_t(n) &&
-                      std::equal(ids, ids + n, p->plan_ids.begin());
-  if (!cached) {
-    if ((st = build_plan(p, n, ids, true, s)) != MKV_OK) {
-      p->plan_gen = 0;
-      return st;
-    }
-    p->plan_gen = p->generation;
-    p->plan_ids.assign(ids, ids + n);
-  }
+  if ((st = ensure_plan(p, n, ids, 1, true, s)) != MKV_OK) return st;
   return enqueue_decode(p, layer, q, q_dtype, p->workspace, k, v, kv_dtype, out, lse, s);
 }
 
@@ -1119,7 +1142,7 @@ mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* 
   if (!p || !n_chunks) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
   mkv_status st = check_batch(p, n, ids, true);
   if (st != MKV_OK) return st;
-  if ((st = build_plan(p, n, ids, false, nullptr)) != MKV_OK) return st;
+  if ((st = build_plan(p, n, ids, 1, false, nullptr)) != MKV_OK) return st;
   p->plan_gen = 0;   // the device copy (if any) no longer matches
   const int nc = int(p->plan_debug.size() / 6);
   *n_chunks = nc;

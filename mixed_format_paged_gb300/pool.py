@@ -86,6 +86,22 @@ class MkvPool:
         B.mkv_decode_attention(self.handle, layer, seq_ids, q, dtype, out, lse, self._stream(stream))
         return out, lse
 
+    def decode_multi(self, layer: int, seq_ids, q: torch.Tensor, out: torch.Tensor | None = None,
+                     lse: torch.Tensor | None = None, stream=None):
+        """Attention of each request's last nq tokens (q: [n, nq, H_q, d]), query
+        token i seeing the request's tokens up to its own position; returns
+        out [n, nq, H_q, d] and lse [n, nq, H_q]."""
+        n, nq = len(seq_ids), q.shape[1]
+        if q.dtype not in (torch.bfloat16, torch.float32) or not q.is_contiguous() or q.dim() != 4:
+            raise TypeError("q must be a contiguous [n, nq, H_q, d] float32 or bfloat16 tensor")
+        if out is None:
+            out = torch.empty((n, nq, self.num_q_heads, self.head_dim), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((n, nq, self.num_q_heads), dtype=torch.float32, device=q.device)
+        dtype = B.MKV_BF16 if q.dtype == torch.bfloat16 else B.MKV_F32
+        B.mkv_decode_attention_multi(self.handle, layer, seq_ids, nq, q, dtype, out, lse, self._stream(stream))
+        return out, lse
+
     def append_decode(self, layer: int, seq_ids, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
                       out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
         """Append each sequence's newest token (k, v: [n, H_kv, d]) and decode (q: [n, H_q, d])."""

@@ -246,3 +246,20 @@ def test_decode_argument_errors(mkv):
     with pytest.raises(mkv.MkvError):
         mkv.mkv_decode_attention(p.handle, 0, [0], None, 0, q, q)     # NULL q
     mkv.mkv_decode_attention(p.handle, 0, [0], q, 0, q, q)            # host-only: validates, no launch
+
+
+def test_decode_multi_argument_errors(mkv):
+    p = _host_pool(mkv)                                # P = 64, max_batch 4
+    p.extend([0, 1], [64 * 3 + 2, 40])
+    p.demote([0], [2])                                 # page 2 TQ3, tail page 3 holds 2 tokens
+    q = _FakeTensor()
+    call = lambda ids, nq: mkv.mkv_decode_attention_multi(p.handle, 0, ids, nq, q, 0, q, q)
+    call([0, 1], 2)                                    # host-only: validates and plans, no launch
+    call([1], 4)
+    for ids, nq in (([0], 0), ([0, 1], 3), ([1], 41), ([1], 5)):   # nq < 1; 2 x 3 and 5 > max_batch
+        with pytest.raises(mkv.MkvError) as e:
+            call(ids, nq)
+        assert e.value.status == 1
+    with pytest.raises(mkv.MkvError) as e:
+        call([0], 3)                                   # the first query token sits in TQ3 page 2
+    assert e.value.status == 4

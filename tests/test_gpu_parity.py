@@ -393,3 +393,49 @@ def test_dequantize_pages_matches_oracle(mkv, P):
     # bf16 output is the fp32 result rounded to nearest even
     assert torch.equal(kb, k32[P:5 * P].to(torch.bfloat16)) and torch.equal(vb, v32[P:5 * P].to(torch.bfloat16))
     pool.check_device_errors()
+
+
+# ------------------------------------------------------------------ several query tokens per request
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("qdtype", [torch.float32, torch.bfloat16])
+def test_decode_multi_query_causal(mkv, P, qdtype):
+    """mkv_decode_attention_multi: query token i of each request attends to the
+    request's tokens up to its own position (oracle: causal attention over the
+    stored pages)."""
+    from oracle.paged import decode_attention_multi
+    g = torch.Generator().manual_seed(23)
+    pool = _small_pool(mkv, P=P, fp8=96, tq3=96, nseq=32, maxp=24)   # 4 requests x 8 query tokens
+    # (tokens, anchors, stale pages): tails of 1, 5 and P tokens, so that the
+    # query tokens of some requests start in the page before the tail
+    specs = [(4 * P + 5, [0], [1, 2]), (9, [], []), (6 * P + 1, [], [0, 1, 2, 3]), (3 * P, [1], [0])]
+    for r, (n, anc, st) in enumerate(specs):
+        K, V = _kv(n, torch.bfloat16, g)
+        pool.extend([r], [n])
+        pool.append(0, [r], [n], K.to(DEV), V.to(DEV))
+        for a in anc:
+            pool.set_tier(r, a, 2)
+        if st:
+            pool.demote([r] * len(st), st)
+    ids = list(range(len(specs)))
+    for nq in (1, 3, 8):
+        q = torch.randn(len(ids), nq, 24, 256, generator=g).to(qdtype)
+        out, lse = pool.decode_multi(0, ids, q.to(DEV))
+        torch.cuda.synchronize()
+        pool.check_device_errors()
+        for b, r in enumerate(ids):
+            ro, rl = decode_attention_multi(q[b].double().numpy(), _export(pool, 0, r), P, 4, 256, 4321)
+            o = out[b].double().cpu().numpy()
+            l_ = lse[b].double().cpu().numpy()
+            for i in range(nq):
+                assert np.abs(o[i] - ro[i]).max() <= OUT_TOL * np.abs(ro[i]).max(), (nq, r, i)
+                assert np.abs(l_[i] - rl[i]).max() <= LSE_TOL, (nq, r, i)
+        if nq == 1:
+            # one query token is the decode step itself (same plan, same bits)
+            o1, l1 = pool.decode(0, ids, q[:, 0].contiguous().to(DEV))
+            torch.cuda.synchronize()
+            assert torch.equal(o1, out[:, 0]) and torch.equal(l1, lse[:, 0])
+    # a query token in a TQ3 page is refused; so are too many query tokens
+    with pytest.raises(mkv.MkvError):
+        pool.decode_multi(0, [2], torch.randn(1, 3 * P, 24, 256).to(DEV))
+    with pytest.raises(mkv.MkvError):
+        pool.decode_multi(0, [1], torch.randn(1, 10, 24, 256).to(DEV))
