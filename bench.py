@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--nq", type=int, default=1,
+                    help="query tokens per request and step (> 1: the multi-query path, a separate line)")
     return ap.parse_args()
 
 
@@ -463,10 +465,108 @@ def run_mkv(args):
         dist.destroy_process_group()
 
 
+def run_multi(args):
+    """Several query tokens per request and step (mkv_decode_attention_multi):
+    each step appends nq tokens to every request (mkv_append_tokens) and runs
+    the causal multi-query attention per layer.  No pages are demoted during
+    the few timed steps (the Recent window grows by their tokens).  value =
+    the unique KV bytes of the cache (each byte once per kv head and step) per
+    second; the decode kernel reads each query token's prefix, about nq times
+    those bytes, reported as kernel_read_bytes_per_launch."""
+    import torch
+
+    from mixed_format_paged_gb300 import binding as B
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import make_pool, prefill
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    w = workloads.make(args.workload)
+    L, P, nq, n = w.num_layers, w.P, args.nq, w.n
+    total_steps = args.warmup + args.steps
+    pool = make_pool(w, device=dev, extra_steps=nq * (total_steps + 1), seed=99, max_batch=n * nq)
+    prefill(pool, w, device=dev)
+    ids = list(range(n))
+    g = torch.Generator().manual_seed(7)
+    ins = []
+    for s in range(total_steps):
+        row = []
+        for layer in range(L):
+            k = torch.randn(n * nq, w.Hkv, w.D, generator=g).to(w.kv_dtype).to(dev)
+            v = torch.randn(n * nq, w.Hkv, w.D, generator=g).to(w.kv_dtype).to(dev)
+            q = torch.randn(n, nq, w.Hq, w.D, generator=g).to(w.q_dtype).to(dev)
+            row.append((k, v, q))
+        ins.append(row)
+    outs = [(torch.empty((n, nq, w.Hq, w.D), device=dev), torch.empty((n, nq, w.Hq), device=dev)) for _ in range(L)]
+    TIMED_LAYER = L - 1
+
+    def step(s, ev_pair=None, acc=None):
+        pool.extend(ids, [nq] * n)
+        if acc is not None:
+            acc.append(kv_bytes_now(pool, P, L))
+        for layer in range(L):
+            k, v, q = ins[s][layer]
+            pool.append(layer, ids, [nq] * n, k, v)
+            if ev_pair is not None and layer == TIMED_LAYER:
+                B.mkv_set_timing_events(pool.handle, *ev_pair)
+            pool.decode_multi(layer, ids, q, *outs[layer])
+
+    sampler = ClockSampler(0)
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record()
+        b.record()
+    acc = []
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i, ev[i], acc)
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    pool.check_device_errors()
+    ms = e0.elapsed_time(e1)
+    kv_total = sum(b for b, _ in acc)
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    unique = sum(b for b, _ in acc) / len(acc) / L
+    avg_us = 1e3 * sum(kernel_ms) / len(kernel_ms)
+    ctx = sum(c for _, c in acc) / len(acc)
+    # the kernel reads query token i's prefix: (nq - 1 - i) tokens fewer than the
+    # whole cache, all of them FP8 (the newest pages)
+    per_tok_fp8 = w.Hkv * ROW_BYTES["fp8"]
+    read = nq * unique - per_tok_fp8 * n * nq * (nq - 1) / 2
+    peak, peak_src = measured_peaks()
+    line = {
+        "metric": "multi-query decode-attn KV GB/s (unique cache bytes) and query tokens/s",
+        "value": kv_total / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16xf16->f32 (fp8/tq3 storage)", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "nq": nq, "requests": n, "layers": L,
+                   "context_tokens": int(ctx), "demotion": "none during the timed steps"},
+        "query_tokens_per_s": n * nq * args.steps * L / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": "mkv_decode_kernel (partial attention)",
+                     "unique_bytes_per_launch": unique, "kernel_read_bytes_per_launch": read,
+                     "avg_launch_us": avg_us, "achieved_unique": unique / (avg_us * 1e-6) / 1e9,
+                     "achieved_read": read / (avg_us * 1e-6) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac_read": read / (avg_us * 1e-6) / 1e9 / peak, "peak_source": peak_src},
+        "gpu_launches": args.steps * L * 3, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.nq > 1:
+        run_multi(args)
     else:
         run_mkv(args)
 

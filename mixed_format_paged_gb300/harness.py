@@ -27,10 +27,14 @@ def pool_sizes(w: Workload, extra_steps: int | None = None):
     return fp8, tq3, max(npg)
 
 
-def make_pool(w: Workload, device="cuda", extra_steps: int | None = None, seed: int = 0x5EED, host_only=False):
+def make_pool(w: Workload, device="cuda", extra_steps: int | None = None, seed: int = 0x5EED, host_only=False,
+              max_batch: int | None = None):
+    """A pool sized for the workload; max_batch (batch entries of one decode
+    plan) defaults to the request count, larger for several query tokens."""
     fp8, tq3, maxp = pool_sizes(w, extra_steps)
-    return MkvPool(w.num_layers, w.Hq, w.Hkv, w.D, w.P, fp8, tq3, max_seqs=w.n, max_pages_per_seq=maxp,
-                   max_batch=w.n, rotation_seed=seed, device=device, host_only=host_only)
+    mb = max(w.n, max_batch or w.n)
+    return MkvPool(w.num_layers, w.Hq, w.Hkv, w.D, w.P, fp8, tq3, max_seqs=mb, max_pages_per_seq=maxp,
+                   max_batch=mb, rotation_seed=seed, device=device, host_only=host_only)
 
 
 def prefill(pool: MkvPool, w: Workload, device="cuda", keep_raw: bool = False, layers=None):
