@@ -1245,13 +1245,16 @@ __device__ __forceinline__ void merge_run(const float* part, int stride, int h, 
 
 __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   __shared__ float xs[kHeadDim];
-  // launched as a programmatic dependent of the decode kernel: wait for its
-  // partial states before reading them
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int h = blockIdx.x % p.G;
   const int bk = blockIdx.x / p.G;
   const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+  // the merge descriptors come with the plan (copied in before the decode
+  // kernel started), so they load while the decode kernel still runs
   const MergeDesc md = p.desc[bk];
+  const bool neg = sign_neg(p.signs, threadIdx.x);
+  // launched as a programmatic dependent of the decode kernel: wait for its
+  // partial states before reading them
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int d = threadIdx.x, lane = d & 31;
   const int stride = p.G * (2 + kHeadDim);
   // the first batch of both formats goes out at once
@@ -1275,7 +1278,7 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
     os = (d & bm) ? (other - os) : (os + other);
   }
   os *= (1.0f / 16.0f);
-  if (sign_neg(p.signs, d)) os = -os;
+  if (neg) os = -os;
   merge_run(p.part, stride, h, md.fp8_first, md.fp8_count, d, bf, Mf, Lf, of);
   const float M = fmaxf(Ms, Mf);
   const float fs = (Ms == -INFINITY) ? 0.f : exp2f(Ms - M);
