@@ -66,10 +66,17 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the decode kernel's source with comments and blank lines
+    removed, so that a comment-only edit keeps committed counters valid."""
+    import re
     h = hashlib.sha256()
     for f in ("mkv_kernels.cu", "mkv_internal.h"):
-        with open(os.path.join(ROOT, "mixed_format_paged_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mixed_format_paged_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        lines = [ln.rstrip() for ln in src.splitlines()]
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -326,7 +326,7 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 // block and per piece, in units of one TQ3 token.  Fitted to per-CTA times of
 // the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.31 us of CTA
 // time, a 16-token FP8 block ~0.25 us, a piece ~4 us (its end-of-piece merge
-// and the warps left idle in its last round of blocks).
+// and the warps' drift before it).
 constexpr double kCostTq3Token = 1.0;
 constexpr double kCostFp8Token = 1.45;
 constexpr double kCostBlock = 8.0;
@@ -336,7 +336,8 @@ constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
 
 // Split the batch's pages into groups (request, kv head, format), lay the
 // groups' blocks out in one sequence, and cut that sequence into one
-// contiguous piece per CTA of equal estimated cost.  Each (CTA, group) piece
+// contiguous piece list per CTA so that the largest CTA's estimated cost is
+// as small as the cut points allow.  Each (CTA, group) piece
 // writes one partial state; a group's partial states are contiguous, which is
 // what the merge kernel reads.
 mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq, bool upload, cudaStream_t stream) {

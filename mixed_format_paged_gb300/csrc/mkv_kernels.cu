@@ -451,12 +451,13 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
 
 // ============================================================== decode
 // Persistent partial-attention kernel; one CTA of kDecWarps (12) warps per SM.
-// The host cut the launch's blocks into one contiguous, cost-balanced piece
-// list per CTA (a piece is a run of blocks of one (request, kv head, format)
-// group).  Within a piece, warp w takes blocks w, w + 12, w + 24, ... and runs
-// the whole of attention on them by itself:
+// The host cut the launch's blocks into one contiguous piece list per CTA,
+// minimising the largest CTA's estimated cost (a piece is a run of blocks of
+// one (request, kv head, format) group).  Within a piece, warp w takes blocks
+// w, w + 12, w + 24, ... and runs the whole of attention on them by itself:
 //   S = Q K^T on mma.sync m16n8k16: A = q rows (hi in rows 0-7, lo residual
-//     in rows 8-15, fp16) from the q-prep fragments, B = K dequantised in
+//     in rows 8-15, fp16), fragments the kernel builds in shared memory for
+//     each piece (signs and Walsh-Hadamard rotation for TQ3), B = K dequantised in
 //     registers (TQ3: PRMT byte-table lookups; FP8: cvt e4m3x2);
 //   online softmax in log2 units with a lazy rescale (per warp);
 //   O^T += V^T P^T: A = V dequantised in registers (token pairs), B = P
