@@ -304,6 +304,16 @@ mkv_status mkv_plan_decode(mkv_pool* pool, int32_t n, const int32_t* seq_ids, in
  * that ran out. */
 mkv_status mkv_check_device_errors(mkv_pool* pool, mkv_stream_t stream);
 
+/* Failure-detection self-test (not from the pages).  Enqueues on `stream` a
+ * one-CTA kernel that waits on an mbarrier nothing arrives on, with the
+ * decode kernel's rule for a wait that runs out: after limit_cycles SM clocks
+ * (1 .. 4e9; 2e6 is about 1 ms) it records the timeout bit in the pool's
+ * device error word and returns.  The next mkv_check_device_errors then
+ * reports MKV_ERR_DEVICE_CHECK and clears the word; the CUDA context and the
+ * pool stay usable.  Nothing faults, traps or spins without a bound.
+ * Errors: INVALID_ARGUMENT (limit), UNSUPPORTED on a host-only pool. */
+mkv_status mkv_selftest_wait_timeout(mkv_pool* pool, int64_t limit_cycles, mkv_stream_t stream);
+
 /* Instrumentation: when `start` / `stop` (cudaEvent_t handles owned by the
  * caller) are non-NULL, the next mkv_decode_attention call records `start`
  * right before its partial-attention kernel and `stop` right after it, on the

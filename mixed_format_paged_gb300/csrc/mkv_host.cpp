@@ -24,6 +24,11 @@
 #include <utility>
 #include <vector>
 
+namespace mkv {
+// mkv_selftest.cu: one CTA waits (bounded) on an mbarrier nothing arrives on
+cudaError_t launch_wait_probe(int* err, long long limit_cycles, cudaStream_t s);
+}  // namespace mkv
+
 namespace {
 
 using namespace mkv;
@@ -1151,6 +1156,16 @@ mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* 
     if (cap < nc) return fail(MKV_ERR_INVALID_ARGUMENT, "cap %d < %d chunks", cap, nc);
     std::memcpy(chunks, p->plan_debug.data(), p->plan_debug.size() * sizeof(int32_t));
   }
+  return MKV_OK;
+}
+
+mkv_status mkv_selftest_wait_timeout(mkv_pool* p, int64_t limit_cycles, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (limit_cycles < 1 || limit_cycles > 4000000000LL)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "limit_cycles %lld outside [1, 4e9]", static_cast<long long>(limit_cycles));
+  if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no device error word");
+  const cudaError_t e = launch_wait_probe(p->err, limit_cycles, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
   return MKV_OK;
 }
 

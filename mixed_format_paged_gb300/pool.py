@@ -141,3 +141,7 @@ class MkvPool:
 
     def check_device_errors(self, stream=None):
         B.mkv_check_device_errors(self.handle, self._stream(stream))
+
+    def selftest_wait_timeout(self, limit_cycles: int = 2_000_000, stream=None):
+        """Enqueue a bounded wait that runs out (see mkv_selftest_wait_timeout)."""
+        B.mkv_selftest_wait_timeout(self.handle, limit_cycles, self._stream(stream))

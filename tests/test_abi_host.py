@@ -263,3 +263,14 @@ def test_decode_multi_argument_errors(mkv):
     with pytest.raises(mkv.MkvError) as e:
         call([0], 3)                                   # the first query token sits in TQ3 page 2
     assert e.value.status == 4
+
+
+def test_selftest_wait_timeout_arguments(mkv):
+    p = _host_pool(mkv)
+    for bad in (0, -5, 4_000_000_001):
+        with pytest.raises(mkv.MkvError) as e:
+            p.selftest_wait_timeout(bad)
+        assert e.value.status == 1
+    with pytest.raises(mkv.MkvError) as e:
+        p.selftest_wait_timeout(1000)                  # host-only pool: no device error word
+    assert e.value.status == 2

@@ -439,3 +439,27 @@ def test_decode_multi_query_causal(mkv, P, qdtype):
         pool.decode_multi(0, [2], torch.randn(1, 3 * P, 24, 256).to(DEV))
     with pytest.raises(mkv.MkvError):
         pool.decode_multi(0, [1], torch.randn(1, 10, 24, 256).to(DEV))
+
+
+# ------------------------------------------------------------------ failure detection without a fault
+def test_wait_timeout_is_reported_and_context_stays_usable(mkv):
+    """A bounded wait that runs out (an mbarrier nothing arrives on) records
+    the timeout in the pool's error word; mkv_check_device_errors reports
+    MKV_ERR_DEVICE_CHECK once and clears it, and decode still matches the oracle."""
+    g = torch.Generator().manual_seed(29)
+    pool = _small_pool(mkv)
+    K, V = _kv(3 * 64 + 7, torch.bfloat16, g)
+    pool.extend([0], [3 * 64 + 7])
+    pool.append(0, [0], [3 * 64 + 7], K.to(DEV), V.to(DEV))
+    pool.demote([0], [1])
+    pool.check_device_errors()
+    pool.selftest_wait_timeout(2_000_000)              # ~1 ms at 2 GHz
+    with pytest.raises(mkv.MkvError) as e:
+        pool.check_device_errors()
+    assert e.value.status == 6                         # MKV_ERR_DEVICE_CHECK
+    pool.check_device_errors()                         # cleared
+    q = torch.randn(1, 24, 256, generator=g).to(torch.bfloat16)
+    out, lse = pool.decode(0, [0], q.to(DEV))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    _check_decode(pool, 0, [0], q.float(), out, lse, 4321)
