@@ -291,11 +291,12 @@ mkv_status mkv_rotation_signs(const mkv_pool* pool, int8_t* host_dst, int32_t ca
 mkv_status mkv_tq3_codebook(float* levels8, float* thresholds7);
 
 /* Decode plan for a batch (host only, no device access): the number of
- * partial-state splits the decode kernels would use, and per split 6 ints
+ * partial-state splits the decode kernels would use, and per split 9 ints
  * {batch index, kv head, tier (1 = FP8, 3 = TQ3), first page entry, page
- * count, tokens}.  Splits cut a tier's pages at block granularity (16 FP8
- * or 32 TQ3 tokens), so two consecutive splits may share one page.  chunks
- * may be NULL to query the count. */
+ * count, tokens, CTA, first block, blocks}, CTA by CTA.  Blocks are counted
+ * within the split's (request, kv head, tier) group: 16 FP8 or 32 TQ3 tokens
+ * each, page by page, so two consecutive splits may share one page.
+ * chunks (cap splits of 9 ints) may be NULL to query the count. */
 mkv_status mkv_plan_decode(mkv_pool* pool, int32_t n, const int32_t* seq_ids, int32_t* chunks,
                            int32_t cap, int32_t* n_chunks);
 

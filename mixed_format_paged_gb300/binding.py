@@ -263,13 +263,16 @@ def mkv_tq3_codebook():
     return list(lv), list(th)
 
 
+PLAN_RECORD = 9   # ints per split: b, kv head, tier, first entry, pages, tokens, CTA, first block, blocks
+
+
 def mkv_plan_decode(pool, seq_ids):
     a, n = _i32(seq_ids)
     nc = ctypes.c_int32()
     check(lib().mkv_plan_decode(pool, n, a, None, 0, ctypes.byref(nc)), "mkv_plan_decode")
-    buf = (ctypes.c_int32 * max(1, 6 * nc.value))()
+    buf = (ctypes.c_int32 * max(1, PLAN_RECORD * nc.value))()
     check(lib().mkv_plan_decode(pool, n, a, buf, nc.value, ctypes.byref(nc)), "mkv_plan_decode")
-    return [tuple(buf[6 * i: 6 * i + 6]) for i in range(nc.value)]
+    return [tuple(buf[PLAN_RECORD * i: PLAN_RECORD * (i + 1)]) for i in range(nc.value)]
 
 
 def mkv_check_device_errors(pool, stream=None) -> None:

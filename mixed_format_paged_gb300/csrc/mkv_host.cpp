@@ -202,7 +202,7 @@ struct mkv_pool {
   DecodeParams plan_params{};
   MergeParams merge_params{};
   int plan_parts = 0;
-  std::vector<int32_t> plan_debug;   // 6 ints per chunk
+  std::vector<int32_t> plan_debug;   // kPlanRecord ints per chunk
   // one-shot timing events around the next decode kernel
   cudaEvent_t t_start = nullptr, t_stop = nullptr;
   // append cache (destinations in the append region)
@@ -338,6 +338,7 @@ constexpr double kCostBlock = 8.0;
 constexpr double kCostPiece = 540.0;
 constexpr double kShortRoundBase = 0.4;  // a round with one busy warp costs 0.4 + 0.6/12 of a full one
 constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
+constexpr int kPlanRecord = 9;           // ints per split in mkv_plan_decode's output
 
 // Split the batch's pages into groups (request, kv head, format), lay the
 // groups' blocks out in one sequence, and cut that sequence into one
@@ -520,16 +521,18 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
       m.fp8_count = g.nparts;
     }
   }
-  // debug record: one line per partial state
+  // debug record: one line per partial state (kPlanRecord ints)
   p->plan_debug.clear();
-  for (const Segment& sg : segs) {
-    const Group& g = groups[sg.group];
-    const int bpp = P / (g.fmt ? kTq3Blk : kFp8Blk);
-    const size_t i = size_t(&sg - segs.data());
-    const int last = g.entry0 + (sg.blk + sg.nblk - 1) / bpp;
-    const int32_t rec[6] = {g.b, g.kvh, g.fmt ? 3 : 1, seg_entry[i], last - seg_entry[i] + 1, seg_tokens[i]};
-    p->plan_debug.insert(p->plan_debug.end(), rec, rec + 6);
-  }
+  for (int c = 0; c < ncta; ++c)
+    for (int i = cta_seg[c]; i < cta_seg[c + 1]; ++i) {
+      const Segment& sg = segs[i];
+      const Group& g = groups[sg.group];
+      const int bpp = P / (g.fmt ? kTq3Blk : kFp8Blk);
+      const int last = g.entry0 + (sg.blk + sg.nblk - 1) / bpp;
+      const int32_t rec[kPlanRecord] = {g.b, g.kvh, g.fmt ? 3 : 1, seg_entry[i], last - seg_entry[i] + 1,
+                                        seg_tokens[i], c, sg.blk, sg.nblk};
+      p->plan_debug.insert(p->plan_debug.end(), rec, rec + kPlanRecord);
+    }
   p->plan_parts = int(segs.size());
   // params
   DecodeParams& dp = p->plan_params;
@@ -1150,7 +1153,7 @@ mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* 
   if (st != MKV_OK) return st;
   if ((st = build_plan(p, n, ids, 1, false, nullptr)) != MKV_OK) return st;
   p->plan_gen = 0;   // the device copy (if any) no longer matches
-  const int nc = int(p->plan_debug.size() / 6);
+  const int nc = int(p->plan_debug.size() / kPlanRecord);
   *n_chunks = nc;
   if (chunks) {
     if (cap < nc) return fail(MKV_ERR_INVALID_ARGUMENT, "cap %d < %d chunks", cap, nc);

@@ -274,3 +274,81 @@ def test_selftest_wait_timeout_arguments(mkv):
     with pytest.raises(mkv.MkvError) as e:
         p.selftest_wait_timeout(1000)                  # host-only pool: no device error word
     assert e.value.status == 2
+
+
+def _rounds_of(layouts, P, H=4):
+    """The planner's work units for requests given as (tokens, tiers per page):
+    per (request, kv head, tier) group, TQ3 before FP8, blocks of 32 TQ3 / 16
+    FP8 tokens page by page, cut into rounds of 12 blocks from the group's
+    start; a round costs 12 x its slowest block (tokens x 1.0 or 1.45, + 8),
+    a short round 0.4 + 0.6 x its share of that."""
+    rounds = []                                            # (group key, cost)
+    for b, (n, tiers) in enumerate(layouts):
+        nv = [min(P, n - i * P) for i in range(len(tiers))]
+        for kvh in range(H):
+            for fmt in (3, 1):
+                pages = [nv[i] for i, t in enumerate(tiers) if (t == 3) == (fmt == 3)]
+                if not pages:
+                    continue
+                bt, rate = (32, 1.0) if fmt == 3 else (16, 1.45)
+                bpp = P // bt
+                nblk = (len(pages) - 1) * bpp + -(-pages[-1] // bt)
+                costs = [max(0, min(bt, pages[k // bpp] - (k % bpp) * bt)) * rate + 8.0 for k in range(nblk)]
+                for r in range(0, nblk, 12):
+                    c = costs[r:r + 12]
+                    rounds.append(((b, kvh, fmt), max(c) * 12 * (0.4 + 0.6 * len(c) / 12)))
+    return rounds
+
+
+def _cta_cost(rounds):
+    return sum(c for _, c in rounds) + 540.0 * (1 + sum(rounds[i][0] != rounds[i - 1][0] for i in range(1, len(rounds))))
+
+
+def test_plan_minimises_the_largest_cta(mkv):
+    """The split is contiguous and its largest CTA cost equals the optimum of
+    an exhaustive dynamic programme over the same cut points (within the
+    bisection's 1e-4)."""
+    P = 64
+    layouts = [(64 * 30 + 17, [2] + [3] * 21 + [1] * 9), (64 * 12, [3] * 9 + [1] * 3),
+               (64 * 5 + 1, [1] * 6), (64 * 18 + 40, [2, 3, 3, 2] + [3] * 11 + [1] * 4)]
+    p = _host_pool(mkv, num_layers=1, fp8_slots=64, tq3_slots=64, max_seqs=4, max_pages_per_seq=40)
+    for r, (n, tiers) in enumerate(layouts):
+        p.extend([r], [n])
+        for pg, t in enumerate(tiers):
+            if t == 2:
+                p.set_tier(r, pg, 2)
+        stale = [pg for pg, t in enumerate(tiers) if t == 3]
+        p.demote([r] * len(stale), stale)
+    plan = p.plan(list(range(len(layouts))))
+    rounds = _rounds_of(layouts, P)
+    index = {}
+    pos = 0
+    for key, _ in rounds:
+        index.setdefault(key, pos)
+        pos += 1
+    # the split as round ranges, CTA by CTA
+    ctas = {}
+    for b, kvh, tier, _, _, _, cta, blk0, nblk in plan:
+        assert blk0 % 12 == 0, "cuts fall on round boundaries"
+        start = index[(b, kvh, tier)] + blk0 // 12
+        ctas.setdefault(cta, []).append((start, start + -(-nblk // 12)))
+    assert sorted(ctas) == list(range(len(ctas)))
+    seq = [rng for c in sorted(ctas) for rng in ctas[c]]
+    assert seq[0][0] == 0 and seq[-1][1] == len(rounds)
+    assert all(a[1] == b[0] for a, b in zip(seq, seq[1:])), "CTAs hold contiguous runs of rounds"
+    got = max(_cta_cost(rounds[min(s for s, _ in r):max(e for _, e in r)]) for r in ctas.values())
+    # exhaustive optimum: f_k[j] = min_i max(f_{k-1}[i], cost(rounds i..j-1))
+    R = len(rounds)
+    nblocks = sum(nblk for *_, nblk in plan)
+    kmax = max(1, min(152, nblocks // 24))
+    C = np.full((R + 1, R + 1), np.inf)
+    for i in range(R):
+        for j in range(i + 1, R + 1):
+            C[i, j] = _cta_cost(rounds[i:j])
+    f = C[0].copy()
+    best = f[R]
+    for _ in range(kmax - 1):
+        f = np.min(np.maximum(f[:, None], C), axis=0)
+        best = min(best, f[R])
+    assert len(ctas) <= kmax
+    assert best <= got <= best * (1 + 1e-4) + 1e-9, (got, best)
