@@ -300,6 +300,12 @@ mkv_status mkv_tq3_codebook(float* levels8, float* thresholds7);
 mkv_status mkv_plan_decode(mkv_pool* pool, int32_t n, const int32_t* seq_ids, int32_t* chunks,
                            int32_t cap, int32_t* n_chunks);
 
+/* The same for mkv_decode_attention_multi with nq query tokens per request:
+ * split records use batch index b * nq + i for query token i of request b
+ * (its prefix up to that token).  Errors: those of mkv_decode_attention_multi. */
+mkv_status mkv_plan_decode_multi(mkv_pool* pool, int32_t n, const int32_t* seq_ids, int32_t nq, int32_t* chunks,
+                                 int32_t cap, int32_t* n_chunks);
+
 /* Synchronise `stream` and report (and clear) the pool's device error word:
  * MKV_ERR_DEVICE_CHECK if a kernel flagged a failed check or a bounded wait
  * that ran out. */

@@ -28,7 +28,7 @@ EXPORTED = [
     "mkv_pool_required_bytes", "mkv_pool_create", "mkv_pool_destroy", "mkv_seq_extend", "mkv_seq_release",
     "mkv_seq_info", "mkv_page_info", "mkv_append_tokens", "mkv_set_tier", "mkv_demote_pages",
     "mkv_decode_attention", "mkv_decode_attention_multi", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
-    "mkv_plan_decode", "mkv_check_device_errors", "mkv_selftest_wait_timeout", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
+    "mkv_plan_decode", "mkv_plan_decode_multi", "mkv_check_device_errors", "mkv_selftest_wait_timeout", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
 ]
 
 
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
         "mkv_rotation_signs": [P, ctypes.POINTER(ctypes.c_int8), I32],
         "mkv_tq3_codebook": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
         "mkv_plan_decode": [P, I32, I32P, I32P, I32, I32P],
+        "mkv_plan_decode_multi": [P, I32, I32P, I32, I32P, I32, I32P],
         "mkv_check_device_errors": [P, P],
         "mkv_selftest_wait_timeout": [P, ctypes.c_int64, P],
         "mkv_set_timing_events": [P, P, P],
@@ -272,6 +273,15 @@ def mkv_plan_decode(pool, seq_ids):
     check(lib().mkv_plan_decode(pool, n, a, None, 0, ctypes.byref(nc)), "mkv_plan_decode")
     buf = (ctypes.c_int32 * max(1, PLAN_RECORD * nc.value))()
     check(lib().mkv_plan_decode(pool, n, a, buf, nc.value, ctypes.byref(nc)), "mkv_plan_decode")
+    return [tuple(buf[PLAN_RECORD * i: PLAN_RECORD * (i + 1)]) for i in range(nc.value)]
+
+
+def mkv_plan_decode_multi(pool, seq_ids, nq: int):
+    a, n = _i32(seq_ids)
+    nc = ctypes.c_int32()
+    check(lib().mkv_plan_decode_multi(pool, n, a, nq, None, 0, ctypes.byref(nc)), "mkv_plan_decode_multi")
+    buf = (ctypes.c_int32 * max(1, PLAN_RECORD * nc.value))()
+    check(lib().mkv_plan_decode_multi(pool, n, a, nq, buf, nc.value, ctypes.byref(nc)), "mkv_plan_decode_multi")
     return [tuple(buf[PLAN_RECORD * i: PLAN_RECORD * (i + 1)]) for i in range(nc.value)]
 
 

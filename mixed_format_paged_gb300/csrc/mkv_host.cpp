@@ -593,6 +593,23 @@ mkv_status ensure_plan(mkv_pool* p, int32_t n, const int32_t* ids, int32_t nq, b
   return MKV_OK;
 }
 
+// nq query tokens per request: each request holds at least nq tokens, the
+// pages of its last nq tokens are FP8, and the plan's n * nq entries fit.
+mkv_status check_queries(const mkv_pool* p, int32_t n, const int32_t* ids, int32_t nq) {
+  if (nq < 1 || nq > effective_batch(p->cfg)) return fail(MKV_ERR_INVALID_ARGUMENT, "nq = %d", nq);
+  if (int64_t(n) * nq > effective_batch(p->cfg))
+    return fail(MKV_ERR_INVALID_ARGUMENT, "%d requests x %d query tokens > max_batch", n, nq);
+  const int P = p->cfg.page_size;
+  for (int i = 0; i < n; ++i) {
+    const SeqRec& sr = p->seqs[ids[i]];
+    if (sr.len < nq) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence %d holds %d < nq tokens", ids[i], sr.len);
+    for (int pg = (sr.len - nq) / P; pg <= (sr.len - 1) / P; ++pg)
+      if (sr.pages[pg].tier == MKV_TIER_STALE)
+        return fail(MKV_ERR_INVALID_STATE, "sequence %d: a query token's page %d is TQ3", ids[i], pg);
+  }
+  return MKV_OK;
+}
+
 mkv_status check_batch(const mkv_pool* p, int32_t n, const int32_t* ids, bool need_nonempty) {
   if (n < 0 || (n > 0 && !ids)) return fail(MKV_ERR_INVALID_ARGUMENT, "bad batch");
   if (n > effective_batch(p->cfg)) return fail(MKV_ERR_INVALID_ARGUMENT, "batch %d > max_batch", n);
@@ -972,19 +989,9 @@ mkv_status mkv_decode_attention_multi(mkv_pool* p, int32_t layer, int32_t n, con
   if (dtype != MKV_F32 && dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
   mkv_status st = check_batch(p, n, ids, true);
   if (st != MKV_OK) return st;
-  if (nq < 1 || nq > effective_batch(p->cfg)) return fail(MKV_ERR_INVALID_ARGUMENT, "nq = %d", nq);
-  if (int64_t(n) * nq > effective_batch(p->cfg))
-    return fail(MKV_ERR_INVALID_ARGUMENT, "%d requests x %d query tokens > max_batch", n, nq);
+  if ((st = check_queries(p, n, ids, nq)) != MKV_OK) return st;
   if (n == 0) return MKV_OK;
   if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
-  const int P = p->cfg.page_size;
-  for (int i = 0; i < n; ++i) {
-    const SeqRec& sr = p->seqs[ids[i]];
-    if (sr.len < nq) return fail(MKV_ERR_INVALID_ARGUMENT, "sequence %d holds %d < nq tokens", ids[i], sr.len);
-    for (int pg = (sr.len - nq) / P; pg <= (sr.len - 1) / P; ++pg)
-      if (sr.pages[pg].tier == MKV_TIER_STALE)
-        return fail(MKV_ERR_INVALID_STATE, "sequence %d: a query token's page %d is TQ3", ids[i], pg);
-  }
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = ensure_plan(p, n, ids, nq, !p->host_only, s)) != MKV_OK) return st;
   if (p->host_only) return MKV_OK;
@@ -1147,11 +1154,13 @@ mkv_status mkv_tq3_codebook(float* levels8, float* thresholds7) {
   return MKV_OK;
 }
 
-mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* chunks, int32_t cap, int32_t* n_chunks) {
+mkv_status mkv_plan_decode_multi(mkv_pool* p, int32_t n, const int32_t* ids, int32_t nq, int32_t* chunks, int32_t cap,
+                                 int32_t* n_chunks) {
   if (!p || !n_chunks) return fail(MKV_ERR_INVALID_ARGUMENT, "NULL argument");
   mkv_status st = check_batch(p, n, ids, true);
   if (st != MKV_OK) return st;
-  if ((st = build_plan(p, n, ids, 1, false, nullptr)) != MKV_OK) return st;
+  if ((st = check_queries(p, n, ids, nq)) != MKV_OK) return st;
+  if ((st = build_plan(p, n, ids, nq, false, nullptr)) != MKV_OK) return st;
   p->plan_gen = 0;   // the device copy (if any) no longer matches
   const int nc = int(p->plan_debug.size() / kPlanRecord);
   *n_chunks = nc;
@@ -1160,6 +1169,10 @@ mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* 
     std::memcpy(chunks, p->plan_debug.data(), p->plan_debug.size() * sizeof(int32_t));
   }
   return MKV_OK;
+}
+
+mkv_status mkv_plan_decode(mkv_pool* p, int32_t n, const int32_t* ids, int32_t* chunks, int32_t cap, int32_t* n_chunks) {
+  return mkv_plan_decode_multi(p, n, ids, 1, chunks, cap, n_chunks);
 }
 
 mkv_status mkv_selftest_wait_timeout(mkv_pool* p, int64_t limit_cycles, mkv_stream_t stream) {

@@ -136,8 +136,10 @@ class MkvPool:
     def rotation_signs(self):
         return B.mkv_rotation_signs(self.handle, self.head_dim)
 
-    def plan(self, seq_ids):
-        return B.mkv_plan_decode(self.handle, seq_ids)
+    def plan(self, seq_ids, nq: int = 1):
+        if nq == 1:
+            return B.mkv_plan_decode(self.handle, seq_ids)
+        return B.mkv_plan_decode_multi(self.handle, seq_ids, nq)
 
     def check_device_errors(self, stream=None):
         B.mkv_check_device_errors(self.handle, self._stream(stream))

@@ -352,3 +352,34 @@ def test_plan_minimises_the_largest_cta(mkv):
         best = min(best, f[R])
     assert len(ctas) <= kmax
     assert best <= got <= best * (1 + 1e-4) + 1e-9, (got, best)
+
+
+def test_multi_query_plan_covers_each_prefix(mkv):
+    """mkv_plan_decode_multi: batch entry b * nq + i reads request b up to its
+    query token i, per kv head and tier exactly once."""
+    P = 64
+    layouts = [(64 * 9 + 3, [2, 3, 3, 3, 3, 1, 1, 1, 1, 1]), (64 * 4, [3, 3, 1, 1]), (5, [1])]
+    p = _host_pool(mkv, num_layers=1, fp8_slots=64, tq3_slots=64, max_seqs=16, max_batch=16, max_pages_per_seq=40)
+    for r, (n, tiers) in enumerate(layouts):
+        p.extend([r], [n])
+        for pg, t in enumerate(tiers):
+            if t == 2:
+                p.set_tier(r, pg, 2)
+        stale = [pg for pg, t in enumerate(tiers) if t == 3]
+        if stale:
+            p.demote([r] * len(stale), stale)
+    nq = 5
+    plan = p.plan([0, 1, 2], nq=nq)
+    for b, (n, tiers) in enumerate(layouts):
+        for i in range(nq):
+            visible = n - nq + 1 + i
+            tq3 = sum(min(P, visible - pg * P) for pg, t in enumerate(tiers) if t == 3 and pg * P < visible)
+            fp8 = visible - tq3
+            for kvh in range(4):
+                mine = [c for c in plan if c[0] == b * nq + i and c[1] == kvh]
+                assert sum(c[5] for c in mine if c[2] == 3) == tq3
+                assert sum(c[5] for c in mine if c[2] == 1) == fp8
+    # nq = 1 is the decode plan
+    assert p.plan([0, 1, 2], nq=1) == p.plan([0, 1, 2])
+    with pytest.raises(mkv.MkvError):
+        p.plan([0, 1, 2], nq=6)                        # request 2 holds 5 tokens
