@@ -380,23 +380,36 @@ def run_mkv(args):
     # ---------------- e2e through host buffers
     e2e = None
     if e2e_steps:
-        hq = [[torch.empty((w.n, w.Hq, w.D), dtype=w.q_dtype).pin_memory() for _ in range(L)]
-              for _ in range(e2e_steps)]
-        hk = [[torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype).pin_memory() for _ in range(L)]
-              for _ in range(e2e_steps)]
-        hv = [[torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype).pin_memory() for _ in range(L)]
-              for _ in range(e2e_steps)]
+        # Each step's inputs (q, k, v of every layer) sit in one pinned host
+        # buffer and go to the device in one copy at the start of the step;
+        # the step's result, the last layer's out and lse, comes back at its
+        # end.  Segments are 256-byte aligned so that typed views of the byte
+        # buffer are legal.
+        elt = lambda dt: torch.tensor([], dtype=dt).element_size()
+        qb = w.n * w.Hq * w.D * elt(w.q_dtype)
+        kb = w.n * w.Hkv * w.D * elt(w.kv_dtype)
+        seg = lambda nb: (nb + 255) // 256 * 256
+        layer_bytes = seg(qb) + 2 * seg(kb)
+        hbuf = [torch.empty(L * layer_bytes, dtype=torch.uint8).pin_memory() for _ in range(e2e_steps)]
         for s in range(e2e_steps):
             for layer in range(L):
                 k, v = w.step_kv(layer, 10_000 + s)
-                hk[s][layer].copy_(k)
-                hv[s][layer].copy_(v)
-                hq[s][layer].copy_(w.query(layer, 10_000 + s))
-        ho = [torch.empty((w.n, w.Hq, w.D), dtype=torch.float32).pin_memory() for _ in range(L)]
-        hl = [torch.empty((w.n, w.Hq), dtype=torch.float32).pin_memory() for _ in range(L)]
-        dq = torch.empty((w.n, w.Hq, w.D), dtype=w.q_dtype, device=dev)
-        dk = torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype, device=dev)
-        dv = torch.empty((w.n, w.Hkv, w.D), dtype=w.kv_dtype, device=dev)
+                q = w.query(layer, 10_000 + s)
+                off = layer * layer_bytes
+                for t, nb in ((q, qb), (k, kb), (v, kb)):
+                    hbuf[s][off:off + nb].copy_(t.contiguous().view(torch.uint8).reshape(-1))
+                    off += seg(nb)
+        dbuf = torch.empty(L * layer_bytes, dtype=torch.uint8, device=dev)
+        views = []
+        for layer in range(L):
+            off = layer * layer_bytes
+            dq = dbuf[off:off + qb].view(w.q_dtype).view(w.n, w.Hq, w.D)
+            dk = dbuf[off + seg(qb):off + seg(qb) + kb].view(w.kv_dtype).view(w.n, w.Hkv, w.D)
+            off2 = off + seg(qb) + seg(kb)
+            dv = dbuf[off2:off2 + kb].view(w.kv_dtype).view(w.n, w.Hkv, w.D)
+            views.append((dq, dk, dv))
+        ho = torch.empty((w.n, w.Hq, w.D), dtype=torch.float32).pin_memory()
+        hl = torch.empty((w.n, w.Hq), dtype=torch.float32).pin_memory()
         e2e_bytes = []
         barrier()
         torch.cuda.synchronize()
@@ -406,23 +419,23 @@ def run_mkv(args):
         for s in range(e2e_steps):
             stepper.pre_step()
             e2e_bytes.append(kv_bytes_now(pool, P, L)[0])
+            dbuf.copy_(hbuf[s], non_blocking=True)
             for layer in range(L):
-                dq.copy_(hq[s][layer], non_blocking=True)
-                dk.copy_(hk[s][layer], non_blocking=True)
-                dv.copy_(hv[s][layer], non_blocking=True)
+                dq, dk, dv = views[layer]
                 o, l_ = stepper.layer(layer, dk, dv, dq, *outs[layer])
-                ho[layer].copy_(o, non_blocking=True)
-                hl[layer].copy_(l_, non_blocking=True)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(l_, non_blocking=True)
         f1.record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
         e2e_ms, e2e_job = job_totals(max(f0.elapsed_time(f1), wall * 1e3), sum(e2e_bytes), world, dev)
-        elt = lambda dt: torch.tensor([], dtype=dt).element_size()
-        h2d = L * w.n * (w.Hq * w.D * elt(w.q_dtype) + 2 * w.Hkv * w.D * elt(w.kv_dtype))
-        d2h = L * w.n * (w.Hq * w.D * 4 + w.Hq * 4)
+        h2d = L * (qb + 2 * kb)
+        d2h = w.n * (w.Hq * w.D * 4 + w.Hq * 4)
         e2e = {"value": e2e_job / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,
+               "copies_per_step": "one host-to-device copy of every layer's q, k, v; the last layer's out "
+                                  "and lse back"}
     # ---------------- CPU oracle baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
