@@ -321,6 +321,20 @@ mkv_status mkv_check_device_errors(mkv_pool* pool, mkv_stream_t stream);
  * Errors: INVALID_ARGUMENT (limit), UNSUPPORTED on a host-only pool. */
 mkv_status mkv_selftest_wait_timeout(mkv_pool* pool, int64_t limit_cycles, mkv_stream_t stream);
 
+/* Fault injection for tests (not from the pages): overwrite the physical slot
+ * of page entry `entry` of the device copy of the current decode plan, the
+ * one the last decode call planned, with `slot`.  The next decode call with
+ * the same batch reuses that plan (mkv_append_decode, which writes through
+ * the plan's slots, always plans again).  The decode kernel checks every slot
+ * before it copies a block: a slot outside the arena skips the copy, stops
+ * the CTA's remaining work and sets the error word, so the call's outputs
+ * are undefined and the next mkv_check_device_errors reports
+ * MKV_ERR_DEVICE_CHECK.  Nothing faults.  Any later change to the pool, or
+ * another batch, plans again from the host tables.  Synchronises `stream`.
+ * Errors: INVALID_ARGUMENT (entry), INVALID_STATE (no current plan),
+ * UNSUPPORTED on a host-only pool. */
+mkv_status mkv_inject_plan_slot(mkv_pool* pool, int32_t entry, int32_t slot, mkv_stream_t stream);
+
 /* Instrumentation: when `start` / `stop` (cudaEvent_t handles owned by the
  * caller) are non-NULL, the next mkv_decode_attention call records `start`
  * right before its partial-attention kernel and `stop` right after it, on the

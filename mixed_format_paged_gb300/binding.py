@@ -28,7 +28,7 @@ EXPORTED = [
     "mkv_pool_required_bytes", "mkv_pool_create", "mkv_pool_destroy", "mkv_seq_extend", "mkv_seq_release",
     "mkv_seq_info", "mkv_page_info", "mkv_append_tokens", "mkv_set_tier", "mkv_demote_pages",
     "mkv_decode_attention", "mkv_decode_attention_multi", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
-    "mkv_plan_decode", "mkv_plan_decode_multi", "mkv_check_device_errors", "mkv_selftest_wait_timeout", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
+    "mkv_plan_decode", "mkv_plan_decode_multi", "mkv_check_device_errors", "mkv_selftest_wait_timeout", "mkv_inject_plan_slot", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
 ]
 
 
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
         "mkv_plan_decode_multi": [P, I32, I32P, I32, I32P, I32, I32P],
         "mkv_check_device_errors": [P, P],
         "mkv_selftest_wait_timeout": [P, ctypes.c_int64, P],
+        "mkv_inject_plan_slot": [P, I32, I32, P],
         "mkv_set_timing_events": [P, P, P],
         "mkv_last_error": [],
         "mkv_version": [],
@@ -291,6 +292,10 @@ def mkv_check_device_errors(pool, stream=None) -> None:
 
 def mkv_selftest_wait_timeout(pool, limit_cycles: int, stream=None) -> None:
     check(lib().mkv_selftest_wait_timeout(pool, limit_cycles, _stream(stream)), "mkv_selftest_wait_timeout")
+
+
+def mkv_inject_plan_slot(pool, entry: int, slot: int, stream=None) -> None:
+    check(lib().mkv_inject_plan_slot(pool, entry, slot, _stream(stream)), "mkv_inject_plan_slot")
 
 
 def mkv_set_timing_events(pool, start_event, stop_event) -> None:

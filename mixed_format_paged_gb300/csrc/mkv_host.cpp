@@ -17,6 +17,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <cstddef>
 #include <functional>
 #include <new>
 #include <queue>
@@ -202,6 +203,8 @@ struct mkv_pool {
   DecodeParams plan_params{};
   MergeParams merge_params{};
   int plan_parts = 0;
+  int plan_entries = 0;             // page entries of the last plan built
+  bool plan_injected = false;       // the device plan holds an injected entry (mkv_inject_plan_slot)
   std::vector<int32_t> plan_debug;   // kPlanRecord ints per chunk
   // one-shot timing events around the next decode kernel
   cudaEvent_t t_start = nullptr, t_stop = nullptr;
@@ -534,6 +537,8 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
       p->plan_debug.insert(p->plan_debug.end(), rec, rec + kPlanRecord);
     }
   p->plan_parts = int(segs.size());
+  p->plan_entries = int(entries.size());
+  p->plan_injected = false;
   // params
   DecodeParams& dp = p->plan_params;
   dp = DecodeParams{};
@@ -1043,6 +1048,7 @@ mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_
   }
   if (p->host_only) return MKV_OK;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->plan_injected) p->plan_gen = 0;   // the fused append writes through the plan's slots: replan
   if ((st = ensure_plan(p, n, ids, 1, true, s)) != MKV_OK) return st;
   return enqueue_decode(p, layer, q, q_dtype, p->workspace, k, v, kv_dtype, out, lse, s);
 }
@@ -1182,6 +1188,23 @@ mkv_status mkv_selftest_wait_timeout(mkv_pool* p, int64_t limit_cycles, mkv_stre
   if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no device error word");
   const cudaError_t e = launch_wait_probe(p->err, limit_cycles, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+  return MKV_OK;
+}
+
+mkv_status mkv_inject_plan_slot(mkv_pool* p, int32_t entry, int32_t slot, mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no device plan");
+  if (p->plan_gen != p->generation || p->plan_gen == 0)
+    return fail(MKV_ERR_INVALID_STATE, "no current device plan (decode a batch first)");
+  if (entry < 0 || entry >= p->plan_entries)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "entry %d outside the plan's %d", entry, p->plan_entries);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const PlanLayout L = plan_layout(p->entry_cap, p->chunk_cap, effective_batch(p->cfg), p->cfg.num_kv_heads);
+  uint8_t* dst = p->plan_region + L.entries + size_t(entry) * sizeof(PageEntry) + offsetof(PageEntry, slot);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(dst, &slot, sizeof slot, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "plan entry write");
+  p->plan_injected = true;
   return MKV_OK;
 }
 

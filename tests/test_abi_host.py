@@ -383,3 +383,10 @@ def test_multi_query_plan_covers_each_prefix(mkv):
     assert p.plan([0, 1, 2], nq=1) == p.plan([0, 1, 2])
     with pytest.raises(mkv.MkvError):
         p.plan([0, 1, 2], nq=6)                        # request 2 holds 5 tokens
+
+
+def test_inject_plan_slot_needs_a_device_plan(mkv):
+    p = _host_pool(mkv)
+    with pytest.raises(mkv.MkvError) as e:
+        mkv.binding.mkv_inject_plan_slot(p.handle, 0, 5)
+    assert e.value.status == 2                         # host-only pool

@@ -463,3 +463,34 @@ def test_wait_timeout_is_reported_and_context_stays_usable(mkv):
     torch.cuda.synchronize()
     pool.check_device_errors()
     _check_decode(pool, 0, [0], q.float(), out, lse, 4321)
+
+
+def test_corrupt_plan_entry_is_caught(mkv):
+    """A page entry injected with a slot outside the arena (host-side fault
+    injection) is caught by the decode kernel's slot check: no copy, an error
+    word, MKV_ERR_DEVICE_CHECK on the next check, no fault.  A replanned
+    decode is right again."""
+    from mixed_format_paged_gb300 import binding as B
+    g = torch.Generator().manual_seed(31)
+    pool = _small_pool(mkv)
+    n = 5 * 64 + 9
+    K, V = _kv(n, torch.bfloat16, g)
+    pool.extend([0], [n])
+    pool.append(0, [0], [n], K.to(DEV), V.to(DEV))
+    pool.demote([0], [1, 2])
+    q = torch.randn(1, 24, 256, generator=g).to(torch.bfloat16)
+    for entry, slot in ((0, 1 << 20), (4, -7)):       # an FP8 entry, then a TQ3 entry
+        pool.decode(0, [0], q.to(DEV))                 # plans and uploads
+        torch.cuda.synchronize()
+        pool.check_device_errors()
+        B.mkv_inject_plan_slot(pool.handle, entry, slot)
+        pool.decode(0, [0], q.to(DEV))                 # same batch: the injected plan
+        torch.cuda.synchronize()
+        with pytest.raises(mkv.MkvError) as e:
+            pool.check_device_errors()
+        assert e.value.status == 6
+        pool.plan([0])                                 # drops the device plan: the next decode replans
+    out, lse = pool.decode(0, [0], q.to(DEV))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    _check_decode(pool, 0, [0], q.float(), out, lse, 4321)
