@@ -18,8 +18,13 @@
  * Calls: mkv_pool_create (page pool + page table + tier tags),
  * mkv_append_tokens (FP8 quantise into the tail page), mkv_demote_pages
  * (FP8 -> TQ3 repack), mkv_decode_attention (FP8 partials + TQ3 partials +
- * LSE merge).  Every step runs in this library's CUDA kernels; there is no
- * CPU or dense fallback.
+ * LSE merge).  Beyond the pages: mkv_append_decode (append fused into the
+ * decode kernel), mkv_decode_attention_multi (several causal query tokens
+ * per request), mkv_decode_attention_noalloc, mkv_dequantize_pages (dense
+ * export), plan inspection, and failure-detection hooks
+ * (mkv_check_device_errors, mkv_selftest_wait_timeout, mkv_inject_plan_slot).
+ * Every step runs in this library's CUDA kernels; there is no CPU or dense
+ * fallback.
  *
  * ============================================================ Storage formats
  * The pages name FP8 and TQ3 but define neither; this section is the
