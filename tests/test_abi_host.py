@@ -390,3 +390,13 @@ def test_inject_plan_slot_needs_a_device_plan(mkv):
     with pytest.raises(mkv.MkvError) as e:
         mkv.binding.mkv_inject_plan_slot(p.handle, 0, 5)
     assert e.value.status == 2                         # host-only pool
+
+
+def test_missing_library_fails_loudly(mkv, monkeypatch):
+    """No CPU or dense fallback: without libmkv.so every call raises."""
+    monkeypatch.setattr(mkv.binding, "_lib", None)
+    monkeypatch.setattr(mkv.binding, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libmkv.so"))
+    with pytest.raises(ImportError):
+        mkv.binding.lib()
+    with pytest.raises(ImportError):
+        _host_pool(mkv)
