@@ -406,15 +406,21 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     int group, index, tokens;
   };
   std::vector<Blk> blocks;
-  for (int gi = 0; gi < int(groups.size()); ++gi) {
+  {
+    size_t total = 0;
+    for (const Group& g : groups) total += size_t(g.nentry) * (P / (g.fmt ? kTq3Blk : kFp8Blk));
+    blocks.reserve(total);
+  }
+  for (int gi = 0; gi < int(groups.size()); ++gi) {     // page by page: no division per block
     const Group& g = groups[gi];
     const int bt = g.fmt ? kTq3Blk : kFp8Blk;
     const int bpp = P / bt;
     const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
     const int nblk = (g.nentry - 1) * bpp + (last_nv + bt - 1) / bt;
-    for (int k = 0; k < nblk; ++k) {
-      const int nv = entries[g.entry0 + k / bpp].nvalid - (k % bpp) * bt;
-      blocks.push_back({gi, k, std::max(0, std::min(bt, nv))});
+    int k = 0;
+    for (int pg = 0; pg < g.nentry && k < nblk; ++pg) {
+      const int nv_page = entries[g.entry0 + pg].nvalid;
+      for (int j = 0; j < bpp && k < nblk; ++j, ++k) blocks.push_back({gi, k, std::max(0, std::min(bt, nv_page - j * bt))});
     }
   }
   auto cost = [&](const Blk& b) {
