@@ -358,10 +358,14 @@ mkv_status mkv_set_timing_events(mkv_pool* pool, void* start, void* stop);
  * or other allocating routine.
  * Limit: splits x G x (2 + d) x 4 bytes of partial states must fit in 8 MiB
  * (1,354 splits at G = 6, d = 256); larger batches return MKV_ERR_CAPACITY
- * and change nothing.
- * Set-up: the first call on each device looks the array's device address up
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array, which keeps the
+ * and launch nothing.  The size is known only once the batch is planned, so
+ * a refused call leaves the pool's plan for these ids built and its upload
+ * enqueued on the stream, as a mkv_decode_attention call would.
+ * Device: the call must be made with the pool's device current (else
+ * MKV_ERR_INVALID_ARGUMENT).  Every call looks the array's address up for
+ * that device (cudaGetSymbolAddress; the first lookup in a process may load
+ * the library's device code, so make the first call before any stream
+ * capture).  All calls share the one array, which keeps the
  * last call's contents; nothing in it needs to start at zero (every partial
  * state is written in full before it is read).  Calls whose GPU work
  * overlaps -- on different streams, or from different pools -- race on the

@@ -1021,11 +1021,17 @@ mkv_status mkv_decode_attention_noalloc(mkv_pool* p, int32_t layer, int32_t n, c
   if (n == 0) return MKV_OK;
   if (!q || !out || !lse) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse is NULL");
   if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no device scratch");
+  // the scratch address is per device: it must be the pool's
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != p->device)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "current device %d is not the pool's device %d", cur, p->device);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = ensure_plan(p, n, ids, 1, true, s)) != MKV_OK) return st;
   float* scratch = nullptr;
   size_t scratch_bytes = 0;
-  cudaError_t e = noalloc_scratch(&scratch, &scratch_bytes);
+  e = noalloc_scratch(&scratch, &scratch_bytes);
   if (e != cudaSuccess) return cuda_fail(e, "device scratch address (cudaGetSymbolAddress)");
   // scratch = the partial states
   const size_t need = size_t(p->plan_parts) * p->G * (2 + kHeadDim) * sizeof(float);

@@ -152,8 +152,8 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s);
 size_t decode_smem_bytes();
 // Device address and size of the library's fixed partial-state scratch (see
-// mkv_decode_attention_noalloc).  The first call on a device looks the address
-// up with that device current; later calls return the cached value.
+// mkv_decode_attention_noalloc), looked up for the current device on every
+// call.
 cudaError_t noalloc_scratch(float** ptr, size_t* bytes);
 int decode_threads();
 

@@ -21,7 +21,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
-#include <mutex>
+#include <atomic>
 
 namespace mkv {
 namespace {
@@ -1314,23 +1314,13 @@ constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchBytes / sizeof(float)];
 
 cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static float* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // looked up on every call (cheap, and not a stream operation): a cached
+  // address would dangle after the device's context is reset and rebuilt.
+  // Host code must not use the symbol itself as a device address.
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    // host code must not use the symbol itself as a device address: ask the
-    // runtime for this device's copy (the current device is `dev`)
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<float*>(p);
-  }
-  *ptr = addr[dev];
+  *ptr = static_cast<float*>(p);
   *bytes = kNoallocScratchBytes;
   return cudaSuccess;
 }
@@ -1343,12 +1333,17 @@ cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
+  // the shared-memory limit is a per-device attribute: set it once per device
+  // (setting it twice from racing threads is harmless)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.fetch_or(bit, std::memory_order_acq_rel);
   }
   if (p.n_ctas <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};

@@ -74,11 +74,21 @@ def boundary_distance(u: np.ndarray) -> np.ndarray:
 
 
 def fp16_tie_distance(v: np.ndarray) -> np.ndarray:
-    """Relative distance of a real value to the nearest fp16 rounding boundary
-    (midpoint between adjacent fp16 values).  Used for the scale exemption."""
+    """Relative distance |v - m| / |v| of a real value to the nearest fp16
+    rounding boundary m (a midpoint between adjacent fp16 values).  Used for
+    the scale exemption.
+
+    The two candidate boundaries are the midpoints on either side of the
+    largest fp16 value at or below |v|: the one above it and the one below
+    it (the latter lies in the binade below when that value is a power of
+    two, where the spacing halves)."""
     v = np.abs(np.asarray(v, dtype=np.float64))
-    _, E = np.frexp(v)
-    e = np.maximum(E - 1, -14)
-    q = np.ldexp(1.0, e - 10)
-    frac = v / q - np.floor(v / q)
-    return np.abs(frac - 0.5) * q / np.maximum(v, 1e-300)
+    lo = v.astype(np.float16)
+    lo = np.where(lo.astype(np.float64) > v, np.nextafter(lo, np.float16(0)), lo)   # largest fp16 <= v
+    up = np.nextafter(lo, np.float16(np.inf)).astype(np.float64)
+    down = np.nextafter(lo, np.float16(0)).astype(np.float64)
+    lo64 = lo.astype(np.float64)
+    mid_up = (lo64 + up) / 2.0
+    mid_down = np.where(lo64 > 0.0, (lo64 + down) / 2.0, np.inf)
+    dist = np.minimum(np.abs(v - mid_up), np.abs(v - mid_down))
+    return dist / np.maximum(v, 1e-300)

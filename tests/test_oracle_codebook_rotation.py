@@ -124,3 +124,14 @@ def test_rotation_properties():
     assert np.allclose(unrotate(y, seed), x, atol=1e-13)
     # R^T = D H / sqrt(d)
     assert np.allclose(unrotate(x, seed), rotation_signs(seed, 256) * _fwht(x) / 16.0, atol=1e-13)
+
+
+def test_signs_literal_prefix():
+    # sign_i = -1 iff bit (i mod 64) of SplitMix64 output floor(i/64) is set.
+    # The published first output for seed 1234567 is 6457827717110365317 =
+    # 0x599ED017FB08FC85; its low 16 bits 0xFC85 = 1111 1100 1000 0101 (bit 15
+    # .. bit 0) give the first 16 signs.  The second output 3203168211198807973
+    # = 0x2C73F08458540FA5 has low byte 0xA5 = 1010 0101: signs 64..71.
+    s = rotation_signs(1234567, 256)
+    assert list(s[:16]) == [-1, 1, -1, 1, 1, 1, 1, -1, 1, 1, -1, -1, -1, -1, -1, -1]
+    assert list(s[64:72]) == [-1, 1, -1, 1, 1, -1, 1, -1]
