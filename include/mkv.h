@@ -52,24 +52,18 @@
  * quantiser of N(0,1) (fp64 fixed point); tau_k = (L_{k-1} + L_k) / 2
  * (exact).  mkv_tq3_codebook() returns the values.
  *
- * Page layout: one (layer, slot) page holds P tokens (P = 64 or 128).  For
- * kv head h = 0..H_kv-1 in order: a K plane, then a V plane.  A plane is the
- * code bytes followed by P little-endian fp16 scales in token order.
+ * Page layout: one (layer, slot) page holds P tokens.  For kv head
+ * h = 0..H_kv-1 in order: a K plane, then a V plane.  A plane is the code
+ * bytes followed by P little-endian fp16 scales in token order.
  *   FP8 plane codes (P*d bytes):
- *     K: byte (t/64)*64d + (j/16)*1024 + (t%64)*16 + j%16
- *        (64-token blocks, each d/16 columns of 16 bytes: a token's 16
- *        consecutive dims are 16 contiguous bytes, the block's tokens follow
- *        one another within a column)
- *     V: byte (t/8)*8d + 8j + t%8
- *        (8-token groups: the 8 tokens of one dim are 8 contiguous bytes)
- *   TQ3 plane codes (P*3d/8 bytes; 3 bits per code, 32 codes per 12 bytes):
- *   12-byte units of 32 codes = three little-endian 32-bit words W0, W1, W2:
+ *     K: byte t*d + j                      (row-major)
+ *     V: byte (t/2)*2d + 2j + (t%2)        (rows of a token pair interleaved)
+ *   TQ3 plane codes (P*3d/8 bytes, 8 codes per 3 bytes): 12-byte units of
+ *   32 codes = three little-endian 32-bit words W0, W1, W2:
  *     bits [4i, 4i+3) of W_k = code (8k + i)           i = 0..7, k = 0..2
  *     bit  4i+3       of W_k = bit k of code (24 + i)
- *     K: unit t*(d/32) + j/32, code j%32        (token-major)
- *     V: unit j*(P/32) + t/32, code t%32        (dimension-major)
- * The orders serve the decode kernel: a K row feeds one row of the QK^T
- * operand, a V dimension one row of the V^T operand of P V.
+ *     K: unit t*(d/32) + j/32, code j%32
+ *     V: unit (t/2)*(d/16) + j/16, code 2*(j%16) + (t%2)
  * Sizes per page, d = 256, 4 kv heads: FP8 P*2064 B (132,096 at P = 64),
  * TQ3 P*784 B (50,176 at P = 64); slot s of layer l is at
  * arena + (l * slots + s) * page_bytes.

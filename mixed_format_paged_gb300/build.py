@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libmkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
           "-I", CSRC]
-SOURCES = ["mkv_host.cpp", "mkv_kernels.cu", "mkv_decode.cu", "mkv_selftest.cu"]
+SOURCES = ["mkv_host.cpp", "mkv_kernels.cu", "mkv_selftest.cu"]
 
 
 def _nvcc() -> str:

@@ -331,18 +331,20 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 
 // ------------------------------------------------------------------ planner
 // Relative cost of one token of one kv head, per format, plus a fixed cost per
-// tile and per piece, in units of one TQ3 token.  A TQ3 tile is 128 tokens,
-// an FP8 tile 64; a piece's end-of-piece merge costs about 3 us of CTA time.
+// block and per piece, in units of one TQ3 token.  Fitted to per-CTA times of
+// the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.31 us of CTA
+// time, a 16-token FP8 block ~0.25 us, a piece ~4 us (its end-of-piece merge
+// and the warps' drift before it).
 constexpr double kCostTq3Token = 1.0;
 constexpr double kCostFp8Token = 1.45;
-constexpr double kCostTile = 24.0;
+constexpr double kCostBlock = 8.0;
 constexpr double kCostPiece = 540.0;
-constexpr double kShortRoundBase = 0.5;  // a round with one busy WG costs 0.5 + 0.5/3 of a full one
-constexpr int kMinTilesPerCta = 6;       // two tiles per warpgroup at least
+constexpr double kShortRoundBase = 0.4;  // a round with one busy warp costs 0.4 + 0.6/12 of a full one
+constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
 constexpr int kPlanRecord = 9;           // ints per split in mkv_plan_decode's output
 
 // Split the batch's pages into groups (request, kv head, format), lay the
-// groups' tiles out in one sequence, and cut that sequence into one
+// groups' blocks out in one sequence, and cut that sequence into one
 // contiguous piece list per CTA so that the largest CTA's estimated cost is
 // as small as the cut points allow.  Each (CTA, group) piece
 // writes one partial state; a group's partial states are contiguous, which is
@@ -396,61 +398,57 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
         for (int i = 0; i < count; ++i) g.tokens += entries[first + i].nvalid;
         groups.push_back(g);
       }
-  // Tiles: a TQ3 tile is 128 tokens (ppt = 128 / P full pages, the last tile
-  // of a group possibly one page short); an FP8 tile is 64 tokens of one page
-  // (tpp = P / 64 per page), numbered page by page up to the last valid token
-  // (only a group's last page can be partial).
-  struct Tile {
+  // Blocks: an FP8 block is kFp8Blk tokens and a TQ3 block kTq3Blk tokens
+  // of one page; a group's blocks are numbered page by page, bpp = P / bt per
+  // page, up to the last valid token (a block past a page's valid tokens is
+  // empty and only costs its overhead).
+  struct Blk {
     int group, index, tokens;
   };
-  std::vector<Tile> tiles;
+  std::vector<Blk> blocks;
   {
     size_t total = 0;
-    for (const Group& g : groups) total += size_t(g.nentry) * (g.fmt ? 1 : P / kFp8Tile);
-    tiles.reserve(total);
+    for (const Group& g : groups) total += size_t(g.nentry) * (P / (g.fmt ? kTq3Blk : kFp8Blk));
+    blocks.reserve(total);
   }
-  const int ppt = kTq3Tile / P, tpp = P / kFp8Tile;
-  for (int gi = 0; gi < int(groups.size()); ++gi) {
+  for (int gi = 0; gi < int(groups.size()); ++gi) {     // page by page: no division per block
     const Group& g = groups[gi];
-    if (g.fmt) {
-      for (int k = 0; k * ppt < g.nentry; ++k) tiles.push_back({gi, k, std::min(ppt, g.nentry - k * ppt) * P});
-    } else {
-      int k = 0;
-      for (int pg = 0; pg < g.nentry; ++pg) {
-        const int nv_page = entries[g.entry0 + pg].nvalid;
-        for (int j = 0; j < tpp && j * kFp8Tile < nv_page; ++j, ++k)
-          tiles.push_back({gi, k, std::min(kFp8Tile, nv_page - j * kFp8Tile)});
-        if (pg + 1 < g.nentry) k = (pg + 1) * tpp;       // pages before the last are full
-      }
+    const int bt = g.fmt ? kTq3Blk : kFp8Blk;
+    const int bpp = P / bt;
+    const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
+    const int nblk = (g.nentry - 1) * bpp + (last_nv + bt - 1) / bt;
+    int k = 0;
+    for (int pg = 0; pg < g.nentry && k < nblk; ++pg) {
+      const int nv_page = entries[g.entry0 + pg].nvalid;
+      for (int j = 0; j < bpp && k < nblk; ++j, ++k) blocks.push_back({gi, k, std::max(0, std::min(bt, nv_page - j * bt))});
     }
   }
-  auto cost = [&](const Tile& t) {
-    return t.tokens * (groups[t.group].fmt ? kCostTq3Token : kCostFp8Token) + kCostTile;
+  auto cost = [&](const Blk& b) {
+    return b.tokens * (groups[b.group].fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
   };
-  // Rounds: runs of up to kDecWGs consecutive tiles of one group, from the
-  // group's first tile on.  A CTA's warpgroups take one round together, so a
-  // cut inside a group falls only between rounds and every warpgroup of a
-  // piece gets the same number of tiles (one fewer for some in a group's last
-  // round).  A round costs its slowest tile on every warpgroup; a short
-  // round, with warpgroups idle, runs its tiles faster and is priced between
-  // the two.
+  // Rounds: runs of up to kDecWarps consecutive blocks of one group, from the
+  // group's first block on.  A CTA's warps take one round together, so a cut
+  // inside a group falls only between rounds and every warp of a piece gets
+  // the same number of blocks (one fewer for some in a group's last round).
+  // A round costs its slowest block on every warp; a short round, with warps
+  // idle, runs its blocks faster and is priced between the two.
   struct Round {
-    int group, first, ntile;
+    int group, first, nblk;
     double cost;
   };
   std::vector<Round> rounds;
-  for (size_t i = 0; i < tiles.size();) {
-    const int g = tiles[i].group;
+  for (size_t i = 0; i < blocks.size();) {
+    const int g = blocks[i].group;
     size_t j = i;
     double worst = 0.0;
-    while (j < tiles.size() && tiles[j].group == g && int(j - i) < kDecWGs) worst = std::max(worst, cost(tiles[j++]));
-    const double busy = double(j - i) / kDecWGs;
-    rounds.push_back({g, int(i), int(j - i), worst * kDecWGs * (kShortRoundBase + (1.0 - kShortRoundBase) * busy)});
+    while (j < blocks.size() && blocks[j].group == g && int(j - i) < kDecWarps) worst = std::max(worst, cost(blocks[j++]));
+    const double busy = double(j - i) / kDecWarps;
+    rounds.push_back({g, int(i), int(j - i), worst * kDecWarps * (kShortRoundBase + (1.0 - kShortRoundBase) * busy)});
     i = j;
   }
-  // one CTA per SM at most, each with at least kMinTilesPerCta tiles
+  // one CTA per SM at most, each with at least kMinBlocksPerCta blocks
   const int max_cta = int(std::max<int64_t>(
-      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), int64_t(tiles.size()) / kMinTilesPerCta})));
+      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), int64_t(blocks.size()) / kMinBlocksPerCta})));
   // Contiguous split of the rounds into at most max_cta CTAs that minimises
   // the largest CTA cost, a piece costing kCostPiece on top of its rounds (its
   // end-of-piece merge): the greedy fill below needs the fewest CTAs for a
@@ -487,7 +485,7 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   const int ncta = rounds.empty() ? 0 : fill(lo, &starts);
   starts.push_back(int(rounds.size()));
   std::vector<Segment> segs;
-  std::vector<int32_t> seg_tokens;   // valid tokens of each piece
+  std::vector<int32_t> seg_entry, seg_tokens;   // first page entry and valid tokens of each piece
   std::vector<int32_t> cta_seg(ncta + 1, 0);
   for (int c = 0; c < ncta; ++c) {
     cta_seg[c] = int(segs.size());
@@ -495,19 +493,20 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
       const Round& rd = rounds[r];
       if (r == starts[c] || rd.group != rounds[r - 1].group) {
         const Group& g = groups[rd.group];
+        const int blk = blocks[rd.first].index;
         Segment sg{};
         sg.fmt = g.fmt;
         sg.b = g.b;
         sg.kvh = g.kvh;
         sg.entry0 = g.entry0;
-        sg.nentry = g.nentry;
         sg.group = rd.group;
-        sg.tile = tiles[rd.first].index;
+        sg.blk = blk;
         segs.push_back(sg);
+        seg_entry.push_back(g.entry0 + blk / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
         seg_tokens.push_back(0);
       }
-      segs.back().ntile += rd.ntile;
-      for (int k = rd.first; k < rd.first + rd.ntile; ++k) seg_tokens.back() += tiles[k].tokens;
+      segs.back().nblk += rd.nblk;
+      for (int k = rd.first; k < rd.first + rd.nblk; ++k) seg_tokens.back() += blocks[k].tokens;
     }
   }
   cta_seg[ncta] = int(segs.size());
@@ -537,16 +536,10 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     for (int i = cta_seg[c]; i < cta_seg[c + 1]; ++i) {
       const Segment& sg = segs[i];
       const Group& g = groups[sg.group];
-      int first, last;
-      if (g.fmt) {
-        first = g.entry0 + sg.tile * ppt;
-        last = std::min(g.entry0 + (sg.tile + sg.ntile) * ppt, g.entry0 + g.nentry) - 1;
-      } else {
-        first = g.entry0 + sg.tile / tpp;
-        last = g.entry0 + (sg.tile + sg.ntile - 1) / tpp;
-      }
-      const int32_t rec[kPlanRecord] = {g.b, g.kvh, g.fmt ? 3 : 1, first, last - first + 1,
-                                        seg_tokens[i], c, sg.tile, sg.ntile};
+      const int bpp = P / (g.fmt ? kTq3Blk : kFp8Blk);
+      const int last = g.entry0 + (sg.blk + sg.nblk - 1) / bpp;
+      const int32_t rec[kPlanRecord] = {g.b, g.kvh, g.fmt ? 3 : 1, seg_entry[i], last - seg_entry[i] + 1,
+                                        seg_tokens[i], c, sg.blk, sg.nblk};
       p->plan_debug.insert(p->plan_debug.end(), rec, rec + kPlanRecord);
     }
   p->plan_parts = int(segs.size());

@@ -10,11 +10,13 @@
 namespace mkv {
 
 constexpr int kHeadDim = 256;      // head_dim the kernels are written for
-constexpr int kMaxGroup = 8;       // q heads per kv head (one MMA N tile holds their hi and lo rows)
-constexpr int kDecWGs = 3;         // warpgroups of a decode CTA (a piece's tiles go round-robin)
-constexpr int kFp8Tile = 64;       // tokens per FP8 decode tile (one 64-token block of a page)
-constexpr int kTq3Tile = 128;      // tokens per TQ3 decode tile (two 64-token pages or one 128-token page)
+constexpr int kMaxGroup = 8;       // q heads per kv head held in one MMA tile
+constexpr int kDecWarps = 12;     // warps of a decode CTA (a piece's blocks go round-robin)
+constexpr int kFp8Blk = 16;        // tokens per FP8 decode block (one MMA tile)
+constexpr int kTq3Blk = 32;        // tokens per TQ3 decode block (two MMA tiles)
+constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
 constexpr int kMaxCtas = 160;      // upper bound on decode CTAs (their plan heads travel as kernel parameters)
+constexpr int kQfragWords = 2048;  // A-fragment words of one piece's q rows (16 x 256 fp16)
 
 // Error bits written by kernels into the pool's device error word.
 enum : int {
@@ -45,14 +47,10 @@ struct Segment {           // one CTA's piece of one group: all the decode kerne
   int32_t b;               // batch index
   int32_t kvh;             // kv head
   int32_t entry0;          // the group's first PageEntry
-  int32_t nentry;          // the group's page entries
-  int32_t tile;            // first tile of the piece, counted within the group:
-                           //   TQ3: tile k = entries entry0 + k*(128/P) .. (two 64-token
-                           //        pages, the second absent at the group's end, or
-                           //        one 128-token page);
-                           //   FP8: tile k = tokens [64 (k % (P/64)), +64) of entry
-                           //        entry0 + k / (P/64)
-  int32_t ntile;           // tiles in the piece
+  int32_t blk;             // first block of the piece, counted within the group:
+                           // block k covers tokens [bt (k % bpp), +bt) of page
+                           // entry0 + k / bpp (bt = kFp8Blk or kTq3Blk, bpp = P / bt)
+  int32_t nblk;            // blocks in the piece
   int32_t part;            // partial-state index the piece writes
   int32_t group;           // the group (host bookkeeping)
 };

@@ -1,5 +1,4 @@
-// CUDA kernels (sm_103a) of the mixed-format paged decode-attention library,
-// other than the decode kernel itself (mkv_decode.cu).
+// CUDA kernels (sm_103a) of the mixed-format paged decode-attention library.
 //
 // Method: "Minima-KV: Retention-Preserving KV Cache Compression with
 // Mixed-Format Paged Attention" (arXiv 2608.23834), abstract on the
@@ -12,17 +11,183 @@
 //   mkv_append_kernel  -- FP8 quantise new K/V rows into their pages
 //   mkv_demote_kernel  -- FP8 page -> TQ3 page (dequantise, rotate, RMS scale,
 //                         Lloyd-Max codes, pack)
-//   mkv_dequant_kernel -- dense export of pages (FP8 or TQ3, rotated back)
+//   mkv_decode_kernel  -- persistent partial-attention kernel over both
+//                         formats: 12 independent warps per CTA, each with its
+//                         own ring of bulk-copied page blocks
 //   mkv_merge_kernel   -- LSE merge: TQ3 partials in the rotated domain,
 //                         one R^T, then FP8 partials; writes out and lse
-#include "mkv_device.cuh"
+#include "mkv_internal.h"
+
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
 
 namespace mkv {
 namespace {
 
-using namespace dev;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr long long kWaitCycles = 4000000000LL;   // ~2 s at 2 GHz: bound on any wait
+constexpr float kLazyRescale = 8.0f;               // log2 units a max may grow before O is rescaled
+constexpr float kFp8PScale = 512.0f;               // keeps p * s in fp16 normal range for FP8 V
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// The same copy with an L2 cache policy (createpolicy): KV page data is read
+// once per launch and should not push the small, reused data (plan tables, q,
+// partial states) out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// two E4M3 codes (low byte -> low half) to an f16x2 register; exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ bool sign_neg(const uint64_t (&signs)[4], int i) {
+  // select the word instead of indexing the parameter array (keeps it out of local memory)
+  const int w = i >> 6;
+  const uint64_t word = w == 0 ? signs[0] : w == 1 ? signs[1] : w == 2 ? signs[2] : signs[3];
+  return (word >> (i & 63)) & 1ull;
+}
+
+// TQ3: four 3-bit codes held as nibbles in sel[15:0] -> two f16x2 registers
+// (codes 0,1) and (codes 2,3).  PRMT looks the low and the high byte of each
+// level up in 8-byte tables, then interleaves them.
+__device__ __forceinline__ void tq3_lookup4(uint32_t sel, const Lut& t, uint32_t& h01, uint32_t& h23) {
+  const uint32_t lo = __byte_perm(t.lo_a, t.lo_b, sel);
+  const uint32_t hi = __byte_perm(t.hi_a, t.hi_b, sel);
+  h01 = __byte_perm(lo, hi, 0x5140);
+  h23 = __byte_perm(lo, hi, 0x7362);
+}
+// One 12-byte unit (32 codes) -> eight nibble selectors (4 codes each):
+// codes 8k+i sit in nibbles of word k already (mask off bit 3); codes 24+i
+// gather bit 3 of nibble i of the three words.  PRMT reads selector bits
+// [15:0] only, so the upper four codes of a word take a 16-bit right shift.
+__device__ __forceinline__ void tq3_unit_selectors(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&s)[8]) {
+  const uint32_t m0 = w0 & 0x77777777u, m1 = w1 & 0x77777777u, m2 = w2 & 0x77777777u;
+  const uint32_t e = ((w0 >> 3) & 0x11111111u) | ((w1 >> 2) & 0x22222222u) | ((w2 >> 1) & 0x44444444u);
+  s[0] = m0; s[1] = m0 >> 16; s[2] = m1; s[3] = m1 >> 16;
+  s[4] = m2; s[5] = m2 >> 16; s[6] = e;  s[7] = e >> 16;
+}
 
 // ============================================================== append
+// FP8-quantise one row (one token, kv head, K|V) held by the calling warp:
+// s = fp16(amax / 448), codes = e4m3_rn_satfinite(x / s) with IEEE fp32
+// divisions.  Lane l gets the codes of dims 8l .. 8l+7 (two per c[i]).
+__device__ __forceinline__ void fp8_quantize_row(const void* src_rows, size_t row, int bf16, int lane,
+                                                 uint32_t (&c)[4], __half& s16) {
+  float x[8];
+  if (bf16) {
+    const uint4 raw = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src_rows) + row)[lane];
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b2[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else {
+    const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(src_rows) + row) + 2 * lane;
+    const float4 a = f4[0], b = f4[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+  s16 = __float2half_rn(__fdiv_rn(amax, 448.0f));
+  const float s = __half2float(s16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint16_t two = 0;
+    if (s != 0.f) {
+      const float a = __fdiv_rn(x[2 * i], s), b = __fdiv_rn(x[2 * i + 1], s);
+      // cvt packs its first source into the upper byte
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(two) : "f"(b), "f"(a));
+    }
+    c[i] = two;
+  }
+}
+// Store a quantised row at position pos of a K (kv = 0) or V (kv = 1) plane
+// of P tokens: K codes row-major, V codes pair-interleaved, then P fp16 scales.
+// Works on a page plane in global memory and on a staged block in shared
+// memory alike (a staged FP8 block has the layout of a 16-token page).
+__device__ __forceinline__ void fp8_store_row(uint8_t* plane, int P, int kv, int pos, int lane,
+                                              const uint32_t (&c)[4], __half s16) {
+  if (kv == 0) {
+    uint2 w;
+    w.x = c[0] | (c[1] << 16);
+    w.y = c[2] | (c[3] << 16);
+    *reinterpret_cast<uint2*>(plane + pos * kHeadDim + 8 * lane) = w;
+  } else {
+    uint8_t* base = plane + (pos >> 1) * (2 * kHeadDim) + (pos & 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      base[2 * (8 * lane + 2 * i)] = static_cast<uint8_t>(c[i] & 0xff);
+      base[2 * (8 * lane + 2 * i + 1)] = static_cast<uint8_t>(c[i] >> 8);
+    }
+  }
+  if (lane == 0) reinterpret_cast<__half*>(plane + P * kHeadDim)[pos] = s16;
+}
+
 // One warp per (token, kv head, K|V) row.
 __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -40,14 +205,13 @@ __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
   uint32_t c[4];
   __half s16;
   fp8_quantize_row(kv ? p.v : p.k, (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim, p.kv_bf16, lane, c, s16);
-  fp8_store_row(plane, plane + P * kHeadDim, kv, pos, lane, c, s16);
+  fp8_store_row(plane, P, kv, pos, lane, c, s16);
 }
 
 // ============================================================== demote
 // One block per (page pair, layer, kv head, K|V plane).  Each warp encodes
 // rows (dequantise, sign flip, 8-stage FWHT, RMS scale, threshold count);
-// the block then packs 12-byte units (K token-major, V dimension-major) and
-// writes the TQ3 plane.
+// the block then packs 12-byte units and writes the TQ3 plane.
 __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
   const int P = p.P;
@@ -71,7 +235,18 @@ __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
   const __half* sc = reinterpret_cast<const __half*>(src + P * kHeadDim);
   for (int t = warp; t < P; t += 8) {
     uint8_t b[8];
-    fp8_load_row(src, kv, t, lane, b);
+    if (kv == 0) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src + t * kHeadDim + 8 * lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        b[i] = (w.x >> (8 * i)) & 0xff;
+        b[4 + i] = (w.y >> (8 * i)) & 0xff;
+      }
+    } else {
+      const uint8_t* r = src + (t >> 1) * (2 * kHeadDim) + (t & 1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = r[2 * (8 * lane + i)];
+    }
     const float s = __half2float(sc[t]);
     float x[8];
     float ss = 0.f;
@@ -129,30 +304,25 @@ __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
     if (lane == 0) sig[t] = sg16;
   }
   __syncthreads();
-  // pack units: word w -> unit w/3, word index k = w%3; unit u holds
-  // K: token u/(d/32), dims 32*(u%(d/32)) + e;  V: dim u/(P/32), tokens 32*(u%(P/32)) + e
+  // pack units: word w -> unit w/3, word index k = w%3
   const int nwords = P * (kHeadDim / 32) * 3;
   uint32_t* out = reinterpret_cast<uint32_t*>(dst);
   for (int w = threadIdx.x; w < nwords; w += blockDim.x) {
     const int unit = w / 3, k = w - 3 * (w / 3);
-    int t0, j0, dt, dj;
-    if (kv == 0) {
-      t0 = unit / (kHeadDim / 32);
-      j0 = (unit % (kHeadDim / 32)) * 32;
-      dt = 0;
-      dj = 1;
-    } else {
-      j0 = unit / (P / 32);
-      t0 = (unit % (P / 32)) * 32;
-      dt = 1;
-      dj = 0;
-    }
     uint32_t word = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int e0 = 8 * k + i, e1 = 24 + i;
-      const uint32_t c0 = codes[(t0 + dt * e0) * kHeadDim + j0 + dj * e0];
-      const uint32_t c1 = codes[(t0 + dt * e1) * kHeadDim + j0 + dj * e1];
+      int e0 = 8 * k + i, e1 = 24 + i;
+      uint32_t c0, c1;
+      if (kv == 0) {
+        const int t = unit / (kHeadDim / 32), j0 = (unit % (kHeadDim / 32)) * 32;
+        c0 = codes[t * kHeadDim + j0 + e0];
+        c1 = codes[t * kHeadDim + j0 + e1];
+      } else {
+        const int v = unit / (kHeadDim / 16), j0 = (unit % (kHeadDim / 16)) * 16;
+        c0 = codes[(2 * v + (e0 & 1)) * kHeadDim + j0 + (e0 >> 1)];
+        c1 = codes[(2 * v + (e1 & 1)) * kHeadDim + j0 + (e1 >> 1)];
+      }
       word |= (c0 & 7u) << (4 * i);
       word |= ((c1 >> k) & 1u) << (4 * i + 3);
     }
@@ -188,7 +358,18 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
                           static_cast<int64_t>(h) * 2 * plane + kv * plane;
     const float s = __half2float(reinterpret_cast<const __half*>(base + P * kHeadDim)[t]);
     uint8_t b[8];
-    fp8_load_row(base, kv, t, lane, b);
+    if (kv == 0) {
+      const uint2 w = *reinterpret_cast<const uint2*>(base + t * kHeadDim + 8 * lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        b[i] = (w.x >> (8 * i)) & 0xff;
+        b[4 + i] = (w.y >> (8 * i)) & 0xff;
+      }
+    } else {
+      const uint8_t* r = base + (t >> 1) * (2 * kHeadDim) + (t & 1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = r[2 * (8 * lane + i)];
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t f2 = e4m3x2_to_f16x2(b[2 * i] | (b[2 * i + 1] << 8));
@@ -210,11 +391,18 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
         unit = t * (kHeadDim / 32) + j / 32;
         e = j % 32;
       } else {
-        unit = j * (P / 32) + t / 32;
-        e = t % 32;
+        unit = (t >> 1) * (kHeadDim / 16) + j / 16;
+        e = 2 * (j % 16) + (t & 1);
       }
       const uint32_t* w = reinterpret_cast<const uint32_t*>(base + 12 * unit);
-      x[i] = sg * p.level[tq3_unit_code(w, e)];
+      int code;
+      if (e < 24) {
+        code = (w[e >> 3] >> (4 * (e & 7))) & 7;
+      } else {
+        const int i2 = e - 24;
+        code = ((w[0] >> (4 * i2 + 3)) & 1) | (((w[1] >> (4 * i2 + 3)) & 1) << 1) | (((w[2] >> (4 * i2 + 3)) & 1) << 2);
+      }
+      x[i] = sg * p.level[code];
     }
     // x <- H x (natural order), then signs and 1/16
 #pragma unroll
@@ -258,6 +446,744 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
     float4* o = reinterpret_cast<float4*>(static_cast<float*>(dst) + off);
     o[0] = make_float4(x[0], x[1], x[2], x[3]);
     o[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+}
+
+// ============================================================== decode
+// Persistent partial-attention kernel; one CTA of kDecWarps (12) warps per SM.
+// The host cut the launch's blocks into one contiguous piece list per CTA,
+// minimising the largest CTA's estimated cost (a piece is a run of blocks of
+// one (request, kv head, format) group).  Within a piece, warp w takes blocks
+// w, w + 12, w + 24, ... and runs the whole of attention on them by itself:
+//   S = Q K^T on mma.sync m16n8k16: A = q rows (hi in rows 0-7, lo residual
+//     in rows 8-15, fp16), fragments the kernel builds in shared memory for
+//     each piece (signs and Walsh-Hadamard rotation for TQ3), B = K dequantised in
+//     registers (TQ3: PRMT byte-table lookups; FP8: cvt e4m3x2);
+//   online softmax in log2 units with a lazy rescale (per warp);
+//   O^T += V^T P^T: A = V dequantised in registers (token pairs), B = P
+//     scaled by the V row scales (fp16), the S accumulator layout itself.
+// Each warp owns a ring of kSlots shared-memory slots; its lane 0 moves a
+// block in with four cp.async.bulk copies (K codes, K scales, V codes, V
+// scales) counted by the slot's mbarrier, and refills the slot with the
+// warp's block kSlots further on as soon as the warp is done with it.  No
+// warp waits for another except at the end of a piece, where the warps'
+// states merge, in a fixed order, into one partial state (m, l, o) per q head.
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kSlots = 2;                 // staging slots per warp
+constexpr int kSlotBytes = 2 * (kFp8Blk * kHeadDim + 2 * kFp8Blk);   // an FP8 block; a TQ3 block fits
+
+template <int FMT>
+struct Blk {                              // a block of format FMT in a slot
+  static constexpr int kTokens = FMT == 0 ? kFp8Blk : kTq3Blk;
+  static constexpr int kTiles = kTokens / kTileTokens;
+  static constexpr int kRow = FMT == 0 ? kHeadDim : 3 * kHeadDim / 8;      // K row bytes
+  static constexpr int kPairRow = 2 * kRow;                                 // V pair-row bytes
+  static constexpr int kCode = kTokens * kRow;
+  static constexpr int kK = 0, kKs = kCode, kV = kCode + 2 * kTokens, kVs = 2 * kCode + 2 * kTokens;
+  static constexpr int kBytes = 2 * (kCode + 2 * kTokens);
+};
+static_assert(Blk<0>::kBytes <= kSlotBytes && Blk<1>::kBytes <= kSlotBytes, "a block must fit a slot");
+static_assert(kSlotBytes % 16 == 0 && Blk<0>::kV % 16 == 0 && Blk<1>::kV % 16 == 0 && Blk<0>::kVs % 16 == 0 &&
+                  Blk<1>::kVs % 16 == 0 && Blk<1>::kKs % 16 == 0,
+              "bulk copies need 16-byte aligned destinations");
+
+constexpr int kRedBufs = 2;                    // O buffers of the piece-end reduction
+constexpr int kRedFloats = 16 * 4 * 32;        // one warp's O fragments, lane-major
+constexpr int kQBytes = kQfragWords * 4;       // one piece's q fragments
+
+struct DecSmem {
+  uint8_t* ring;                               // [warp][slot] kSlotBytes
+  uint4* qbuf;                                 // [2][k-step 16][lane 32]: q fragments of pieces i, i+1
+  float* red;                                  // [kRedBufs][kRedFloats]
+  float* epi_m;                                // [warp][kMaxGroup]
+  float* epi_l;
+  uint64_t* full;                              // [warp][slot]
+  int* abort_flag;
+};
+constexpr int kDecSmemRing = kDecWarps * kSlots * kSlotBytes;
+constexpr int kDecSmemQ = 2 * kQBytes;
+constexpr int kDecSmemRed = kRedBufs * kRedFloats * 4;
+constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
+constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
+constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
+static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+static_assert(kQBytes == kRedFloats * 4, "a q buffer doubles as a reduction buffer");
+static_assert(kDecWarps >= kMaxGroup, "warp h builds row h of a piece's q fragments");
+
+__device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
+  DecSmem s;
+  s.ring = base;
+  s.qbuf = reinterpret_cast<uint4*>(base + kDecSmemRing);
+  s.red = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemQ);
+  s.epi_m = s.red + kRedBufs * kRedFloats;
+  s.epi_l = s.epi_m + kDecWarps * kMaxGroup;
+  s.full = reinterpret_cast<uint64_t*>(s.epi_l + kDecWarps * kMaxGroup);
+  s.abort_flag = reinterpret_cast<int*>(s.full + kDecWarps * kSlots);
+  return s;
+}
+
+__device__ __forceinline__ bool aborted(const DecSmem& sm) {
+  return *reinterpret_cast<volatile int*>(sm.abort_flag) != 0;
+}
+// Bounded wait (kWaitCycles); gives up at once when the CTA has aborted.
+__device__ __forceinline__ bool dec_wait(const DecSmem& sm, uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (aborted(sm)) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, kErrWaitTimeout);
+      *reinterpret_cast<volatile int*>(sm.abort_flag) = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct Piece {                                 // one CTA piece (its Segment)
+  int fmt, b, kvh, entry0, blk0, nblk, part;
+};
+__device__ __forceinline__ Piece piece_of(const Segment& s) {
+  return Piece{s.fmt, s.b, s.kvh, s.entry0, s.blk, s.nblk, s.part};
+}
+// Piece si of this CTA: the first one travels in the kernel parameters.
+__device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
+  return si == p.cta_seg[blockIdx.x] ? piece_of(p.first[blockIdx.x]) : piece_of(p.segs[si]);
+}
+
+// Block k of a piece: page entry, first token within the page, valid tokens
+// (<= 0: the block is empty).
+__device__ __forceinline__ int block_locate(const DecodeParams& p, const Piece& pc, int k, int& e, int& tok0) {
+  const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
+  const int bpp = p.P / bt;
+  const int bb = pc.blk0 + k;
+  e = pc.entry0 + bb / bpp;
+  tok0 = (bb % bpp) * bt;
+  return min(bt, static_cast<int>(p.entries[e].nvalid) - tok0);
+}
+
+// The warp's sequence of blocks over the CTA's pieces (block k of piece si,
+// k = warp, warp + kDecWarps, ...).  Every lane keeps the same cursor.
+struct BlockCursor {
+  int si, s1, k;
+  int issued;              // lane 0: blocks copied in so far
+  Piece pc;
+  __device__ void start(const DecodeParams& p, int s0, int s1_, int warp) {
+    issued = 0;
+    si = s0;
+    s1 = s1_;
+    k = warp;
+    if (si < s1) pc = load_piece(p, si);
+    settle(p, warp);
+  }
+  __device__ void settle(const DecodeParams& p, int warp) {
+    while (si < s1 && k >= pc.nblk) {
+      if (++si < s1) pc = load_piece(p, si);
+      k = warp;
+    }
+  }
+  __device__ bool valid() const { return si < s1; }
+  __device__ void advance(const DecodeParams& p, int warp) {
+    k += kDecWarps;
+    settle(p, warp);
+  }
+};
+
+// Lane 0: copy a block (page entry pe, first token tok0, nv valid tokens) of
+// piece pc into slot st (mbarrier bar), or complete the slot's phase without
+// bytes for an empty block or a bad plan entry.
+__device__ __noinline__ void dec_issue_entry(const DecodeParams& p, Piece pc, PageEntry pe, int tok0, int nv,
+                                             uint8_t* st, uint64_t* bar, int* abort_flag) {
+  const int nslots = pc.fmt ? p.tq3_slots : p.fp8_slots;
+  if (nv <= 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  if (pe.slot < 0 || pe.slot >= nslots) {
+    atomicOr(p.err, kErrBadPlan);
+    *reinterpret_cast<volatile int*>(abort_flag) = 1;
+    mbar_arrive(bar);
+    return;
+  }
+  const int row = pc.fmt ? 3 * kHeadDim / 8 : kHeadDim;
+  const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
+  const int plane = p.P * (row + 2);
+  const uint8_t* hp = (pc.fmt ? p.tq3_layer : p.fp8_layer) +
+                      static_cast<int64_t>(pe.slot) * (pc.fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
+                      static_cast<int64_t>(pc.kvh) * 2 * plane;
+  const uint32_t code = bt * row;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, 2 * (code + 2 * bt));
+  const uint64_t pol = l2_evict_first_policy();
+  bulk_g2s_hint(st, hp + tok0 * row, code, bar, pol);
+  bulk_g2s_hint(st + code, hp + p.P * row + 2 * tok0, 2 * bt, bar, pol);
+  bulk_g2s_hint(st + code + 2 * bt, hp + plane + tok0 * row, code, bar, pol);
+  bulk_g2s_hint(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar, pol);
+}
+
+// Lane 0: locate block k of piece pc and copy it into slot st.
+__device__ __forceinline__ void dec_issue(const DecodeParams& p, const Piece& pc, int k, uint8_t* st, uint64_t* bar,
+                                          int* abort_flag) {
+  int e = 0, tok0 = 0;
+  const int nv = block_locate(p, pc, k, e, tok0);
+  dec_issue_entry(p, pc, p.entries[e], tok0, nv, st, bar, abort_flag);
+}
+
+// Raw q row h of piece pc (8 dims per lane, bf16 in r[0] or fp32 in r[0..1]);
+// zeros for h >= G.  Split from dec_build_q_row so the load can be issued a
+// piece ahead.
+struct QRow {
+  uint4 r[2];
+};
+__device__ __forceinline__ QRow dec_load_q_row(const DecodeParams& p, const Piece& pc, int h, int lane) {
+  QRow q{};
+  if (h < p.G) {
+    const size_t off = (static_cast<size_t>(pc.b) * p.Hq + pc.kvh * p.G + h) * kHeadDim + 8 * lane;
+    if (p.q_bf16) {
+      q.r[0] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
+    } else {
+      const uint4* f4 = reinterpret_cast<const uint4*>(static_cast<const float*>(p.q) + off);
+      q.r[0] = f4[0];
+      q.r[1] = f4[1];
+    }
+  } else {
+    q.r[0] = q.r[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  return q;
+}
+
+// Row h of piece pc's A fragments from its raw q row, written by one warp
+// into q buffer qb: rows 0-7 hold fp16(x), rows 8-15 the fp16 residual
+// x - fp16(x), where x is q (FP8 pieces) or q' = R q = (H D q)/16 (TQ3
+// pieces; signs, then the Walsh-Hadamard butterflies, 8 dims per lane in
+// registers and across lanes by shuffles).  Fragment layout [k-step 16]
+// [lane 32][4 regs]: lane (g, c) at k-step j covers dims 64c + 4j .. +3 of
+// row g, so lane l of this warp (dims 8l .. 8l+7) fills fragment lane
+// 4h + l/8 at k-steps 2(l%8) and 2(l%8) + 1.
+__device__ __forceinline__ void dec_build_q_row(const DecodeParams& p, uint4* qb, const Piece& pc, int h, int lane,
+                                                const QRow& q, uint32_t qsign) {
+  float x[8];
+  if (p.q_bf16) {
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&q.r[0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b2[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else {
+    const float* f = reinterpret_cast<const float*>(&q.r[0]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = f[i];
+  }
+  if (pc.fmt) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((qsign >> i) & 1u) x[i] = -x[i];
+#pragma unroll
+    for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((i & hs) == 0) {
+          const float a = x[i], c = x[i + hs];
+          x[i] = a + c;
+          x[i + hs] = a - c;
+        }
+    }
+#pragma unroll
+    for (int lm = 1; lm < 32; lm <<= 1) {
+      const bool upper = (lane & lm) != 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float o = __shfl_xor_sync(kFull, x[i], lm);
+        x[i] = upper ? (o - x[i]) : (x[i] + o);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] *= (1.0f / 16.0f);
+  }
+#pragma unroll
+  for (int jj = 0; jj < 2; ++jj) {
+    float hi[4], lo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      hi[i] = __half2float(__float2half_rn(x[4 * jj + i]));
+      lo[i] = x[4 * jj + i] - hi[i];
+    }
+    qb[(2 * (lane & 7) + jj) * 32 + 4 * h + (lane >> 3)] =
+        make_uint4(pack_half2(hi[0], hi[1]), pack_half2(lo[0], lo[1]), pack_half2(hi[2], hi[3]),
+                   pack_half2(lo[2], lo[3]));
+  }
+}
+
+// The two 12-byte units at p (8-byte aligned): words of unit 0 in u[0..2],
+// unit 1 in u[3..5], read as three aligned 8-byte loads.
+__device__ __forceinline__ void load_unit_pair(const uint8_t* p, uint32_t (&u)[6]) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p);
+  const uint2 b = *reinterpret_cast<const uint2*>(p + 8);
+  const uint2 c = *reinterpret_cast<const uint2*>(p + 16);
+  u[0] = a.x; u[1] = a.y; u[2] = b.x; u[3] = b.y; u[4] = c.x; u[5] = c.y;
+}
+
+// S for the one 16-token tile of an FP8 block (two n8 halves: tokens g and
+// 8+g as B columns); K rows are row-major, the thread's 64 dims are 64 bytes.
+// A (q) comes k-step by k-step from shared memory.
+__device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint4* qs, float (&s0)[4],
+                                           float (&s1)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint4 w0 = *reinterpret_cast<const uint4*>(kt + g * kHeadDim + 64 * c + 16 * q4);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(kt + (8 + g) * kHeadDim + 64 * c + 16 * q4);
+    const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w};
+    const uint32_t x1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = qs[(4 * q4 + i) * 32 + lane];
+      mma16816(s0, a.x, a.y, a.z, a.w, e4m3x2_to_f16x2(x0[i]), e4m3x2_to_f16x2(x0[i] >> 16));
+      mma16816(s1, a.x, a.y, a.z, a.w, e4m3x2_to_f16x2(x1[i]), e4m3x2_to_f16x2(x1[i] >> 16));
+    }
+  }
+}
+
+// S for the two 16-token tiles of a TQ3 block: tile t, row (16t + 8r + g),
+// units 2c, 2c+1 (24 bytes at 24c).  Each k-step's A fragment is read once
+// and feeds the four MMAs (two tiles x two n8 halves).
+__device__ __forceinline__ void dec_qk_tq3(const uint8_t* kb, int g, int c, const uint4* qs, const Lut& lut,
+                                           float (&s)[2][2][4]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t u[2][2][6];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) load_unit_pair(kb + (16 * t + 8 * r + g) * 96 + 24 * c, u[t][r]);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t sel[2][2][8];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        tq3_unit_selectors(u[t][r][3 * half], u[t][r][3 * half + 1], u[t][r][3 * half + 2], sel[t][r]);
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      const uint4 a = qs[(8 * half + st) * 32 + lane];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          uint32_t x0, x1;
+          tq3_lookup4(sel[t][r][st], lut, x0, x1);
+          mma16816(s[t][r], a.x, a.y, a.z, a.w, x0, x1);
+        }
+    }
+  }
+}
+
+// O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32)
+__device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, uint2 pb, float (&o)[16][4]) {
+  const uint8_t* ra = vt + c * (2 * kHeadDim) + 64 * g;
+  const uint8_t* rb = vt + (c + 4) * (2 * kHeadDim) + 64 * g;
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint4 wa = *reinterpret_cast<const uint4*>(ra + 16 * q4);
+    const uint4 wb = *reinterpret_cast<const uint4*>(rb + 16 * q4);
+    const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t xb[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      mma16816(o[4 * q4 + i], e4m3x2_to_f16x2(xa[i]), e4m3x2_to_f16x2(xa[i] >> 16), e4m3x2_to_f16x2(xb[i]),
+               e4m3x2_to_f16x2(xb[i] >> 16), pb.x, pb.y);
+  }
+}
+
+// O^T += V^T P^T for TQ3 V: pair-rows c and c+4, units 2g, 2g+1 (24 bytes at 24g)
+__device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint2 pb, const Lut& lut,
+                                           float (&o)[16][4]) {
+  uint32_t ua[6], ub[6];
+  load_unit_pair(vt + c * 192 + 24 * g, ua);
+  load_unit_pair(vt + (c + 4) * 192 + 24 * g, ub);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t sa[8], sb[8];
+    tq3_unit_selectors(ua[3 * half], ua[3 * half + 1], ua[3 * half + 2], sa);
+    tq3_unit_selectors(ub[3 * half], ub[3 * half + 1], ub[3 * half + 2], sb);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t x0, x1, y0, y1;
+      tq3_lookup4(sa[s], lut, x0, x1);
+      tq3_lookup4(sb[s], lut, y0, y1);
+      mma16816(o[8 * half + s], x0, x1, y0, y1, pb.x, pb.y);
+    }
+  }
+}
+
+// Per-warp running state of a piece.
+struct WarpState {
+  float o[16][4];          // O^T fragments: m-tile i rows (dims) 32g+2i, 32g+2i+1; columns heads 2c, 2c+1
+  float m_run, l_run;      // head g: running max (log2 units) and this lane's share of the sum
+};
+
+// One block of format FMT at st (nv valid tokens): scores, online softmax, PV.
+template <int FMT>
+__device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* st, int nv, const uint4* qs,
+                                          WarpState& ws) {
+  using B = Blk<FMT>;
+  constexpr int NT = B::kTiles;
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const Lut& lut = p.lut;
+  float sacc[2][2][4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) sacc[t][h][0] = sacc[t][h][1] = sacc[t][h][2] = sacc[t][h][3] = 0.f;
+  if (FMT == 0)
+    dec_qk_fp8(st + B::kK, g, c, qs, sacc[0][0], sacc[0][1]);
+  else
+    dec_qk_tq3(st + B::kK, g, c, qs, lut, sacc);
+  const __half2* ks = reinterpret_cast<const __half2*>(st + B::kKs);
+  const __half2* vs = reinterpret_cast<const __half2*>(st + B::kVs);
+  const float scale = p.score_scale;
+  // lane's tokens in tile t: 16t + 2c + {0, 1} (half 0) and 16t + 8 + 2c + {0, 1} (half 1)
+  float sc[NT][4];
+  float mt = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const float2 k0 = __half22float2(ks[8 * t + c]), k1 = __half22float2(ks[8 * t + 4 + c]);
+    sc[t][0] = (sacc[t][0][0] + sacc[t][0][2]) * (k0.x * scale);
+    sc[t][1] = (sacc[t][0][1] + sacc[t][0][3]) * (k0.y * scale);
+    sc[t][2] = (sacc[t][1][0] + sacc[t][1][2]) * (k1.x * scale);
+    sc[t][3] = (sacc[t][1][1] + sacc[t][1][3]) * (k1.y * scale);
+    if (g >= p.G) {
+      sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = -INFINITY;
+    } else if (nv < B::kTokens) {
+      const int tb = 16 * t + 2 * c;
+      if (tb >= nv) sc[t][0] = -INFINITY;
+      if (tb + 1 >= nv) sc[t][1] = -INFINITY;
+      if (tb + 8 >= nv) sc[t][2] = -INFINITY;
+      if (tb + 9 >= nv) sc[t][3] = -INFINITY;
+    }
+    mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
+  }
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+  if (__any_sync(kFull, mt > ws.m_run + kLazyRescale)) {
+    const float m_new = fmaxf(ws.m_run, mt);
+    const float alpha = (ws.m_run == -INFINITY) ? 0.f : ex2(ws.m_run - m_new);
+    ws.m_run = m_new;
+    ws.l_run *= alpha;
+    // O columns are heads 2c and 2c+1: their factors live in lanes 8c and 8c+4
+    const float a0 = __shfl_sync(kFull, alpha, 8 * c), a1 = __shfl_sync(kFull, alpha, 8 * c + 4);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      ws.o[i][0] *= a0;
+      ws.o[i][1] *= a1;
+      ws.o[i][2] *= a0;
+      ws.o[i][3] *= a1;
+    }
+  }
+  // m_run stays -inf only for heads g >= G (all their scores -inf); a masked
+  // score gives ex2(-inf) = 0, and 0 times a (finite, possibly stale) scale is 0
+  const float mref = (ws.m_run == -INFINITY) ? 0.f : ws.m_run;
+  const float vsc = FMT == 0 ? kFp8PScale : 1.f;
+  uint2 pb[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    float pr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pr[i] = ex2(sc[t][i] - mref);
+    ws.l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    const float2 v0 = __half22float2(vs[8 * t + c]), v1 = __half22float2(vs[8 * t + 4 + c]);
+    pb[t] = make_uint2(pack_half2(pr[0] * (v0.x * vsc), pr[1] * (v0.y * vsc)),
+                       pack_half2(pr[2] * (v1.x * vsc), pr[3] * (v1.y * vsc)));
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    if (FMT == 0)
+      dec_pv_fp8(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], ws.o);
+    else
+      dec_pv_tq3(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], lut, ws.o);
+  }
+}
+
+// Store / add one warp's O fragments to / from a reduction buffer: m-tile i
+// of lane l as one float4 at [i][l] (conflict-free 16-byte accesses).
+__device__ __forceinline__ void red_store(float* buf, const WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+  float4* b4 = reinterpret_cast<float4*>(buf) + lane;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) b4[i * 32] = make_float4(ws.o[i][0], ws.o[i][1], ws.o[i][2], ws.o[i][3]);
+}
+__device__ __forceinline__ void red_add(const float* buf, WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+  const float4* b4 = reinterpret_cast<const float4*>(buf) + lane;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 v = b4[i * 32];
+    ws.o[i][0] += v.x;
+    ws.o[i][1] += v.y;
+    ws.o[i][2] += v.z;
+    ws.o[i][3] += v.w;
+  }
+}
+
+// End of a piece: the CTA's warps' states merge into the
+// piece's partial state.  Each warp rescales its O to the common max of each
+// head; O then sums up a fixed tree (four buffers) so the result does not
+// depend on timing; warp 0 writes (m, l, o) per q head.
+__device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
+                                              WarpState& ws, int warp) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int G = p.G;
+  float l = ws.l_run;
+  l += __shfl_xor_sync(kFull, l, 1);
+  l += __shfl_xor_sync(kFull, l, 2);
+  if (c == 0) {
+    sm.epi_m[warp * kMaxGroup + g] = (g < G) ? ws.m_run : -INFINITY;
+    sm.epi_l[warp * kMaxGroup + g] = (g < G) ? l : 0.f;
+  }
+  named_bar(1, kDecThreads);
+  const float osc = pc.fmt == 0 ? 1.f / kFp8PScale : 1.f;
+  float f0, f1, Mg = -INFINITY, Lg = 0.f;
+  {
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      M0 = fmaxf(M0, sm.epi_m[w * kMaxGroup + 2 * c]);
+      M1 = fmaxf(M1, sm.epi_m[w * kMaxGroup + 2 * c + 1]);
+      Mg = fmaxf(Mg, sm.epi_m[w * kMaxGroup + g]);
+    }
+    const float m0 = sm.epi_m[warp * kMaxGroup + 2 * c], m1 = sm.epi_m[warp * kMaxGroup + 2 * c + 1];
+    f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0) * osc;
+    f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1) * osc;
+    if (warp == 0 && Mg != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mw = sm.epi_m[w * kMaxGroup + g];
+        if (mw != -INFINITY) Lg += ex2(mw - Mg) * sm.epi_l[w * kMaxGroup + g];
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    ws.o[i][0] *= f0;
+    ws.o[i][1] *= f1;
+    ws.o[i][2] *= f0;
+    ws.o[i][3] *= f1;
+  }
+  // the tree: with n warps holding sums, warps [n - h, n) add into warps
+  // [0, h), h = min(4, n / 2): one round per level through four 8 KB buffers
+  // (the two reduction buffers and both q buffers: the next piece's q
+  // fragments are built only after this merge)
+  float* const q0 = reinterpret_cast<float*>(sm.qbuf);
+  float* const q1 = reinterpret_cast<float*>(sm.qbuf + kQBytes / 16);
+  auto buf = [&](int i) { return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : i == 2 ? q0 : q1; };
+#pragma unroll
+  for (int n = kDecWarps; n > 1;) {
+    const int h = min(4, n / 2), lo = n - h;
+    const int i = warp - lo;                             // this warp as a source
+    if (i >= 0 && i < h) red_store(buf(i), ws);
+    named_bar(1, kDecThreads);
+    if (warp < h) red_add(buf(warp), ws);
+    n = lo;
+    if (n > 1) named_bar(1, kDecThreads);
+  }
+  if (warp == 0) {
+    float* dst = p.part + static_cast<size_t>(pc.part) * G * (2 + kHeadDim);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int d = 32 * g + 2 * i;
+      if (2 * c < G)
+        *reinterpret_cast<float2*>(dst + (2 * c) * (2 + kHeadDim) + 2 + d) = make_float2(ws.o[i][0], ws.o[i][2]);
+      if (2 * c + 1 < G)
+        *reinterpret_cast<float2*>(dst + (2 * c + 1) * (2 + kHeadDim) + 2 + d) =
+            make_float2(ws.o[i][1], ws.o[i][3]);
+    }
+    if (c == 0 && g < G) {
+      dst[g * (2 + kHeadDim)] = Mg;
+      dst[g * (2 + kHeadDim) + 1] = Lg;
+    }
+  }
+}
+
+// The warp's position in its own ring: slot and phase parity of the next
+// block it consumes.
+struct RingPos {
+  int slot, phase;
+  __device__ void step() {
+    if (++slot == kSlots) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// Fused append (mkv_append_decode): the warp whose FP8 block holds a
+// request's newest token quantises the token's K and V rows, stores them into
+// the page (global memory, for later steps) and into the staged block it has
+// just received (whose copy predates them).
+__device__ __forceinline__ void dec_append_tail(const DecodeParams& p, const Piece& pc, const PageEntry& pe, int tok0,
+                                                uint8_t* st, int lane) {
+  const int pos = pe.nvalid - 1;
+  const size_t row = (static_cast<size_t>(pc.b) * p.Hkv + pc.kvh) * kHeadDim;
+  const int plane = p.P * (kHeadDim + 2);
+  uint8_t* hp = p.fp8_layer + static_cast<int64_t>(pe.slot) * p.fp8_page_bytes + static_cast<int64_t>(pc.kvh) * 2 * plane;
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    uint32_t c[4];
+    __half s16;
+    fp8_quantize_row(kv ? p.v : p.k, row, p.kv_bf16, lane, c, s16);
+    fp8_store_row(hp + kv * plane, p.P, kv, pos, lane, c, s16);
+    fp8_store_row(st + kv * (Blk<0>::kBytes / 2), kFp8Blk, kv, pos - tok0, lane, c, s16);
+  }
+  __syncwarp();
+}
+
+// The warp's blocks of piece number pi (piece pc); `ic` is the cursor of the
+// next block to copy in.
+template <int FMT>
+__device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int pi,
+                                          BlockCursor& ic, RingPos& rp, int warp, WarpState& ws) {
+  const int lane = threadIdx.x & 31;
+  const uint4* qs = sm.qbuf + (pi & 1) * (kQBytes / 16);
+  for (int k = warp; k < pc.nblk; k += kDecWarps) {
+    int nv = Blk<FMT>::kTokens, e = 0, tok0 = 0;
+    if (FMT == 0) nv = block_locate(p, pc, k, e, tok0);
+    const bool ok = dec_wait(sm, sm.full + warp * kSlots + rp.slot, rp.phase, p.err);
+    uint8_t* st = sm.ring + (warp * kSlots + rp.slot) * kSlotBytes;
+    if (ok && nv > 0) {
+      if (FMT == 0 && p.append) {
+        const PageEntry pe = p.entries[e];
+        if (pe.tail && pe.nvalid - 1 >= tok0 && pe.nvalid - 1 < tok0 + kFp8Blk) dec_append_tail(p, pc, pe, tok0, st, lane);
+      }
+      dec_block<FMT>(p, st, nv, qs, ws);
+    }
+    __syncwarp();
+    // the slot is free again: copy in the warp's block kSlots further on
+    if (ic.valid()) {
+      if (lane == 0 && !aborted(sm)) {
+        dec_issue(p, ic.pc, ic.k, sm.ring + (warp * kSlots + rp.slot) * kSlotBytes, sm.full + warp * kSlots + rp.slot,
+                  sm.abort_flag);
+        ++ic.issued;
+      }
+      ic.advance(p, warp);
+    }
+    rp.step();
+  }
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const DecSmem sm = dec_carve(smem);
+  const int s0 = p.cta_seg[blockIdx.x], s1 = p.cta_seg[blockIdx.x + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the merge kernel that follows waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the rotation signs of this lane's q dims 8 lane .. 8 lane + 7, loaded
+  // before the barrier so that the q build does not wait for them
+  const uint32_t qsign = static_cast<uint32_t>(
+      (lane < 8 ? p.signs[0] : lane < 16 ? p.signs[1] : lane < 24 ? p.signs[2] : p.signs[3]) >> (8 * (lane & 7))) & 0xFFu;
+  if (lane == 0) {
+    for (int i = 0; i < kSlots; ++i) mbar_init(sm.full + warp * kSlots + i, 1);
+    if (warp == 0) *sm.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // q and the partial-state workspace belong to the preceding kernels (the
+  // previous launch's merge reads the workspace): wait for them first
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // warp h < kMaxGroup builds row h of each piece's q fragments; piece s0's
+  // row load goes out now, the next piece's at the start of each piece
+  const bool q_warp = warp < kMaxGroup;
+  BlockCursor ic;
+  {
+    QRow qr{};
+    Piece p0{};
+    if (q_warp && s0 < s1) {
+      p0 = load_piece(p, s0);
+      qr = dec_load_q_row(p, p0, warp, lane);
+    }
+    // the warp's first kSlots blocks
+    ic.start(p, s0, s1, warp);
+    Piece fp[kSlots];
+    int fk[kSlots];
+    int nfirst = 0;
+    for (; nfirst < kSlots && ic.valid(); ++nfirst) {
+      fp[nfirst] = ic.pc;
+      fk[nfirst] = ic.k;
+      ic.advance(p, warp);
+    }
+    // page-entry loads of the first blocks go out together
+    PageEntry pe[kSlots];
+    int tok0[kSlots], nv[kSlots];
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i)
+        if (i < nfirst) {
+          int e = 0;
+          nv[i] = block_locate(p, fp[i], fk[i], e, tok0[i]);
+          pe[i] = p.entries[e];
+        }
+      // the first block now; the rest after the q fragments, so that a full
+      // copy queue does not hold the warp's q build back
+      if (nfirst > 0)
+        dec_issue_entry(p, fp[0], pe[0], tok0[0], nv[0], sm.ring + warp * kSlots * kSlotBytes, sm.full + warp * kSlots,
+                        sm.abort_flag);
+      ic.issued = nfirst;
+    }
+    if (q_warp && s0 < s1) dec_build_q_row(p, sm.qbuf, p0, warp, lane, qr, qsign);
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 1; i < kSlots; ++i)
+        if (i < nfirst)
+          dec_issue_entry(p, fp[i], pe[i], tok0[i], nv[i], sm.ring + (warp * kSlots + i) * kSlotBytes,
+                          sm.full + warp * kSlots + i, sm.abort_flag);
+    }
+    named_bar(1, kDecThreads);
+  }
+  RingPos rp{0, 0};
+  WarpState ws;
+  for (int si = s0; si < s1; ++si) {
+    const int pi = si - s0;
+    const Piece pc = load_piece(p, si);
+    const bool prep_next = si + 1 < s1 && q_warp;
+    Piece pn{};
+    QRow qn{};
+    if (prep_next) {
+      pn = load_piece(p, si + 1);
+      qn = dec_load_q_row(p, pn, warp, lane);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ws.o[i][0] = ws.o[i][1] = ws.o[i][2] = ws.o[i][3] = 0.f;
+    ws.m_run = -INFINITY;
+    ws.l_run = 0.f;
+    if (pc.fmt)
+      dec_piece<1>(p, sm, pc, pi, ic, rp, warp, ws);
+    else
+      dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
+    dec_piece_end(p, sm, pc, ws, warp);
+    // every warp is past piece pi; the other q buffer (piece pi - 1's, free
+    // since its end) takes piece pi + 1
+    if (si + 1 < s1) {
+      if (prep_next) dec_build_q_row(p, sm.qbuf + ((pi + 1) & 1) * (kQBytes / 16), pn, warp, lane, qn, qsign);
+      named_bar(1, kDecThreads);
+    }
+  }
+  // on the normal path every copy issued was waited for; after an abort, wait
+  // (bounded) for copies still in flight before the CTA exits
+  __syncthreads();
+  if (aborted(sm) && lane == 0) {
+    for (int j = ic.issued > kSlots ? ic.issued - kSlots : 0; j < ic.issued; ++j) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(sm.full + warp * kSlots + j % kSlots, (j / kSlots) & 1))
+        if (clock64() - t0 > kWaitCycles) break;
+    }
   }
 }
 
@@ -380,6 +1306,8 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+size_t decode_smem_bytes() { return kDecSmemBytes; }
+
 // Fixed scratch for the allocation-free decode entry point: 8 MiB of partial
 // states, compiled into the library so a call never needs to allocate.
 constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
@@ -396,11 +1324,39 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
   *bytes = kNoallocScratchBytes;
   return cudaSuccess;
 }
+int decode_threads() { return kDecThreads; }
 
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
   const int rows = p.npages * p.P * p.Hkv * 2;
   if (rows > 0) mkv_dequant_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+  // the shared-memory limit is a per-device attribute: set it once per device
+  // (setting it twice from racing threads is harmless)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  if (p.n_ctas <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_ctas);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kDecSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mkv_decode_kernel, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {

@@ -3,24 +3,22 @@
 implementation; the GPU parity tests compare exported page bytes with what
 this module packs.
 
-One page holds ``P`` tokens of one layer (P a multiple of 64).  For each kv
-head h (in order) the page stores a K plane then a V plane; a plane is the
-code bytes followed by ``P`` little-endian fp16 scales (token order).
+One page holds ``P`` tokens of one layer.  For each kv head h (in order) the
+page stores a K plane then a V plane; a plane is the code bytes followed by
+``P`` little-endian fp16 scales (token order).
 
 FP8 (1 byte per element):
-  K codes: 64-token blocks, each stored as D/16 columns of 16 bytes:
-           byte ``(t//64)*64*D + (j//16)*1024 + (t%64)*16 + j%16``.
-  V codes: 8-token groups, each dimension's 8 bytes together:
-           byte ``(t//8)*8*D + j*8 + t%8``.
+  K codes: row-major, byte ``t*D + j`` for token t, dim j.
+  V codes: tokens paired (2v, 2v+1): byte ``v*2D + 2j + (t % 2)``, i.e. the two
+           rows of a pair interleaved element by element.
 
 TQ3 (3 bits per element): codes are grouped in 12-byte units of 32 codes
-(3 bits per code; no unit boundary falls inside a byte).  A unit is three
-little-endian 32-bit words W0..W2:
+(8 codes per 3 bytes).  A unit is three little-endian 32-bit words W0..W2:
   bits [4i, 4i+3) of W_k hold code (8k + i)          for i = 0..7, k = 0..2;
   bit  4i+3       of W_k holds bit k of code (24 + i).
   K codes: unit ``t*(D/32) + j//32``, code index ``j % 32``   (rows in order).
-  V codes: unit ``j*(P/32) + t//32``, code index ``t % 32``
-           (dimension-major: each dimension's codes in token order).
+  V codes: unit ``(t//2)*(D/16) + j//16``, code index ``2*(j % 16) + t % 2``
+           (the two rows of a token pair interleaved code by code).
 """
 from __future__ import annotations
 
@@ -79,37 +77,16 @@ def _tq3_k_unit_order(codes: np.ndarray) -> np.ndarray:
 
 
 def _tq3_v_unit_order(codes: np.ndarray) -> np.ndarray:
-    """V plane codes [P, D] -> unit-ordered [D*P/32, 32]: unit j*(P/32) + t//32, code t%32."""
+    """V plane codes [P, D] -> unit-ordered [(P/2)*(D/16), 32], code index 2*(j%16)+parity."""
     P, D = codes.shape
-    return np.ascontiguousarray(codes.T).reshape(D * (P // 32), 32)
+    pair = codes.reshape(P // 2, 2, D // 16, 16)           # [v, parity, unit, j%16]
+    unit = pair.transpose(0, 2, 3, 1)                      # [v, unit, j%16, parity]
+    return unit.reshape((P // 2) * (D // 16), 32)
 
 
 def _tq3_v_from_units(units: np.ndarray, P: int, D: int) -> np.ndarray:
-    return units.reshape(D, P).T.copy()
-
-
-def _fp8_k_order(codes: np.ndarray) -> np.ndarray:
-    """K plane codes [P, D] -> plane bytes: 64-token blocks of D/16 16-byte columns."""
-    P, D = codes.shape
-    blk = codes.reshape(P // 64, 64, D // 16, 16)          # [block, t%64, column, j%16]
-    return blk.transpose(0, 2, 1, 3).reshape(-1)
-
-
-def _fp8_k_from_bytes(b: np.ndarray, P: int, D: int) -> np.ndarray:
-    blk = np.asarray(b).reshape(P // 64, D // 16, 64, 16)  # [block, column, t%64, j%16]
-    return blk.transpose(0, 2, 1, 3).reshape(P, D)
-
-
-def _fp8_v_order(codes: np.ndarray) -> np.ndarray:
-    """V plane codes [P, D] -> plane bytes: 8-token groups, each dimension's 8 bytes together."""
-    P, D = codes.shape
-    grp = codes.reshape(P // 8, 8, D)                      # [group, t%8, j]
-    return grp.transpose(0, 2, 1).reshape(-1)
-
-
-def _fp8_v_from_bytes(b: np.ndarray, P: int, D: int) -> np.ndarray:
-    grp = np.asarray(b).reshape(P // 8, D, 8)              # [group, j, t%8]
-    return grp.transpose(0, 2, 1).reshape(P, D)
+    u = units.reshape(P // 2, D // 16, 16, 2).transpose(0, 3, 1, 2)
+    return u.reshape(P, D)
 
 
 def _scales_bytes(scales: np.ndarray) -> np.ndarray:
@@ -126,15 +103,15 @@ def pack_fp8_page(kc, ks, vc, vs) -> np.ndarray:
     kc = np.asarray(kc, dtype=np.uint8)
     vc = np.asarray(vc, dtype=np.uint8)
     P, Hkv, D = kc.shape
-    assert P % 64 == 0 and D % 16 == 0
     plane = fp8_plane_bytes(P, D)
     out = np.zeros(fp8_page_bytes(P, Hkv, D), dtype=np.uint8)
     for h in range(Hkv):
         base = h * 2 * plane
-        out[base: base + P * D] = _fp8_k_order(kc[:, h, :])
+        out[base: base + P * D] = kc[:, h, :].reshape(-1)
         out[base + P * D: base + plane] = _scales_bytes(ks[:, h])
         vb = base + plane
-        out[vb: vb + P * D] = _fp8_v_order(vc[:, h, :])
+        pair = vc[:, h, :].reshape(P // 2, 2, D).transpose(0, 2, 1)   # [v, j, parity]
+        out[vb: vb + P * D] = pair.reshape(-1)
         out[vb + P * D: vb + plane] = _scales_bytes(vs[:, h])
     return out
 
@@ -148,10 +125,10 @@ def unpack_fp8_page(page: np.ndarray, P: int, Hkv: int, D: int):
     vs = np.zeros((P, Hkv))
     for h in range(Hkv):
         base = h * 2 * plane
-        kc[:, h, :] = _fp8_k_from_bytes(page[base: base + P * D], P, D)
+        kc[:, h, :] = page[base: base + P * D].reshape(P, D)
         ks[:, h] = _scales_from_bytes(page[base + P * D: base + plane])
         vb = base + plane
-        vc[:, h, :] = _fp8_v_from_bytes(page[vb: vb + P * D], P, D)
+        vc[:, h, :] = page[vb: vb + P * D].reshape(P // 2, D, 2).transpose(0, 2, 1).reshape(P, D)
         vs[:, h] = _scales_from_bytes(page[vb + P * D: vb + plane])
     return kc, ks, vc, vs
 

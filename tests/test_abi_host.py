@@ -219,16 +219,17 @@ def test_plan_covers_every_page_once(mkv):
                 pool.demote([r] * len(stale), stale)
         ids = list(range(w.n))
         plan = _check_plan_covers(mkv, pool, ids, w.lengths, w.tiers)
-        # balance: a host-only pool plans for up to 152 CTAs (6 tiles each at
-        # least); no chunk is larger than one CTA's share of the estimated
-        # work (tiles of 128 TQ3 / 64 FP8 tokens with a fixed cost each, and
-        # a fixed cost per chunk) plus one round of three tiles
+        # balance: a host-only pool plans for up to 152 CTAs (24 blocks each at
+        # least); no chunk is larger than
+        # one CTA's share of the estimated work (blocks of 32 TQ3 / 16 FP8
+        # tokens with a fixed cost each, and a fixed cost per chunk) plus one
+        # warp-round of blocks; there are at most a few chunks per CTA
         def cost(c):
-            tt, per_tok = (128, 1.0) if c[2] == 3 else (64, 1.45)
-            return c[5] * per_tok + 24.0 * -(-c[5] // tt) + 540.0
-        ntile = sum(-(-c[5] // (128 if c[2] == 3 else 64)) for c in plan)
-        share = sum(cost(c) for c in plan) / max(1, min(152, ntile // 6))
-        assert max(cost(c) for c in plan) <= share + 3 * (128 + 24.0)
+            bt, per_tok = (32, 1.0) if c[2] == 3 else (16, 1.45)
+            return c[5] * per_tok + 8.0 * -(-c[5] // bt) + 540.0
+        nblk = sum(-(-c[5] // (32 if c[2] == 3 else 16)) for c in plan)
+        share = sum(cost(c) for c in plan) / max(1, min(152, nblk // 24))
+        assert max(cost(c) for c in plan) <= share + 12 * 40.0
         assert len(plan) <= w.n * 4 * 2 + 4 * 1024
 
 
@@ -277,11 +278,10 @@ def test_selftest_wait_timeout_arguments(mkv):
 
 def _rounds_of(layouts, P, H=4):
     """The planner's work units for requests given as (tokens, tiers per page):
-    per (request, kv head, tier) group, TQ3 before FP8, tiles of 128 TQ3
-    tokens (whole pages) or 64 FP8 tokens (page by page, up to the last valid
-    token), cut into rounds of 3 tiles from the group's start; a round costs
-    3 x its slowest tile (tokens x 1.0 or 1.45, + 24), a short round
-    0.5 + 0.5 x its share of that."""
+    per (request, kv head, tier) group, TQ3 before FP8, blocks of 32 TQ3 / 16
+    FP8 tokens page by page, cut into rounds of 12 blocks from the group's
+    start; a round costs 12 x its slowest block (tokens x 1.0 or 1.45, + 8),
+    a short round 0.4 + 0.6 x its share of that."""
     rounds = []                                            # (group key, cost)
     for b, (n, tiers) in enumerate(layouts):
         nv = [min(P, n - i * P) for i in range(len(tiers))]
@@ -290,14 +290,13 @@ def _rounds_of(layouts, P, H=4):
                 pages = [nv[i] for i, t in enumerate(tiers) if (t == 3) == (fmt == 3)]
                 if not pages:
                     continue
-                if fmt == 3:
-                    ppt = 128 // P
-                    costs = [sum(pages[k:k + ppt]) * 1.0 + 24.0 for k in range(0, len(pages), ppt)]
-                else:
-                    costs = [min(64, v - j) * 1.45 + 24.0 for v in pages for j in range(0, v, 64)]
-                for r in range(0, len(costs), 3):
-                    c = costs[r:r + 3]
-                    rounds.append(((b, kvh, fmt), max(c) * 3 * (0.5 + 0.5 * len(c) / 3)))
+                bt, rate = (32, 1.0) if fmt == 3 else (16, 1.45)
+                bpp = P // bt
+                nblk = (len(pages) - 1) * bpp + -(-pages[-1] // bt)
+                costs = [max(0, min(bt, pages[k // bpp] - (k % bpp) * bt)) * rate + 8.0 for k in range(nblk)]
+                for r in range(0, nblk, 12):
+                    c = costs[r:r + 12]
+                    rounds.append(((b, kvh, fmt), max(c) * 12 * (0.4 + 0.6 * len(c) / 12)))
     return rounds
 
 
@@ -329,10 +328,10 @@ def test_plan_minimises_the_largest_cta(mkv):
         pos += 1
     # the split as round ranges, CTA by CTA
     ctas = {}
-    for b, kvh, tier, _, _, _, cta, tile0, ntile in plan:
-        assert tile0 % 3 == 0, "cuts fall on round boundaries"
-        start = index[(b, kvh, tier)] + tile0 // 3
-        ctas.setdefault(cta, []).append((start, start + -(-ntile // 3)))
+    for b, kvh, tier, _, _, _, cta, blk0, nblk in plan:
+        assert blk0 % 12 == 0, "cuts fall on round boundaries"
+        start = index[(b, kvh, tier)] + blk0 // 12
+        ctas.setdefault(cta, []).append((start, start + -(-nblk // 12)))
     assert sorted(ctas) == list(range(len(ctas)))
     seq = [rng for c in sorted(ctas) for rng in ctas[c]]
     assert seq[0][0] == 0 and seq[-1][1] == len(rounds)
@@ -340,8 +339,8 @@ def test_plan_minimises_the_largest_cta(mkv):
     got = max(_cta_cost(rounds[min(s for s, _ in r):max(e for _, e in r)]) for r in ctas.values())
     # exhaustive optimum: f_k[j] = min_i max(f_{k-1}[i], cost(rounds i..j-1))
     R = len(rounds)
-    ntiles = sum(ntile for *_, ntile in plan)
-    kmax = max(1, min(152, ntiles // 6))
+    nblocks = sum(nblk for *_, nblk in plan)
+    kmax = max(1, min(152, nblocks // 24))
     C = np.full((R + 1, R + 1), np.inf)
     for i in range(R):
         for j in range(i + 1, R + 1):
