@@ -46,16 +46,28 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mkv", "reference"], default="mkv")
-    ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--workload", default="cfg5",
+                    help="cfg5 (16 x 131K tokens, the largest single-GPU workload) by default; cfg1..cfg4")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--requests", default=None,
+                    help="comma-separated request indices: run a reduced-size slice of the workload "
+                         "(same shapes; e.g. for a profiler capture)")
     ap.add_argument("--nq", type=int, default=1,
                     help="query tokens per request and step (> 1: the multi-query path, a separate line)")
     return ap.parse_args()
 
 
 # ----------------------------------------------------------------- helpers
+def make_workload(args):
+    from mixed_format_paged_gb300 import workloads
+    w = workloads.make(args.workload)
+    if args.requests:
+        w = w.subset([int(x) for x in args.requests.split(",")])
+    return w
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -80,9 +92,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload):
-    """Per-launch DRAM bytes of the partial-attention kernel from the committed
-    ncu summary, only if it was taken on the current kernel source."""
+def committed_traffic(workload, alg_bytes_per_launch):
+    """Per-launch DRAM bytes (read + write) of the partial-attention kernel
+    from the committed ncu summary, only if it was taken on the current
+    kernel source.  A capture of the full workload gives them directly; a
+    capture of a reduced-size slice of the same shape gives DRAM bytes per
+    algorithmic byte, scaled here by the launch's algorithmic bytes."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
@@ -91,7 +106,9 @@ def committed_traffic(workload):
     e = d.get(workload)
     if not e or e.get("kernel_hash") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    if "dram_bytes_per_launch" in e:
+        return e["dram_bytes_per_launch"]
+    return e["dram_bytes_per_alg_byte"] * alg_bytes_per_launch
 
 
 class ClockSampler:
@@ -225,7 +242,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = workloads.make(args.workload)
+    w = make_workload(args)
     r = 0
     K, V = w.prefill_kv(0, r, device="cpu")
     K = K.float().numpy()
@@ -285,7 +302,7 @@ def run_mkv(args):
         if world > 1:
             dist.barrier()
 
-    w = workloads.make(args.workload)
+    w = make_workload(args)
     L, P = w.num_layers, w.P
     e2e_steps = 0 if args.no_e2e else args.steps
     total_steps = args.warmup + args.steps + e2e_steps
@@ -467,7 +484,8 @@ def run_mkv(args):
         "us_per_layer_step": per_layer_step_s * 1e6,
         "frac_of_hbm_peak": value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": committed_traffic(w.name), "kernel": "mkv_decode_kernel (partial attention)",
+                     "traffic": committed_traffic(w.name, sum(kernel_bytes) / len(kernel_bytes)),
+                     "kernel": "mkv_decode_kernel (partial attention)",
                      "peak_source": peak_src, "launches": len(kernel_ms),
                      "timed_launches": f"layer {TIMED_LAYER} of each timed step (CUDA events on the call's stream)",
                      "avg_launch_us": 1e3 * sum(kernel_ms) / len(kernel_ms)},
@@ -501,7 +519,7 @@ def run_multi(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(0)
-    w = workloads.make(args.workload)
+    w = make_workload(args)
     L, P, nq, n = w.num_layers, w.P, args.nq, w.n
     total_steps = args.warmup + args.steps
     pool = make_pool(w, device=dev, extra_steps=nq * (total_steps + 1), seed=99, max_batch=n * nq)

@@ -68,6 +68,32 @@ class Workload:
     def tiers(self, r: int, length: int | None = None) -> list:
         return [self.tier(r, p, length) for p in range(self.npages(r, length))]
 
+    def subset(self, idx) -> "Workload":
+        """The same workload restricted to requests `idx` (in that order): a
+        reduced-size case of the same shape, e.g. for a profiler capture."""
+        idx = [int(i) for i in idx]
+        w = Workload(f"{self.name}[{','.join(map(str, idx))}]", self.num_layers, self.Hq, self.Hkv, self.D, self.P,
+                     [self.lengths[i] for i in idx], [self.windows[i] for i in idx],
+                     [set(self.anchors[i]) for i in idx], self.steps, self.kv_dtype, self.q_dtype, self.v_student_t,
+                     self.seed, self.outlier_ch, self.outlier_off,
+                     f"requests {idx} of: {self.description}")
+        return w
+
+    def layout_classes(self) -> dict:
+        """Request indices by tier layout: 'all_fp8' (every page Recent or
+        Anchor), 'mostly_tq3' (at least 98 % of pages TQ3) and 'mixed'."""
+        out = {"all_fp8": [], "mostly_tq3": [], "mixed": []}
+        for r in range(self.n):
+            t = self.tiers(r)
+            stale = sum(1 for x in t if x == S)
+            if stale == 0:
+                out["all_fp8"].append(r)
+            elif stale >= 0.98 * len(t):
+                out["mostly_tq3"].append(r)
+            else:
+                out["mixed"].append(r)
+        return out
+
     # ------------------------------------------------------------------ data
     def _gen(self, device, *key) -> torch.Generator:
         g = torch.Generator(device=device)

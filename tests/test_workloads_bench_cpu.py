@@ -77,4 +77,4 @@ def test_bench_reference_arm_prints_one_json_line():
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in d, key
     assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["config"]["workload"].startswith("cfg2")
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["config"]["workload"].startswith("cfg5")
