@@ -194,8 +194,11 @@ struct mkv_pool {
   uint64_t generation = 1;
   uint64_t signs[4] = {0, 0, 0, 0};
   Lut lut{};
-  // staging
-  Staging st_plan, st_append, st_demote;
+  // staging: two plan buffers, so that building a plan never waits for the
+  // previous plan's upload (the device plan region is overwritten in stream
+  // order, after the kernels that read it)
+  Staging st_plan[2], st_append, st_demote;
+  int plan_buf = 0;
   // plan cache
   uint64_t plan_gen = 0;
   std::vector<int32_t> plan_ids;
@@ -334,12 +337,15 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 // block and per piece, in units of one TQ3 token.  Fitted to per-CTA times of
 // the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.31 us of CTA
 // time, a 16-token FP8 block ~0.25 us, a piece ~4 us (its end-of-piece merge
-// and the warps' drift before it).
-constexpr double kCostTq3Token = 1.0;
-constexpr double kCostFp8Token = 1.45;
-constexpr double kCostBlock = 8.0;
-constexpr double kCostPiece = 540.0;
-constexpr double kShortRoundBase = 0.4;  // a round with one busy warp costs 0.4 + 0.6/12 of a full one
+// and the warps' drift before it).  The planner works in integers, 1/100 of
+// these units, so that its split is exact: a block costs
+//   (20 per TQ3 token or 29 per FP8 token + 160) / 20 units,
+// a round of n <= 12 blocks its slowest block times 12 (0.4 + 0.6 n / 12) =
+// (24 + 3 n) / 5, and a piece 540.
+constexpr int64_t kCostTq3Token = 20;    // 1.0 x 20
+constexpr int64_t kCostFp8Token = 29;    // 1.45 x 20
+constexpr int64_t kCostBlock = 160;      // 8 x 20
+constexpr int64_t kCostPiece = 54000;    // 540 x 100
 constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
 constexpr int kPlanRecord = 9;           // ints per split in mkv_plan_decode's output
 
@@ -401,112 +407,147 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   // Blocks: an FP8 block is kFp8Blk tokens and a TQ3 block kTq3Blk tokens
   // of one page; a group's blocks are numbered page by page, bpp = P / bt per
   // page, up to the last valid token (a block past a page's valid tokens is
-  // empty and only costs its overhead).
-  struct Blk {
-    int group, index, tokens;
-  };
-  std::vector<Blk> blocks;
-  {
-    size_t total = 0;
-    for (const Group& g : groups) total += size_t(g.nentry) * (P / (g.fmt ? kTq3Blk : kFp8Blk));
-    blocks.reserve(total);
-  }
-  for (int gi = 0; gi < int(groups.size()); ++gi) {     // page by page: no division per block
-    const Group& g = groups[gi];
-    const int bt = g.fmt ? kTq3Blk : kFp8Blk;
-    const int bpp = P / bt;
-    const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
-    const int nblk = (g.nentry - 1) * bpp + (last_nv + bt - 1) / bt;
-    int k = 0;
-    for (int pg = 0; pg < g.nentry && k < nblk; ++pg) {
-      const int nv_page = entries[g.entry0 + pg].nvalid;
-      for (int j = 0; j < bpp && k < nblk; ++j, ++k) blocks.push_back({gi, k, std::max(0, std::min(bt, nv_page - j * bt))});
-    }
-  }
-  auto cost = [&](const Blk& b) {
-    return b.tokens * (groups[b.group].fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
-  };
+  // empty and only costs its overhead).  Only a group's last page can be
+  // partial, so a block's tokens never increase along the group.
   // Rounds: runs of up to kDecWarps consecutive blocks of one group, from the
   // group's first block on.  A CTA's warps take one round together, so a cut
   // inside a group falls only between rounds and every warp of a piece gets
   // the same number of blocks (one fewer for some in a group's last round).
-  // A round costs its slowest block on every warp; a short round, with warps
-  // idle, runs its blocks faster and is priced between the two.
-  struct Round {
-    int group, first, nblk;
-    double cost;
+  // A round costs its slowest block -- its first -- on every warp; a short
+  // round, with warps idle, runs its blocks faster and is priced between the
+  // two.  All of a group's rounds but its last one or two are alike, so the
+  // rounds are kept as runs of equal rounds.
+  const int ng = int(groups.size());
+  std::vector<int> g_nblk(ng), g_round0(ng + 1, 0);
+  auto blk_tokens = [&](const Group& g, int k) {
+    const int bt = g.fmt ? kTq3Blk : kFp8Blk, bpp = P / bt;
+    const int full = (g.nentry - 1) * bpp;
+    if (k < full) return bt;
+    return std::max(0, std::min(bt, int(entries[g.entry0 + g.nentry - 1].nvalid) - (k - full) * bt));
   };
-  std::vector<Round> rounds;
-  for (size_t i = 0; i < blocks.size();) {
-    const int g = blocks[i].group;
-    size_t j = i;
-    double worst = 0.0;
-    while (j < blocks.size() && blocks[j].group == g && int(j - i) < kDecWarps) worst = std::max(worst, cost(blocks[j++]));
-    const double busy = double(j - i) / kDecWarps;
-    rounds.push_back({g, int(i), int(j - i), worst * kDecWarps * (kShortRoundBase + (1.0 - kShortRoundBase) * busy)});
-    i = j;
+  auto round_cost = [&](const Group& g, int r, int nblk) {
+    const int n = std::min(kDecWarps, nblk - r * kDecWarps);
+    const int64_t worst = blk_tokens(g, r * kDecWarps) * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
+    return worst * (24 + 3 * int64_t(n));
+  };
+  struct Run {
+    int group, first, count;   // rounds [first, first + count) in the global round order
+    int64_t cost;              // cost of each of its rounds
+  };
+  std::vector<Run> runs;
+  runs.reserve(size_t(ng) * 3);
+  int64_t total_blocks = 0;
+  for (int gi = 0; gi < ng; ++gi) {
+    const Group& g = groups[gi];
+    const int bt = g.fmt ? kTq3Blk : kFp8Blk;
+    const int nblk = (g.nentry - 1) * (P / bt) + (entries[g.entry0 + g.nentry - 1].nvalid + bt - 1) / bt;
+    const int nround = (nblk + kDecWarps - 1) / kDecWarps;
+    g_nblk[gi] = nblk;
+    g_round0[gi + 1] = g_round0[gi] + nround;
+    total_blocks += nblk;
+    // rounds [0, uniform) hold 12 blocks each and start with a full block
+    const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
+    const int full_blocks = std::min(nblk, (g.nentry - 1) * (P / bt) + last_nv / bt);
+    const int uniform = std::min(nblk / kDecWarps, (full_blocks + kDecWarps - 1) / kDecWarps);
+    if (uniform > 0) runs.push_back({gi, g_round0[gi], uniform, round_cost(g, 0, nblk)});
+    for (int r = uniform; r < nround; ++r) {
+      const int64_t c = round_cost(g, r, nblk);
+      if (!runs.empty() && runs.back().group == gi && runs.back().cost == c)
+        ++runs.back().count;
+      else
+        runs.push_back({gi, g_round0[gi] + r, 1, c});
+    }
   }
+  const int nrounds = g_round0[ng];
   // one CTA per SM at most, each with at least kMinBlocksPerCta blocks
   const int max_cta = int(std::max<int64_t>(
-      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), int64_t(blocks.size()) / kMinBlocksPerCta})));
+      1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), total_blocks / kMinBlocksPerCta})));
   // Contiguous split of the rounds into at most max_cta CTAs that minimises
   // the largest CTA cost, a piece costing kCostPiece on top of its rounds (its
   // end-of-piece merge): the greedy fill below needs the fewest CTAs for a
-  // given bound, so a bisection on the bound finds the smallest feasible one.
-  auto fill = [&](double bound, std::vector<int>* starts) {
+  // given bound, so a bisection on the (integer) bound finds the smallest one
+  // that fits.  The fill takes a run of equal rounds in O(1) per CTA it opens.
+  auto fill = [&](int64_t bound, std::vector<int>* starts) {
     int n_cta = 0, last_group = -1;
-    double acc = 0.0;
-    for (int r = 0; r < int(rounds.size()); ++r) {
-      const double add = rounds[r].cost + (rounds[r].group != last_group ? kCostPiece : 0.0);
+    int64_t acc = 0;
+    for (const Run& rn : runs) {
+      int left = rn.count, at = rn.first;
+      // the run's first round (a new group adds a piece)
+      const int64_t add = rn.cost + (rn.group != last_group ? kCostPiece : 0);
       if (n_cta == 0 || acc + add > bound) {
         ++n_cta;
-        if (starts) starts->push_back(r);
-        acc = kCostPiece + rounds[r].cost;
+        if (starts) starts->push_back(at);
+        acc = kCostPiece + rn.cost;
       } else {
         acc += add;
       }
-      last_group = rounds[r].group;
+      last_group = rn.group;
+      --left;
+      ++at;
+      while (left > 0) {
+        const int64_t fit = std::min<int64_t>(left, acc + rn.cost <= bound ? (bound - acc) / rn.cost : 0);
+        acc += fit * rn.cost;
+        left -= int(fit);
+        at += int(fit);
+        if (left > 0) {          // a new CTA takes the next round
+          ++n_cta;
+          if (starts) starts->push_back(at);
+          acc = kCostPiece + rn.cost;
+          --left;
+          ++at;
+        }
+      }
     }
     return n_cta;
   };
-  double lo = 0.0, hi = 0.0;
-  for (const Round& r : rounds) {
-    lo = std::max(lo, kCostPiece + r.cost);
-    hi += kCostPiece + r.cost;
+  int64_t lo = 0, hi = 0;
+  for (const Run& rn : runs) {
+    lo = std::max(lo, kCostPiece + rn.cost);
+    hi += (kCostPiece + rn.cost) * rn.count;
   }
   if (fill(lo, nullptr) > max_cta) {
-    while (hi - lo > 1e-4 * hi) {
-      const double mid = 0.5 * (lo + hi);
+    // the smallest feasible bound: fill(hi) fits, fill(lo) does not
+    while (hi - lo > 1) {
+      const int64_t mid = lo + (hi - lo) / 2;
       (fill(mid, nullptr) <= max_cta ? hi : lo) = mid;
     }
     lo = hi;
   }
   std::vector<int> starts;
-  const int ncta = rounds.empty() ? 0 : fill(lo, &starts);
-  starts.push_back(int(rounds.size()));
+  const int ncta = nrounds == 0 ? 0 : fill(lo, &starts);
+  starts.push_back(nrounds);
+  // group of a global round index
+  auto group_of = [&](int r) { return int(std::upper_bound(g_round0.begin(), g_round0.end(), r) - g_round0.begin()) - 1; };
+  auto tokens_in = [&](const Group& g, int b0, int b1) {   // valid tokens of blocks [b0, b1)
+    int64_t t = 0;
+    const int bt = g.fmt ? kTq3Blk : kFp8Blk, full = (g.nentry - 1) * (P / bt);
+    if (b0 < full) t += int64_t(std::min(b1, full) - b0) * bt;
+    for (int k = std::max(b0, full); k < b1; ++k) t += blk_tokens(g, k);
+    return int32_t(t);
+  };
   std::vector<Segment> segs;
   std::vector<int32_t> seg_entry, seg_tokens;   // first page entry and valid tokens of each piece
   std::vector<int32_t> cta_seg(ncta + 1, 0);
   for (int c = 0; c < ncta; ++c) {
     cta_seg[c] = int(segs.size());
-    for (int r = starts[c]; r < starts[c + 1]; ++r) {
-      const Round& rd = rounds[r];
-      if (r == starts[c] || rd.group != rounds[r - 1].group) {
-        const Group& g = groups[rd.group];
-        const int blk = blocks[rd.first].index;
-        Segment sg{};
-        sg.fmt = g.fmt;
-        sg.b = g.b;
-        sg.kvh = g.kvh;
-        sg.entry0 = g.entry0;
-        sg.group = rd.group;
-        sg.blk = blk;
-        segs.push_back(sg);
-        seg_entry.push_back(g.entry0 + blk / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
-        seg_tokens.push_back(0);
-      }
-      segs.back().nblk += rd.nblk;
-      for (int k = rd.first; k < rd.first + rd.nblk; ++k) seg_tokens.back() += blocks[k].tokens;
+    for (int r = starts[c]; r < starts[c + 1];) {
+      const int gi = group_of(r);
+      const Group& g = groups[gi];
+      const int r_end = std::min(starts[c + 1], g_round0[gi + 1]);
+      const int b0 = (r - g_round0[gi]) * kDecWarps;
+      const int b1 = std::min(g_nblk[gi], (r_end - g_round0[gi]) * kDecWarps);
+      Segment sg{};
+      sg.fmt = g.fmt;
+      sg.b = g.b;
+      sg.kvh = g.kvh;
+      sg.entry0 = g.entry0;
+      sg.group = gi;
+      sg.blk = b0;
+      sg.nblk = b1 - b0;
+      segs.push_back(sg);
+      seg_entry.push_back(g.entry0 + b0 / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
+      seg_tokens.push_back(tokens_in(g, b0, b1));
+      r = r_end;
     }
   }
   cta_seg[ncta] = int(segs.size());
@@ -577,14 +618,16 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   mp.G = p->G;
   std::memcpy(mp.signs, p->signs, sizeof mp.signs);
   if (!upload) return MKV_OK;
-  mkv_status st = staging_acquire(p->st_plan);
+  Staging& sp = p->st_plan[p->plan_buf];
+  mkv_status st = staging_acquire(sp);
   if (st != MKV_OK) return st;
-  uint8_t* h = static_cast<uint8_t*>(p->st_plan.host);
+  p->plan_buf ^= 1;
+  uint8_t* h = static_cast<uint8_t*>(sp.host);
   std::memcpy(h + L.entries, entries.data(), entries.size() * sizeof(PageEntry));
   std::memcpy(h + L.groups, groups.data(), groups.size() * sizeof(Group));
   std::memcpy(h + L.segs, segs.data(), segs.size() * sizeof(Segment));
   std::memcpy(h + L.merge, md.data(), md.size() * sizeof(MergeDesc));
-  return staging_upload(p->st_plan, p->plan_region, L.total, stream);
+  return staging_upload(sp, p->plan_region, L.total, stream);
 }
 
 // The decode plan of (ids, nq query tokens per request), rebuilt only when
@@ -714,9 +757,10 @@ mkv_status mkv_pool_create(const mkv_pool_config* cfg, void* device_buf, size_t 
       delete p;
       return cuda_fail(e, "cudaMemsetAsync");
     }
-    if ((st = staging_alloc(p->st_plan, S.plan)) != MKV_OK || (st = staging_alloc(p->st_append, S.append)) != MKV_OK ||
-        (st = staging_alloc(p->st_demote, S.demote)) != MKV_OK) {
-      staging_free(p->st_plan);
+    if ((st = staging_alloc(p->st_plan[0], S.plan)) != MKV_OK || (st = staging_alloc(p->st_plan[1], S.plan)) != MKV_OK ||
+        (st = staging_alloc(p->st_append, S.append)) != MKV_OK || (st = staging_alloc(p->st_demote, S.demote)) != MKV_OK) {
+      staging_free(p->st_plan[0]);
+      staging_free(p->st_plan[1]);
       staging_free(p->st_append);
       staging_free(p->st_demote);
       delete p;
@@ -730,7 +774,8 @@ mkv_status mkv_pool_create(const mkv_pool_config* cfg, void* device_buf, size_t 
 mkv_status mkv_pool_destroy(mkv_pool* p) {
   if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
   if (!p->host_only) {
-    staging_free(p->st_plan);
+    staging_free(p->st_plan[0]);
+    staging_free(p->st_plan[1]);
     staging_free(p->st_append);
     staging_free(p->st_demote);
   }

@@ -400,3 +400,103 @@ def test_missing_library_fails_loudly(mkv, monkeypatch):
         mkv.binding.lib()
     with pytest.raises(ImportError):
         _host_pool(mkv)
+
+
+def _int_rounds(layouts, P, H=4):
+    """Per-round integer costs of the planner's model (1/100 of the float
+    model above): a block costs tokens x (20 TQ3 | 29 FP8) + 160, a round of
+    n blocks its slowest block x (24 + 3 n), a piece 54000.  One entry per
+    round, in the planner's group order: (group key, cost, blocks)."""
+    rounds = []
+    for b, (n, tiers) in enumerate(layouts):
+        nv = [min(P, n - i * P) for i in range(len(tiers))]
+        for kvh in range(H):
+            for fmt in (3, 1):
+                pages = [nv[i] for i, t in enumerate(tiers) if (t == 3) == (fmt == 3)]
+                if not pages:
+                    continue
+                bt, rate = (32, 20) if fmt == 3 else (16, 29)
+                bpp = P // bt
+                nblk = (len(pages) - 1) * bpp + -(-pages[-1] // bt)
+                costs = [max(0, min(bt, pages[k // bpp] - (k % bpp) * bt)) * rate + 160 for k in range(nblk)]
+                for r in range(0, nblk, 12):
+                    c = costs[r:r + 12]
+                    rounds.append(((b, kvh, fmt), max(c) * (24 + 3 * len(c)), len(c)))
+    return rounds
+
+
+def _reference_split(rounds, max_cta):
+    """The plain split the planner computes: a greedy fill round by round
+    (a piece adds 54000 when the group changes) and the smallest integer
+    bound that fits in max_cta CTAs.  Returns the CTAs' first rounds."""
+    piece = 54000
+
+    def fill(bound, starts=None):
+        n_cta, acc, last = 0, 0, None
+        for i, (key, c, _) in enumerate(rounds):
+            add = c + (piece if key != last else 0)
+            if n_cta == 0 or acc + add > bound:
+                n_cta += 1
+                if starts is not None:
+                    starts.append(i)
+                acc = piece + c
+            else:
+                acc += add
+            last = key
+        return n_cta
+    lo = max(piece + c for _, c, _ in rounds)
+    hi = sum(piece + c for _, c, _ in rounds)
+    if fill(lo) > max_cta:
+        while hi - lo > 1:
+            mid = lo + (hi - lo) // 2
+            if fill(mid) <= max_cta:
+                hi = mid
+            else:
+                lo = mid
+        lo = hi
+    starts = []
+    fill(lo, starts)
+    return starts
+
+
+def test_plan_split_matches_per_round_reference(mkv):
+    """The planner takes runs of equal rounds in O(1) per CTA; on all five
+    workloads its split must equal the plain round-by-round algorithm's."""
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import make_pool
+    for name in ("cfg1", "cfg2", "cfg3", "cfg4", "cfg5"):
+        w = workloads.make(name)
+        w.num_layers = 1
+        pool = make_pool(w, host_only=True, extra_steps=0)
+        layouts = []
+        for r in range(w.n):
+            pool.extend([r], [w.lengths[r]])
+            tiers = w.tiers(r)
+            for pg, t in enumerate(tiers):
+                if t == 2:
+                    pool.set_tier(r, pg, 2)
+            stale = [pg for pg, t in enumerate(tiers) if t == 3]
+            if stale:
+                pool.demote([r] * len(stale), stale)
+            layouts.append((w.lengths[r], tiers))
+        plan = pool.plan(list(range(w.n)))
+        rounds = _int_rounds(layouts, w.P)
+        max_cta = max(1, min(152, sum(nb for *_, nb in rounds) // 24))
+        starts = _reference_split(rounds, max_cta) + [len(rounds)]
+        # expected pieces: (b, kvh, tier, cta, first block, blocks)
+        first = {}
+        for i, (key, _, _) in enumerate(rounds):
+            first.setdefault(key, i)
+        exp = []
+        for c in range(len(starts) - 1):
+            i = starts[c]
+            while i < starts[c + 1]:
+                key = rounds[i][0]
+                j = i
+                while j < starts[c + 1] and rounds[j][0] == key:
+                    j += 1
+                blk0 = 12 * (i - first[key])
+                exp.append((key[0], key[1], key[2], c, blk0, sum(nb for *_, nb in rounds[i:j])))
+                i = j
+        got = [(b, kvh, tier, cta, blk0, nblk) for b, kvh, tier, _, _, _, cta, blk0, nblk in plan]
+        assert got == exp, name
