@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="also time the oracle over a full layer-step (every request and kv head of layer 0); "
+                         "minutes on the larger workloads, so off by default")
     ap.add_argument("--requests", default=None,
                     help="comma-separated request indices: run a reduced-size slice of the workload "
                          "(same shapes; e.g. for a profiler capture)")
@@ -226,7 +229,27 @@ def cpu_threads():
             return int(max(n))
     except Exception:
         pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
     return os.cpu_count()
+
+
+def oracle_layer_step(w, pages_by_req, q):
+    """Time the oracle's streaming decode over every (request, kv head) of one
+    layer: one full layer-step.  q: [n, Hq, D] (the GPU step's query).
+    Returns (GB/s, bytes, seconds)."""
+    import numpy as np
+    from oracle.paged import TIER_STALE, decode_attention_streaming
+    t0 = time.perf_counter()
+    nbytes = 0
+    for r, pages in pages_by_req.items():
+        decode_attention_streaming(np.asarray(q[r], dtype=np.float64), pages, w.P, w.Hkv, w.D, 99)
+        for t, _, n in pages:
+            nbytes += w.Hkv * n * (ROW_BYTES["tq3"] if t == TIER_STALE else ROW_BYTES["fp8"])
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, nbytes, dt
 
 
 # ----------------------------------------------------------------- reference arm
@@ -465,6 +488,17 @@ def run_mkv(args):
         gbs, nb, dt, desc = oracle_sample(w, pages_by_req, args.cpu_seconds)
         cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_threads(), "kind": "oracle", "sample": desc,
                "seconds": dt}
+        if args.cpu_full:
+            for r in range(len(pages_by_req), w.n):
+                pages_by_req[r] = []
+                for p in range(pool.seq_info(r)[1]):
+                    b, t, nv = pool.export_page(0, r, p)
+                    pages_by_req[r].append((t, np.frombuffer(b, dtype=np.uint8).copy(), nv))
+            qf = ins[args.warmup + args.steps - 1][0][2].float().cpu().numpy()
+            fg, fb, fdt = oracle_layer_step(w, pages_by_req, qf)
+            cpu["layer_step"] = {"value": fg, "unit": "GB/s", "seconds": fdt, "bytes": fb,
+                                 "us_per_layer_step": fdt * 1e6, "cores": cpu_threads(),
+                                 "sample": f"full layer-step: every request and kv head of layer 0 of {w.name}"}
     if rank != 0:
         return
     value = kv_job / (t_max * 1e-3) / 1e9
