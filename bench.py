@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--requests", default=None,
                     help="comma-separated request indices: run a reduced-size slice of the workload "
                          "(same shapes; e.g. for a profiler capture)")
+    ap.add_argument("--graph", action="store_true",
+                    help="run each step as one recorded CUDA graph over all layers (mkv_step_graph_*): a "
+                         "separate line, on fixed input buffers filled by one copy per step")
     ap.add_argument("--nq", type=int, default=1,
                     help="query tokens per request and step (> 1: the multi-query path, a separate line)")
     return ap.parse_args()
@@ -366,10 +369,46 @@ def run_mkv(args):
     # shape, so the last layer's launches stand for all of them.
     TIMED_LAYER = L - 1
 
+    graph = [None]
+    if args.graph:
+        # every step's inputs (all layers' q, k, v) packed in one device
+        # buffer; the graph reads fixed views of `gbuf`, filled by one copy
+        def nbytes(t):
+            return t.numel() * t.element_size()
+        seg = lambda nb: (nb + 255) // 256 * 256
+        k0, v0, q0 = ins[0][0]
+        lay = seg(nbytes(q0)) + seg(nbytes(k0)) + seg(nbytes(v0))
+        packed = []
+        for srow in ins:
+            buf = torch.empty(L * lay, dtype=torch.uint8, device=dev)
+            for layer, (k, v, q) in enumerate(srow):
+                off = layer * lay
+                for t in (q, k, v):
+                    buf[off:off + nbytes(t)].copy_(t.contiguous().view(torch.uint8).reshape(-1))
+                    off += seg(nbytes(t))
+            packed.append(buf)
+        gbuf = torch.empty(L * lay, dtype=torch.uint8, device=dev)
+        gviews = []
+        for layer in range(L):
+            off = layer * lay
+            gq = gbuf[off:off + nbytes(q0)].view(q0.dtype).view(q0.shape)
+            off += seg(nbytes(q0))
+            gk = gbuf[off:off + nbytes(k0)].view(k0.dtype).view(k0.shape)
+            off += seg(nbytes(k0))
+            gv = gbuf[off:off + nbytes(v0)].view(v0.dtype).view(v0.shape)
+            gviews.append((gq, gk, gv))
+
     def step(s, ev_pair=None, bytes_acc=None):
         stepper.pre_step()
         if bytes_acc is not None:
             bytes_acc.append(kv_bytes_now(pool, P, L))
+        if args.graph:
+            gbuf.copy_(packed[s])
+            if graph[0] is None:
+                graph[0] = pool.step_graph(stepper.ids, [x[0] for x in gviews], [o for o, _ in outs],
+                                           [l_ for _, l_ in outs], k=[x[1] for x in gviews], v=[x[2] for x in gviews])
+            graph[0].launch()
+            return
         for layer in range(L):
             k, v, q = ins[s][layer]
             if ev_pair is not None and layer == TIMED_LAYER:
@@ -411,8 +450,13 @@ def run_mkv(args):
     kv_total = sum(b for b, _ in bytes_acc)
     t_max, kv_job = job_totals(ms, kv_total, world, dev)
     ctx_total = sum(c for _, c in bytes_acc)
-    kernel_ms = [a.elapsed_time(b) for a, b in ev]
     kernel_bytes = [b / L for b, _ in bytes_acc]
+    if args.graph:
+        # no events can sit between the kernels of a graph: the whole step's
+        # time per layer stands in for the decode kernel's (an upper bound)
+        kernel_ms = [ms / args.steps / L] * args.steps
+    else:
+        kernel_ms = [a.elapsed_time(b) for a, b in ev]
     achieved = (sum(kernel_bytes) / len(kernel_bytes)) / (sum(kernel_ms) / len(kernel_ms) * 1e-3) / 1e9
     peak, peak_src = measured_peaks()
     # per layer and step: the decode kernel (with the fused append) and the merge
@@ -513,6 +557,8 @@ def run_mkv(args):
                    "context_tokens": int(ctx_total / max(1, len(bytes_acc))),
                    "l2": "inputs larger than L2: per-layer KV working set cycled over 16 layers",
                    "parallelism": f"replicas x{world}"},
+        "path": "step graph (mkv_step_graph_launch, one launch per step)" if args.graph else
+                "per-layer calls (mkv_append_decode)",
         "kv_gbs": value,
         "ctx_tokens_per_s_per_layer": world * (ctx_total / len(bytes_acc)) / per_layer_step_s,
         "us_per_layer_step": per_layer_step_s * 1e6,
@@ -521,7 +567,9 @@ def run_mkv(args):
                      "traffic": committed_traffic(w.name, sum(kernel_bytes) / len(kernel_bytes)),
                      "kernel": "mkv_decode_kernel (partial attention)",
                      "peak_source": peak_src, "launches": len(kernel_ms),
-                     "timed_launches": f"layer {TIMED_LAYER} of each timed step (CUDA events on the call's stream)",
+                     "timed_launches": ("whole step / layers (graph launches: no events between kernels)"
+                                        if args.graph else
+                                        f"layer {TIMED_LAYER} of each timed step (CUDA events on the call's stream)"),
                      "avg_launch_us": 1e3 * sum(kernel_ms) / len(kernel_ms)},
         "bytes_per_token_per_tier": {"fp8": 2064 * L, "tq3": 784 * L, "bf16": 4096 * L,
                                      "pool_kv_bytes_per_live_token": st.kv_bytes_per_live_token,

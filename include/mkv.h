@@ -374,6 +374,43 @@ mkv_status mkv_decode_attention_noalloc(mkv_pool* pool, int32_t layer, int32_t n
                                         const void* q, mkv_dtype dtype, float* out, float* lse,
                                         mkv_stream_t stream);
 
+/* ------------------------------------------------------------ step graph
+ * One decode step over every layer as a single CUDA graph launch.  The
+ * pages describe one query token per request and step, attended over the
+ * whole paged cache layer by layer (Minima-KV abstract, mlsanity.com paper
+ * page); a serving loop repeats exactly that launch sequence every step, so
+ * it can be recorded once and replayed.  The graph holds, for each layer l in
+ * order, what mkv_append_decode (k, v given) or mkv_decode_attention (k, v
+ * NULL) would enqueue: the partial-attention kernel (with the fused append)
+ * and the LSE merge.
+ *
+ * mkv_step_graph_create: records the graph for the batch `seq_ids[0..n)` on
+ * caller-owned device buffers that stay fixed for the graph's life, one per
+ * layer (arrays of num_layers pointers): q[l] [n, Hq, d] (q_dtype), k[l],
+ * v[l] [n, Hkv, d] (kv_dtype) or k = v = NULL, out[l] [n, Hq, d] fp32,
+ * lse[l] [n, Hq] fp32.  Plans the batch and uploads the plan on `stream`;
+ * the recording itself runs on a private stream and executes nothing.
+ * The kernels read their per-CTA piece ranges from the pool's device plan,
+ * so one recording serves every later plan of the same batch.  Errors: as
+ * mkv_append_decode / mkv_decode_attention, plus MKV_ERR_UNSUPPORTED on a
+ * host-only pool and MKV_ERR_CUDA when capture or instantiation fails.
+ *
+ * mkv_step_graph_launch: one step.  The caller first writes the step's
+ * inputs into the fixed buffers and makes the pool's host updates
+ * (mkv_seq_extend, mkv_demote_pages) as for the per-layer calls.  The call
+ * re-plans if the pool changed (host work, then an upload in stream order)
+ * and launches the graph on `stream`; asynchronous like the per-layer calls.
+ * The batch must still be valid (same ids, none released).
+ *
+ * mkv_step_graph_destroy: frees the graph (not the buffers).  A pool must
+ * outlive its graphs. */
+typedef struct mkv_step_graph mkv_step_graph;
+mkv_status mkv_step_graph_create(mkv_pool* pool, int32_t n, const int32_t* seq_ids, const void* const* q,
+                                 const void* const* k, const void* const* v, mkv_dtype q_dtype, mkv_dtype kv_dtype,
+                                 float* const* out, float* const* lse, mkv_stream_t stream, mkv_step_graph** graph);
+mkv_status mkv_step_graph_launch(mkv_step_graph* graph, mkv_stream_t stream);
+mkv_status mkv_step_graph_destroy(mkv_step_graph* graph);
+
 /* Thread-local text of the last error (never NULL). */
 const char* mkv_last_error(void);
 

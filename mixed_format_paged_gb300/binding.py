@@ -29,6 +29,7 @@ EXPORTED = [
     "mkv_seq_info", "mkv_page_info", "mkv_append_tokens", "mkv_set_tier", "mkv_demote_pages",
     "mkv_decode_attention", "mkv_decode_attention_multi", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
     "mkv_plan_decode", "mkv_plan_decode_multi", "mkv_check_device_errors", "mkv_selftest_wait_timeout", "mkv_inject_plan_slot", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
+    "mkv_step_graph_create", "mkv_step_graph_launch", "mkv_step_graph_destroy",
 ]
 
 
@@ -98,6 +99,11 @@ def lib() -> ctypes.CDLL:
         "mkv_selftest_wait_timeout": [P, ctypes.c_int64, P],
         "mkv_inject_plan_slot": [P, I32, I32, P],
         "mkv_set_timing_events": [P, P, P],
+        "mkv_step_graph_create": [P, I32, I32P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P),
+                                  ctypes.c_int, ctypes.c_int, ctypes.POINTER(P), ctypes.POINTER(P), P,
+                                  ctypes.POINTER(P)],
+        "mkv_step_graph_launch": [P, P],
+        "mkv_step_graph_destroy": [P],
         "mkv_last_error": [],
         "mkv_version": [],
     }
@@ -229,6 +235,34 @@ def mkv_append_decode(pool, layer: int, seq_ids, k, v, kv_dtype: int, q, q_dtype
     a, n = _i32(seq_ids)
     check(lib().mkv_append_decode(pool, layer, n, a, _ptr(k), _ptr(v), kv_dtype, _ptr(q), q_dtype, _ptr(out),
                                   _ptr(lse), _stream(stream)), "mkv_append_decode")
+
+
+def _ptr_array(xs):
+    """Array of device pointers (one per layer), or NULL for None."""
+    if xs is None:
+        return None
+    arr = (ctypes.c_void_p * len(xs))(*[_ptr(x).value for x in xs])
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), arr
+
+
+def mkv_step_graph_create(pool, seq_ids, q, k, v, q_dtype: int, kv_dtype: int, out, lse, stream=None):
+    """q, k, v, out, lse: one device buffer per layer (k = v = None: no fused
+    append).  Returns the graph handle."""
+    a, n = _i32(seq_ids)
+    keep = [_ptr_array(x) for x in (q, k, v, out, lse)]
+    args = [x[0] if x is not None else None for x in keep]
+    g = ctypes.c_void_p()
+    check(lib().mkv_step_graph_create(pool, n, a, args[0], args[1], args[2], q_dtype, kv_dtype, args[3], args[4],
+                                      _stream(stream), ctypes.byref(g)), "mkv_step_graph_create")
+    return g
+
+
+def mkv_step_graph_launch(graph, stream=None) -> None:
+    check(lib().mkv_step_graph_launch(graph, _stream(stream)), "mkv_step_graph_launch")
+
+
+def mkv_step_graph_destroy(graph) -> None:
+    check(lib().mkv_step_graph_destroy(graph), "mkv_step_graph_destroy")
 
 
 def mkv_dequantize_pages(pool, layer: int, seq: int, page0: int, npages: int, k_out, v_out, out_dtype: int,

@@ -221,7 +221,7 @@ struct mkv_pool {
 namespace {
 
 struct PlanLayout {
-  size_t entries, groups, segs, merge, total;
+  size_t entries, groups, segs, merge, heads, total;
 };
 
 PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
@@ -235,6 +235,8 @@ PlanLayout plan_layout(int entry_cap, int chunk_cap, int max_batch, int Hkv) {
   off += align256(size_t(chunk_cap) * sizeof(Segment));
   L.merge = off;
   off += align256(size_t(max_batch) * Hkv * sizeof(MergeDesc));
+  L.heads = off;                         // per-CTA piece ranges (graph launches)
+  off += align256(size_t(kMaxCtas + 1) * sizeof(int32_t));
   L.total = off;
   return L;
 }
@@ -627,6 +629,10 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   std::memcpy(h + L.groups, groups.data(), groups.size() * sizeof(Group));
   std::memcpy(h + L.segs, segs.data(), segs.size() * sizeof(Segment));
   std::memcpy(h + L.merge, md.data(), md.size() * sizeof(MergeDesc));
+  {
+    int32_t* hd = reinterpret_cast<int32_t*>(h + L.heads);
+    for (int i = 0; i <= kMaxCtas; ++i) hd[i] = cta_seg[std::min(i, ncta)];   // CTAs past ncta: no pieces
+  }
   return staging_upload(sp, p->plan_region, L.total, stream);
 }
 
@@ -997,8 +1003,16 @@ mkv_status mkv_demote_pages(mkv_pool* p, int32_t n, const int32_t* ids, const in
 // Enqueue the decode kernel (with the fused append when k is non-NULL) and
 // the merge for the pool's current plan; partial states go to `part`.
 mkv_status enqueue_decode(mkv_pool* p, int32_t layer, const void* q, mkv_dtype q_dtype, float* part, const void* k,
-                          const void* v, mkv_dtype kv_dtype, float* out, float* lse, cudaStream_t s) {
+                          const void* v, mkv_dtype kv_dtype, float* out, float* lse, cudaStream_t s,
+                          bool fixed_params = false) {
   DecodeParams dp = p->plan_params;
+  if (fixed_params) {
+    // parameters that stay valid for every later plan: the CTAs read their
+    // piece ranges from the plan region, and the grid is one CTA per SM
+    const PlanLayout L = plan_layout(p->entry_cap, p->chunk_cap, effective_batch(p->cfg), p->cfg.num_kv_heads);
+    dp.heads = reinterpret_cast<const int32_t*>(p->plan_region + L.heads);
+    dp.n_ctas = std::min(p->n_sm, kMaxCtas);
+  }
   dp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
   dp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
   dp.q = q;
@@ -1108,6 +1122,120 @@ mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_
   if (p->plan_injected) p->plan_gen = 0;   // the fused append writes through the plan's slots: replan
   if ((st = ensure_plan(p, n, ids, 1, true, s)) != MKV_OK) return st;
   return enqueue_decode(p, layer, q, q_dtype, p->workspace, k, v, kv_dtype, out, lse, s);
+}
+
+// ------------------------------------------------------------------ step graph
+struct mkv_step_graph {
+  mkv_pool* pool = nullptr;
+  std::vector<int32_t> ids;
+  bool append = false;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+mkv_status mkv_step_graph_create(mkv_pool* p, int32_t n, const int32_t* ids, const void* const* q,
+                                 const void* const* k, const void* const* v, mkv_dtype q_dtype, mkv_dtype kv_dtype,
+                                 float* const* out, float* const* lse, mkv_stream_t stream, mkv_step_graph** graph) {
+  if (!p || !graph) return fail(MKV_ERR_INVALID_ARGUMENT, "pool or graph is NULL");
+  *graph = nullptr;
+  if (p->host_only) return fail(MKV_ERR_UNSUPPORTED, "host-only pool: no graph");
+  if ((q_dtype != MKV_F32 && q_dtype != MKV_BF16) || (kv_dtype != MKV_F32 && kv_dtype != MKV_BF16))
+    return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if (n == 0) return fail(MKV_ERR_INVALID_ARGUMENT, "empty batch");
+  const int L = p->cfg.num_layers;
+  if (!q || !out || !lse || (!k) != (!v)) return fail(MKV_ERR_INVALID_ARGUMENT, "q/out/lse (or one of k, v) is NULL");
+  for (int l = 0; l < L; ++l)
+    if (!q[l] || !out[l] || !lse[l] || (k && (!k[l] || !v[l])))
+      return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d: a buffer pointer is NULL", l);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (k) {
+    const int P = p->cfg.page_size;
+    for (int i = 0; i < n; ++i) {
+      const SeqRec& sr = p->seqs[ids[i]];
+      if (sr.pages[(sr.len - 1) / P].tier == MKV_TIER_STALE)
+        return fail(MKV_ERR_INVALID_STATE, "sequence %d: the newest token's page is TQ3", ids[i]);
+    }
+  }
+  if (p->plan_injected) p->plan_gen = 0;
+  if ((st = ensure_plan(p, n, ids, 1, true, s)) != MKV_OK) return st;
+  // the kernels' shared-memory limit is a per-device attribute, set outside the capture
+  cudaError_t e = prepare_decode_launch();
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel attribute");
+  auto* g = new mkv_step_graph;
+  g->pool = p;
+  g->ids.assign(ids, ids + n);
+  g->append = k != nullptr;
+  // record on a private stream (the caller's may be the legacy default
+  // stream, which cannot be captured); the recording executes nothing
+  cudaStream_t cap = nullptr;
+  e = cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    delete g;
+    return cuda_fail(e, "cudaStreamCreate");
+  }
+  e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cap);
+    delete g;
+    return cuda_fail(e, "cudaStreamBeginCapture");
+  }
+  void* t_start = p->t_start;
+  void* t_stop = p->t_stop;
+  p->t_start = p->t_stop = nullptr;     // timing events are not part of a graph
+  mkv_status rec = MKV_OK;
+  for (int l = 0; l < L && rec == MKV_OK; ++l)
+    rec = enqueue_decode(p, l, q[l], q_dtype, p->workspace, k ? k[l] : nullptr, k ? v[l] : nullptr, kv_dtype, out[l],
+                         lse[l], cap, true);
+  p->t_start = static_cast<cudaEvent_t>(t_start);
+  p->t_stop = static_cast<cudaEvent_t>(t_stop);
+  e = cudaStreamEndCapture(cap, &g->graph);
+  cudaStreamDestroy(cap);
+  if (rec != MKV_OK || e != cudaSuccess) {
+    if (g->graph) cudaGraphDestroy(g->graph);
+    delete g;
+    return rec != MKV_OK ? rec : cuda_fail(e, "cudaStreamEndCapture");
+  }
+  e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g->graph);
+    delete g;
+    return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  *graph = g;
+  return MKV_OK;
+}
+
+mkv_status mkv_step_graph_launch(mkv_step_graph* g, mkv_stream_t stream) {
+  if (!g) return fail(MKV_ERR_INVALID_ARGUMENT, "graph is NULL");
+  mkv_pool* p = g->pool;
+  const int n = int(g->ids.size());
+  mkv_status st = check_batch(p, n, g->ids.data(), true);
+  if (st != MKV_OK) return st;
+  if (g->append) {
+    const int P = p->cfg.page_size;
+    for (int i = 0; i < n; ++i) {
+      const SeqRec& sr = p->seqs[g->ids[i]];
+      if (sr.pages[(sr.len - 1) / P].tier == MKV_TIER_STALE)
+        return fail(MKV_ERR_INVALID_STATE, "sequence %d: the newest token's page is TQ3", g->ids[i]);
+    }
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->plan_injected) p->plan_gen = 0;
+  // the plan (re-)uploaded here in stream order is what the graph's kernels read
+  if ((st = ensure_plan(p, n, g->ids.data(), 1, true, s)) != MKV_OK) return st;
+  const cudaError_t e = cudaGraphLaunch(g->exec, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+  return MKV_OK;
+}
+
+mkv_status mkv_step_graph_destroy(mkv_step_graph* g) {
+  if (!g) return fail(MKV_ERR_INVALID_ARGUMENT, "graph is NULL");
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+  return MKV_OK;
 }
 
 mkv_status mkv_dequantize_pages(mkv_pool* p, int32_t layer, int32_t seq, int32_t page0, int32_t npages,

@@ -93,7 +93,9 @@ struct DecodeParams {
   float score_scale;               // log2(e) / sqrt(d)
   int32_t append;
   int32_t kv_bf16;
-  // per CTA
+  // per CTA: when `heads` is set (graph launches), CTA i's pieces are
+  // segs[heads[i] .. heads[i + 1]) and cta_seg / first are unused
+  const int32_t* heads;
   int32_t cta_seg[kMaxCtas + 1];   // CTA i's pieces: segs[cta_seg[i] .. cta_seg[i + 1])
   Segment first[kMaxCtas];         // each CTA's first piece (a copy of segs[cta_seg[i]])
 };
@@ -148,6 +150,9 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
 // while the preceding kernel finishes; it waits for that kernel before reading
 // q or writing partial states.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+// Sets the decode kernel's per-device launch attributes (done by launch_decode
+// too); call it before capturing decode launches into a graph.
+cudaError_t prepare_decode_launch();
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s);
 size_t decode_smem_bytes();

@@ -554,6 +554,7 @@ __device__ __forceinline__ Piece piece_of(const Segment& s) {
 }
 // Piece si of this CTA: the first one travels in the kernel parameters.
 __device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
+  if (p.heads) return piece_of(p.segs[si]);
   return si == p.cta_seg[blockIdx.x] ? piece_of(p.first[blockIdx.x]) : piece_of(p.segs[si]);
 }
 
@@ -1081,7 +1082,11 @@ __device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& 
 __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const DecSmem sm = dec_carve(smem);
-  const int s0 = p.cta_seg[blockIdx.x], s1 = p.cta_seg[blockIdx.x + 1];
+  // the CTA's pieces: from the kernel parameters, or (a launch whose
+  // parameters must not change between steps, e.g. in a CUDA graph) from the
+  // plan region in device memory, which is stable while the kernel runs
+  const int s0 = p.heads ? p.heads[blockIdx.x] : p.cta_seg[blockIdx.x];
+  const int s1 = p.heads ? p.heads[blockIdx.x + 1] : p.cta_seg[blockIdx.x + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the merge kernel that follows waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1332,7 +1337,7 @@ cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+cudaError_t prepare_decode_launch() {
   // the shared-memory limit is a per-device attribute: set it once per device
   // (setting it twice from racing threads is harmless)
   static std::atomic<uint64_t> attr_set{0};
@@ -1345,6 +1350,12 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_acq_rel);
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+  cudaError_t e = prepare_decode_launch();
+  if (e != cudaSuccess) return e;
   if (p.n_ctas <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_ctas);

@@ -115,6 +115,15 @@ class MkvPool:
         B.mkv_append_decode(self.handle, layer, seq_ids, k, v, kvd, q, qd, out, lse, self._stream(stream))
         return out, lse
 
+    def step_graph(self, seq_ids, q, out, lse, k=None, v=None, stream=None):
+        """Record one decode step over every layer as a CUDA graph on fixed
+        buffers (lists with one tensor per layer; k = v = None: no fused
+        append).  Returns a StepGraph; its launch() runs one step."""
+        qd = B.MKV_BF16 if q[0].dtype == torch.bfloat16 else B.MKV_F32
+        kvd = B.MKV_BF16 if (k is not None and k[0].dtype == torch.bfloat16) else B.MKV_F32
+        g = B.mkv_step_graph_create(self.handle, seq_ids, q, k, v, qd, kvd, out, lse, self._stream(stream))
+        return StepGraph(self, g, (q, k, v, out, lse))
+
     def dequantize(self, layer: int, seq: int, page0: int, npages: int, dtype=torch.float32, stream=None):
         """Dense K, V [npages * P, H_kv, d] of pages [page0, page0 + npages)."""
         shape = (npages * self.page_size, self.num_kv_heads, self.head_dim)
@@ -147,3 +156,26 @@ class MkvPool:
     def selftest_wait_timeout(self, limit_cycles: int = 2_000_000, stream=None):
         """Enqueue a bounded wait that runs out (see mkv_selftest_wait_timeout)."""
         B.mkv_selftest_wait_timeout(self.handle, limit_cycles, self._stream(stream))
+
+
+class StepGraph:
+    """A recorded decode step (mkv_step_graph_*); keeps its buffers alive."""
+
+    def __init__(self, pool, handle, buffers):
+        self.pool = pool
+        self.handle = handle
+        self.buffers = buffers
+
+    def launch(self, stream=None):
+        B.mkv_step_graph_launch(self.handle, self.pool._stream(stream))
+
+    def close(self):
+        if self.handle is not None:
+            B.mkv_step_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -370,6 +370,79 @@ def test_append_decode_matches_separate_calls(mkv):
         pool.check_device_errors()
 
 
+# ------------------------------------------------------------------ step graph
+@pytest.mark.parametrize("append", [True, False])
+def test_step_graph_matches_per_layer_calls(mkv, append):
+    """mkv_step_graph_*: one recorded launch per step over every layer gives,
+    bit for bit, what the per-layer calls give -- through re-plans (the
+    batch grows every step) and a demotion between steps -- and the oracle
+    agrees with it."""
+    g = torch.Generator().manual_seed(31)
+    L = 3
+    pools = [_small_pool(mkv, P=64, layers=L, fp8=64, tq3=64, maxp=24, seed=79) for _ in range(2)]
+    lens = [64 * 5 + 62, 64 * 3 + 1, 7]
+    data = [[(torch.randn(n, 4, 256, generator=g).to(torch.bfloat16), torch.randn(n, 4, 256, generator=g).to(torch.bfloat16))
+             for _ in range(L)] for n in lens]
+    for pool in pools:
+        for r, n in enumerate(lens):
+            pool.extend([r], [n])
+            for layer in range(L):
+                pool.append(layer, [r], [n], data[r][layer][0].to(DEV), data[r][layer][1].to(DEV))
+        pool.set_tier(0, 0, 2)
+        pool.demote([0, 0, 1], [1, 2, 0])
+    ids = [0, 1, 2]
+    n = len(ids)
+    # fixed buffers of the graph path
+    qb = [torch.empty(n, 24, 256, dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    kb = [torch.empty(n, 4, 256, dtype=torch.bfloat16, device=DEV) for _ in range(L)] if append else None
+    vb = [torch.empty(n, 4, 256, dtype=torch.bfloat16, device=DEV) for _ in range(L)] if append else None
+    ob = [torch.empty(n, 24, 256, dtype=torch.float32, device=DEV) for _ in range(L)]
+    lb = [torch.empty(n, 24, dtype=torch.float32, device=DEV) for _ in range(L)]
+    graph = None
+    for step in range(3):
+        ks = [torch.randn(n, 4, 256, generator=g).to(torch.bfloat16).to(DEV) for _ in range(L)]
+        vs = [torch.randn(n, 4, 256, generator=g).to(torch.bfloat16).to(DEV) for _ in range(L)]
+        qs = [torch.randn(n, 24, 256, generator=g).to(torch.bfloat16).to(DEV) for _ in range(L)]
+        if step == 2:
+            for pool in pools:
+                pool.demote([0], [3])               # page 3 of request 0 leaves the Recent window
+        # per-layer calls
+        pools[0].extend(ids, [1] * n)
+        ref = []
+        for layer in range(L):
+            if append:
+                o, l_ = pools[0].append_decode(layer, ids, ks[layer], vs[layer], qs[layer])
+            else:
+                pools[0].append(layer, ids, [1] * n, ks[layer], vs[layer])
+                o, l_ = pools[0].decode(layer, ids, qs[layer])
+            ref.append((o.clone(), l_.clone()))
+        # the graph
+        pools[1].extend(ids, [1] * n)
+        for layer in range(L):
+            qb[layer].copy_(qs[layer])
+            if append:
+                kb[layer].copy_(ks[layer])
+                vb[layer].copy_(vs[layer])
+            else:
+                pools[1].append(layer, ids, [1] * n, ks[layer], vs[layer])
+        if graph is None:
+            graph = pools[1].step_graph(ids, qb, ob, lb, k=kb, v=vb)
+        graph.launch()
+        torch.cuda.synchronize()
+        for layer in range(L):
+            assert torch.equal(ref[layer][0], ob[layer]), (step, layer)
+            assert torch.equal(ref[layer][1], lb[layer]), (step, layer)
+    for layer in range(L):
+        for r in ids:
+            a = _export(pools[0], layer, r)
+            b = _export(pools[1], layer, r)
+            assert all(np.array_equal(x[1], y[1]) for x, y in zip(a, b))
+    _check_decode(pools[1], L - 1, ids, qs[L - 1].float(), ob[L - 1], lb[L - 1], 79)
+    graph.close()
+    for pool in pools:
+        pool.check_device_errors()
+
+
 # ------------------------------------------------------------------ materialising export
 @pytest.mark.parametrize("P", [64, 128])
 def test_dequantize_pages_matches_oracle(mkv, P):
