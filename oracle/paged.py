@@ -180,3 +180,31 @@ def decode_attention_multi(q: np.ndarray, pages, P: int, Hkv: int, D: int, seed:
         outs.append(o)
         lses.append(l)
     return np.stack(outs), np.stack(lses)
+
+
+def page_attention_mass(q: np.ndarray, pages, P: int, Hkv: int, D: int, seed: int):
+    """Relevance of each page to a query: the softmax weight its tokens get,
+    averaged over the query heads, i.e. for page j
+
+        mass_j = (1 / Hq) * sum_h sum_{t in page j} softmax_h(s_h)_t,
+        s_h,t  = q_h . k_t / sqrt(D)  (kv head floor(h / G), K dequantised
+                 per the page's tier).
+
+    The pages speak of protecting Anchor pages by "age and relevance"
+    (insight.aitobox.com post, "执行摘要") without defining relevance; this is
+    the library's definition (attention mass, the weight decode attention
+    itself puts on the page).  Returns float64 [npages]; the masses sum to 1."""
+    q = np.asarray(q, dtype=np.float64)
+    Hq = q.shape[0]
+    G = Hq // Hkv
+    K, _ = dequant_pages(pages, P, Hkv, D, seed)
+    n = K.shape[0]
+    owner = np.concatenate([np.full(nv, j) for j, (_, _, nv) in enumerate(pages)])
+    mass = np.zeros(len(pages))
+    for h in range(Hq):
+        s = K[:, h // G, :] @ q[h] / np.sqrt(D)
+        w = np.exp(s - s.max())
+        w /= w.sum()
+        mass += np.bincount(owner, weights=w, minlength=len(pages))
+    assert owner.shape[0] == n
+    return mass / Hq
