@@ -58,7 +58,7 @@
  *   FP8 plane codes (P*d bytes):
  *     K: byte t*d + j                      (row-major)
  *     V: byte (t/2)*2d + 2j + (t%2)        (rows of a token pair interleaved)
- *   TQ3 plane codes (P*3d/8 bytes, 8 codes per 3 bytes): 12-byte units of
+ *   TQ3 plane codes (P*3d/8 bytes, 3 bits per code): 12-byte units of
  *   32 codes = three little-endian 32-bit words W0, W1, W2:
  *     bits [4i, 4i+3) of W_k = code (8k + i)           i = 0..7, k = 0..2
  *     bit  4i+3       of W_k = bit k of code (24 + i)
@@ -373,6 +373,26 @@ mkv_status mkv_set_timing_events(mkv_pool* pool, void* start, void* stop);
 mkv_status mkv_decode_attention_noalloc(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids,
                                         const void* q, mkv_dtype dtype, float* out, float* lse,
                                         mkv_stream_t stream);
+
+/* Page relevance: for each request b of `seq_ids` and each of its pages j,
+ *   mass[b * mass_stride + j] = (1 / Hq) sum_h sum_{t in page j}
+ *                               exp(q_h . k_t / sqrt(d) - lse_h),
+ * the softmax weight the page's tokens receive, averaged over the query
+ * heads (kv head floor(h/G); TQ3 pages scored in the rotated domain).  The
+ * pages protect Anchor pages by "age and relevance" (insight.aitobox.com
+ * post, "执行摘要") without defining relevance; this attention mass is the
+ * library's definition, the signal of a relevance-based Anchor policy.
+ * q: [n, Hq, d] device (dtype), the query of a decode step of `layer`;
+ * lse: [n, Hq] fp32 device, that decode call's lse for the same q (so a
+ * request's masses sum to 1 up to rounding).  mass: [n, mass_stride] fp32
+ * device; entries past a sequence's page count are left untouched;
+ * mass_stride >= the longest sequence's page count (else
+ * INVALID_ARGUMENT).  Reads K only; one 128-thread block per page.  Async on
+ * `stream`; shares the demotion staging region, so a later mkv_demote_pages
+ * on another stream must be ordered by the caller. */
+mkv_status mkv_page_relevance(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids, const void* q,
+                              mkv_dtype q_dtype, const float* lse, float* mass, int32_t mass_stride,
+                              mkv_stream_t stream);
 
 /* ------------------------------------------------------------ step graph
  * One decode step over every layer as a single CUDA graph launch.  The

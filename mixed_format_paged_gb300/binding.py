@@ -29,7 +29,7 @@ EXPORTED = [
     "mkv_seq_info", "mkv_page_info", "mkv_append_tokens", "mkv_set_tier", "mkv_demote_pages",
     "mkv_decode_attention", "mkv_decode_attention_multi", "mkv_decode_attention_noalloc", "mkv_append_decode", "mkv_dequantize_pages", "mkv_pool_stats", "mkv_export_page", "mkv_rotation_signs", "mkv_tq3_codebook",
     "mkv_plan_decode", "mkv_plan_decode_multi", "mkv_check_device_errors", "mkv_selftest_wait_timeout", "mkv_inject_plan_slot", "mkv_set_timing_events", "mkv_last_error", "mkv_version",
-    "mkv_step_graph_create", "mkv_step_graph_launch", "mkv_step_graph_destroy",
+    "mkv_step_graph_create", "mkv_step_graph_launch", "mkv_step_graph_destroy", "mkv_page_relevance",
 ]
 
 
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
                                   ctypes.c_int, ctypes.c_int, ctypes.POINTER(P), ctypes.POINTER(P), P,
                                   ctypes.POINTER(P)],
         "mkv_step_graph_launch": [P, P],
+        "mkv_page_relevance": [P, I32, I32, I32P, P, ctypes.c_int, P, P, I32, P],
         "mkv_step_graph_destroy": [P],
         "mkv_last_error": [],
         "mkv_version": [],
@@ -235,6 +236,13 @@ def mkv_append_decode(pool, layer: int, seq_ids, k, v, kv_dtype: int, q, q_dtype
     a, n = _i32(seq_ids)
     check(lib().mkv_append_decode(pool, layer, n, a, _ptr(k), _ptr(v), kv_dtype, _ptr(q), q_dtype, _ptr(out),
                                   _ptr(lse), _stream(stream)), "mkv_append_decode")
+
+
+def mkv_page_relevance(pool, layer: int, seq_ids, q, q_dtype: int, lse, mass, mass_stride: int,
+                       stream=None) -> None:
+    a, n = _i32(seq_ids)
+    check(lib().mkv_page_relevance(pool, layer, n, a, _ptr(q), q_dtype, _ptr(lse), _ptr(mass), mass_stride,
+                                   _stream(stream)), "mkv_page_relevance")
 
 
 def _ptr_array(xs):

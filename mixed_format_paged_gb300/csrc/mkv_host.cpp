@@ -1124,6 +1124,63 @@ mkv_status mkv_append_decode(mkv_pool* p, int32_t layer, int32_t n, const int32_
   return enqueue_decode(p, layer, q, q_dtype, p->workspace, k, v, kv_dtype, out, lse, s);
 }
 
+// ------------------------------------------------------------------ page relevance
+mkv_status mkv_page_relevance(mkv_pool* p, int32_t layer, int32_t n, const int32_t* ids, const void* q,
+                              mkv_dtype q_dtype, const float* lse, float* mass, int32_t mass_stride,
+                              mkv_stream_t stream) {
+  if (!p) return fail(MKV_ERR_INVALID_ARGUMENT, "pool is NULL");
+  if (layer < 0 || layer >= p->cfg.num_layers) return fail(MKV_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  if (q_dtype != MKV_F32 && q_dtype != MKV_BF16) return fail(MKV_ERR_INVALID_ARGUMENT, "dtype");
+  mkv_status st = check_batch(p, n, ids, true);
+  if (st != MKV_OK) return st;
+  if (n == 0) return MKV_OK;
+  if (!q || !lse || !mass) return fail(MKV_ERR_INVALID_ARGUMENT, "q/lse/mass is NULL");
+  const int P = p->cfg.page_size;
+  int max_pages = 0;
+  for (int i = 0; i < n; ++i) max_pages = std::max(max_pages, npages_for(p->seqs[ids[i]].len, P));
+  if (mass_stride < max_pages)
+    return fail(MKV_ERR_INVALID_ARGUMENT, "mass_stride %d < %d pages of the longest sequence", mass_stride, max_pages);
+  if (p->host_only) return MKV_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  RelevanceParams rp{};
+  rp.fp8_layer = p->fp8_arena + int64_t(layer) * p->cfg.fp8_slots * p->fp8_page_bytes;
+  rp.tq3_layer = p->tq3_arena + int64_t(layer) * p->cfg.tq3_slots * p->tq3_page_bytes;
+  rp.fp8_page_bytes = p->fp8_page_bytes;
+  rp.tq3_page_bytes = p->tq3_page_bytes;
+  rp.pages = reinterpret_cast<const int4*>(p->demote_region);
+  rp.Hq = p->cfg.num_q_heads;
+  rp.Hkv = p->cfg.num_kv_heads;
+  rp.G = p->G;
+  rp.P = P;
+  rp.q = q;
+  rp.q_bf16 = q_dtype == MKV_BF16;
+  rp.lse = lse;
+  rp.mass = mass;
+  rp.mass_stride = mass_stride;
+  std::memcpy(rp.signs, p->signs, sizeof rp.signs);
+  std::memcpy(rp.level, codebook().level, sizeof rp.level);
+  // the (request, page) list goes through the demotion staging region, as
+  // many int4 records per launch as its int2 capacity holds
+  const int cap = p->demote_cap / 2;
+  std::vector<int4> list;
+  for (int i = 0; i < n; ++i) {
+    const SeqRec& sr = p->seqs[ids[i]];
+    const int np = npages_for(sr.len, P);
+    for (int pg = 0; pg < np; ++pg)
+      list.push_back(make_int4(i, pg, sr.pages[pg].slot, (int(sr.pages[pg].tier) << 16) | std::min(P, sr.len - pg * P)));
+  }
+  for (size_t at = 0; at < list.size(); at += cap) {
+    const int cnt = int(std::min<size_t>(cap, list.size() - at));
+    if ((st = staging_acquire(p->st_demote)) != MKV_OK) return st;
+    std::memcpy(p->st_demote.host, list.data() + at, size_t(cnt) * sizeof(int4));
+    if ((st = staging_upload(p->st_demote, p->demote_region, size_t(cnt) * sizeof(int4), s)) != MKV_OK) return st;
+    rp.npages = cnt;
+    const cudaError_t e = launch_relevance(rp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "relevance launch");
+  }
+  return MKV_OK;
+}
+
 // ------------------------------------------------------------------ step graph
 struct mkv_step_graph {
   mkv_pool* pool = nullptr;

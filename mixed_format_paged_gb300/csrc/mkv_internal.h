@@ -143,6 +143,21 @@ struct DequantParams {
   float level[8];
 };
 
+struct RelevanceParams {
+  const uint8_t* fp8_layer;
+  const uint8_t* tq3_layer;
+  int64_t fp8_page_bytes, tq3_page_bytes;
+  const int4* pages;               // per CTA: (batch index, page index, slot, tier << 16 | valid tokens)
+  int32_t npages, Hq, Hkv, G, P;
+  const void* q;                   // [n, Hq, D]
+  int32_t q_bf16;
+  const float* lse;                // [n, Hq], natural log over q . k / sqrt(D)
+  float* mass;                     // [n, mass_stride]
+  int32_t mass_stride;
+  uint64_t signs[4];
+  float level[8];
+};
+
 // Kernel launchers (mkv_kernels.cu).  Return cudaGetLastError() of the launch.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
@@ -155,6 +170,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 cudaError_t prepare_decode_launch();
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s);
+cudaError_t launch_relevance(const RelevanceParams& p, cudaStream_t s);
 size_t decode_smem_bytes();
 // Device address and size of the library's fixed partial-state scratch (see
 // mkv_decode_attention_noalloc), looked up for the current device on every

@@ -449,6 +449,136 @@ __global__ void __launch_bounds__(256) mkv_dequant_kernel(DequantParams p) {
   }
 }
 
+// Code e (0..31) of a 12-byte unit (words w[0..2]).
+__device__ __forceinline__ int tq3_unit_code(const uint32_t* w, int e) {
+  if (e < 24) return (w[e >> 3] >> (4 * (e & 7))) & 7;
+  const int i = e - 24;
+  return ((w[0] >> (4 * i + 3)) & 1) | (((w[1] >> (4 * i + 3)) & 1) << 1) | (((w[2] >> (4 * i + 3)) & 1) << 2);
+}
+
+// ============================================================== page relevance
+// One CTA (4 warps) per (request, page): the page's attention mass, i.e. the
+// softmax weight its valid tokens receive averaged over the query heads,
+// with each head's weights normalised by the lse of the decode call that
+// used the same query: mass = (1/Hq) sum_h sum_t exp(q_h . k_t / sqrt(d) -
+// lse_h).  q (or q' = R q for a TQ3 page, whose keys are scored in the
+// rotated domain) sits in shared memory; lane l of warp w scores tokens l,
+// l + 32, ... of kv head w (and w + 4, ...) against that head's G query
+// rows, dequantising each K row as it goes.  Sums reduce in a fixed order.
+__global__ void __launch_bounds__(128) mkv_relevance_kernel(RelevanceParams p) {
+  extern __shared__ float qs[];                       // [Hq][kHeadDim]
+  __shared__ float part[4];
+  const int4 pe = p.pages[blockIdx.x];
+  const int b = pe.x, page = pe.y, slot = pe.z, tier = pe.w >> 16, nvalid = pe.w & 0xffff;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = p.P;
+  // q rows of request b (rotated for a TQ3 page): warp w takes rows w, w + 4, ...
+  for (int h = warp; h < p.Hq; h += 4) {
+    float x[8];
+    const size_t off = (static_cast<size_t>(b) * p.Hq + h) * kHeadDim + 8 * lane;
+    if (p.q_bf16) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(b2[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+      }
+    } else {
+      const float4* f4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.q) + off);
+      const float4 a = f4[0], c = f4[1];
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = c.x; x[5] = c.y; x[6] = c.z; x[7] = c.w;
+    }
+    if (tier == 3) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
+#pragma unroll
+      for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((i & hs) == 0) {
+            const float a = x[i], c = x[i + hs];
+            x[i] = a + c;
+            x[i + hs] = a - c;
+          }
+      }
+#pragma unroll
+      for (int lm = 1; lm < 32; lm <<= 1) {
+        const bool upper = (lane & lm) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float o = __shfl_xor_sync(kFull, x[i], lm);
+          x[i] = upper ? (o - x[i]) : (x[i] + o);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[i] *= (1.0f / 16.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qs[h * kHeadDim + 8 * lane + i] = x[i];
+  }
+  __syncthreads();
+  constexpr float inv_sqrt_d = 1.0f / 16.0f;          // 1 / sqrt(256), exact
+  float acc = 0.f;
+  for (int kvh = warp; kvh < p.Hkv; kvh += 4) {
+    const int rowb = tier == 3 ? 3 * kHeadDim / 8 : kHeadDim;
+    const int plane = P * (rowb + 2);
+    const uint8_t* kp = (tier == 3 ? p.tq3_layer + static_cast<int64_t>(slot) * p.tq3_page_bytes
+                                   : p.fp8_layer + static_cast<int64_t>(slot) * p.fp8_page_bytes) +
+                        static_cast<int64_t>(kvh) * 2 * plane;
+    const __half* ksc = reinterpret_cast<const __half*>(kp + P * rowb);
+    for (int t = lane; t < nvalid; t += 32) {
+      const float sc = __half2float(ksc[t]);
+      float dot[kMaxGroup];
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g) dot[g] = 0.f;
+      for (int u = 0; u < kHeadDim / 32; ++u) {        // 32 dims at a time
+        float kv[32];
+        if (tier == 3) {
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(kp + t * rowb + 12 * u);
+          const uint32_t wv[3] = {w[0], w[1], w[2]};
+#pragma unroll
+          for (int e = 0; e < 32; ++e) kv[e] = p.level[tq3_unit_code(wv, e)] * sc;
+        } else {
+          const uint4* r4 = reinterpret_cast<const uint4*>(kp + t * rowb + 32 * u);
+          const uint4 a = r4[0], c = r4[1];
+          const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = e4m3x2_to_f16x2(wv[i]), hi = e4m3x2_to_f16x2(wv[i] >> 16);
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            kv[4 * i] = f0.x * sc;
+            kv[4 * i + 1] = f0.y * sc;
+            kv[4 * i + 2] = f1.x * sc;
+            kv[4 * i + 3] = f1.y * sc;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) {
+          if (g < p.G) {
+            const float* qr = qs + (kvh * p.G + g) * kHeadDim + 32 * u;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dot[g] = fmaf(qr[e], kv[e], dot[g]);
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kMaxGroup; ++g)
+        if (g < p.G)
+          acc += __expf(dot[g] * inv_sqrt_d - p.lse[static_cast<size_t>(b) * p.Hq + kvh * p.G + g]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+  if (lane == 0) part[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0)
+    p.mass[static_cast<size_t>(b) * p.mass_stride + page] = ((part[0] + part[1]) + (part[2] + part[3])) / p.Hq;
+}
+
 // ============================================================== decode
 // Persistent partial-attention kernel; one CTA of kDecWarps (12) warps per SM.
 // The host cut the launch's blocks into one contiguous piece list per CTA,
@@ -1330,6 +1460,12 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
   return cudaSuccess;
 }
 int decode_threads() { return kDecThreads; }
+
+cudaError_t launch_relevance(const RelevanceParams& p, cudaStream_t s) {
+  if (p.npages > 0)
+    mkv_relevance_kernel<<<p.npages, 128, static_cast<size_t>(p.Hq) * kHeadDim * sizeof(float), s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
   const int rows = p.npages * p.P * p.Hkv * 2;

@@ -99,3 +99,108 @@ class Stepper:
         """The same through the two separate calls (append, then decode)."""
         self.pool.append(layer, self.ids, [1] * len(self.ids), k, v)
         return self.pool.decode(layer, self.ids, q, out, lse)
+
+
+class RelevanceAnchors:
+    """Relevance-based Anchor protection: which FP8 pages stay FP8 when they
+    leave the Recent window.  The pages protect Anchor pages by "age and
+    relevance" (insight.aitobox.com post, "执行摘要") and define neither; this
+    policy is the library's own design.
+
+    Age: the last W pages of a request are Recent (as in Stepper).
+    Relevance: `observe(mass)` folds a decode step's attention mass per page
+    (MkvPool.relevance, i.e. mkv_page_relevance) into a moving average per
+    page, rho <- (1 - beta) rho + beta mass.  When page j leaves the Recent
+    window (`decide`), with `older` the request's pages older than the window
+    and budget = max(1, ceil(frac * older)) Anchors per request:
+      * room in the budget: j becomes an Anchor if rho_j * older >= kappa,
+        i.e. it draws at least kappa times an even share of the weight;
+      * budget full: j replaces the weakest Anchor a if rho_j > (1 +
+        hysteresis) rho_a and rho_j * older >= kappa; a is then released
+        (back to an ordinary FP8 page, then demoted to TQ3);
+      * otherwise j is demoted to TQ3.
+    Ties go to the older page.  `decide` only returns actions; `apply` makes
+    them through the C ABI (mkv_set_tier, mkv_demote_pages)."""
+
+    def __init__(self, frac: float = 0.05, kappa: float = 2.0, beta: float = 0.25, hysteresis: float = 0.25):
+        self.frac, self.kappa, self.beta, self.hysteresis = frac, kappa, beta, hysteresis
+        self.rho = {}                     # (request, page) -> moving average of the mass
+        self.anchors = {}                 # request -> set of Anchor pages chosen by the policy
+
+    def observe(self, seq_ids, mass, npages):
+        """mass: [n, >= max pages] (host array or tensor); npages: page count per request."""
+        import numpy as np
+        m = mass.detach().float().cpu().numpy() if hasattr(mass, "detach") else np.asarray(mass, dtype=np.float64)
+        for b, r in enumerate(seq_ids):
+            for j in range(int(npages[b])):
+                key = (r, j)
+                self.rho[key] = (1.0 - self.beta) * self.rho.get(key, 0.0) + self.beta * float(m[b, j])
+
+    def decide(self, r: int, leaving: int, older: int):
+        """Actions for page `leaving` of request r as it leaves the Recent
+        window; `older` = the request's pages older than the window after
+        this one left.  Returns a list of ("anchor", page), ("demote", page)
+        and ("release", page)."""
+        import math
+        held = self.anchors.setdefault(r, set())
+        budget = max(1, math.ceil(self.frac * older))
+        rho = self.rho.get((r, leaving), 0.0)
+        strong = rho * older >= self.kappa
+        if strong and len(held) < budget:
+            held.add(leaving)
+            return [("anchor", leaving)]
+        if strong and held:
+            weakest = min(held, key=lambda a: (self.rho.get((r, a), 0.0), -a))
+            if rho > (1.0 + self.hysteresis) * self.rho.get((r, weakest), 0.0):
+                held.discard(weakest)
+                held.add(leaving)
+                return [("release", weakest), ("anchor", leaving)]
+        return [("demote", leaving)]
+
+    def apply(self, pool, r: int, actions):
+        demote = []
+        for act, page in actions:
+            if act == "anchor":
+                pool.set_tier(r, page, A)
+            elif act == "release":
+                pool.set_tier(r, page, R)      # an ordinary FP8 page again, then demoted
+                demote.append(page)
+            else:
+                demote.append(page)
+        if demote:
+            pool.demote([r] * len(demote), demote)
+
+
+class RelevanceStepper(Stepper):
+    """Stepper whose Anchors come from RelevanceAnchors instead of the
+    workload's seeded draw: at each page roll-over the leaving page is
+    anchored, demoted, or swapped with the weakest Anchor; after the decode
+    of `layer` (every `every` steps) the step's attention mass per page is
+    observed."""
+
+    def __init__(self, pool: MkvPool, w: Workload, policy: RelevanceAnchors, layer: int = 0, every: int = 1,
+                 device="cuda"):
+        super().__init__(pool, w, device)
+        self.policy, self.obs_layer, self.every = policy, layer, every
+
+    def pre_step(self):
+        w = self.w
+        ids = self.ids
+        self.pool.extend(ids, [1] * len(ids))
+        for r in ids:
+            self.lengths[r] += 1
+            if (self.lengths[r] - 1) % w.P == 0:            # a new page was opened
+                npg = (self.lengths[r] + w.P - 1) // w.P
+                leaving = npg - 1 - w.windows[r]
+                if leaving >= 0:
+                    tier, _ = self.pool.page_info(r, leaving)
+                    if tier == R:
+                        self.policy.apply(self.pool, r, self.policy.decide(r, leaving, leaving + 1))
+        self.step_no += 1
+
+    def layer(self, layer: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, out=None, lse=None):
+        out, lse = super().layer(layer, k, v, q, out, lse)
+        if layer == self.obs_layer and self.step_no % self.every == 0:
+            mass = self.pool.relevance(layer, self.ids, q, lse)
+            self.policy.observe(self.ids, mass, [self.pool.seq_info(r)[1] for r in self.ids])
+        return out, lse

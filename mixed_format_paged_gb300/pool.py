@@ -115,6 +115,16 @@ class MkvPool:
         B.mkv_append_decode(self.handle, layer, seq_ids, k, v, kvd, q, qd, out, lse, self._stream(stream))
         return out, lse
 
+    def relevance(self, layer: int, seq_ids, q: torch.Tensor, lse: torch.Tensor, stream=None):
+        """Attention mass per page ([n, max pages] fp32; zero past a sequence's
+        pages) of the decode query q with that call's lse (mkv_page_relevance)."""
+        n = len(seq_ids)
+        npg = max(self.seq_info(r)[1] for r in seq_ids)
+        mass = torch.zeros((n, npg), dtype=torch.float32, device=q.device)
+        qd = B.MKV_BF16 if q.dtype == torch.bfloat16 else B.MKV_F32
+        B.mkv_page_relevance(self.handle, layer, seq_ids, q, qd, lse, mass, npg, self._stream(stream))
+        return mass
+
     def step_graph(self, seq_ids, q, out, lse, k=None, v=None, stream=None):
         """Record one decode step over every layer as a CUDA graph on fixed
         buffers (lists with one tensor per layer; k = v = None: no fused

@@ -13,7 +13,8 @@ FP8 (1 byte per element):
            rows of a pair interleaved element by element.
 
 TQ3 (3 bits per element): codes are grouped in 12-byte units of 32 codes
-(8 codes per 3 bytes).  A unit is three little-endian 32-bit words W0..W2:
+(3 bits per code, 32 codes per 12 bytes).  A unit is three little-endian
+32-bit words W0..W2:
   bits [4i, 4i+3) of W_k hold code (8k + i)          for i = 0..7, k = 0..2;
   bit  4i+3       of W_k holds bit k of code (24 + i).
   K codes: unit ``t*(D/32) + j//32``, code index ``j % 32``   (rows in order).

@@ -370,6 +370,83 @@ def test_append_decode_matches_separate_calls(mkv):
         pool.check_device_errors()
 
 
+# ------------------------------------------------------------------ page relevance
+@pytest.mark.parametrize("P", [64, 128])
+@pytest.mark.parametrize("qdtype", [torch.float32, torch.bfloat16])
+def test_page_relevance_matches_oracle(mkv, P, qdtype):
+    """mkv_page_relevance against oracle.paged.page_attention_mass on the
+    GPU's stored pages.  It normalises with the decode call's lse, whose
+    error is <= 1e-4, so each mass carries a relative error of about 1e-4."""
+    from oracle.paged import page_attention_mass
+    g = torch.Generator().manual_seed(41)
+    pool = _small_pool(mkv, P=P, fp8=96, tq3=96, maxp=24)
+    specs = [(5 * P + 9, [0], [1, 2, 3]), (9 * P + 33, [], list(range(8))), (2 * P + 1, [0], [])]
+    for r, (n, anc, st) in enumerate(specs):
+        K, V = _kv(n, torch.bfloat16, g)
+        if r == 1:
+            K[3 * P: 3 * P + 5] *= 3.0                 # a few loud keys: one page draws most of the weight
+        pool.extend([r], [n])
+        pool.append(0, [r], [n], K.to(DEV), V.to(DEV))
+        for a in anc:
+            pool.set_tier(r, a, 2)
+        if st:
+            pool.demote([r] * len(st), st)
+    ids = [0, 1, 2]
+    q = torch.randn(3, 24, 256, generator=g).to(qdtype)
+    out, lse = pool.decode(0, ids, q.to(DEV))
+    mass = pool.relevance(0, ids, q.to(DEV), lse)
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    m = mass.double().cpu().numpy()
+    for b, r in enumerate(ids):
+        pages = _export(pool, 0, r)
+        ref = page_attention_mass(q[b].double().numpy(), pages, P, 4, 256, 4321)
+        got = m[b, :len(pages)]
+        assert np.all(np.abs(got - ref) <= 3e-4 * ref + 1e-7), (r, np.abs(got - ref).max())
+        assert abs(got.sum() - 1.0) <= 3e-4
+        assert np.all(m[b, len(pages):] == 0.0)        # entries past the sequence stay untouched
+        top = np.sort(ref)[::-1]
+        if top[0] > 1.01 * top[1]:
+            assert got.argmax() == ref.argmax()         # the same most relevant page
+
+
+def test_relevance_stepper_anchors_the_attended_page(mkv):
+    """RelevanceStepper end to end: the page whose keys line up with every
+    query draws most of the attention mass (mkv_page_relevance), so when it
+    leaves the Recent window it becomes an Anchor and stays FP8; the next
+    page to leave draws little and goes to TQ3.  Decode still matches the
+    oracle on the resulting mixed layout."""
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import RelevanceAnchors, RelevanceStepper, make_pool
+    g = torch.Generator().manual_seed(53)
+    w = workloads.make("cfg3")
+    w.lengths, w.windows, w.anchors, w.num_layers, w.steps = [64 * 6 - 2], [3], [set()], 1, 70
+    pool = make_pool(w, device=DEV, seed=53)
+    u = torch.randn(256, generator=g)
+    u /= u.norm()
+    K = torch.randn(w.lengths[0], 4, 256, generator=g)
+    V = torch.randn(w.lengths[0], 4, 256, generator=g)
+    K[3 * 64: 4 * 64] = 6.0 * u                          # page 3: q.k / 16 = 3 for every token
+    pool.extend([0], [w.lengths[0]])
+    pool.append(0, [0], [w.lengths[0]], K.to(torch.bfloat16).to(DEV), V.to(torch.bfloat16).to(DEV))
+    pool.demote([0, 0, 0], [0, 1, 2])
+    pol = RelevanceAnchors(frac=0.05, kappa=2.0, beta=1.0)
+    st = RelevanceStepper(pool, w, pol, layer=0, device=DEV)
+    for step in range(w.steps):
+        st.pre_step()
+        k = torch.randn(1, 4, 256, generator=g).to(torch.bfloat16)
+        v = torch.randn(1, 4, 256, generator=g).to(torch.bfloat16)
+        q = (8.0 * u + 0.1 * torch.randn(1, 24, 256, generator=g)).to(torch.bfloat16)
+        out, lse = st.layer(0, k.to(DEV), v.to(DEV), q.to(DEV))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    tiers = [pool.page_info(0, p)[0] for p in range(pool.seq_info(0)[1])]
+    assert tiers[:5] == [3, 3, 3, 2, 3], tiers           # page 3 anchored, page 4 demoted
+    assert all(t == 1 for t in tiers[5:])
+    assert pol.anchors[0] == {3} and pol.rho[(0, 3)] > 0.5
+    _check_decode(pool, 0, [0], q.float(), out, lse, 53)
+
+
 # ------------------------------------------------------------------ step graph
 @pytest.mark.parametrize("append", [True, False])
 def test_step_graph_matches_per_layer_calls(mkv, append):
