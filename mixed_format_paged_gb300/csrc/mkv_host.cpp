@@ -411,103 +411,115 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   // page, up to the last valid token (a block past a page's valid tokens is
   // empty and only costs its overhead).  Only a group's last page can be
   // partial, so a block's tokens never increase along the group.
-  // Rounds: runs of up to kDecWarps consecutive blocks of one group, from the
-  // group's first block on.  A CTA's warps take one round together, so a cut
-  // inside a group falls only between rounds and every warp of a piece gets
-  // the same number of blocks (one fewer for some in a group's last round).
-  // A round costs its slowest block -- its first -- on every warp; a short
+  // Rounds: a CTA's warps take a piece's blocks round-robin (block k of the
+  // piece on warp k mod kDecWarps), so a piece runs in rounds of up to
+  // kDecWarps blocks from its own first block on, and the next piece starts
+  // after all of them.  A round costs its slowest block -- its first, since a
+  // block's tokens never increase along a group -- on every warp; a short
   // round, with warps idle, runs its blocks faster and is priced between the
-  // two.  All of a group's rounds but its last one or two are alike, so the
-  // rounds are kept as runs of equal rounds.
+  // two.  Cuts may fall on any block.  A group's blocks are all alike but for
+  // the last page's, so each group keeps the count and cost of its leading
+  // full blocks.
   const int ng = int(groups.size());
-  std::vector<int> g_nblk(ng), g_round0(ng + 1, 0);
+  std::vector<int> g_nblk(ng), g_uni(ng);
+  std::vector<int64_t> g_w(ng);
   auto blk_tokens = [&](const Group& g, int k) {
     const int bt = g.fmt ? kTq3Blk : kFp8Blk, bpp = P / bt;
     const int full = (g.nentry - 1) * bpp;
     if (k < full) return bt;
     return std::max(0, std::min(bt, int(entries[g.entry0 + g.nentry - 1].nvalid) - (k - full) * bt));
   };
-  auto round_cost = [&](const Group& g, int r, int nblk) {
-    const int n = std::min(kDecWarps, nblk - r * kDecWarps);
-    const int64_t worst = blk_tokens(g, r * kDecWarps) * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
-    return worst * (24 + 3 * int64_t(n));
+  auto blk_cost = [&](int gi, int k) {
+    const Group& g = groups[gi];
+    return int64_t(blk_tokens(g, k)) * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
   };
-  struct Run {
-    int group, first, count;   // rounds [first, first + count) in the global round order
-    int64_t cost;              // cost of each of its rounds
-  };
-  std::vector<Run> runs;
-  runs.reserve(size_t(ng) * 3);
-  int64_t total_blocks = 0;
+  int64_t total_blocks = 0, lo = 0, hi = 0;
   for (int gi = 0; gi < ng; ++gi) {
     const Group& g = groups[gi];
     const int bt = g.fmt ? kTq3Blk : kFp8Blk;
-    const int nblk = (g.nentry - 1) * (P / bt) + (entries[g.entry0 + g.nentry - 1].nvalid + bt - 1) / bt;
-    const int nround = (nblk + kDecWarps - 1) / kDecWarps;
-    g_nblk[gi] = nblk;
-    g_round0[gi + 1] = g_round0[gi] + nround;
-    total_blocks += nblk;
-    // rounds [0, uniform) hold 12 blocks each and start with a full block
     const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
-    const int full_blocks = std::min(nblk, (g.nentry - 1) * (P / bt) + last_nv / bt);
-    const int uniform = std::min(nblk / kDecWarps, (full_blocks + kDecWarps - 1) / kDecWarps);
-    if (uniform > 0) runs.push_back({gi, g_round0[gi], uniform, round_cost(g, 0, nblk)});
-    for (int r = uniform; r < nround; ++r) {
-      const int64_t c = round_cost(g, r, nblk);
-      if (!runs.empty() && runs.back().group == gi && runs.back().cost == c)
-        ++runs.back().count;
-      else
-        runs.push_back({gi, g_round0[gi] + r, 1, c});
-    }
+    g_nblk[gi] = (g.nentry - 1) * (P / bt) + (last_nv + bt - 1) / bt;
+    g_uni[gi] = (g.nentry - 1) * (P / bt) + last_nv / bt;
+    g_w[gi] = int64_t(bt) * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
+    total_blocks += g_nblk[gi];
+    // a CTA holds one block at least; the whole batch as one CTA fits hi
+    lo = std::max(lo, kCostPiece + blk_cost(gi, 0) * 27);
+    hi += kCostPiece + blk_cost(gi, 0) * 60 * ((g_nblk[gi] + kDecWarps - 1) / kDecWarps);
   }
-  const int nrounds = g_round0[ng];
+  // The largest b1 in [b0, nblk] such that the piece [b0, b1) of group gi
+  // costs at most `budget` (b0 when not one block fits); *cost gets its cost.
+  // Whole rounds of full blocks are taken in O(1).
+  auto piece_end = [&](int gi, int b0, int64_t budget, int64_t* cost) {
+    const int nblk = g_nblk[gi], uni = g_uni[gi];
+    int b = b0;
+    int64_t used = 0;
+    auto short_round = [&](int64_t worst, int avail) {   // blocks of a short round that fit what is left
+      const int64_t left = budget - used;
+      const int n = left >= 27 * worst ? int(std::min<int64_t>(avail - 1, (left / worst - 24) / 3)) : 0;
+      b += n;
+      used += n > 0 ? worst * (24 + 3 * int64_t(n)) : 0;
+    };
+    if (b < uni) {
+      const int64_t w = g_w[gi], whole = (uni - b) / kDecWarps;
+      const int64_t take = std::min<int64_t>(whole, budget / (60 * w));
+      b += int(take) * kDecWarps;
+      used += take * 60 * w;
+      if (take < whole) {       // the budget ends among full blocks
+        short_round(w, kDecWarps);
+        *cost = used;
+        return b;
+      }
+    }
+    while (b < nblk) {
+      const int64_t worst = blk_cost(gi, b);
+      const int avail = std::min(kDecWarps, nblk - b);
+      if (used + worst * (24 + 3 * avail) > budget) {
+        short_round(worst, avail);
+        break;
+      }
+      used += worst * (24 + 3 * avail);
+      b += avail;
+    }
+    *cost = used;
+    return b;
+  };
   // one CTA per SM at most, each with at least kMinBlocksPerCta blocks
   const int max_cta = int(std::max<int64_t>(
       1, std::min<int64_t>({int64_t(p->n_sm), int64_t(kMaxCtas), total_blocks / kMinBlocksPerCta})));
-  // Contiguous split of the rounds into at most max_cta CTAs that minimises
-  // the largest CTA cost, a piece costing kCostPiece on top of its rounds (its
-  // end-of-piece merge): the greedy fill below needs the fewest CTAs for a
-  // given bound, so a bisection on the (integer) bound finds the smallest one
-  // that fits.  The fill takes a run of equal rounds in O(1) per CTA it opens.
-  auto fill = [&](int64_t bound, std::vector<int>* starts) {
-    int n_cta = 0, last_group = -1;
+  // Contiguous split of the block sequence into at most max_cta CTAs that
+  // minimises the largest CTA cost, a piece costing kCostPiece on top of its
+  // rounds (its end-of-piece merge): the greedy fill below, which gives each
+  // CTA the longest run that fits, needs the fewest CTAs for a given bound
+  // (a run's cost only grows when it is extended and only falls when its
+  // start moves later), so a bisection on the (integer) bound finds the
+  // smallest one that fits.
+  struct Cut {
+    int group, blk;
+  };
+  // (it stops counting past max_cta CTAs)
+  auto fill = [&](int64_t bound, std::vector<Cut>* starts) {
+    int n_cta = 0;
     int64_t acc = 0;
-    for (const Run& rn : runs) {
-      int left = rn.count, at = rn.first;
-      // the run's first round (a new group adds a piece)
-      const int64_t add = rn.cost + (rn.group != last_group ? kCostPiece : 0);
-      if (n_cta == 0 || acc + add > bound) {
-        ++n_cta;
-        if (starts) starts->push_back(at);
-        acc = kCostPiece + rn.cost;
-      } else {
-        acc += add;
-      }
-      last_group = rn.group;
-      --left;
-      ++at;
-      while (left > 0) {
-        const int64_t fit = std::min<int64_t>(left, acc + rn.cost <= bound ? (bound - acc) / rn.cost : 0);
-        acc += fit * rn.cost;
-        left -= int(fit);
-        at += int(fit);
-        if (left > 0) {          // a new CTA takes the next round
-          ++n_cta;
-          if (starts) starts->push_back(at);
-          acc = kCostPiece + rn.cost;
-          --left;
-          ++at;
+    for (int gi = 0; gi < ng; ++gi)
+      for (int b = 0; b < g_nblk[gi];) {
+        int64_t c = 0;
+        int b1 = (n_cta > 0 && acc + kCostPiece < bound) ? piece_end(gi, b, bound - acc - kCostPiece, &c) : b;
+        if (b1 == b) {           // a new CTA takes the next block
+          if (++n_cta > max_cta) return n_cta;
+          if (starts) starts->push_back({gi, b});
+          acc = 0;
+          b1 = piece_end(gi, b, bound - kCostPiece, &c);
+          if (b1 == b) {         // below the one-block bound (not reached: bound >= lo)
+            b1 = b + 1;
+            c = blk_cost(gi, b) * 27;
+          }
         }
+        acc += kCostPiece + c;
+        b = b1;
       }
-    }
     return n_cta;
   };
-  int64_t lo = 0, hi = 0;
-  for (const Run& rn : runs) {
-    lo = std::max(lo, kCostPiece + rn.cost);
-    hi += (kCostPiece + rn.cost) * rn.count;
-  }
-  if (fill(lo, nullptr) > max_cta) {
+  if (ng > 0 && fill(lo, nullptr) > max_cta) {
     // the smallest feasible bound: fill(hi) fits, fill(lo) does not
     while (hi - lo > 1) {
       const int64_t mid = lo + (hi - lo) / 2;
@@ -515,11 +527,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     }
     lo = hi;
   }
-  std::vector<int> starts;
-  const int ncta = nrounds == 0 ? 0 : fill(lo, &starts);
-  starts.push_back(nrounds);
-  // group of a global round index
-  auto group_of = [&](int r) { return int(std::upper_bound(g_round0.begin(), g_round0.end(), r) - g_round0.begin()) - 1; };
+  std::vector<Cut> starts;
+  const int ncta = ng == 0 ? 0 : fill(lo, &starts);
+  starts.push_back({ng, 0});
   auto tokens_in = [&](const Group& g, int b0, int b1) {   // valid tokens of blocks [b0, b1)
     int64_t t = 0;
     const int bt = g.fmt ? kTq3Blk : kFp8Blk, full = (g.nentry - 1) * (P / bt);
@@ -532,12 +542,12 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   std::vector<int32_t> cta_seg(ncta + 1, 0);
   for (int c = 0; c < ncta; ++c) {
     cta_seg[c] = int(segs.size());
-    for (int r = starts[c]; r < starts[c + 1];) {
-      const int gi = group_of(r);
+    const Cut from = starts[c], to = starts[c + 1];
+    for (int gi = from.group; gi <= std::min(to.group, ng - 1); ++gi) {
+      const int b0 = gi == from.group ? from.blk : 0;
+      const int b1 = gi == to.group ? to.blk : g_nblk[gi];
+      if (b1 <= b0) continue;
       const Group& g = groups[gi];
-      const int r_end = std::min(starts[c + 1], g_round0[gi + 1]);
-      const int b0 = (r - g_round0[gi]) * kDecWarps;
-      const int b1 = std::min(g_nblk[gi], (r_end - g_round0[gi]) * kDecWarps);
       Segment sg{};
       sg.fmt = g.fmt;
       sg.b = g.b;
@@ -549,7 +559,6 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
       segs.push_back(sg);
       seg_entry.push_back(g.entry0 + b0 / (P / (g.fmt ? kTq3Blk : kFp8Blk)));
       seg_tokens.push_back(tokens_in(g, b0, b1));
-      r = r_end;
     }
   }
   cta_seg[ncta] = int(segs.size());

@@ -276,13 +276,12 @@ def test_selftest_wait_timeout_arguments(mkv):
     assert e.value.status == 2
 
 
-def _rounds_of(layouts, P, H=4):
+def _blocks_of(layouts, P, H=4):
     """The planner's work units for requests given as (tokens, tiers per page):
     per (request, kv head, tier) group, TQ3 before FP8, blocks of 32 TQ3 / 16
-    FP8 tokens page by page, cut into rounds of 12 blocks from the group's
-    start; a round costs 12 x its slowest block (tokens x 1.0 or 1.45, + 8),
-    a short round 0.4 + 0.6 x its share of that."""
-    rounds = []                                            # (group key, cost)
+    FP8 tokens page by page, each with its integer cost: tokens x (20 TQ3 |
+    29 FP8) + 160.  Returns [(group key, [block costs])] in plan order."""
+    groups = []
     for b, (n, tiers) in enumerate(layouts):
         nv = [min(P, n - i * P) for i in range(len(tiers))]
         for kvh in range(H):
@@ -290,24 +289,36 @@ def _rounds_of(layouts, P, H=4):
                 pages = [nv[i] for i, t in enumerate(tiers) if (t == 3) == (fmt == 3)]
                 if not pages:
                     continue
-                bt, rate = (32, 1.0) if fmt == 3 else (16, 1.45)
+                bt, rate = (32, 20) if fmt == 3 else (16, 29)
                 bpp = P // bt
                 nblk = (len(pages) - 1) * bpp + -(-pages[-1] // bt)
-                costs = [max(0, min(bt, pages[k // bpp] - (k % bpp) * bt)) * rate + 8.0 for k in range(nblk)]
-                for r in range(0, nblk, 12):
-                    c = costs[r:r + 12]
-                    rounds.append(((b, kvh, fmt), max(c) * 12 * (0.4 + 0.6 * len(c) / 12)))
-    return rounds
+                groups.append(((b, kvh, fmt), [max(0, min(bt, pages[k // bpp] - (k % bpp) * bt)) * rate + 160
+                                              for k in range(nblk)]))
+    return groups
 
 
-def _cta_cost(rounds):
-    return sum(c for _, c in rounds) + 540.0 * (1 + sum(rounds[i][0] != rounds[i - 1][0] for i in range(1, len(rounds))))
+PIECE = 54000
+
+
+def _piece_cost(costs):
+    """A piece of blocks with these costs, in the planner's model: rounds of
+    12 blocks from the piece's first, each costing its slowest block x
+    (24 + 3 n) for n blocks, plus 54000 for the piece."""
+    return PIECE + sum(max(costs[i:i + 12]) * (24 + 3 * len(costs[i:i + 12])) for i in range(0, len(costs), 12))
+
+
+def _plan_cta_costs(plan, groups):
+    cost = dict(groups)
+    ctas = {}
+    for b, kvh, tier, _, _, _, cta, blk0, nblk in plan:
+        ctas[cta] = ctas.get(cta, 0) + _piece_cost(cost[(b, kvh, tier)][blk0:blk0 + nblk])
+    return ctas
 
 
 def test_plan_minimises_the_largest_cta(mkv):
-    """The split is contiguous and its largest CTA cost equals the optimum of
-    an exhaustive dynamic programme over the same cut points (within the
-    bisection's 1e-4)."""
+    """The split is contiguous over the block sequence and its largest CTA
+    cost equals the optimum of an exhaustive dynamic programme over every
+    cut point (any block), in the planner's integer cost model."""
     P = 64
     layouts = [(64 * 30 + 17, [2] + [3] * 21 + [1] * 9), (64 * 12, [3] * 9 + [1] * 3),
                (64 * 5 + 1, [1] * 6), (64 * 18 + 40, [2, 3, 3, 2] + [3] * 11 + [1] * 4)]
@@ -320,38 +331,38 @@ def test_plan_minimises_the_largest_cta(mkv):
         stale = [pg for pg, t in enumerate(tiers) if t == 3]
         p.demote([r] * len(stale), stale)
     plan = p.plan(list(range(len(layouts))))
-    rounds = _rounds_of(layouts, P)
-    index = {}
-    pos = 0
-    for key, _ in rounds:
-        index.setdefault(key, pos)
-        pos += 1
-    # the split as round ranges, CTA by CTA
-    ctas = {}
-    for b, kvh, tier, _, _, _, cta, blk0, nblk in plan:
-        assert blk0 % 12 == 0, "cuts fall on round boundaries"
-        start = index[(b, kvh, tier)] + blk0 // 12
-        ctas.setdefault(cta, []).append((start, start + -(-nblk // 12)))
-    assert sorted(ctas) == list(range(len(ctas)))
-    seq = [rng for c in sorted(ctas) for rng in ctas[c]]
-    assert seq[0][0] == 0 and seq[-1][1] == len(rounds)
-    assert all(a[1] == b[0] for a, b in zip(seq, seq[1:])), "CTAs hold contiguous runs of rounds"
-    got = max(_cta_cost(rounds[min(s for s, _ in r):max(e for _, e in r)]) for r in ctas.values())
-    # exhaustive optimum: f_k[j] = min_i max(f_{k-1}[i], cost(rounds i..j-1))
-    R = len(rounds)
-    nblocks = sum(nblk for *_, nblk in plan)
-    kmax = max(1, min(152, nblocks // 24))
+    groups = _blocks_of(layouts, P)
+    first = {}
+    blocks = []                                        # (group key, block cost) in plan order
+    for key, costs in groups:
+        first[key] = len(blocks)
+        blocks += [(key, c) for c in costs]
+    # the split as block ranges, CTA by CTA, contiguous and covering every block once
+    seq = sorted((cta, first[(b, kvh, tier)] + blk0, nblk) for b, kvh, tier, _, _, _, cta, blk0, nblk in plan)
+    assert [c for c, _, _ in seq] == sorted(c for c, _, _ in seq)
+    assert seq[0][1] == 0 and seq[-1][1] + seq[-1][2] == len(blocks)
+    assert all(a[1] + a[2] == b[1] for a, b in zip(seq, seq[1:])), "CTAs hold contiguous runs of blocks"
+    assert any(blk0 % 12 for *_, blk0, _ in plan), "cuts are not held to round boundaries"
+    got = max(_plan_cta_costs(plan, groups).values())
+    # exhaustive optimum over all cut points: C[i, j] = cost of blocks i..j-1
+    # as one CTA, f_k[j] = min_i max(f_{k-1}[i], C[i, j])
+    R = len(blocks)
     C = np.full((R + 1, R + 1), np.inf)
     for i in range(R):
-        for j in range(i + 1, R + 1):
-            C[i, j] = _cta_cost(rounds[i:j])
+        acc, start, key = 0, i, blocks[i][0]
+        for j in range(i, R):
+            if blocks[j][0] != key:                    # a new piece
+                acc += _piece_cost([c for _, c in blocks[start:j]])
+                start, key = j, blocks[j][0]
+            C[i, j + 1] = acc + _piece_cost([c for _, c in blocks[start:j + 1]])
+    kmax = max(1, min(152, R // 24))
     f = C[0].copy()
     best = f[R]
     for _ in range(kmax - 1):
         f = np.min(np.maximum(f[:, None], C), axis=0)
         best = min(best, f[R])
-    assert len(ctas) <= kmax
-    assert best <= got <= best * (1 + 1e-4) + 1e-9, (got, best)
+    assert len({c for *_, c, _, _ in plan}) <= kmax
+    assert got == best, (got, best)
 
 
 def test_multi_query_plan_covers_each_prefix(mkv):
@@ -402,50 +413,42 @@ def test_missing_library_fails_loudly(mkv, monkeypatch):
         _host_pool(mkv)
 
 
-def _int_rounds(layouts, P, H=4):
-    """Per-round integer costs of the planner's model (1/100 of the float
-    model above): a block costs tokens x (20 TQ3 | 29 FP8) + 160, a round of
-    n blocks its slowest block x (24 + 3 n), a piece 54000.  One entry per
-    round, in the planner's group order: (group key, cost, blocks)."""
-    rounds = []
-    for b, (n, tiers) in enumerate(layouts):
-        nv = [min(P, n - i * P) for i in range(len(tiers))]
-        for kvh in range(H):
-            for fmt in (3, 1):
-                pages = [nv[i] for i, t in enumerate(tiers) if (t == 3) == (fmt == 3)]
-                if not pages:
-                    continue
-                bt, rate = (32, 20) if fmt == 3 else (16, 29)
-                bpp = P // bt
-                nblk = (len(pages) - 1) * bpp + -(-pages[-1] // bt)
-                costs = [max(0, min(bt, pages[k // bpp] - (k % bpp) * bt)) * rate + 160 for k in range(nblk)]
-                for r in range(0, nblk, 12):
-                    c = costs[r:r + 12]
-                    rounds.append(((b, kvh, fmt), max(c) * (24 + 3 * len(c)), len(c)))
-    return rounds
+def _reference_split(groups, max_cta):
+    """The plain split the planner computes: a greedy fill that gives each CTA
+    the longest run of blocks that fits the bound (a round at a time, then
+    block by block within the round that does not fit), and the smallest
+    integer bound that fits in max_cta CTAs.  Returns the pieces
+    (group key, CTA, first block, blocks)."""
+    lo = max(PIECE + 27 * costs[0] for _, costs in groups)
+    hi = sum(PIECE + 60 * costs[0] * -(-len(costs) // 12) for _, costs in groups)
 
-
-def _reference_split(rounds, max_cta):
-    """The plain split the planner computes: a greedy fill round by round
-    (a piece adds 54000 when the group changes) and the smallest integer
-    bound that fits in max_cta CTAs.  Returns the CTAs' first rounds."""
-    piece = 54000
-
-    def fill(bound, starts=None):
-        n_cta, acc, last = 0, 0, None
-        for i, (key, c, _) in enumerate(rounds):
-            add = c + (piece if key != last else 0)
-            if n_cta == 0 or acc + add > bound:
-                n_cta += 1
-                if starts is not None:
-                    starts.append(i)
-                acc = piece + c
-            else:
-                acc += add
-            last = key
+    def fill(bound, pieces=None):
+        n_cta, acc = 0, 0
+        for key, costs in groups:
+            b = 0
+            while b < len(costs):
+                def longest(budget):
+                    used, e = 0, b
+                    while e < len(costs):
+                        n = min(12, len(costs) - e)
+                        full = costs[e] * (24 + 3 * n)
+                        if used + full <= budget:
+                            used, e = used + full, e + n
+                            continue
+                        k = 0
+                        while k + 1 < n and used + costs[e] * (24 + 3 * (k + 1)) <= budget:
+                            k += 1
+                        return e + k, used + (costs[e] * (24 + 3 * k) if k else 0)
+                    return e, used
+                e, c = longest(bound - acc - PIECE) if n_cta and acc + PIECE < bound else (b, 0)
+                if e == b:
+                    n_cta, acc = n_cta + 1, 0
+                    e, c = longest(bound - PIECE)
+                if pieces is not None:
+                    pieces.append((key, n_cta - 1, b, e - b))
+                acc += PIECE + c
+                b = e
         return n_cta
-    lo = max(piece + c for _, c, _ in rounds)
-    hi = sum(piece + c for _, c, _ in rounds)
     if fill(lo) > max_cta:
         while hi - lo > 1:
             mid = lo + (hi - lo) // 2
@@ -454,14 +457,15 @@ def _reference_split(rounds, max_cta):
             else:
                 lo = mid
         lo = hi
-    starts = []
-    fill(lo, starts)
-    return starts
+    pieces = []
+    fill(lo, pieces)
+    return pieces
 
 
-def test_plan_split_matches_per_round_reference(mkv):
-    """The planner takes runs of equal rounds in O(1) per CTA; on all five
-    workloads its split must equal the plain round-by-round algorithm's."""
+def test_plan_split_matches_reference(mkv):
+    """The planner takes whole rounds of full blocks in O(1) per CTA; on all
+    five workloads its split must equal the plain round-by-round, then
+    block-by-block, algorithm's."""
     from mixed_format_paged_gb300 import workloads
     from mixed_format_paged_gb300.harness import make_pool
     for name in ("cfg1", "cfg2", "cfg3", "cfg4", "cfg5"):
@@ -480,23 +484,8 @@ def test_plan_split_matches_per_round_reference(mkv):
                 pool.demote([r] * len(stale), stale)
             layouts.append((w.lengths[r], tiers))
         plan = pool.plan(list(range(w.n)))
-        rounds = _int_rounds(layouts, w.P)
-        max_cta = max(1, min(152, sum(nb for *_, nb in rounds) // 24))
-        starts = _reference_split(rounds, max_cta) + [len(rounds)]
-        # expected pieces: (b, kvh, tier, cta, first block, blocks)
-        first = {}
-        for i, (key, _, _) in enumerate(rounds):
-            first.setdefault(key, i)
-        exp = []
-        for c in range(len(starts) - 1):
-            i = starts[c]
-            while i < starts[c + 1]:
-                key = rounds[i][0]
-                j = i
-                while j < starts[c + 1] and rounds[j][0] == key:
-                    j += 1
-                blk0 = 12 * (i - first[key])
-                exp.append((key[0], key[1], key[2], c, blk0, sum(nb for *_, nb in rounds[i:j])))
-                i = j
+        groups = _blocks_of(layouts, w.P)
+        max_cta = max(1, min(152, sum(len(c) for _, c in groups) // 24))
+        exp = [(key[0], key[1], key[2], cta, b0, nb) for key, cta, b0, nb in _reference_split(groups, max_cta)]
         got = [(b, kvh, tier, cta, blk0, nblk) for b, kvh, tier, _, _, _, cta, blk0, nblk in plan]
         assert got == exp, name
