@@ -56,16 +56,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-// The same copy with an L2 cache policy (createpolicy): KV page data is read
-// once per launch and should not push the small, reused data (plan tables, q,
-// partial states) out of L2.
+// A 1-D bulk copy global -> shared counted by an mbarrier, with an L2 cache
+// policy (createpolicy): KV page data is read once per launch and should not
+// push the small, reused data (plan tables, q, partial states) out of L2.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
