@@ -543,6 +543,12 @@ def run_mkv(args):
             cpu["layer_step"] = {"value": fg, "unit": "GB/s", "seconds": fdt, "bytes": fb,
                                  "us_per_layer_step": fdt * 1e6, "cores": cpu_threads(),
                                  "sample": f"full layer-step: every request and kv head of layer 0 of {w.name}"}
+        else:
+            lb = sum(kernel_bytes) / len(kernel_bytes)
+            cpu["layer_step_estimate"] = {
+                "seconds": lb / (gbs * 1e9), "bytes": lb, "kind": "extrapolated, not timed",
+                "how": "one full layer-step's algorithmic bytes at the sample's bytes per second "
+                       "(--cpu-full times it whole)"}
     if rank != 0:
         return
     value = kv_job / (t_max * 1e-3) / 1e9
