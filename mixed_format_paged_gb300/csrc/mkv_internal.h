@@ -165,8 +165,8 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s);
 // while the preceding kernel finishes; it waits for that kernel before reading
 // q or writing partial states.
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
-// Sets the decode kernel's per-device launch attributes (done by launch_decode
-// too); call it before capturing decode launches into a graph.
+// Sets the decode and merge kernels' per-device launch attributes (done by
+// launch_decode too); call it before capturing decode launches into a graph.
 cudaError_t prepare_decode_launch();
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s);

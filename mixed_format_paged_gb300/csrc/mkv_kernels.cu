@@ -1324,6 +1324,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
 // then the signs and 1/16), the FP8 partials join, and out = O / L,
 // lse = (M + log2 L) ln 2.
 constexpr int kMergeBatch = 8;
+constexpr size_t kMergeSmemCap = 200 * 1024;   // dynamic shared memory a merge block may request (unused)
 
 // Loads of partial states [first + base, + kMergeBatch) of head h at dim d.
 struct MergeBatch {
@@ -1358,20 +1359,35 @@ __device__ __forceinline__ void merge_fold(const MergeBatch& mb, float& M, float
   }
 }
 // Partial states [first, first + count) of head h merged at dim d; the first
-// batch is passed in already loaded.
+// batch is passed in already loaded.  With PREFETCH the next batch's loads go
+// out before the current batch is folded (two batches in flight, more
+// registers); the fold order, and so the result, is the same either way.
+template <bool PREFETCH>
 __device__ __forceinline__ void merge_run(const float* part, int stride, int h, int first, int count, int d,
                                           const MergeBatch& first_batch, float& M, float& L, float& O) {
   M = -INFINITY;
   L = 0.f;
   O = 0.f;
-  merge_fold(first_batch, M, L, O);
-  for (int base = kMergeBatch; base < count; base += kMergeBatch) {
-    MergeBatch mb;
-    merge_load(part, stride, h, first, base, count, d, mb);
-    merge_fold(mb, M, L, O);
+  if (PREFETCH) {
+    MergeBatch cur = first_batch;
+    for (int base = kMergeBatch; base < count; base += kMergeBatch) {
+      MergeBatch nxt;
+      merge_load(part, stride, h, first, base, count, d, nxt);
+      merge_fold(cur, M, L, O);
+      cur = nxt;
+    }
+    merge_fold(cur, M, L, O);
+  } else {
+    merge_fold(first_batch, M, L, O);
+    for (int base = kMergeBatch; base < count; base += kMergeBatch) {
+      MergeBatch mb;
+      merge_load(part, stride, h, first, base, count, d, mb);
+      merge_fold(mb, M, L, O);
+    }
   }
 }
 
+template <bool PREFETCH>
 __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   __shared__ float xs[kHeadDim];
   const int h = blockIdx.x % p.G;
@@ -1391,7 +1407,7 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   merge_load(p.part, stride, h, md.tq3_first, 0, md.tq3_count, d, bs);
   merge_load(p.part, stride, h, md.fp8_first, 0, md.fp8_count, d, bf);
   float Ms, Ls, os, Mf, Lf, of;
-  merge_run(p.part, stride, h, md.tq3_first, md.tq3_count, d, bs, Ms, Ls, os);
+  merge_run<PREFETCH>(p.part, stride, h, md.tq3_first, md.tq3_count, d, bs, Ms, Ls, os);
   // o_S = R^T o'_S = signs .* (H o'_S) / 16: butterflies over lane bits by
   // shuffle, over warp bits through shared memory
 #pragma unroll
@@ -1408,7 +1424,7 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   }
   os *= (1.0f / 16.0f);
   if (neg) os = -os;
-  merge_run(p.part, stride, h, md.fp8_first, md.fp8_count, d, bf, Mf, Lf, of);
+  merge_run<PREFETCH>(p.part, stride, h, md.fp8_first, md.fp8_count, d, bf, Mf, Lf, of);
   const float M = fmaxf(Ms, Mf);
   const float fs = (Ms == -INFINITY) ? 0.f : exp2f(Ms - M);
   const float ff = (Mf == -INFINITY) ? 0.f : exp2f(Mf - M);
@@ -1435,6 +1451,7 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s) {
 }
 
 size_t decode_smem_bytes() { return kDecSmemBytes; }
+
 
 // Fixed scratch for the allocation-free decode entry point: 8 MiB of partial
 // states, compiled into the library so a call never needs to allocate.
@@ -1467,8 +1484,9 @@ cudaError_t launch_dequant(const DequantParams& p, cudaStream_t s) {
 }
 
 cudaError_t prepare_decode_launch() {
-  // the shared-memory limit is a per-device attribute: set it once per device
-  // (setting it twice from racing threads is harmless)
+  // the shared-memory limits (the decode kernel's, and the merge kernel's
+  // unused request) are per-device attributes: set them once per device
+  // (setting them twice from racing threads is harmless)
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1476,6 +1494,8 @@ cudaError_t prepare_decode_launch() {
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
   if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mkv_merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmemCap);
     if (e != cudaSuccess) return e;
     attr_set.fetch_or(bit, std::memory_order_acq_rel);
   }
@@ -1501,17 +1521,37 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   if (p.n * p.Hkv <= 0) return cudaSuccess;
+  // The merge blocks land on SMs as the decode CTAs leave them, so the first
+  // SMs to free up would take as many blocks as fit; an unused dynamic
+  // shared-memory request caps the blocks per SM at what spreads the grid
+  // over all SMs in one wave.  At one or two blocks per SM the registers of
+  // the prefetching variant cost no occupancy, so that variant runs.
+  // (the kernel's shared-memory limit is raised by prepare_decode_launch,
+  // which every decode launch, and a graph capture, runs first)
+  int dev = 0, n_sm = 0, smem_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e != cudaSuccess) return e;
+  const int grid = p.n * p.Hkv * p.G;
+  const int per_sm = (grid + n_sm - 1) / n_sm;
+  size_t dyn = 0;
+  if (per_sm <= 2) {
+    dyn = static_cast<size_t>(smem_sm / per_sm - 4096);
+    if (dyn > kMergeSmemCap) dyn = kMergeSmemCap;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n * p.Hkv * p.G);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kHeadDim);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mkv_merge_kernel, p);
+  return per_sm <= 2 ? cudaLaunchKernelEx(&cfg, mkv_merge_kernel<true>, p)
+                     : cudaLaunchKernelEx(&cfg, mkv_merge_kernel<false>, p);
 }
 
 }  // namespace mkv
