@@ -483,33 +483,54 @@ def run_mkv(args):
                 for t, nb in ((q, qb), (k, kb), (v, kb)):
                     hbuf[s][off:off + nb].copy_(t.contiguous().view(torch.uint8).reshape(-1))
                     off += seg(nb)
-        dbuf = torch.empty(L * layer_bytes, dtype=torch.uint8, device=dev)
+        # two device input buffers: step s + 1's copy (on a copy stream) runs
+        # while step s computes, as a serving loop would stage its inputs
+        dbufs = [torch.empty(L * layer_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
         views = []
-        for layer in range(L):
-            off = layer * layer_bytes
-            dq = dbuf[off:off + qb].view(w.q_dtype).view(w.n, w.Hq, w.D)
-            dk = dbuf[off + seg(qb):off + seg(qb) + kb].view(w.kv_dtype).view(w.n, w.Hkv, w.D)
-            off2 = off + seg(qb) + seg(kb)
-            dv = dbuf[off2:off2 + kb].view(w.kv_dtype).view(w.n, w.Hkv, w.D)
-            views.append((dq, dk, dv))
+        for dbuf in dbufs:
+            vb = []
+            for layer in range(L):
+                off = layer * layer_bytes
+                dq = dbuf[off:off + qb].view(w.q_dtype).view(w.n, w.Hq, w.D)
+                dk = dbuf[off + seg(qb):off + seg(qb) + kb].view(w.kv_dtype).view(w.n, w.Hkv, w.D)
+                off2 = off + seg(qb) + seg(kb)
+                dv = dbuf[off2:off2 + kb].view(w.kv_dtype).view(w.n, w.Hkv, w.D)
+                vb.append((dq, dk, dv))
+            views.append(vb)
         ho = torch.empty((w.n, w.Hq, w.D), dtype=torch.float32).pin_memory()
         hl = torch.empty((w.n, w.Hq), dtype=torch.float32).pin_memory()
         e2e_bytes = []
+        comp = torch.cuda.current_stream()
+        copy_stream = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]      # buffer i holds its step's inputs
+        ev_free = [torch.cuda.Event() for _ in range(2)]    # buffer i's previous step is done with it
         barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record()
+        f0.record(comp)
+
+        def stage(s):
+            i = s % 2
+            copy_stream.wait_event(f0 if s < 2 else ev_free[i])
+            with torch.cuda.stream(copy_stream):
+                dbufs[i].copy_(hbuf[s], non_blocking=True)
+            ev_in[i].record(copy_stream)
+
+        stage(0)
         for s in range(e2e_steps):
+            if s + 1 < e2e_steps:
+                stage(s + 1)
             stepper.pre_step()
             e2e_bytes.append(kv_bytes_now(pool, P, L)[0])
-            dbuf.copy_(hbuf[s], non_blocking=True)
+            comp.wait_event(ev_in[s % 2])
             for layer in range(L):
-                dq, dk, dv = views[layer]
+                dq, dk, dv = views[s % 2][layer]
                 o, l_ = stepper.layer(layer, dk, dv, dq, *outs[layer])
+            ev_free[s % 2].record(comp)
             ho.copy_(o, non_blocking=True)
             hl.copy_(l_, non_blocking=True)
-        f1.record()
+        f1.record(comp)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
@@ -518,8 +539,9 @@ def run_mkv(args):
         d2h = w.n * (w.Hq * w.D * 4 + w.Hq * 4)
         e2e = {"value": e2e_job / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps,
-               "copies_per_step": "one host-to-device copy of every layer's q, k, v; the last layer's out "
-                                  "and lse back"}
+               "copies_per_step": "one host-to-device copy of every layer's q, k, v (on a copy stream, into "
+                                  "one of two device buffers, overlapping the previous step); the last "
+                                  "layer's out and lse back"}
     # ---------------- CPU oracle baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
