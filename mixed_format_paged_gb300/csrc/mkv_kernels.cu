@@ -630,6 +630,7 @@ constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
 constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
 constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
 static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+static_assert(kFp8Blk == 16 && kTq3Blk == 32, "block_locate shifts by log2 of the blocks per 64- or 128-token page");
 static_assert(kQBytes == kRedFloats * 4, "a q buffer doubles as a reduction buffer");
 static_assert(kDecWarps >= kMaxGroup, "warp h builds row h of a piece's q fragments");
 
@@ -685,10 +686,12 @@ __device__ __forceinline__ Piece load_piece(const DecodeParams& p, int si) {
 // (<= 0: the block is empty).
 __device__ __forceinline__ int block_locate(const DecodeParams& p, const Piece& pc, int k, int& e, int& tok0) {
   const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
-  const int bpp = p.P / bt;
+  // blocks per page P / bt is a power of two (P is 64 or 128, bt 16 or 32):
+  // shift and mask instead of a division by a run-time value
+  const int lg = (p.P == 128 ? 3 : 2) - (pc.fmt ? 1 : 0);
   const int bb = pc.blk0 + k;
-  e = pc.entry0 + bb / bpp;
-  tok0 = (bb % bpp) * bt;
+  e = pc.entry0 + (bb >> lg);
+  tok0 = (bb & ((1 << lg) - 1)) * bt;
   return min(bt, static_cast<int>(p.entries[e].nvalid) - tok0);
 }
 
