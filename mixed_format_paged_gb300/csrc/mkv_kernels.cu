@@ -724,10 +724,12 @@ struct BlockCursor {
 
 // Lane 0: copy a block (page entry pe, first token tok0, nv valid tokens) of
 // piece pc into slot st (mbarrier bar), or complete the slot's phase without
-// bytes for an empty block or a bad plan entry.
-__device__ __noinline__ void dec_issue_entry(const DecodeParams& p, Piece pc, PageEntry pe, int tok0, int nv,
-                                             uint8_t* st, uint64_t* bar, int* abort_flag) {
-  const int nslots = pc.fmt ? p.tq3_slots : p.fp8_slots;
+// bytes for an empty block or a bad plan entry.  Inlined, per format: as an
+// out-of-line call it cost 5 % of the kernel (the call once per block).
+template <int FMT>
+__device__ __forceinline__ void dec_issue_fmt(const DecodeParams& p, const Piece& pc, PageEntry pe, int tok0, int nv,
+                                              uint8_t* st, uint64_t* bar, int* abort_flag) {
+  const int nslots = FMT ? p.tq3_slots : p.fp8_slots;
   if (nv <= 0) {
     mbar_arrive(bar);
     return;
@@ -738,13 +740,13 @@ __device__ __noinline__ void dec_issue_entry(const DecodeParams& p, Piece pc, Pa
     mbar_arrive(bar);
     return;
   }
-  const int row = pc.fmt ? 3 * kHeadDim / 8 : kHeadDim;
-  const int bt = pc.fmt ? kTq3Blk : kFp8Blk;
+  constexpr int row = FMT ? 3 * kHeadDim / 8 : kHeadDim;
+  constexpr int bt = FMT ? kTq3Blk : kFp8Blk;
   const int plane = p.P * (row + 2);
-  const uint8_t* hp = (pc.fmt ? p.tq3_layer : p.fp8_layer) +
-                      static_cast<int64_t>(pe.slot) * (pc.fmt ? p.tq3_page_bytes : p.fp8_page_bytes) +
+  const uint8_t* hp = (FMT ? p.tq3_layer : p.fp8_layer) +
+                      static_cast<int64_t>(pe.slot) * (FMT ? p.tq3_page_bytes : p.fp8_page_bytes) +
                       static_cast<int64_t>(pc.kvh) * 2 * plane;
-  const uint32_t code = bt * row;
+  constexpr uint32_t code = bt * row;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   mbar_expect_tx(bar, 2 * (code + 2 * bt));
   const uint64_t pol = l2_evict_first_policy();
@@ -752,6 +754,13 @@ __device__ __noinline__ void dec_issue_entry(const DecodeParams& p, Piece pc, Pa
   bulk_g2s_hint(st + code, hp + p.P * row + 2 * tok0, 2 * bt, bar, pol);
   bulk_g2s_hint(st + code + 2 * bt, hp + plane + tok0 * row, code, bar, pol);
   bulk_g2s_hint(st + 2 * code + 2 * bt, hp + plane + p.P * row + 2 * tok0, 2 * bt, bar, pol);
+}
+__device__ __forceinline__ void dec_issue_entry(const DecodeParams& p, const Piece& pc, PageEntry pe, int tok0, int nv,
+                                                uint8_t* st, uint64_t* bar, int* abort_flag) {
+  if (pc.fmt)
+    dec_issue_fmt<1>(p, pc, pe, tok0, nv, st, bar, abort_flag);
+  else
+    dec_issue_fmt<0>(p, pc, pe, tok0, nv, st, bar, abort_flag);
 }
 
 // Lane 0: locate block k of piece pc and copy it into slot st.
