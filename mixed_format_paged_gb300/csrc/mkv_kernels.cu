@@ -996,9 +996,9 @@ __device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* 
     sc[t][1] = (sacc[t][0][1] + sacc[t][0][3]) * (k0.y * scale);
     sc[t][2] = (sacc[t][1][0] + sacc[t][1][2]) * (k1.x * scale);
     sc[t][3] = (sacc[t][1][1] + sacc[t][1][3]) * (k1.y * scale);
-    if (g >= p.G) {
-      sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = -INFINITY;
-    } else if (nv < B::kTokens) {
+    // rows g >= G of q are zero, so those heads score 0 on every token: they
+    // never trigger a rescale, and the piece end drops them (m = -inf)
+    if (nv < B::kTokens) {
       const int tb = 16 * t + 2 * c;
       if (tb >= nv) sc[t][0] = -INFINITY;
       if (tb + 1 >= nv) sc[t][1] = -INFINITY;
