@@ -844,6 +844,10 @@ __device__ __forceinline__ void dec_build_q_row(const DecodeParams& p, uint4* qb
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] *= (1.0f / 16.0f);
   }
+  // the score scale log2(e)/sqrt(d) goes into q here, once per piece, so the
+  // scores come out of the MMAs already in log2 units
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] *= p.score_scale;
 #pragma unroll
   for (int jj = 0; jj < 2; ++jj) {
     float hi[4], lo[4];
@@ -985,17 +989,16 @@ __device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* 
     dec_qk_tq3(st + B::kK, g, c, qs, lut, sacc);
   const __half2* ks = reinterpret_cast<const __half2*>(st + B::kKs);
   const __half2* vs = reinterpret_cast<const __half2*>(st + B::kVs);
-  const float scale = p.score_scale;
   // lane's tokens in tile t: 16t + 2c + {0, 1} (half 0) and 16t + 8 + 2c + {0, 1} (half 1)
   float sc[NT][4];
   float mt = -INFINITY;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const float2 k0 = __half22float2(ks[8 * t + c]), k1 = __half22float2(ks[8 * t + 4 + c]);
-    sc[t][0] = (sacc[t][0][0] + sacc[t][0][2]) * (k0.x * scale);
-    sc[t][1] = (sacc[t][0][1] + sacc[t][0][3]) * (k0.y * scale);
-    sc[t][2] = (sacc[t][1][0] + sacc[t][1][2]) * (k1.x * scale);
-    sc[t][3] = (sacc[t][1][1] + sacc[t][1][3]) * (k1.y * scale);
+    sc[t][0] = (sacc[t][0][0] + sacc[t][0][2]) * k0.x;
+    sc[t][1] = (sacc[t][0][1] + sacc[t][0][3]) * k0.y;
+    sc[t][2] = (sacc[t][1][0] + sacc[t][1][2]) * k1.x;
+    sc[t][3] = (sacc[t][1][1] + sacc[t][1][3]) * k1.y;
     // rows g >= G of q are zero, so those heads score 0 on every token: they
     // never trigger a rescale, and the piece end drops them (m = -inf)
     if (nv < B::kTokens) {
