@@ -339,15 +339,16 @@ int npages_for(int len, int P) { return (len + P - 1) / P; }
 // block and per piece, in units of one TQ3 token.  Fitted to per-CTA times of
 // the decode kernel (GB300, 12 warps): a 32-token TQ3 block ~0.31 us of CTA
 // time, a 16-token FP8 block ~0.25 us, a piece ~4 us (its end-of-piece merge
-// and the warps' drift before it).  The planner works in integers, 1/100 of
-// these units, so that its split is exact: a block costs
+// and the warps' drift before it; set to 630 after the blocks got cheaper, by
+// a sweep of step times on four workloads).  The planner works in integers,
+// 1/100 of these units, so that its split is exact: a block costs
 //   (20 per TQ3 token or 29 per FP8 token + 160) / 20 units,
 // a round of n <= 12 blocks its slowest block times 12 (0.4 + 0.6 n / 12) =
-// (24 + 3 n) / 5, and a piece 540.
+// (24 + 3 n) / 5, and a piece 630.
 constexpr int64_t kCostTq3Token = 20;    // 1.0 x 20
 constexpr int64_t kCostFp8Token = 29;    // 1.45 x 20
 constexpr int64_t kCostBlock = 160;      // 8 x 20
-constexpr int64_t kCostPiece = 54000;    // 540 x 100
+constexpr int64_t kCostPiece = 63000;    // 630 x 100
 constexpr int kMinBlocksPerCta = 24;     // two blocks per warp at least
 constexpr int kPlanRecord = 9;           // ints per split in mkv_plan_decode's output
 

@@ -226,7 +226,7 @@ def test_plan_covers_every_page_once(mkv):
         # warp-round of blocks; there are at most a few chunks per CTA
         def cost(c):
             bt, per_tok = (32, 1.0) if c[2] == 3 else (16, 1.45)
-            return c[5] * per_tok + 8.0 * -(-c[5] // bt) + 540.0
+            return c[5] * per_tok + 8.0 * -(-c[5] // bt) + 630.0
         nblk = sum(-(-c[5] // (32 if c[2] == 3 else 16)) for c in plan)
         share = sum(cost(c) for c in plan) / max(1, min(152, nblk // 24))
         assert max(cost(c) for c in plan) <= share + 12 * 40.0
@@ -297,13 +297,13 @@ def _blocks_of(layouts, P, H=4):
     return groups
 
 
-PIECE = 54000
+PIECE = 63000
 
 
 def _piece_cost(costs):
     """A piece of blocks with these costs, in the planner's model: rounds of
     12 blocks from the piece's first, each costing its slowest block x
-    (24 + 3 n) for n blocks, plus 54000 for the piece."""
+    (24 + 3 n) for n blocks, plus 63000 for the piece."""
     return PIECE + sum(max(costs[i:i + 12]) * (24 + 3 * len(costs[i:i + 12])) for i in range(0, len(costs), 12))
 
 
