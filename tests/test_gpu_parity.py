@@ -448,16 +448,17 @@ def test_relevance_stepper_anchors_the_attended_page(mkv):
 
 
 # ------------------------------------------------------------------ step graph
+@pytest.mark.parametrize("P", [64, 128])
 @pytest.mark.parametrize("append", [True, False])
-def test_step_graph_matches_per_layer_calls(mkv, append):
+def test_step_graph_matches_per_layer_calls(mkv, append, P):
     """mkv_step_graph_*: one recorded launch per step over every layer gives,
     bit for bit, what the per-layer calls give -- through re-plans (the
     batch grows every step) and a demotion between steps -- and the oracle
     agrees with it."""
     g = torch.Generator().manual_seed(31)
     L = 3
-    pools = [_small_pool(mkv, P=64, layers=L, fp8=64, tq3=64, maxp=24, seed=79) for _ in range(2)]
-    lens = [64 * 5 + 62, 64 * 3 + 1, 7]
+    pools = [_small_pool(mkv, P=P, layers=L, fp8=64, tq3=64, maxp=24, seed=79) for _ in range(2)]
+    lens = [P * 5 + P - 2, P * 3 + 1, 7]              # request 0 opens a new page during the steps
     data = [[(torch.randn(n, 4, 256, generator=g).to(torch.bfloat16), torch.randn(n, 4, 256, generator=g).to(torch.bfloat16))
              for _ in range(L)] for n in lens]
     for pool in pools:
