@@ -241,13 +241,17 @@ mkv_status mkv_decode_attention(mkv_pool* pool, int32_t layer, int32_t n, const 
  * token per step; this call extends the same attention, partial states and
  * merge causally: the last nq tokens of each sequence (already appended, so
  * the sequence holds len >= nq tokens) are the queries, and query token i
- * (position len - nq + i) attends to tokens 0 .. len - nq + i.  The result
- * is exactly mkv_decode_attention run nq times over the growing prefix.
+ * (position len - nq + i) attends to tokens 0 .. len - nq + i: the
+ * attention of mkv_decode_attention run nq times over the growing prefix
+ * (bit-identical to it for nq = 1; within rounding for nq >= 2).
  * q: device [n, nq, H_q, d] of `dtype`; out: device fp32 [n, nq, H_q, d];
  * lse: device fp32 [n, nq, H_q].  The pages that hold the query tokens must
- * be FP8 (they are the newest, so Recent).  The plan holds n * nq batch
- * entries (query token i of request b is entry b * nq + i), each reading its
- * own prefix.  Errors: those of mkv_decode_attention; INVALID_ARGUMENT for
+ * be FP8 (they are the newest, so Recent).  With nq >= 2 the query tokens
+ * go in pairs: the plan holds n * ceil(nq / 2) batch entries, entry
+ * b * ceil(nq / 2) + j reading request b's prefix up to its query token
+ * min(2j + 1, nq - 1) for query tokens 2j and 2j + 1 together (each block is
+ * dequantised once for both; token 2j masks the prefix's last token).
+ * Errors: those of mkv_decode_attention; INVALID_ARGUMENT for
  * nq < 1, n * nq > max_batch or a sequence shorter than nq; INVALID_STATE
  * when a query token sits in a TQ3 page. */
 mkv_status mkv_decode_attention_multi(mkv_pool* pool, int32_t layer, int32_t n, const int32_t* seq_ids,
@@ -306,8 +310,10 @@ mkv_status mkv_plan_decode(mkv_pool* pool, int32_t n, const int32_t* seq_ids, in
                            int32_t cap, int32_t* n_chunks);
 
 /* The same for mkv_decode_attention_multi with nq query tokens per request:
- * split records use batch index b * nq + i for query token i of request b
- * (its prefix up to that token).  Errors: those of mkv_decode_attention_multi. */
+ * with nq = 1 the decode plan; with nq >= 2 split records use batch index
+ * b * ceil(nq / 2) + j for query tokens 2j and 2j + 1 of request b (the
+ * prefix up to query token min(2j + 1, nq - 1)).  Errors: those of
+ * mkv_decode_attention_multi. */
 mkv_status mkv_plan_decode_multi(mkv_pool* pool, int32_t n, const int32_t* seq_ids, int32_t nq, int32_t* chunks,
                                  int32_t cap, int32_t* n_chunks);
 

@@ -361,11 +361,23 @@ constexpr int kPlanRecord = 9;           // ints per split in mkv_plan_decode's 
 mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq, bool upload, cudaStream_t stream) {
   const int P = p->cfg.page_size, H = p->cfg.num_kv_heads;
   const PlanLayout L = plan_layout(p->entry_cap, p->chunk_cap, effective_batch(p->cfg), H);
-  // With nq query tokens per request the plan holds n_req * nq batch
-  // entries: entry b * nq + i is request ids[b] cut after its token
-  // len - nq + i (query token i sees that prefix).
-  const int n = n_req * nq;
+  // One query token per request (nq = 1): entry b is request ids[b].  Several
+  // (nq >= 2): the query tokens go in pairs, qpe = 2 per batch entry, which
+  // the decode kernel serves from one dequantisation of each block; entry
+  // b * npair + j (npair = ceil(nq / 2)) is request ids[b] cut after its query
+  // token i1 = min(2j + 1, nq - 1), i.e. after its token len - nq + i1; query
+  // token 2j sees that prefix but its last token (when 2j + 1 < nq).
+  const int qpe = nq == 1 ? 1 : 2;
+  const int npair = (nq + qpe - 1) / qpe;
+  const int W = dec_warps(qpe);
+  const int n = n_req * npair;
   if (n > effective_batch(p->cfg)) return fail(MKV_ERR_CAPACITY, "%d requests x %d query tokens > max_batch", n_req, nq);
+  // planner costs: a paired block runs both query tokens' MMAs and softmax on
+  // one dequantisation, and a paired piece ends with two merges
+  const int64_t cost_tq3 = qpe == 1 ? kCostTq3Token : kCostTq3Token * 3 / 2;
+  const int64_t cost_fp8 = qpe == 1 ? kCostFp8Token : kCostFp8Token * 3 / 2;
+  const int64_t cost_piece = qpe == 1 ? kCostPiece : 2 * kCostPiece;
+  const int64_t round_full = 24 + 3 * int64_t(W);   // a round of W blocks, in units of its slowest block
   std::vector<PageEntry> entries;
   entries.reserve(size_t(n) * 64);
   struct BatchPages {
@@ -373,15 +385,17 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   };
   std::vector<BatchPages> bp(n);
   for (int b = 0; b < n; ++b) {
-    const SeqRec& s = p->seqs[ids[b / nq]];
-    const int len = s.len - (nq - 1 - b % nq);
+    const SeqRec& s = p->seqs[ids[b / npair]];
+    const int i1 = std::min(2 * (b % npair) + 1, nq - 1);
+    const int len = s.len - (nq - 1 - i1);
+    const int16_t tail = nq == 1 ? 1 : (2 * (b % npair) + 1 < nq ? kTailPairLast : 0);
     const int np = npages_for(len, P);
     BatchPages& B = bp[b];
     B.f_first = int(entries.size());
     for (int i = 0; i < np; ++i) {
       const int nv = (i == np - 1) ? len - i * P : P;
       if (s.pages[i].tier != MKV_TIER_STALE)
-        entries.push_back({s.pages[i].slot, int16_t(nv), int16_t(i == np - 1 && nq == 1 ? 1 : 0)});
+        entries.push_back({s.pages[i].slot, int16_t(nv), int16_t(i == np - 1 ? tail : 0)});
     }
     B.f_count = int(entries.size()) - B.f_first;
     B.t_first = int(entries.size());
@@ -412,9 +426,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   // page, up to the last valid token (a block past a page's valid tokens is
   // empty and only costs its overhead).  Only a group's last page can be
   // partial, so a block's tokens never increase along the group.
-  // Rounds: a CTA's warps take a piece's blocks round-robin (block k of the
-  // piece on warp k mod kDecWarps), so a piece runs in rounds of up to
-  // kDecWarps blocks from its own first block on, and the next piece starts
+  // Rounds: a CTA's W warps take a piece's blocks round-robin (block k of the
+  // piece on warp k mod W), so a piece runs in rounds of up to W blocks from
+  // its own first block on, and the next piece starts
   // after all of them.  A round costs its slowest block -- its first, since a
   // block's tokens never increase along a group -- on every warp; a short
   // round, with warps idle, runs its blocks faster and is priced between the
@@ -432,7 +446,7 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   };
   auto blk_cost = [&](int gi, int k) {
     const Group& g = groups[gi];
-    return int64_t(blk_tokens(g, k)) * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
+    return int64_t(blk_tokens(g, k)) * (g.fmt ? cost_tq3 : cost_fp8) + kCostBlock;
   };
   int64_t total_blocks = 0, lo = 0, hi = 0;
   for (int gi = 0; gi < ng; ++gi) {
@@ -441,11 +455,11 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     const int last_nv = entries[g.entry0 + g.nentry - 1].nvalid;
     g_nblk[gi] = (g.nentry - 1) * (P / bt) + (last_nv + bt - 1) / bt;
     g_uni[gi] = (g.nentry - 1) * (P / bt) + last_nv / bt;
-    g_w[gi] = int64_t(bt) * (g.fmt ? kCostTq3Token : kCostFp8Token) + kCostBlock;
+    g_w[gi] = int64_t(bt) * (g.fmt ? cost_tq3 : cost_fp8) + kCostBlock;
     total_blocks += g_nblk[gi];
     // a CTA holds one block at least; the whole batch as one CTA fits hi
-    lo = std::max(lo, kCostPiece + blk_cost(gi, 0) * 27);
-    hi += kCostPiece + blk_cost(gi, 0) * 60 * ((g_nblk[gi] + kDecWarps - 1) / kDecWarps);
+    lo = std::max(lo, cost_piece + blk_cost(gi, 0) * 27);
+    hi += cost_piece + blk_cost(gi, 0) * round_full * ((g_nblk[gi] + W - 1) / W);
   }
   // The largest b1 in [b0, nblk] such that the piece [b0, b1) of group gi
   // costs at most `budget` (b0 when not one block fits); *cost gets its cost.
@@ -461,19 +475,19 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
       used += n > 0 ? worst * (24 + 3 * int64_t(n)) : 0;
     };
     if (b < uni) {
-      const int64_t w = g_w[gi], whole = (uni - b) / kDecWarps;
-      const int64_t take = std::min<int64_t>(whole, budget / (60 * w));
-      b += int(take) * kDecWarps;
-      used += take * 60 * w;
+      const int64_t w = g_w[gi], whole = (uni - b) / W;
+      const int64_t take = std::min<int64_t>(whole, budget / (round_full * w));
+      b += int(take) * W;
+      used += take * round_full * w;
       if (take < whole) {       // the budget ends among full blocks
-        short_round(w, kDecWarps);
+        short_round(w, W);
         *cost = used;
         return b;
       }
     }
     while (b < nblk) {
       const int64_t worst = blk_cost(gi, b);
-      const int avail = std::min(kDecWarps, nblk - b);
+      const int avail = std::min(W, nblk - b);
       if (used + worst * (24 + 3 * avail) > budget) {
         short_round(worst, avail);
         break;
@@ -504,18 +518,18 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     for (int gi = 0; gi < ng; ++gi)
       for (int b = 0; b < g_nblk[gi];) {
         int64_t c = 0;
-        int b1 = (n_cta > 0 && acc + kCostPiece < bound) ? piece_end(gi, b, bound - acc - kCostPiece, &c) : b;
+        int b1 = (n_cta > 0 && acc + cost_piece < bound) ? piece_end(gi, b, bound - acc - cost_piece, &c) : b;
         if (b1 == b) {           // a new CTA takes the next block
           if (++n_cta > max_cta) return n_cta;
           if (starts) starts->push_back({gi, b});
           acc = 0;
-          b1 = piece_end(gi, b, bound - kCostPiece, &c);
+          b1 = piece_end(gi, b, bound - cost_piece, &c);
           if (b1 == b) {         // below the one-block bound (not reached: bound >= lo)
             b1 = b + 1;
             c = blk_cost(gi, b) * 27;
           }
         }
-        acc += kCostPiece + c;
+        acc += cost_piece + c;
         b = b1;
       }
     return n_cta;
@@ -563,7 +577,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     }
   }
   cta_seg[ncta] = int(segs.size());
-  if (int(segs.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
+  // the workspace holds chunk_cap partial states of G heads; a paired piece
+  // writes qpe of them
+  if (int64_t(segs.size()) * qpe > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
   // partial-state indices: pieces are in group order, so each group's are contiguous
   for (Group& g : groups) g.nparts = 0;
   for (int i = 0; i < int(segs.size()); ++i) {
@@ -620,6 +636,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   dp.score_scale = float(1.4426950408889634 / std::sqrt(double(kHeadDim)));
   dp.lut = p->lut;
   dp.err = p->err;
+  dp.qpe = qpe;
+  dp.nq = nq;
+  dp.npair = npair;
   MergeParams& mp = p->merge_params;
   mp = MergeParams{};
   mp.part = p->workspace;
@@ -628,6 +647,9 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   mp.Hq = p->cfg.num_q_heads;
   mp.Hkv = H;
   mp.G = p->G;
+  mp.qpe = qpe;
+  mp.nq = nq;
+  mp.npair = npair;
   std::memcpy(mp.signs, p->signs, sizeof mp.signs);
   if (!upload) return MKV_OK;
   Staging& sp = p->st_plan[p->plan_buf];

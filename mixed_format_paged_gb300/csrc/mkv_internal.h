@@ -12,6 +12,9 @@ namespace mkv {
 constexpr int kHeadDim = 256;      // head_dim the kernels are written for
 constexpr int kMaxGroup = 8;       // q heads per kv head held in one MMA tile
 constexpr int kDecWarps = 12;     // warps of a decode CTA (a piece's blocks go round-robin)
+constexpr int kDecWarpsPair = 8;  // warps of a decode CTA whose batch entries hold two query tokens
+// warps of a decode CTA with `qpe` query tokens per batch entry
+constexpr int dec_warps(int qpe) { return qpe == 1 ? kDecWarps : kDecWarpsPair; }
 constexpr int kFp8Blk = 16;        // tokens per FP8 decode block (one MMA tile)
 constexpr int kTq3Blk = 32;        // tokens per TQ3 decode block (two MMA tiles)
 constexpr int kTileTokens = 16;    // tokens per consumer-warp tile
@@ -28,8 +31,11 @@ struct PageEntry {         // one page of one batch entry in a decode plan
   int32_t slot;            // physical slot in the tier's arena
   int16_t nvalid;          // tokens written in the page (1..P)
   int16_t tail;            // 1 for a request's last page: it may be written by the
-                           // kernel just before the decode kernel (fused append)
+                           // kernel just before the decode kernel (fused append);
+                           // kTailPairLast for the last page of a paired entry
+                           // whose first query token does not see the last token
 };
+constexpr int16_t kTailPairLast = 2;
 
 struct Group {             // one run of pages: (request, kv head, format)
   int32_t b;               // batch index
@@ -78,7 +84,7 @@ struct DecodeParams {
   const Group* groups;
   const Segment* segs;             // per-CTA pieces, CTA by CTA
   const void* q;                   // [n, Hq, D], fp32 or bf16
-  float* part;                     // [parts][G][2 + D] (m in log2 units, l, o)
+  float* part;                     // [parts][qpe * G][2 + D] (m in log2 units, l, o)
   // fused single-token append (mkv_append_decode): each request's newest
   // token (the last valid one of its tail page), rows k/v [n, Hkv, D]
   const void* k;
@@ -93,6 +99,9 @@ struct DecodeParams {
   float score_scale;               // log2(e) / sqrt(d)
   int32_t append;
   int32_t kv_bf16;
+  // query tokens: batch entry b holds query tokens s < qpe (1, or 2 for the
+  // paired multi-query decode); its q / out row is q_row(b, s) (see below)
+  int32_t qpe, nq, npair;
   // per CTA: when `heads` is set (graph launches), CTA i's pieces are
   // segs[heads[i] .. heads[i + 1]) and cta_seg / first are unused
   const int32_t* heads;
@@ -103,11 +112,24 @@ struct DecodeParams {
 struct MergeParams {
   const float* part;
   const MergeDesc* desc;           // [n * Hkv]
-  float* out;                      // [n, Hq, D]
-  float* lse;                      // [n, Hq]
+  float* out;                      // [rows, Hq, D]
+  float* lse;                      // [rows, Hq]
   int32_t n, Hq, Hkv, G;
+  int32_t qpe, nq, npair;          // as in DecodeParams
   uint64_t signs[4];
 };
+
+// Row of q / out / lse for query token s of batch entry b.  One query token
+// per entry (qpe 1): row b.  Paired entries (qpe 2; nq query tokens per
+// request, npair = ceil(nq / 2) entries per request): entry b is request
+// b / npair with its query tokens 2 (b % npair) and 2 (b % npair) + 1; with
+// nq odd the last entry's second token repeats its first.
+__host__ __device__ inline int q_row(int b, int s, int qpe, int nq, int npair) {
+  if (qpe == 1) return b;
+  const int r = b / npair, j = b - r * npair;
+  const int i = 2 * j + s;
+  return r * nq + (i < nq ? i : nq - 1);
+}
 
 struct AppendParams {
   uint8_t* fp8_layer;              // FP8 arena base of this layer

@@ -573,7 +573,8 @@ __global__ void __launch_bounds__(128) mkv_relevance_kernel(RelevanceParams p) {
 }
 
 // ============================================================== decode
-// Persistent partial-attention kernel; one CTA of kDecWarps (12) warps per SM.
+// Persistent partial-attention kernel; one CTA of 12 warps per SM (8 for
+// batch entries of two query tokens).
 // The host cut the launch's blocks into one contiguous piece list per CTA,
 // minimising the largest CTA's estimated cost (a piece is a run of blocks of
 // one (request, kv head, format) group).  Within a piece, warp w takes blocks
@@ -591,7 +592,6 @@ __global__ void __launch_bounds__(128) mkv_relevance_kernel(RelevanceParams p) {
 // warp's block kSlots further on as soon as the warp is done with it.  No
 // warp waits for another except at the end of a piece, where the warps'
 // states merge, in a fixed order, into one partial state (m, l, o) per q head.
-constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kSlots = 2;                 // staging slots per warp
 constexpr int kSlotBytes = 2 * (kFp8Blk * kHeadDim + 2 * kFp8Blk);   // an FP8 block; a TQ3 block fits
 
@@ -614,35 +614,46 @@ constexpr int kRedBufs = 2;                    // O buffers of the piece-end red
 constexpr int kRedFloats = 16 * 4 * 32;        // one warp's O fragments, lane-major
 constexpr int kQBytes = kQfragWords * 4;       // one piece's q fragments
 
+// CTA shape for NQ query tokens per batch entry (1, or 2 for the paired
+// multi-query decode: both queries' O in registers take 8 warps' worth of
+// the register file where one query's take 12).
+template <int NQ>
+struct DecCfg {
+  static constexpr int kWarps = dec_warps(NQ);
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kSmemRing = kWarps * kSlots * kSlotBytes;
+  static constexpr int kSmemQ = 2 * NQ * kQBytes;             // [piece i, i+1][query][k-step][lane]
+  static constexpr int kSmemRed = kRedBufs * kRedFloats * 4;
+  static constexpr int kSmemEpi = 2 * NQ * kWarps * kMaxGroup * 4;
+  static constexpr int kSmemBars = kWarps * kSlots * 8 + 16;
+  static constexpr int kSmemBytes = kSmemRing + kSmemQ + kSmemRed + kSmemEpi + kSmemBars;
+  static_assert(kSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+  static_assert(kWarps >= kMaxGroup, "warp h builds row h of a piece's q fragments");
+};
+
 struct DecSmem {
   uint8_t* ring;                               // [warp][slot] kSlotBytes
-  uint4* qbuf;                                 // [2][k-step 16][lane 32]: q fragments of pieces i, i+1
+  uint4* qbuf;                                 // [2][NQ][k-step 16][lane 32]: q fragments of pieces i, i+1
   float* red;                                  // [kRedBufs][kRedFloats]
-  float* epi_m;                                // [warp][kMaxGroup]
+  float* epi_m;                                // [query][warp][kMaxGroup]
   float* epi_l;
   uint64_t* full;                              // [warp][slot]
   int* abort_flag;
 };
-constexpr int kDecSmemRing = kDecWarps * kSlots * kSlotBytes;
-constexpr int kDecSmemQ = 2 * kQBytes;
-constexpr int kDecSmemRed = kRedBufs * kRedFloats * 4;
-constexpr int kDecSmemEpi = 2 * kDecWarps * kMaxGroup * 4;
-constexpr int kDecSmemBars = kDecWarps * kSlots * 8 + 16;
-constexpr int kDecSmemBytes = kDecSmemRing + kDecSmemQ + kDecSmemRed + kDecSmemEpi + kDecSmemBars;
-static_assert(kDecSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
 static_assert(kFp8Blk == 16 && kTq3Blk == 32, "block_locate shifts by log2 of the blocks per 64- or 128-token page");
 static_assert(kQBytes == kRedFloats * 4, "a q buffer doubles as a reduction buffer");
-static_assert(kDecWarps >= kMaxGroup, "warp h builds row h of a piece's q fragments");
 
+template <int NQ>
 __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
+  using C = DecCfg<NQ>;
   DecSmem s;
   s.ring = base;
-  s.qbuf = reinterpret_cast<uint4*>(base + kDecSmemRing);
-  s.red = reinterpret_cast<float*>(base + kDecSmemRing + kDecSmemQ);
+  s.qbuf = reinterpret_cast<uint4*>(base + C::kSmemRing);
+  s.red = reinterpret_cast<float*>(base + C::kSmemRing + C::kSmemQ);
   s.epi_m = s.red + kRedBufs * kRedFloats;
-  s.epi_l = s.epi_m + kDecWarps * kMaxGroup;
-  s.full = reinterpret_cast<uint64_t*>(s.epi_l + kDecWarps * kMaxGroup);
-  s.abort_flag = reinterpret_cast<int*>(s.full + kDecWarps * kSlots);
+  s.epi_l = s.epi_m + NQ * C::kWarps * kMaxGroup;
+  s.full = reinterpret_cast<uint64_t*>(s.epi_l + NQ * C::kWarps * kMaxGroup);
+  s.abort_flag = reinterpret_cast<int*>(s.full + C::kWarps * kSlots);
   return s;
 }
 
@@ -696,7 +707,8 @@ __device__ __forceinline__ int block_locate(const DecodeParams& p, const Piece& 
 }
 
 // The warp's sequence of blocks over the CTA's pieces (block k of piece si,
-// k = warp, warp + kDecWarps, ...).  Every lane keeps the same cursor.
+// k = warp, warp + W, ... for W warps).  Every lane keeps the same cursor.
+template <int W>
 struct BlockCursor {
   int si, s1, k;
   int issued;              // lane 0: blocks copied in so far
@@ -717,7 +729,7 @@ struct BlockCursor {
   }
   __device__ bool valid() const { return si < s1; }
   __device__ void advance(const DecodeParams& p, int warp) {
-    k += kDecWarps;
+    k += W;
     settle(p, warp);
   }
 };
@@ -771,16 +783,17 @@ __device__ __forceinline__ void dec_issue(const DecodeParams& p, const Piece& pc
   dec_issue_entry(p, pc, p.entries[e], tok0, nv, st, bar, abort_flag);
 }
 
-// Raw q row h of piece pc (8 dims per lane, bf16 in r[0] or fp32 in r[0..1]);
-// zeros for h >= G.  Split from dec_build_q_row so the load can be issued a
-// piece ahead.
+// Raw q row h of query token s of piece pc (8 dims per lane, bf16 in r[0]
+// or fp32 in r[0..1]); zeros for h >= G.  Split from dec_build_q_row so the
+// load can be issued a piece ahead.
 struct QRow {
   uint4 r[2];
 };
-__device__ __forceinline__ QRow dec_load_q_row(const DecodeParams& p, const Piece& pc, int h, int lane) {
+__device__ __forceinline__ QRow dec_load_q_row(const DecodeParams& p, const Piece& pc, int s, int h, int lane) {
   QRow q{};
   if (h < p.G) {
-    const size_t off = (static_cast<size_t>(pc.b) * p.Hq + pc.kvh * p.G + h) * kHeadDim + 8 * lane;
+    const int row = q_row(pc.b, s, p.qpe, p.nq, p.npair);
+    const size_t off = (static_cast<size_t>(row) * p.Hq + pc.kvh * p.G + h) * kHeadDim + 8 * lane;
     if (p.q_bf16) {
       q.r[0] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + off);
     } else {
@@ -872,10 +885,12 @@ __device__ __forceinline__ void load_unit_pair(const uint8_t* p, uint32_t (&u)[6
 }
 
 // S for the one 16-token tile of an FP8 block (two n8 halves: tokens g and
-// 8+g as B columns); K rows are row-major, the thread's 64 dims are 64 bytes.
-// A (q) comes k-step by k-step from shared memory.
-__device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint4* qs, float (&s0)[4],
-                                           float (&s1)[4]) {
+// 8+g as B columns) and each of the NQ query tokens; K rows are row-major,
+// the thread's 64 dims are 64 bytes.  A (q) comes k-step by k-step from
+// shared memory; each dequantised K fragment feeds every query's MMAs.
+template <int NQ>
+__device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, const uint4* const (&qs)[NQ],
+                                           float (&s)[NQ][2][2][4]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
@@ -885,18 +900,25 @@ __device__ __forceinline__ void dec_qk_fp8(const uint8_t* kt, int g, int c, cons
     const uint32_t x1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 a = qs[(4 * q4 + i) * 32 + lane];
-      mma16816(s0, a.x, a.y, a.z, a.w, e4m3x2_to_f16x2(x0[i]), e4m3x2_to_f16x2(x0[i] >> 16));
-      mma16816(s1, a.x, a.y, a.z, a.w, e4m3x2_to_f16x2(x1[i]), e4m3x2_to_f16x2(x1[i] >> 16));
+      const uint32_t b00 = e4m3x2_to_f16x2(x0[i]), b01 = e4m3x2_to_f16x2(x0[i] >> 16);
+      const uint32_t b10 = e4m3x2_to_f16x2(x1[i]), b11 = e4m3x2_to_f16x2(x1[i] >> 16);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const uint4 a = qs[q][(4 * q4 + i) * 32 + lane];
+        mma16816(s[q][0][0], a.x, a.y, a.z, a.w, b00, b01);
+        mma16816(s[q][0][1], a.x, a.y, a.z, a.w, b10, b11);
+      }
     }
   }
 }
 
 // S for the two 16-token tiles of a TQ3 block: tile t, row (16t + 8r + g),
 // units 2c, 2c+1 (24 bytes at 24c).  Each k-step's A fragment is read once
-// and feeds the four MMAs (two tiles x two n8 halves).
-__device__ __forceinline__ void dec_qk_tq3(const uint8_t* kb, int g, int c, const uint4* qs, const Lut& lut,
-                                           float (&s)[2][2][4]) {
+// per query token and feeds the four MMAs (two tiles x two n8 halves); each
+// dequantised K fragment feeds every query's MMAs.
+template <int NQ>
+__device__ __forceinline__ void dec_qk_tq3(const uint8_t* kb, int g, int c, const uint4* const (&qs)[NQ],
+                                           const Lut& lut, float (&s)[NQ][2][2][4]) {
   const int lane = threadIdx.x & 31;
   uint32_t u[2][2][6];
 #pragma unroll
@@ -913,21 +935,27 @@ __device__ __forceinline__ void dec_qk_tq3(const uint8_t* kb, int g, int c, cons
         tq3_unit_selectors(u[t][r][3 * half], u[t][r][3 * half + 1], u[t][r][3 * half + 2], sel[t][r]);
 #pragma unroll
     for (int st = 0; st < 8; ++st) {
-      const uint4 a = qs[(8 * half + st) * 32 + lane];
+      uint4 a[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) a[q] = qs[q][(8 * half + st) * 32 + lane];
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           uint32_t x0, x1;
           tq3_lookup4(sel[t][r][st], lut, x0, x1);
-          mma16816(s[t][r], a.x, a.y, a.z, a.w, x0, x1);
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) mma16816(s[q][t][r], a[q].x, a[q].y, a[q].z, a[q].w, x0, x1);
         }
     }
   }
 }
 
-// O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32)
-__device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, uint2 pb, float (&o)[16][4]) {
+// O^T += V^T P^T for FP8 V: pair-rows c and c+4 of the tile, dims [32g, 32g+32);
+// each dequantised V fragment feeds every query's MMA.
+template <int NQ>
+__device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, const uint2 (&pb)[NQ],
+                                           float (&o)[NQ][16][4]) {
   const uint8_t* ra = vt + c * (2 * kHeadDim) + 64 * g;
   const uint8_t* rb = vt + (c + 4) * (2 * kHeadDim) + 64 * g;
 #pragma unroll
@@ -937,15 +965,19 @@ __device__ __forceinline__ void dec_pv_fp8(const uint8_t* vt, int g, int c, uint
     const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w};
     const uint32_t xb[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      mma16816(o[4 * q4 + i], e4m3x2_to_f16x2(xa[i]), e4m3x2_to_f16x2(xa[i] >> 16), e4m3x2_to_f16x2(xb[i]),
-               e4m3x2_to_f16x2(xb[i] >> 16), pb.x, pb.y);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a0 = e4m3x2_to_f16x2(xa[i]), a1 = e4m3x2_to_f16x2(xa[i] >> 16);
+      const uint32_t a2 = e4m3x2_to_f16x2(xb[i]), a3 = e4m3x2_to_f16x2(xb[i] >> 16);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) mma16816(o[q][4 * q4 + i], a0, a1, a2, a3, pb[q].x, pb[q].y);
+    }
   }
 }
 
 // O^T += V^T P^T for TQ3 V: pair-rows c and c+4, units 2g, 2g+1 (24 bytes at 24g)
-__device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint2 pb, const Lut& lut,
-                                           float (&o)[16][4]) {
+template <int NQ>
+__device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, const uint2 (&pb)[NQ], const Lut& lut,
+                                           float (&o)[NQ][16][4]) {
   uint32_t ua[6], ub[6];
   load_unit_pair(vt + c * 192 + 24 * g, ua);
   load_unit_pair(vt + (c + 4) * 192 + 24 * g, ub);
@@ -959,194 +991,217 @@ __device__ __forceinline__ void dec_pv_tq3(const uint8_t* vt, int g, int c, uint
       uint32_t x0, x1, y0, y1;
       tq3_lookup4(sa[s], lut, x0, x1);
       tq3_lookup4(sb[s], lut, y0, y1);
-      mma16816(o[8 * half + s], x0, x1, y0, y1, pb.x, pb.y);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) mma16816(o[q][8 * half + s], x0, x1, y0, y1, pb[q].x, pb[q].y);
     }
   }
 }
 
-// Per-warp running state of a piece.
+// Per-warp running state of a piece, per query token.
+template <int NQ>
 struct WarpState {
-  float o[16][4];          // O^T fragments: m-tile i rows (dims) 32g+2i, 32g+2i+1; columns heads 2c, 2c+1
-  float m_run, l_run;      // head g: running max (log2 units) and this lane's share of the sum
+  float o[NQ][16][4];      // O^T fragments: m-tile i rows (dims) 32g+2i, 32g+2i+1; columns heads 2c, 2c+1
+  float m_run[NQ], l_run[NQ];  // head g: running max (log2 units) and this lane's share of the sum
 };
 
-// One block of format FMT at st (nv valid tokens): scores, online softmax, PV.
-template <int FMT>
-__device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* st, int nv, const uint4* qs,
-                                          WarpState& ws) {
+// One block of format FMT at st (nv valid tokens; query token 0 of a paired
+// entry sees nv0 of them): scores, online softmax, PV, for each query token.
+template <int FMT, int NQ>
+__device__ __forceinline__ void dec_block(const DecodeParams& p, const uint8_t* st, int nv, int nv0,
+                                          const uint4* const (&qs)[NQ], WarpState<NQ>& ws) {
   using B = Blk<FMT>;
   constexpr int NT = B::kTiles;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const Lut& lut = p.lut;
-  float sacc[2][2][4];
+  float sacc[NQ][2][2][4];
 #pragma unroll
-  for (int t = 0; t < 2; ++t)
+  for (int q = 0; q < NQ; ++q)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) sacc[t][h][0] = sacc[t][h][1] = sacc[t][h][2] = sacc[t][h][3] = 0.f;
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) sacc[q][t][h][0] = sacc[q][t][h][1] = sacc[q][t][h][2] = sacc[q][t][h][3] = 0.f;
   if (FMT == 0)
-    dec_qk_fp8(st + B::kK, g, c, qs, sacc[0][0], sacc[0][1]);
+    dec_qk_fp8<NQ>(st + B::kK, g, c, qs, sacc);
   else
-    dec_qk_tq3(st + B::kK, g, c, qs, lut, sacc);
+    dec_qk_tq3<NQ>(st + B::kK, g, c, qs, lut, sacc);
   const __half2* ks = reinterpret_cast<const __half2*>(st + B::kKs);
   const __half2* vs = reinterpret_cast<const __half2*>(st + B::kVs);
-  // lane's tokens in tile t: 16t + 2c + {0, 1} (half 0) and 16t + 8 + 2c + {0, 1} (half 1)
-  float sc[NT][4];
-  float mt = -INFINITY;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const float2 k0 = __half22float2(ks[8 * t + c]), k1 = __half22float2(ks[8 * t + 4 + c]);
-    sc[t][0] = (sacc[t][0][0] + sacc[t][0][2]) * k0.x;
-    sc[t][1] = (sacc[t][0][1] + sacc[t][0][3]) * k0.y;
-    sc[t][2] = (sacc[t][1][0] + sacc[t][1][2]) * k1.x;
-    sc[t][3] = (sacc[t][1][1] + sacc[t][1][3]) * k1.y;
-    // rows g >= G of q are zero, so those heads score 0 on every token: they
-    // never trigger a rescale, and the piece end drops them (m = -inf)
-    if (nv < B::kTokens) {
-      const int tb = 16 * t + 2 * c;
-      if (tb >= nv) sc[t][0] = -INFINITY;
-      if (tb + 1 >= nv) sc[t][1] = -INFINITY;
-      if (tb + 8 >= nv) sc[t][2] = -INFINITY;
-      if (tb + 9 >= nv) sc[t][3] = -INFINITY;
-    }
-    mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
-  }
-  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
-  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-  if (__any_sync(kFull, mt > ws.m_run + kLazyRescale)) {
-    const float m_new = fmaxf(ws.m_run, mt);
-    const float alpha = (ws.m_run == -INFINITY) ? 0.f : ex2(ws.m_run - m_new);
-    ws.m_run = m_new;
-    ws.l_run *= alpha;
-    // O columns are heads 2c and 2c+1: their factors live in lanes 8c and 8c+4
-    const float a0 = __shfl_sync(kFull, alpha, 8 * c), a1 = __shfl_sync(kFull, alpha, 8 * c + 4);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      ws.o[i][0] *= a0;
-      ws.o[i][1] *= a1;
-      ws.o[i][2] *= a0;
-      ws.o[i][3] *= a1;
-    }
-  }
-  // m_run stays -inf only for heads g >= G (all their scores -inf); a masked
-  // score gives ex2(-inf) = 0, and 0 times a (finite, possibly stale) scale is 0
-  const float mref = (ws.m_run == -INFINITY) ? 0.f : ws.m_run;
   const float vsc = FMT == 0 ? kFp8PScale : 1.f;
-  uint2 pb[NT];
+  uint2 pb[NT][NQ];
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    float pr[4];
+  for (int q = 0; q < NQ; ++q) {
+    const int nvq = q == 0 ? nv0 : nv;
+    // lane's tokens in tile t: 16t + 2c + {0, 1} (half 0) and 16t + 8 + 2c + {0, 1} (half 1)
+    float sc[NT][4];
+    float mt = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = ex2(sc[t][i] - mref);
-    ws.l_run += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-    const float2 v0 = __half22float2(vs[8 * t + c]), v1 = __half22float2(vs[8 * t + 4 + c]);
-    pb[t] = make_uint2(pack_half2(pr[0] * (v0.x * vsc), pr[1] * (v0.y * vsc)),
-                       pack_half2(pr[2] * (v1.x * vsc), pr[3] * (v1.y * vsc)));
+    for (int t = 0; t < NT; ++t) {
+      const float2 k0 = __half22float2(ks[8 * t + c]), k1 = __half22float2(ks[8 * t + 4 + c]);
+      sc[t][0] = (sacc[q][t][0][0] + sacc[q][t][0][2]) * k0.x;
+      sc[t][1] = (sacc[q][t][0][1] + sacc[q][t][0][3]) * k0.y;
+      sc[t][2] = (sacc[q][t][1][0] + sacc[q][t][1][2]) * k1.x;
+      sc[t][3] = (sacc[q][t][1][1] + sacc[q][t][1][3]) * k1.y;
+      // rows g >= G of q are zero, so those heads score 0 on every token: they
+      // never trigger a rescale, and the piece end drops them (m = -inf)
+      if (nvq < B::kTokens) {
+        const int tb = 16 * t + 2 * c;
+        if (tb >= nvq) sc[t][0] = -INFINITY;
+        if (tb + 1 >= nvq) sc[t][1] = -INFINITY;
+        if (tb + 8 >= nvq) sc[t][2] = -INFINITY;
+        if (tb + 9 >= nvq) sc[t][3] = -INFINITY;
+      }
+      mt = fmaxf(mt, fmaxf(fmaxf(sc[t][0], sc[t][1]), fmaxf(sc[t][2], sc[t][3])));
+    }
+    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+    if (__any_sync(kFull, mt > ws.m_run[q] + kLazyRescale)) {
+      const float m_new = fmaxf(ws.m_run[q], mt);
+      const float alpha = (ws.m_run[q] == -INFINITY) ? 0.f : ex2(ws.m_run[q] - m_new);
+      ws.m_run[q] = m_new;
+      ws.l_run[q] *= alpha;
+      // O columns are heads 2c and 2c+1: their factors live in lanes 8c and 8c+4
+      const float a0 = __shfl_sync(kFull, alpha, 8 * c), a1 = __shfl_sync(kFull, alpha, 8 * c + 4);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        ws.o[q][i][0] *= a0;
+        ws.o[q][i][1] *= a1;
+        ws.o[q][i][2] *= a0;
+        ws.o[q][i][3] *= a1;
+      }
+    }
+    // m_run stays -inf only for heads g >= G (all their scores -inf); a masked
+    // score gives ex2(-inf) = 0, and 0 times a (finite, possibly stale) scale is 0
+    const float mref = (ws.m_run[q] == -INFINITY) ? 0.f : ws.m_run[q];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = ex2(sc[t][i] - mref);
+      ws.l_run[q] += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+      const float2 v0 = __half22float2(vs[8 * t + c]), v1 = __half22float2(vs[8 * t + 4 + c]);
+      pb[t][q] = make_uint2(pack_half2(pr[0] * (v0.x * vsc), pr[1] * (v0.y * vsc)),
+                            pack_half2(pr[2] * (v1.x * vsc), pr[3] * (v1.y * vsc)));
+    }
   }
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     if (FMT == 0)
-      dec_pv_fp8(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], ws.o);
+      dec_pv_fp8<NQ>(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], ws.o);
     else
-      dec_pv_tq3(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], lut, ws.o);
+      dec_pv_tq3<NQ>(st + B::kV + t * (kTileTokens / 2) * B::kPairRow, g, c, pb[t], lut, ws.o);
   }
 }
 
 // Store / add one warp's O fragments to / from a reduction buffer: m-tile i
 // of lane l as one float4 at [i][l] (conflict-free 16-byte accesses).
-__device__ __forceinline__ void red_store(float* buf, const WarpState& ws) {
+__device__ __forceinline__ void red_store(float* buf, const float (&o)[16][4]) {
   const int lane = threadIdx.x & 31;
   float4* b4 = reinterpret_cast<float4*>(buf) + lane;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) b4[i * 32] = make_float4(ws.o[i][0], ws.o[i][1], ws.o[i][2], ws.o[i][3]);
+  for (int i = 0; i < 16; ++i) b4[i * 32] = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
 }
-__device__ __forceinline__ void red_add(const float* buf, WarpState& ws) {
+__device__ __forceinline__ void red_add(const float* buf, float (&o)[16][4]) {
   const int lane = threadIdx.x & 31;
   const float4* b4 = reinterpret_cast<const float4*>(buf) + lane;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float4 v = b4[i * 32];
-    ws.o[i][0] += v.x;
-    ws.o[i][1] += v.y;
-    ws.o[i][2] += v.z;
-    ws.o[i][3] += v.w;
+    o[i][0] += v.x;
+    o[i][1] += v.y;
+    o[i][2] += v.z;
+    o[i][3] += v.w;
   }
 }
 
 // End of a piece: the CTA's warps' states merge into the
-// piece's partial state.  Each warp rescales its O to the common max of each
-// head; O then sums up a fixed tree (four buffers) so the result does not
-// depend on timing; warp 0 writes (m, l, o) per q head.
+// piece's partial state, query token by query token.  Each warp rescales its
+// O to the common max of each head; O then sums up a fixed tree (four
+// buffers) so the result does not depend on timing; warp 0 writes (m, l, o)
+// per q head (heads s G .. s G + G - 1 of the piece's partial state for
+// query token s).
+template <int NQ>
 __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSmem& sm, const Piece& pc,
-                                              WarpState& ws, int warp) {
+                                              WarpState<NQ>& ws, int warp) {
+  using C = DecCfg<NQ>;
+  constexpr int W = C::kWarps;
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int G = p.G;
-  float l = ws.l_run;
-  l += __shfl_xor_sync(kFull, l, 1);
-  l += __shfl_xor_sync(kFull, l, 2);
-  if (c == 0) {
-    sm.epi_m[warp * kMaxGroup + g] = (g < G) ? ws.m_run : -INFINITY;
-    sm.epi_l[warp * kMaxGroup + g] = (g < G) ? l : 0.f;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    float l = ws.l_run[q];
+    l += __shfl_xor_sync(kFull, l, 1);
+    l += __shfl_xor_sync(kFull, l, 2);
+    if (c == 0) {
+      sm.epi_m[(q * W + warp) * kMaxGroup + g] = (g < G) ? ws.m_run[q] : -INFINITY;
+      sm.epi_l[(q * W + warp) * kMaxGroup + g] = (g < G) ? l : 0.f;
+    }
   }
-  named_bar(1, kDecThreads);
+  named_bar(1, C::kThreads);
   const float osc = pc.fmt == 0 ? 1.f / kFp8PScale : 1.f;
-  float f0, f1, Mg = -INFINITY, Lg = 0.f;
-  {
-    float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-      M0 = fmaxf(M0, sm.epi_m[w * kMaxGroup + 2 * c]);
-      M1 = fmaxf(M1, sm.epi_m[w * kMaxGroup + 2 * c + 1]);
-      Mg = fmaxf(Mg, sm.epi_m[w * kMaxGroup + g]);
-    }
-    const float m0 = sm.epi_m[warp * kMaxGroup + 2 * c], m1 = sm.epi_m[warp * kMaxGroup + 2 * c + 1];
-    f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0) * osc;
-    f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1) * osc;
-    if (warp == 0 && Mg != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float mw = sm.epi_m[w * kMaxGroup + g];
-        if (mw != -INFINITY) Lg += ex2(mw - Mg) * sm.epi_l[w * kMaxGroup + g];
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    ws.o[i][0] *= f0;
-    ws.o[i][1] *= f1;
-    ws.o[i][2] *= f0;
-    ws.o[i][3] *= f1;
-  }
   // the tree: with n warps holding sums, warps [n - h, n) add into warps
   // [0, h), h = min(4, n / 2): one round per level through four 8 KB buffers
-  // (the two reduction buffers and both q buffers: the next piece's q
-  // fragments are built only after this merge)
+  // (the two reduction buffers and the first two q buffers: the next piece's
+  // q fragments are built only after this merge)
   float* const q0 = reinterpret_cast<float*>(sm.qbuf);
   float* const q1 = reinterpret_cast<float*>(sm.qbuf + kQBytes / 16);
   auto buf = [&](int i) { return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : i == 2 ? q0 : q1; };
 #pragma unroll
-  for (int n = kDecWarps; n > 1;) {
-    const int h = min(4, n / 2), lo = n - h;
-    const int i = warp - lo;                             // this warp as a source
-    if (i >= 0 && i < h) red_store(buf(i), ws);
-    named_bar(1, kDecThreads);
-    if (warp < h) red_add(buf(warp), ws);
-    n = lo;
-    if (n > 1) named_bar(1, kDecThreads);
-  }
-  if (warp == 0) {
-    float* dst = p.part + static_cast<size_t>(pc.part) * G * (2 + kHeadDim);
+  for (int q = 0; q < NQ; ++q) {
+    const float* em = sm.epi_m + q * W * kMaxGroup;
+    const float* el = sm.epi_l + q * W * kMaxGroup;
+    float f0, f1, Mg = -INFINITY, Lg = 0.f;
+    {
+      float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        M0 = fmaxf(M0, em[w * kMaxGroup + 2 * c]);
+        M1 = fmaxf(M1, em[w * kMaxGroup + 2 * c + 1]);
+        Mg = fmaxf(Mg, em[w * kMaxGroup + g]);
+      }
+      const float m0 = em[warp * kMaxGroup + 2 * c], m1 = em[warp * kMaxGroup + 2 * c + 1];
+      f0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - M0) * osc;
+      f1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - M1) * osc;
+      if (warp == 0 && Mg != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float mw = em[w * kMaxGroup + g];
+          if (mw != -INFINITY) Lg += ex2(mw - Mg) * el[w * kMaxGroup + g];
+        }
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int d = 32 * g + 2 * i;
-      if (2 * c < G)
-        *reinterpret_cast<float2*>(dst + (2 * c) * (2 + kHeadDim) + 2 + d) = make_float2(ws.o[i][0], ws.o[i][2]);
-      if (2 * c + 1 < G)
-        *reinterpret_cast<float2*>(dst + (2 * c + 1) * (2 + kHeadDim) + 2 + d) =
-            make_float2(ws.o[i][1], ws.o[i][3]);
+      ws.o[q][i][0] *= f0;
+      ws.o[q][i][1] *= f1;
+      ws.o[q][i][2] *= f0;
+      ws.o[q][i][3] *= f1;
     }
-    if (c == 0 && g < G) {
-      dst[g * (2 + kHeadDim)] = Mg;
-      dst[g * (2 + kHeadDim) + 1] = Lg;
+    if (q > 0) named_bar(1, C::kThreads);         // the previous query's tree is done with the buffers
+#pragma unroll
+    for (int n = W; n > 1;) {
+      const int h = min(4, n / 2), lo = n - h;
+      const int i = warp - lo;                     // this warp as a source
+      if (i >= 0 && i < h) red_store(buf(i), ws.o[q]);
+      named_bar(1, C::kThreads);
+      if (warp < h) red_add(buf(warp), ws.o[q]);
+      n = lo;
+      if (n > 1) named_bar(1, C::kThreads);
+    }
+    if (warp == 0) {
+      float* dst = p.part + (static_cast<size_t>(pc.part) * NQ + q) * G * (2 + kHeadDim);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int d = 32 * g + 2 * i;
+        if (2 * c < G)
+          *reinterpret_cast<float2*>(dst + (2 * c) * (2 + kHeadDim) + 2 + d) = make_float2(ws.o[q][i][0], ws.o[q][i][2]);
+        if (2 * c + 1 < G)
+          *reinterpret_cast<float2*>(dst + (2 * c + 1) * (2 + kHeadDim) + 2 + d) =
+              make_float2(ws.o[q][i][1], ws.o[q][i][3]);
+      }
+      if (c == 0 && g < G) {
+        dst[g * (2 + kHeadDim)] = Mg;
+        dst[g * (2 + kHeadDim) + 1] = Lg;
+      }
     }
   }
 }
@@ -1186,22 +1241,33 @@ __device__ __forceinline__ void dec_append_tail(const DecodeParams& p, const Pie
 
 // The warp's blocks of piece number pi (piece pc); `ic` is the cursor of the
 // next block to copy in.
-template <int FMT>
+template <int FMT, int NQ>
 __device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int pi,
-                                          BlockCursor& ic, RingPos& rp, int warp, WarpState& ws) {
+                                          BlockCursor<DecCfg<NQ>::kWarps>& ic, RingPos& rp, int warp,
+                                          WarpState<NQ>& ws) {
+  constexpr int W = DecCfg<NQ>::kWarps;
   const int lane = threadIdx.x & 31;
-  const uint4* qs = sm.qbuf + (pi & 1) * (kQBytes / 16);
-  for (int k = warp; k < pc.nblk; k += kDecWarps) {
+  const uint4* qs[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) qs[q] = sm.qbuf + ((pi & 1) * NQ + q) * (kQBytes / 16);
+  for (int k = warp; k < pc.nblk; k += W) {
     int nv = Blk<FMT>::kTokens, e = 0, tok0 = 0;
     if (FMT == 0) nv = block_locate(p, pc, k, e, tok0);
     const bool ok = dec_wait(sm, sm.full + warp * kSlots + rp.slot, rp.phase, p.err);
     uint8_t* st = sm.ring + (warp * kSlots + rp.slot) * kSlotBytes;
     if (ok && nv > 0) {
-      if (FMT == 0 && p.append) {
+      int nv0 = nv;
+      if (FMT == 0 && NQ == 1 && p.append) {
         const PageEntry pe = p.entries[e];
         if (pe.tail && pe.nvalid - 1 >= tok0 && pe.nvalid - 1 < tok0 + kFp8Blk) dec_append_tail(p, pc, pe, tok0, st, lane);
       }
-      dec_block<FMT>(p, st, nv, qs, ws);
+      if (FMT == 0 && NQ == 2) {
+        // a paired entry's prefix ends at its second query token, which its
+        // first query token does not see (the causal mask)
+        const PageEntry pe = p.entries[e];
+        if (pe.tail == kTailPairLast && tok0 + nv == pe.nvalid) nv0 = nv - 1;
+      }
+      dec_block<FMT, NQ>(p, st, nv, nv0, qs, ws);
     }
     __syncwarp();
     // the slot is free again: copy in the warp's block kSlots further on
@@ -1217,9 +1283,12 @@ __device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& 
   }
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams p) {
+template <int NQ>
+__global__ void __launch_bounds__(DecCfg<NQ>::kThreads, 1) mkv_decode_kernel(DecodeParams p) {
+  using C = DecCfg<NQ>;
+  constexpr int W = C::kWarps;
   extern __shared__ __align__(128) uint8_t smem[];
-  const DecSmem sm = dec_carve(smem);
+  const DecSmem sm = dec_carve<NQ>(smem);
   // the CTA's pieces: from the kernel parameters, or (a launch whose
   // parameters must not change between steps, e.g. in a CUDA graph) from the
   // plan region in device memory, which is stable while the kernel runs
@@ -1241,16 +1310,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
   // q and the partial-state workspace belong to the preceding kernels (the
   // previous launch's merge reads the workspace): wait for them first
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // warp h < kMaxGroup builds row h of each piece's q fragments; piece s0's
-  // row load goes out now, the next piece's at the start of each piece
+  // warp h < kMaxGroup builds row h of each piece's q fragments (of every
+  // query token); piece s0's row loads go out now, the next piece's at the
+  // start of each piece
   const bool q_warp = warp < kMaxGroup;
-  BlockCursor ic;
+  BlockCursor<W> ic;
   {
-    QRow qr{};
+    QRow qr[NQ];
     Piece p0{};
     if (q_warp && s0 < s1) {
       p0 = load_piece(p, s0);
-      qr = dec_load_q_row(p, p0, warp, lane);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) qr[q] = dec_load_q_row(p, p0, q, warp, lane);
     }
     // the warp's first kSlots blocks
     ic.start(p, s0, s1, warp);
@@ -1280,7 +1351,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
                         sm.abort_flag);
       ic.issued = nfirst;
     }
-    if (q_warp && s0 < s1) dec_build_q_row(p, sm.qbuf, p0, warp, lane, qr, qsign);
+    if (q_warp && s0 < s1) {
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) dec_build_q_row(p, sm.qbuf + q * (kQBytes / 16), p0, warp, lane, qr[q], qsign);
+    }
     if (lane == 0) {
 #pragma unroll
       for (int i = 1; i < kSlots; ++i)
@@ -1288,34 +1362,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) mkv_decode_kernel(DecodeParams
           dec_issue_entry(p, fp[i], pe[i], tok0[i], nv[i], sm.ring + (warp * kSlots + i) * kSlotBytes,
                           sm.full + warp * kSlots + i, sm.abort_flag);
     }
-    named_bar(1, kDecThreads);
+    named_bar(1, C::kThreads);
   }
   RingPos rp{0, 0};
-  WarpState ws;
+  WarpState<NQ> ws;
   for (int si = s0; si < s1; ++si) {
     const int pi = si - s0;
     const Piece pc = load_piece(p, si);
     const bool prep_next = si + 1 < s1 && q_warp;
     Piece pn{};
-    QRow qn{};
+    QRow qn[NQ];
     if (prep_next) {
       pn = load_piece(p, si + 1);
-      qn = dec_load_q_row(p, pn, warp, lane);
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) qn[q] = dec_load_q_row(p, pn, q, warp, lane);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) ws.o[i][0] = ws.o[i][1] = ws.o[i][2] = ws.o[i][3] = 0.f;
-    ws.m_run = -INFINITY;
-    ws.l_run = 0.f;
+    for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ws.o[q][i][0] = ws.o[q][i][1] = ws.o[q][i][2] = ws.o[q][i][3] = 0.f;
+      ws.m_run[q] = -INFINITY;
+      ws.l_run[q] = 0.f;
+    }
     if (pc.fmt)
-      dec_piece<1>(p, sm, pc, pi, ic, rp, warp, ws);
+      dec_piece<1, NQ>(p, sm, pc, pi, ic, rp, warp, ws);
     else
-      dec_piece<0>(p, sm, pc, pi, ic, rp, warp, ws);
-    dec_piece_end(p, sm, pc, ws, warp);
-    // every warp is past piece pi; the other q buffer (piece pi - 1's, free
-    // since its end) takes piece pi + 1
+      dec_piece<0, NQ>(p, sm, pc, pi, ic, rp, warp, ws);
+    dec_piece_end<NQ>(p, sm, pc, ws, warp);
+    // every warp is past piece pi; the other q buffers (piece pi - 1's, free
+    // since its end) take piece pi + 1
     if (si + 1 < s1) {
-      if (prep_next) dec_build_q_row(p, sm.qbuf + ((pi + 1) & 1) * (kQBytes / 16), pn, warp, lane, qn, qsign);
-      named_bar(1, kDecThreads);
+      if (prep_next) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          dec_build_q_row(p, sm.qbuf + (((pi + 1) & 1) * NQ + q) * (kQBytes / 16), pn, warp, lane, qn[q], qsign);
+      }
+      named_bar(1, C::kThreads);
     }
   }
   // on the normal path every copy issued was waited for; after an abort, wait
@@ -1405,8 +1487,10 @@ __device__ __forceinline__ void merge_run(const float* part, int stride, int h, 
 template <bool PREFETCH>
 __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   __shared__ float xs[kHeadDim];
-  const int h = blockIdx.x % p.G;
-  const int bk = blockIdx.x / p.G;
+  // head h of the entry's partial states: query token h / G, q head h % G
+  const int Ge = p.qpe * p.G;
+  const int h = blockIdx.x % Ge;
+  const int bk = blockIdx.x / Ge;
   const int b = bk / p.Hkv, kvh = bk % p.Hkv;
   // the merge descriptors come with the plan (copied in before the decode
   // kernel started), so they load while the decode kernel still runs
@@ -1416,7 +1500,7 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   // partial states before reading them
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int d = threadIdx.x, lane = d & 31;
-  const int stride = p.G * (2 + kHeadDim);
+  const int stride = Ge * (2 + kHeadDim);
   // the first batch of both formats goes out at once
   MergeBatch bs, bf;
   merge_load(p.part, stride, h, md.tq3_first, 0, md.tq3_count, d, bs);
@@ -1444,9 +1528,10 @@ __global__ void __launch_bounds__(256) mkv_merge_kernel(MergeParams p) {
   const float fs = (Ms == -INFINITY) ? 0.f : exp2f(Ms - M);
   const float ff = (Mf == -INFINITY) ? 0.f : exp2f(Mf - M);
   const float L = Ls * fs + Lf * ff;
-  const int hq = kvh * p.G + h;
-  p.out[(static_cast<size_t>(b) * p.Hq + hq) * kHeadDim + d] = (os * fs + of * ff) / L;
-  if (d == 0) p.lse[b * p.Hq + hq] = (M + log2f(L)) * 0.69314718055994530942f;
+  const int hq = kvh * p.G + h % p.G;
+  const int row = q_row(b, h / p.G, p.qpe, p.nq, p.npair);
+  p.out[(static_cast<size_t>(row) * p.Hq + hq) * kHeadDim + d] = (os * fs + of * ff) / L;
+  if (d == 0) p.lse[row * p.Hq + hq] = (M + log2f(L)) * 0.69314718055994530942f;
 }
 
 }  // namespace
@@ -1465,7 +1550,7 @@ cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-size_t decode_smem_bytes() { return kDecSmemBytes; }
+size_t decode_smem_bytes() { return DecCfg<1>::kSmemBytes; }
 
 
 // Fixed scratch for the allocation-free decode entry point: 8 MiB of partial
@@ -1484,7 +1569,7 @@ cudaError_t noalloc_scratch(float** ptr, size_t* bytes) {
   *bytes = kNoallocScratchBytes;
   return cudaSuccess;
 }
-int decode_threads() { return kDecThreads; }
+int decode_threads() { return DecCfg<1>::kThreads; }
 
 cudaError_t launch_relevance(const RelevanceParams& p, cudaStream_t s) {
   if (p.npages > 0)
@@ -1508,7 +1593,11 @@ cudaError_t prepare_decode_launch() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
   if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(mkv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmemBytes);
+    e = cudaFuncSetAttribute(mkv_decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<1>::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mkv_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DecCfg<2>::kSmemBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(mkv_merge_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmemCap);
     if (e != cudaSuccess) return e;
@@ -1523,15 +1612,16 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
   if (p.n_ctas <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_ctas);
-  cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = kDecSmemBytes;
+  const bool pair = p.qpe == 2;
+  cfg.blockDim = dim3(pair ? DecCfg<2>::kThreads : DecCfg<1>::kThreads);
+  cfg.dynamicSmemBytes = pair ? DecCfg<2>::kSmemBytes : DecCfg<1>::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mkv_decode_kernel, p);
+  return pair ? cudaLaunchKernelEx(&cfg, mkv_decode_kernel<2>, p) : cudaLaunchKernelEx(&cfg, mkv_decode_kernel<1>, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
@@ -1548,7 +1638,7 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t s) {
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
-  const int grid = p.n * p.Hkv * p.G;
+  const int grid = p.n * p.Hkv * p.qpe * p.G;
   const int per_sm = (grid + n_sm - 1) / n_sm;
   size_t dyn = 0;
   if (per_sm <= 2) {

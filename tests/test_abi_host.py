@@ -366,8 +366,9 @@ def test_plan_minimises_the_largest_cta(mkv):
 
 
 def test_multi_query_plan_covers_each_prefix(mkv):
-    """mkv_plan_decode_multi: batch entry b * nq + i reads request b up to its
-    query token i, per kv head and tier exactly once."""
+    """mkv_plan_decode_multi: query tokens go in pairs; batch entry
+    b * ceil(nq / 2) + j reads request b up to its query token
+    min(2j + 1, nq - 1), per kv head and tier exactly once."""
     P = 64
     layouts = [(64 * 9 + 3, [2, 3, 3, 3, 3, 1, 1, 1, 1, 1]), (64 * 4, [3, 3, 1, 1]), (5, [1])]
     p = _host_pool(mkv, num_layers=1, fp8_slots=64, tq3_slots=64, max_seqs=16, max_batch=16, max_pages_per_seq=40)
@@ -380,14 +381,16 @@ def test_multi_query_plan_covers_each_prefix(mkv):
         if stale:
             p.demote([r] * len(stale), stale)
     nq = 5
+    npair = (nq + 1) // 2
     plan = p.plan([0, 1, 2], nq=nq)
+    assert {c[0] for c in plan} == set(range(3 * npair))
     for b, (n, tiers) in enumerate(layouts):
-        for i in range(nq):
-            visible = n - nq + 1 + i
+        for j in range(npair):
+            visible = n - nq + 1 + min(2 * j + 1, nq - 1)
             tq3 = sum(min(P, visible - pg * P) for pg, t in enumerate(tiers) if t == 3 and pg * P < visible)
             fp8 = visible - tq3
             for kvh in range(4):
-                mine = [c for c in plan if c[0] == b * nq + i and c[1] == kvh]
+                mine = [c for c in plan if c[0] == b * npair + j and c[1] == kvh]
                 assert sum(c[5] for c in mine if c[2] == 3) == tq3
                 assert sum(c[5] for c in mine if c[2] == 1) == fp8
     # nq = 1 is the decode plan

@@ -577,7 +577,7 @@ def test_decode_multi_query_causal(mkv, P, qdtype):
         if st:
             pool.demote([r] * len(st), st)
     ids = list(range(len(specs)))
-    for nq in (1, 3, 8):
+    for nq in (1, 2, 3, 8):
         q = torch.randn(len(ids), nq, 24, 256, generator=g).to(qdtype)
         out, lse = pool.decode_multi(0, ids, q.to(DEV))
         torch.cuda.synchronize()
