@@ -592,7 +592,6 @@ __global__ void __launch_bounds__(128) mkv_relevance_kernel(RelevanceParams p) {
 // warp's block kSlots further on as soon as the warp is done with it.  No
 // warp waits for another except at the end of a piece, where the warps'
 // states merge, in a fixed order, into one partial state (m, l, o) per q head.
-constexpr int kSlots = 2;                 // staging slots per warp
 constexpr int kSlotBytes = 2 * (kFp8Blk * kHeadDim + 2 * kFp8Blk);   // an FP8 block; a TQ3 block fits
 
 template <int FMT>
@@ -621,9 +620,13 @@ template <int NQ>
 struct DecCfg {
   static constexpr int kWarps = dec_warps(NQ);
   static constexpr int kThreads = kWarps * 32;
+  // staging slots per warp: 12 x 2 or 8 x 3, 24 blocks in flight per SM
+  static constexpr int kSlots = NQ == 1 ? 2 : 3;
   static constexpr int kSmemRing = kWarps * kSlots * kSlotBytes;
   static constexpr int kSmemQ = 2 * NQ * kQBytes;             // [piece i, i+1][query][k-step][lane]
-  static constexpr int kSmemRed = kRedBufs * kRedFloats * 4;
+  // the piece-end tree's four buffers: two of their own and the two q
+  // buffers (one query token), or the four q buffers (two)
+  static constexpr int kSmemRed = NQ == 1 ? kRedBufs * kRedFloats * 4 : 0;
   static constexpr int kSmemEpi = 2 * NQ * kWarps * kMaxGroup * 4;
   static constexpr int kSmemBars = kWarps * kSlots * 8 + 16;
   static constexpr int kSmemBytes = kSmemRing + kSmemQ + kSmemRed + kSmemEpi + kSmemBars;
@@ -650,10 +653,10 @@ __device__ __forceinline__ DecSmem dec_carve(uint8_t* base) {
   s.ring = base;
   s.qbuf = reinterpret_cast<uint4*>(base + C::kSmemRing);
   s.red = reinterpret_cast<float*>(base + C::kSmemRing + C::kSmemQ);
-  s.epi_m = s.red + kRedBufs * kRedFloats;
+  s.epi_m = reinterpret_cast<float*>(base + C::kSmemRing + C::kSmemQ + C::kSmemRed);
   s.epi_l = s.epi_m + NQ * C::kWarps * kMaxGroup;
   s.full = reinterpret_cast<uint64_t*>(s.epi_l + NQ * C::kWarps * kMaxGroup);
-  s.abort_flag = reinterpret_cast<int*>(s.full + C::kWarps * kSlots);
+  s.abort_flag = reinterpret_cast<int*>(s.full + C::kWarps * C::kSlots);
   return s;
 }
 
@@ -1140,11 +1143,13 @@ __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSm
   const float osc = pc.fmt == 0 ? 1.f / kFp8PScale : 1.f;
   // the tree: with n warps holding sums, warps [n - h, n) add into warps
   // [0, h), h = min(4, n / 2): one round per level through four 8 KB buffers
-  // (the two reduction buffers and the first two q buffers: the next piece's
-  // q fragments are built only after this merge)
-  float* const q0 = reinterpret_cast<float*>(sm.qbuf);
-  float* const q1 = reinterpret_cast<float*>(sm.qbuf + kQBytes / 16);
-  auto buf = [&](int i) { return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : i == 2 ? q0 : q1; };
+  // (see DecCfg; q buffers are free here: the next piece's q fragments are
+  // built only after this merge)
+  float* const qf = reinterpret_cast<float*>(sm.qbuf);
+  auto buf = [&](int i) {
+    if (NQ == 1) return i == 0 ? sm.red : i == 1 ? sm.red + kRedFloats : qf + (i - 2) * kRedFloats;
+    return qf + i * kRedFloats;
+  };
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     const float* em = sm.epi_m + q * W * kMaxGroup;
@@ -1208,10 +1213,11 @@ __device__ __forceinline__ void dec_piece_end(const DecodeParams& p, const DecSm
 
 // The warp's position in its own ring: slot and phase parity of the next
 // block it consumes.
+template <int S>
 struct RingPos {
   int slot, phase;
   __device__ void step() {
-    if (++slot == kSlots) {
+    if (++slot == S) {
       slot = 0;
       phase ^= 1;
     }
@@ -1243,9 +1249,9 @@ __device__ __forceinline__ void dec_append_tail(const DecodeParams& p, const Pie
 // next block to copy in.
 template <int FMT, int NQ>
 __device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& sm, const Piece& pc, int pi,
-                                          BlockCursor<DecCfg<NQ>::kWarps>& ic, RingPos& rp, int warp,
-                                          WarpState<NQ>& ws) {
-  constexpr int W = DecCfg<NQ>::kWarps;
+                                          BlockCursor<DecCfg<NQ>::kWarps>& ic, RingPos<DecCfg<NQ>::kSlots>& rp,
+                                          int warp, WarpState<NQ>& ws) {
+  constexpr int W = DecCfg<NQ>::kWarps, kSlots = DecCfg<NQ>::kSlots;
   const int lane = threadIdx.x & 31;
   const uint4* qs[NQ];
 #pragma unroll
@@ -1286,7 +1292,7 @@ __device__ __forceinline__ void dec_piece(const DecodeParams& p, const DecSmem& 
 template <int NQ>
 __global__ void __launch_bounds__(DecCfg<NQ>::kThreads, 1) mkv_decode_kernel(DecodeParams p) {
   using C = DecCfg<NQ>;
-  constexpr int W = C::kWarps;
+  constexpr int W = C::kWarps, kSlots = C::kSlots;
   extern __shared__ __align__(128) uint8_t smem[];
   const DecSmem sm = dec_carve<NQ>(smem);
   // the CTA's pieces: from the kernel parameters, or (a launch whose
@@ -1364,7 +1370,7 @@ __global__ void __launch_bounds__(DecCfg<NQ>::kThreads, 1) mkv_decode_kernel(Dec
     }
     named_bar(1, C::kThreads);
   }
-  RingPos rp{0, 0};
+  RingPos<kSlots> rp{0, 0};
   WarpState<NQ> ws;
   for (int si = s0; si < s1; ++si) {
     const int pi = si - s0;
