@@ -619,8 +619,9 @@ def run_multi(args):
     the causal multi-query attention per layer.  No pages are demoted during
     the few timed steps (the Recent window grows by their tokens).  value =
     the unique KV bytes of the cache (each byte once per kv head and step) per
-    second; the decode kernel reads each query token's prefix, about nq times
-    those bytes, reported as kernel_read_bytes_per_launch."""
+    second; the decode kernel reads each batch entry's prefix once (a pair of
+    query tokens per entry for nq >= 2), about ceil(nq / 2) times those
+    bytes, reported as kernel_read_bytes_per_launch."""
     import torch
 
     from mixed_format_paged_gb300 import binding as B
@@ -686,10 +687,13 @@ def run_multi(args):
     unique = sum(b for b, _ in acc) / len(acc) / L
     avg_us = 1e3 * sum(kernel_ms) / len(kernel_ms)
     ctx = sum(c for _, c in acc) / len(acc)
-    # the kernel reads query token i's prefix: (nq - 1 - i) tokens fewer than the
-    # whole cache, all of them FP8 (the newest pages)
+    # the kernel reads each batch entry's prefix once: with nq >= 2 the query
+    # tokens go in pairs and entry j reads up to query token min(2j + 1, nq - 1),
+    # (nq - 1 - that) tokens fewer than the whole cache, all of them FP8 (the
+    # newest pages)
     per_tok_fp8 = w.Hkv * ROW_BYTES["fp8"]
-    read = nq * unique - per_tok_fp8 * n * nq * (nq - 1) / 2
+    last = [0] if nq == 1 else [min(2 * j + 1, nq - 1) for j in range((nq + 1) // 2)]
+    read = sum(unique - per_tok_fp8 * n * (nq - 1 - i) for i in last)
     peak, peak_src = measured_peaks()
     line = {
         "metric": "multi-query decode-attn KV GB/s (unique cache bytes) and query tokens/s",
