@@ -376,7 +376,7 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
   // one dequantisation, and a paired piece ends with two merges
   const int64_t cost_tq3 = qpe == 1 ? kCostTq3Token : kCostTq3Token * 3 / 2;
   const int64_t cost_fp8 = qpe == 1 ? kCostFp8Token : kCostFp8Token * 3 / 2;
-  const int64_t cost_piece = qpe == 1 ? kCostPiece : 2 * kCostPiece;
+  const int64_t cost_piece = qpe == 1 ? kCostPiece : kCostPiece * 3 / 2;
   const int64_t round_full = 24 + 3 * int64_t(W);   // a round of W blocks, in units of its slowest block
   std::vector<PageEntry> entries;
   entries.reserve(size_t(n) * 64);
