@@ -601,6 +601,51 @@ def test_decode_multi_query_causal(mkv, P, qdtype):
         pool.decode_multi(0, [1], torch.randn(1, 10, 24, 256).to(DEV))
 
 
+def _prefix(pages, P, visible):
+    """The exported pages cut to their first `visible` tokens."""
+    out = []
+    for i, (tier, b, nv) in enumerate(pages):
+        if i * P >= visible:
+            break
+        out.append((tier, b, min(nv, visible - i * P)))
+    return out
+
+
+def test_multi_query_full_size_sampled(mkv):
+    """Paired multi-query decode on the 2 x 59,008-token workload (one layer,
+    nq = 4 query tokens appended to each request): query tokens 0 and 3 of a
+    sampled (request, kv head), each against the oracle over its own causal
+    prefix of the stored pages."""
+    from mixed_format_paged_gb300 import workloads
+    from mixed_format_paged_gb300.harness import make_pool, prefill
+    from oracle.paged import decode_attention_streaming
+    w = workloads.make("cfg3")
+    nq = 4
+    pool = make_pool(w, device=DEV, extra_steps=nq + 2, seed=77, max_batch=w.n * nq)
+    prefill(pool, w, device=DEV, layers=[0])
+    ids = list(range(w.n))
+    g = torch.Generator().manual_seed(41)
+    pool.extend(ids, [nq] * w.n)
+    K, V = _kv(w.n * nq, torch.bfloat16, g)
+    pool.append(0, ids, [nq] * w.n, K.to(DEV), V.to(DEV))
+    q = torch.randn(w.n, nq, 24, 256, generator=g).to(torch.bfloat16)
+    out, lse = pool.decode_multi(0, ids, q.to(DEV))
+    torch.cuda.synchronize()
+    pool.check_device_errors()
+    rng = np.random.default_rng(8)
+    r = int(rng.integers(0, w.n))
+    kvh = int(rng.integers(0, 4))
+    pages = _export(pool, 0, r)
+    T = sum(nv for _, _, nv in pages)
+    sl = slice(kvh * 6, kvh * 6 + 6)
+    for i in (0, nq - 1):
+        ro, rl = decode_attention_streaming(q[r, i].double().numpy(), _prefix(pages, w.P, T - nq + i + 1), w.P, 4,
+                                            256, 77, kv_heads=[kvh])
+        o = out[r, i].double().cpu().numpy()[sl]
+        assert np.abs(o - ro[sl]).max() <= OUT_TOL * np.abs(ro[sl]).max(), (r, kvh, i)
+        assert np.abs(lse[r, i].double().cpu().numpy()[sl] - rl[sl]).max() <= LSE_TOL, (r, kvh, i)
+
+
 # ------------------------------------------------------------------ failure detection without a fault
 def test_wait_timeout_is_reported_and_context_stays_usable(mkv):
     """A bounded wait that runs out (an mbarrier nothing arrives on) records
