@@ -13,7 +13,9 @@
 //                         Lloyd-Max codes, pack)
 //   mkv_decode_kernel  -- persistent partial-attention kernel over both
 //                         formats: 12 independent warps per CTA, each with its
-//                         own ring of bulk-copied page blocks
+//                         own ring of bulk-copied page blocks (<1>); <2> serves
+//                         two query tokens per batch entry (8 warps, several
+//                         query tokens per request)
 //   mkv_merge_kernel   -- LSE merge: TQ3 partials in the rotated domain,
 //                         one R^T, then FP8 partials; writes out and lse
 #include "mkv_internal.h"
