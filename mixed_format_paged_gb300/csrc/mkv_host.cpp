@@ -286,7 +286,9 @@ Sizes compute_sizes(const mkv_pool_config& c) {
   s.append = align256(size_t(kAppendCap) * 4);
   s.demote = align256(size_t(kDemoteCap) * 8);
   const int G = c.num_q_heads / c.num_kv_heads;
-  s.workspace = align256(size_t(s.chunk_cap) * G * (2 + D) * 4);
+  // partial states: one per plan piece (at most chunk_cap), two per piece of
+  // a paired multi-query plan
+  s.workspace = align256(size_t(2) * s.chunk_cap * G * (2 + D) * 4);
   s.err = 256;
   s.total = s.fp8_arena + s.tq3_arena + s.plan + s.append + s.demote + s.workspace + s.err;
   return s;
@@ -577,9 +579,8 @@ mkv_status build_plan(mkv_pool* p, int32_t n_req, const int32_t* ids, int32_t nq
     }
   }
   cta_seg[ncta] = int(segs.size());
-  // the workspace holds chunk_cap partial states of G heads; a paired piece
-  // writes qpe of them
-  if (int64_t(segs.size()) * qpe > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
+  // (the workspace holds 2 chunk_cap partial states of G heads: qpe per piece)
+  if (int(segs.size()) > p->chunk_cap) return fail(MKV_ERR_CAPACITY, "plan pieces exceed capacity");
   // partial-state indices: pieces are in group order, so each group's are contiguous
   for (Group& g : groups) g.nparts = 0;
   for (int i = 0; i < int(segs.size()); ++i) {

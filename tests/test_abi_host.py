@@ -399,6 +399,23 @@ def test_multi_query_plan_covers_each_prefix(mkv):
         p.plan([0, 1, 2], nq=6)                        # request 2 holds 5 tokens
 
 
+def test_paired_plan_fits_a_full_batch(mkv):
+    """A paired piece writes two partial states: a batch at max_batch with an
+    odd nq (every request's FP8 and TQ3 groups in every kv head) plans
+    without running out of partial-state room."""
+    n, nq = 100, 3
+    p = _host_pool(mkv, num_layers=1, fp8_slots=3 * n, tq3_slots=n, max_seqs=n * nq, max_batch=n * nq,
+                   max_pages_per_seq=4)
+    ids = list(range(n))
+    for r in ids:
+        p.extend([r], [64 * 2 + 7 + r % 5])
+    p.demote(ids, [0] * n)
+    plan = p.plan(ids, nq=nq)
+    npair = (nq + 1) // 2
+    assert {c[0] for c in plan} == set(range(n * npair))
+    assert sum(1 for c in plan if c[2] == 3) >= n * npair * 4        # every entry's TQ3 group, per kv head
+
+
 def test_inject_plan_slot_needs_a_device_plan(mkv):
     p = _host_pool(mkv)
     with pytest.raises(mkv.MkvError) as e:
