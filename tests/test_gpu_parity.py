@@ -611,15 +611,19 @@ def _prefix(pages, P, visible):
     return out
 
 
-def test_multi_query_full_size_sampled(mkv):
-    """Paired multi-query decode on the 2 x 59,008-token workload (one layer,
-    nq = 4 query tokens appended to each request): query tokens 0 and 3 of a
-    sampled (request, kv head), each against the oracle over its own causal
-    prefix of the stored pages."""
+@pytest.mark.parametrize("name", ["cfg3", "cfg5"])
+def test_multi_query_full_size_sampled(mkv, name):
+    """Paired multi-query decode at full context length (one layer, nq = 4
+    query tokens appended to each request): the 2 x 59,008-token workload
+    (P = 64), and two requests of the 16 x 131K-token one (P = 128).  Query
+    tokens 0 and 3 of a sampled (request, kv head), each against the oracle
+    over its own causal prefix of the stored pages."""
     from mixed_format_paged_gb300 import workloads
     from mixed_format_paged_gb300.harness import make_pool, prefill
     from oracle.paged import decode_attention_streaming
-    w = workloads.make("cfg3")
+    w = workloads.make(name)
+    if w.n > 2:
+        w = w.subset([0, 1])
     nq = 4
     pool = make_pool(w, device=DEV, extra_steps=nq + 2, seed=77, max_batch=w.n * nq)
     prefill(pool, w, device=DEV, layers=[0])
