@@ -639,7 +639,7 @@ struct DecCfg {
 struct DecSmem {
   uint8_t* ring;                               // [warp][slot] kSlotBytes
   uint4* qbuf;                                 // [2][NQ][k-step 16][lane 32]: q fragments of pieces i, i+1
-  float* red;                                  // [kRedBufs][kRedFloats]
+  float* red;                                  // [kRedBufs][kRedFloats] (one query token only)
   float* epi_m;                                // [query][warp][kMaxGroup]
   float* epi_l;
   uint64_t* full;                              // [warp][slot]
