@@ -594,6 +594,11 @@ def test_decode_multi_query_causal(mkv, P, qdtype):
             o1, l1 = pool.decode(0, ids, q[:, 0].contiguous().to(DEV))
             torch.cuda.synchronize()
             assert torch.equal(o1, out[:, 0]) and torch.equal(l1, lse[:, 0])
+        else:
+            # paired entries merge in a fixed order too: a second call repeats every bit
+            o2, l2 = pool.decode_multi(0, ids, q.to(DEV))
+            torch.cuda.synchronize()
+            assert torch.equal(o2, out) and torch.equal(l2, lse)
     # a query token in a TQ3 page is refused; so are too many query tokens
     with pytest.raises(mkv.MkvError):
         pool.decode_multi(0, [2], torch.randn(1, 3 * P, 24, 256).to(DEV))
