@@ -204,14 +204,96 @@ __global__ void __launch_bounds__(256) mkv_append_kernel(AppendParams p) {
 }
 
 // ============================================================== demote
-// One block per (page pair, layer, kv head, K|V plane).  Each warp encodes
-// rows (dequantise, sign flip, 8-stage FWHT, RMS scale, threshold count);
-// the block then packs 12-byte units and writes the TQ3 plane.
+// One block per (page pair, layer, kv head, K|V plane); each warp encodes
+// rows and packs them straight into the TQ3 plane.  Lane l holds dims
+// 8l .. 8l + 7 of a row (dequantise, sign flip, 8-stage FWHT, RMS scale,
+// threshold count).
+//
+// One row's codes: nibble i of the result is the code of dim 8 lane + i;
+// sg16 gets the row's fp16 sigma.  code = #{k : tau_k <= y / sigma}, decided
+// as tau_k * sigma <= y (sigma > 0): the two differ only within about one
+// fp32 rounding of a threshold.  sigma == 0 gives u = 0, code 4 (tau_1 ..
+// tau_4 <= 0 < tau_5).
+__device__ __forceinline__ uint32_t demote_row(float (&x)[8], uint32_t sg8, const float (&thr)[7], int lane,
+                                               __half& sg16) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+  sg16 = __float2half_rn(__fsqrt_rn(ss * (1.0f / kHeadDim)));
+  const float sg = __half2float(sg16);
+  // y = H (signs .* x) / 16; element index j = 8*lane + i
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if ((sg8 >> i) & 1u) x[i] = -x[i];
+#pragma unroll
+  for (int hs = 1; hs < 8; hs <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & hs) == 0) {
+        const float a = x[i], c = x[i + hs];
+        x[i] = a + c;
+        x[i + hs] = a - c;
+      }
+    }
+  }
+#pragma unroll
+  for (int lm = 1; lm < 32; lm <<= 1) {
+    const bool upper = (lane & lm) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float o = __shfl_xor_sync(kFull, x[i], lm);
+      x[i] = upper ? (o - x[i]) : (x[i] + o);
+    }
+  }
+  if (sg == 0.f) return 0x44444444u;
+  float tq[7];
+#pragma unroll
+  for (int q = 0; q < 7; ++q) tq[q] = thr[q] * sg;
+  uint32_t nib = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float y = x[i] * (1.0f / 16.0f);
+    uint32_t k = 0;
+#pragma unroll
+    for (int q = 0; q < 7; ++q) k += (tq[q] <= y) ? 1u : 0u;
+    nib |= k << (4 * i);
+  }
+  return nib;
+}
+// Eight e4m3 codes (two words, code i in byte i) times the row scale s.
+__device__ __forceinline__ void demote_dequant(uint32_t w0, uint32_t w1, float s, float (&x)[8]) {
+  const uint32_t w[2] = {w0, w1};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t f2 = e4m3x2_to_f16x2(w[h] >> (16 * i));
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f2));
+      x[4 * h + 2 * i] = f.x * s;
+      x[4 * h + 2 * i + 1] = f.y * s;
+    }
+  }
+}
+// Nibbles 0..3 of a and b interleaved: nibble 2i = a's nibble i, 2i + 1 = b's.
+__device__ __forceinline__ uint32_t nibble_zip(uint32_t a, uint32_t b) {
+  a &= 0xFFFFu;
+  b &= 0xFFFFu;
+  a = (a | (a << 8)) & 0x00FF00FFu;
+  a = (a | (a << 4)) & 0x0F0F0F0Fu;
+  b = (b | (b << 8)) & 0x00FF00FFu;
+  b = (b | (b << 4)) & 0x0F0F0F0Fu;
+  return a | (b << 4);
+}
+// A unit's word from the nibble word of its own codes and the nibble word e
+// of its codes 24..31 (bit k of each of those goes to bit 3 of nibble i).
+__device__ __forceinline__ uint32_t tq3_word(uint32_t nib, uint32_t e, int k) {
+  return (nib & 0x77777777u) | (((e >> k) & 0x11111111u) << 3);
+}
+
 __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
-  extern __shared__ __align__(16) uint8_t dsm[];
   const int P = p.P;
-  uint8_t* codes = dsm;                                                 // [P][256]
-  __half* sig = reinterpret_cast<__half*>(dsm + P * kHeadDim);          // [P]
   int job = blockIdx.x;
   const int kv = job & 1;
   job >>= 1;
@@ -228,103 +310,56 @@ __global__ void __launch_bounds__(256) mkv_demote_kernel(DemoteParams p) {
                  static_cast<int64_t>(h) * 2 * tq3_plane + kv * tq3_plane;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const __half* sc = reinterpret_cast<const __half*>(src + P * kHeadDim);
-  for (int t = warp; t < P; t += 8) {
-    uint8_t b[8];
-    if (kv == 0) {
-      const uint2 w = *reinterpret_cast<const uint2*>(src + t * kHeadDim + 8 * lane);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        b[i] = (w.x >> (8 * i)) & 0xff;
-        b[4 + i] = (w.y >> (8 * i)) & 0xff;
-      }
-    } else {
-      const uint8_t* r = src + (t >> 1) * (2 * kHeadDim) + (t & 1);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) b[i] = r[2 * (8 * lane + i)];
-    }
-    const float s = __half2float(sc[t]);
-    float x[8];
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t f2 = e4m3x2_to_f16x2(b[2 * i] | (b[2 * i + 1] << 8));
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f2));
-      x[2 * i] = f.x * s;
-      x[2 * i + 1] = f.y * s;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-    const __half sg16 = __float2half_rn(__fsqrt_rn(ss * (1.0f / kHeadDim)));
-    const float sg = __half2float(sg16);
-    // y = H (signs .* x) / 16; element index j = 8*lane + i
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (sign_neg(p.signs, 8 * lane + i)) x[i] = -x[i];
-#pragma unroll
-    for (int hs = 1; hs < 8; hs <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if ((i & hs) == 0) {
-          const float a = x[i], c = x[i + hs];
-          x[i] = a + c;
-          x[i + hs] = a - c;
-        }
-      }
-    }
-#pragma unroll
-    for (int lm = 1; lm < 32; lm <<= 1) {
-      const bool upper = (lane & lm) != 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float o = __shfl_xor_sync(kFull, x[i], lm);
-        x[i] = upper ? (o - x[i]) : (x[i] + o);
-      }
-    }
-    uint8_t cd[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float y = x[i] * (1.0f / 16.0f);
-      const float u = (sg != 0.f) ? __fdiv_rn(y, sg) : 0.f;
-      int k = 0;
-#pragma unroll
-      for (int q = 0; q < 7; ++q) k += (p.thr[q] <= u) ? 1 : 0;
-      cd[i] = static_cast<uint8_t>(k);
-    }
-    uint2 packed;
-    packed.x = cd[0] | (cd[1] << 8) | (cd[2] << 16) | (cd[3] << 24);
-    packed.y = cd[4] | (cd[5] << 8) | (cd[6] << 16) | (cd[7] << 24);
-    *reinterpret_cast<uint2*>(codes + t * kHeadDim + 8 * lane) = packed;
-    if (lane == 0) sig[t] = sg16;
-  }
-  __syncthreads();
-  // pack units: word w -> unit w/3, word index k = w%3
-  const int nwords = P * (kHeadDim / 32) * 3;
-  uint32_t* out = reinterpret_cast<uint32_t*>(dst);
-  for (int w = threadIdx.x; w < nwords; w += blockDim.x) {
-    const int unit = w / 3, k = w - 3 * (w / 3);
-    uint32_t word = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      int e0 = 8 * k + i, e1 = 24 + i;
-      uint32_t c0, c1;
-      if (kv == 0) {
-        const int t = unit / (kHeadDim / 32), j0 = (unit % (kHeadDim / 32)) * 32;
-        c0 = codes[t * kHeadDim + j0 + e0];
-        c1 = codes[t * kHeadDim + j0 + e1];
-      } else {
-        const int v = unit / (kHeadDim / 16), j0 = (unit % (kHeadDim / 16)) * 16;
-        c0 = codes[(2 * v + (e0 & 1)) * kHeadDim + j0 + (e0 >> 1)];
-        c1 = codes[(2 * v + (e1 & 1)) * kHeadDim + j0 + (e1 >> 1)];
-      }
-      word |= (c0 & 7u) << (4 * i);
-      word |= ((c1 >> k) & 1u) << (4 * i + 3);
-    }
-    out[w] = word;
-  }
   __half* osc = reinterpret_cast<__half*>(dst + P * (3 * kHeadDim / 8));
-  for (int t = threadIdx.x; t < P; t += blockDim.x) osc[t] = sig[t];
+  // the rotation signs of this lane's dims (select, not index, the parameter array)
+  const uint32_t sg8 = static_cast<uint32_t>(
+      (lane < 8 ? p.signs[0] : lane < 16 ? p.signs[1] : lane < 24 ? p.signs[2] : p.signs[3]) >> (8 * (lane & 7))) & 0xFFu;
+  float thr[7];
+#pragma unroll
+  for (int q = 0; q < 7; ++q) thr[q] = p.thr[q];
+  if (kv == 0) {
+    // K: row t's unit l / 4 is lanes 4u .. 4u + 3; lane 4u + k (k < 3) writes
+    // word k (its own 8 codes), lane 4u + 3's codes fill the words' bit 3s
+    for (int t = warp; t < P; t += 8) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src + t * kHeadDim + 8 * lane);
+      float x[8];
+      demote_dequant(w.x, w.y, __half2float(sc[t]), x);
+      __half sg16;
+      const uint32_t nib = demote_row(x, sg8, thr, lane, sg16);
+      const uint32_t e = __shfl_sync(kFull, nib, lane | 3);
+      const int k = lane & 3;
+      if (k != 3) reinterpret_cast<uint32_t*>(dst + t * (3 * kHeadDim / 8))[3 * (lane >> 2) + k] = tq3_word(nib, e, k);
+      if (lane == 0) osc[t] = sg16;
+    }
+  } else {
+    // V, one token pair at a time (its rows are interleaved code by code):
+    // unit v * (d / 16) + l / 2 holds dims 8l .. 8l + 7 of lanes 2u and 2u + 1
+    // for both tokens; the even lane writes words 0 and 1 (its dims 0-3 and
+    // 4-7), the odd lane word 2 (its dims 0-3); the odd lane's dims 4-7 fill
+    // the bit 3s
+    for (int v = warp; v < P / 2; v += 8) {
+      const uint4 w = *reinterpret_cast<const uint4*>(src + v * (2 * kHeadDim) + 16 * lane);
+      float x0[8], x1[8];
+      demote_dequant(__byte_perm(w.x, w.y, 0x6420), __byte_perm(w.z, w.w, 0x6420), __half2float(sc[2 * v]), x0);
+      demote_dequant(__byte_perm(w.x, w.y, 0x7531), __byte_perm(w.z, w.w, 0x7531), __half2float(sc[2 * v + 1]), x1);
+      __half sg0, sg1;
+      const uint32_t n0 = demote_row(x0, sg8, thr, lane, sg0);
+      const uint32_t n1 = demote_row(x1, sg8, thr, lane, sg1);
+      const uint32_t lo = nibble_zip(n0, n1), hi = nibble_zip(n0 >> 16, n1 >> 16);
+      const uint32_t e = __shfl_sync(kFull, hi, lane | 1);
+      uint32_t* ud = reinterpret_cast<uint32_t*>(dst + (v * (kHeadDim / 16) + (lane >> 1)) * 12);
+      if ((lane & 1) == 0) {
+        ud[0] = tq3_word(lo, e, 0);
+        ud[1] = tq3_word(hi, e, 1);
+      } else {
+        ud[2] = tq3_word(lo, e, 2);
+      }
+      if (lane == 0) {
+        osc[2 * v] = sg0;
+        osc[2 * v + 1] = sg1;
+      }
+    }
+  }
 }
 
 // ============================================================== dequantise (export)
@@ -1553,8 +1588,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
 
 cudaError_t launch_demote(const DemoteParams& p, cudaStream_t s) {
   const int blocks = p.npairs * p.L * p.Hkv * 2;
-  const size_t smem = static_cast<size_t>(p.P) * kHeadDim + p.P * 2;
-  if (blocks > 0) mkv_demote_kernel<<<blocks, 256, smem, s>>>(p);
+  if (blocks > 0) mkv_demote_kernel<<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
